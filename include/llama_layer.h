@@ -1,0 +1,212 @@
+/*
+ * llama_layer.h -- C ABI of libllama_layer.so: the forward pass of one
+ * Llama-style decoder layer on one sm_103a GPU (prefill over a padded batch,
+ * prefill over packed variable-length sequences, and KV-cache decode).
+ *
+ * The layer, for every token t at position p_t:
+ *   x_n   = RMSNorm(x; g_in)                    RMS(a) = sqrt(mean(a^2) + eps)
+ *   q,k,v = split(x_n W_qkv^T)                  rows of W_qkv: q | k | v
+ *   q',k' = RoPE(q, k; p_t)                     rotate_half pairing (i, i+d/2)
+ *   o     = softmax(q' k'^T / sqrt(d) + causal) v, query head h reads kv head
+ *           h / (n_heads / n_kv_heads)
+ *   h     = x + o W_o^T
+ *   act   = silu(gate) * up, [gate | up] = RMSNorm(h; g_post) W_gate_up^T
+ *   out   = h + act W_down^T
+ * Sources (page title and section):
+ *   - "模型层：从 Embedding 到 Loss 的实现" (nanotron tutorial ch. 9):
+ *     9.3 CausalSelfAttention (fused QKV, GQA, RoPE, causal flash attention),
+ *     9.4 MLP (fused gate_up, silu(gate) * up, down), 9.5 DecoderLayer
+ *     (the two residual branches).
+ *   - "parallel_attention.py -- LLaMA 并行注意力": 1 RoPE (inv_freq = 1 /
+ *     base^(2i/d), cos/sin cache, Llama3 piecewise scaling), 2 attention
+ *     (split q|k|v, repeat_kv, softmax(QK^T/sqrt(d)) V), 3 RmPad (packed
+ *     tokens, cu_seqlens, causal within each sequence).
+ *   - "llama3 结构详解": 3.1 RMSNorm, 3.2 Attention (the KV cache written at
+ *     start_pos and read up to start_pos + seqlen).
+ *   - Llama-3 model.py walkthrough (un.csdn.net): 2 RoPE (apply_scaling),
+ *     3 attention with KV cache, 4 FeedForward w2(silu(w1 x) * w3 x).
+ *   - NJU LLM course lecture 5: LlamaDecoderLayer shapes, RMSNorm,
+ *     "RoPE高效实现" (rotate_half), SwiGLU.
+ *
+ * Conventions for every call:
+ *   - All tensors are row-major and dense.  Element type is the config's dtype
+ *     (fp32 or bf16) for x, out, weights, norm weights and the KV cache;
+ *     position_ids, cu_seqlens and start_pos are int32.
+ *   - Device pointers must be 16-byte aligned (x, out, weights, caches,
+ *     packed, workspace) and 4-byte aligned (int32 arrays).
+ *   - The library never allocates device memory: packed weights, workspace,
+ *     inputs, outputs and caches belong to the caller.  It holds only a small
+ *     host-side handle.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on that stream.  Host-side argument checks run before any
+ *     launch: a failed check returns a negative code and launches nothing.
+ *   - Checks that need device data (cu_seqlens, position_ids, start_pos)
+ *     run in the kernels: an offending token or sequence is skipped and a bit
+ *     is set in a device status word, read by llama_layer_status().
+ *   - Every wait inside a kernel is bounded; a wait that runs out sets the
+ *     status word and the kernel returns (llama_layer_status reports
+ *     LLAMA_ERR_DEVICE_TIMEOUT).
+ */
+#ifndef LLAMA_LAYER_H
+#define LLAMA_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LLAMA_API __attribute__((visibility("default")))
+#else
+#define LLAMA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define LLAMA_OK 0
+#define LLAMA_ERR_INVALID_ARG (-1)        /* null / misaligned pointer, bad size */
+#define LLAMA_ERR_UNSUPPORTED_SHAPE (-2)  /* config outside the supported set */
+#define LLAMA_ERR_WORKSPACE_TOO_SMALL (-3)
+#define LLAMA_ERR_CUDA (-4)               /* a CUDA runtime call failed */
+#define LLAMA_ERR_DEVICE_TIMEOUT (-5)     /* a bounded in-kernel wait ran out */
+#define LLAMA_ERR_DEVICE_BAD_INPUT (-6)   /* bad cu_seqlens / positions / start_pos */
+#define LLAMA_ERR_UNSUPPORTED_DEVICE (-7) /* not an sm_103 device */
+
+#define LLAMA_DTYPE_F32 0
+#define LLAMA_DTYPE_BF16 1
+
+#define LLAMA_ROPE_NONE 0
+#define LLAMA_ROPE_LLAMA3 1
+
+/* Layer shape and RoPE settings.
+ * Supported: head_dim in {64, 128}; n_heads % n_kv_heads == 0;
+ * hidden % 128 == 0; intermediate % 128 == 0; rms_eps > 0; rope_base > 1;
+ * max_position >= 1 (length of the RoPE table: every position used must be
+ * < max_position).  Llama3 scaling (see "parallel_attention.py" section 1 and
+ * the model.py walkthrough section 2, apply_scaling): with wavelength
+ * w_i = 2*pi / f_i, frequencies with w_i < original_max_pos / high_freq_factor
+ * are kept, those with w_i > original_max_pos / low_freq_factor are divided by
+ * rope_factor, and in between f_i becomes (1 - s) f_i / rope_factor + s f_i
+ * with s = (original_max_pos / w_i - low) / (high - low). */
+typedef struct {
+  int hidden;
+  int n_heads;
+  int n_kv_heads;
+  int head_dim;
+  int intermediate;
+  float rms_eps;
+  double rope_base;
+  int rope_scaling; /* LLAMA_ROPE_NONE or LLAMA_ROPE_LLAMA3 */
+  double rope_factor;
+  double rope_low_freq_factor;
+  double rope_high_freq_factor;
+  int rope_original_max_pos;
+  int max_position;
+  int dtype; /* LLAMA_DTYPE_F32 or LLAMA_DTYPE_BF16 */
+} llama_layer_config;
+
+/* Device pointers to the layer's weights in the pages' nn.Linear layout
+ * ([out_features, in_features], row-major), element type = dtype:
+ *   w_qkv     [n_heads*d + 2*n_kv_heads*d, hidden]  rows q | k | v, head-major
+ *   w_o       [hidden, n_heads*d]
+ *   w_gate_up [2*intermediate, hidden]              rows gate | up
+ *   w_down    [hidden, intermediate]
+ *   g_in, g_post [hidden]                           RMSNorm weights
+ * Read only during llama_layer_init; they may be freed afterwards. */
+typedef struct {
+  const void *w_qkv, *w_o, *w_gate_up, *w_down, *g_in, *g_post;
+} llama_layer_weights;
+
+typedef struct llama_layer llama_layer_t;
+
+/* Bytes of device memory llama_layer_init needs for the packed weights, the
+ * RoPE table and the status word.  Host only. */
+LLAMA_API int llama_layer_packed_bytes(const llama_layer_config* cfg, size_t* bytes);
+
+/* Validates cfg, repacks the weights into `packed` (caller-owned device
+ * memory of at least llama_layer_packed_bytes; it must stay allocated and
+ * untouched until llama_layer_destroy), builds the RoPE cos/sin table in
+ * double precision on the host and uploads it as fp32, and returns a host
+ * handle in *out.  Synchronises `stream` before returning.  Repacking folds
+ * g_in into the columns of W_qkv and g_post into those of W_gate_up
+ * (x_n W^T = r * x (g . W)^T with r the row's 1/RMS) and interleaves the
+ * gate and up rows in blocks of 128. */
+LLAMA_API int llama_layer_init(const llama_layer_config* cfg,
+                     const llama_layer_weights* weights, void* packed,
+                     size_t packed_bytes, void* stream, llama_layer_t** out);
+
+/* Workspace bytes for forward calls of up to `max_tokens` tokens and decode
+ * calls of up to `decode_batch` sequences with caches of up to
+ * `decode_max_seq` rows (pass 0 for a mode you do not use).  Host only. */
+LLAMA_API int llama_layer_workspace_bytes(const llama_layer_t* layer, int max_tokens,
+                                int decode_batch, int decode_max_seq,
+                                size_t* bytes);
+
+/* Prefill forward ("模型层" 9.5 DecoderLayer; "parallel_attention.py" 2 and 3).
+ *   x            [total_tokens, hidden] device, input hidden states
+ *   out          [total_tokens, hidden] device, output (must not alias x)
+ *   position_ids [total_tokens] device int32, or NULL: positions restart at 0
+ *                in every sequence.  Every position must be < max_position.
+ *   cu_seqlens   NULL for a padded batch: n_seq sequences of seq_len tokens
+ *                each, total_tokens == n_seq * seq_len.  Otherwise [n_seq + 1]
+ *                device int32 prefix sums of the sequence lengths (packed
+ *                varlen, "parallel_attention.py" 3): cu[0] = 0, non-decreasing,
+ *                cu[n_seq] = total_tokens, no length above seq_len (the
+ *                max_seqlen of the batch).
+ * Attention is causal within each sequence.  `workspace` must hold
+ * llama_layer_workspace_bytes(layer, >= total_tokens, ...). */
+LLAMA_API int llama_layer_forward(llama_layer_t* layer, const void* x, void* out,
+                        const int32_t* position_ids, const int32_t* cu_seqlens,
+                        int n_seq, int seq_len, int total_tokens,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* One decode step ("llama3 结构详解" 3.2; model.py walkthrough 3): one new
+ * token per sequence.
+ *   x          [batch, hidden] device, the new tokens' hidden states
+ *   out        [batch, hidden] device (must not alias x)
+ *   cache_k/v  [batch, max_seq, n_kv_heads, head_dim] device; rows
+ *              0 .. start_pos[b]-1 hold the sequence's rotated keys / values.
+ *              The new token's rotated key and its value are written at row
+ *              start_pos[b]; no other row is written or read beyond it.
+ *   start_pos  [batch] device int32, 0 <= start_pos[b] < max_seq and
+ *              start_pos[b] < max_position; the new token's position.
+ * The new token attends to cache rows 0 .. start_pos[b]. */
+LLAMA_API int llama_layer_decode(llama_layer_t* layer, const void* x, void* out,
+                       void* cache_k, void* cache_v, const int32_t* start_pos,
+                       int batch, int max_seq, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, reads and clears the device status word.  Returns
+ * LLAMA_OK, LLAMA_ERR_DEVICE_TIMEOUT or LLAMA_ERR_DEVICE_BAD_INPUT. */
+LLAMA_API int llama_layer_status(llama_layer_t* layer, void* stream);
+
+/* Byte offsets inside the workspace of the intermediates of the last call
+ * with these sizes, for checking individual stages:
+ *   [0] q|k|v after RoPE   [tokens, n_heads*d + 2*n_kv_heads*d]
+ *   [1] attention output    [tokens, n_heads*d]
+ *   [2] h (after o_proj + residual) [tokens, hidden]
+ *   [3] act = silu(gate)*up [tokens, intermediate]
+ * all of the config's dtype.  decode == 1 gives the decode layout. */
+#define LLAMA_WS_NUM 4
+LLAMA_API int llama_layer_workspace_offsets(const llama_layer_t* layer, int tokens,
+                                  int decode, size_t offsets[LLAMA_WS_NUM]);
+
+/* Frees the host handle only (packed memory stays the caller's). */
+LLAMA_API void llama_layer_destroy(llama_layer_t* layer);
+
+/* Static string for a return code. */
+LLAMA_API const char* llama_layer_strerror(int code);
+
+/* D[M, N] = A[M, K] . B[N, K]^T in bf16 with fp32 accumulation, on the same
+ * tcgen05 / TMA GEMM the layer's projections use (the contraction of every
+ * nn.Linear on the pages).  A, B, D device, row-major, 16-byte aligned;
+ * K % 8 == 0, N % 32 == 0. */
+LLAMA_API int llama_gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K,
+                    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLAMA_LAYER_H */

@@ -1,0 +1,67 @@
+// Internal launch interface between the C ABI (llama_layer.cu) and the kernel
+// files.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace llama {
+
+struct Dims {
+  int H, Hq, Hkv, d, I, Nqkv, max_pos;
+  float eps;
+};
+
+// ----------------------------------------------------------------- simt.cu
+// Element type T is float or __nv_bfloat16 (tag: is_bf16).
+// r[row] = 1 / sqrt(mean(x[row]^2) + eps) for `rows` rows of width H.
+void simt_row_rms(bool is_bf16, const void* x, int rows, int H, float eps,
+                  float* r, cudaStream_t s);
+
+// Positions and sequence checks: pos[t] = t - start of t's sequence (when
+// fill_pos), validates cu_seqlens (device) when given, else padded seq_len.
+void launch_positions(const int32_t* cu, int n_seq, int seq_len, int T,
+                      int32_t* pos, bool fill_pos, int* status,
+                      cudaStream_t s);
+
+// Plain GEMM-with-epilogue, fp32 accumulate, one output element per thread
+// slot.  D[M, N] = A[M, K] . B[N, K]^T then:
+//   EPI_ROWSCALE: out = r[m] * acc
+//   EPI_RESIDUAL: out = res[m, n] + acc
+//   EPI_SWIGLU:   B rows are gate/up interleaved in blocks of 128; output
+//                 column j = silu(r[m] * gate_j) * (r[m] * up_j), N = I.
+enum { EPI_ROWSCALE = 1, EPI_RESIDUAL = 2, EPI_SWIGLU = 3 };
+void simt_gemm(bool is_bf16, int epi, const void* A, const void* B, void* out,
+               int M, int N, int K, const float* rowscale,
+               const void* residual, cudaStream_t s);
+
+// In-place RoPE on the q and k heads of qkv rows [T, Nqkv].
+void simt_rope(bool is_bf16, void* qkv, int T, const Dims& dm,
+               const int32_t* pos, const float* cos_t, const float* sin_t,
+               int* status, cudaStream_t s);
+
+// Prefill attention, one block per (token, q head).
+void simt_attention_prefill(bool is_bf16, const void* qkv, void* attn, int T,
+                            const Dims& dm, const int32_t* cu, int n_seq,
+                            int seq_len, int max_keys, cudaStream_t s);
+
+// Decode: copy k', v of every sequence into its cache row start_pos[b].
+void simt_cache_append(bool is_bf16, const void* qkv, void* cache_k,
+                       void* cache_v, const int32_t* start_pos, int B,
+                       int max_seq, const Dims& dm, int* status,
+                       cudaStream_t s);
+
+// Decode attention over cache rows 0..start_pos[b], one block per (b, head).
+void simt_attention_decode(bool is_bf16, const void* qkv, const void* cache_k,
+                           const void* cache_v, void* attn,
+                           const int32_t* start_pos, int B, int max_seq,
+                           const Dims& dm, cudaStream_t s);
+
+// ----------------------------------------------------------------- pack.cu
+// out[n, k] = W[src(n), k] * (g ? g[k] : 1), src(n) = n, or the gate/up
+// interleave in blocks of 128 when interleave_inter > 0.
+void launch_pack(bool is_bf16, const void* W, const void* g, void* out,
+                 int rows, int cols, int interleave_inter, cudaStream_t s);
+
+}  // namespace llama

@@ -1,0 +1,467 @@
+// The C ABI of libllama_layer.so (declared in include/llama_layer.h):
+// argument checks, weight repacking, the RoPE table, workspace layout, and the
+// launch sequence of each call.  All device memory belongs to the caller.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/llama_layer.h"
+#include "common.cuh"
+#include "gemm_tc.cuh"
+#include "kernels.h"
+
+using namespace llama;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+struct PackedLayout {
+  size_t wqkv, wo, wgu, wd, cos_t, sin_t, status, total;
+};
+
+PackedLayout packed_layout(const llama_layer_config& c) {
+  size_t es = c.dtype == LLAMA_DTYPE_BF16 ? 2 : 4;
+  size_t nqkv = (size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  size_t qs = (size_t)c.n_heads * c.head_dim;
+  PackedLayout p;
+  size_t o = 0;
+  p.wqkv = o; o = align_up(o + nqkv * c.hidden * es);
+  p.wo = o; o = align_up(o + (size_t)c.hidden * qs * es);
+  p.wgu = o; o = align_up(o + 2 * (size_t)c.intermediate * c.hidden * es);
+  p.wd = o; o = align_up(o + (size_t)c.hidden * c.intermediate * es);
+  size_t table = (size_t)c.max_position * (c.head_dim / 2) * sizeof(float);
+  p.cos_t = o; o = align_up(o + table);
+  p.sin_t = o; o = align_up(o + table);
+  p.status = o; o = align_up(o + 64);
+  p.total = o;
+  return p;
+}
+
+int check_config(const llama_layer_config* c) {
+  if (!c) return LLAMA_ERR_INVALID_ARG;
+  if (c->dtype != LLAMA_DTYPE_F32 && c->dtype != LLAMA_DTYPE_BF16)
+    return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (c->hidden <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 ||
+      c->intermediate <= 0 || c->max_position <= 0)
+    return LLAMA_ERR_INVALID_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (c->n_heads % c->n_kv_heads != 0) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (c->hidden % 128 != 0 || c->intermediate % 128 != 0)
+    return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (!(c->rms_eps > 0.f) || !(c->rope_base > 1.0)) return LLAMA_ERR_INVALID_ARG;
+  if (c->rope_scaling == LLAMA_ROPE_LLAMA3) {
+    if (!(c->rope_factor >= 1.0) || !(c->rope_low_freq_factor > 0.0) ||
+        !(c->rope_high_freq_factor > c->rope_low_freq_factor) ||
+        c->rope_original_max_pos <= 0)
+      return LLAMA_ERR_INVALID_ARG;
+  } else if (c->rope_scaling != LLAMA_ROPE_NONE) {
+    return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  }
+  return LLAMA_OK;
+}
+
+// RoPE inverse frequencies in double precision ("parallel_attention.py"
+// section 1: inv_freq_i = 1 / base^(2i/d); Llama3 piecewise scaling as stated
+// in llama_layer.h).
+void rope_inv_freq(const llama_layer_config& c, double* f) {
+  const int half = c.head_dim / 2;
+  for (int i = 0; i < half; ++i) {
+    double v = pow(c.rope_base, -2.0 * i / c.head_dim);
+    if (c.rope_scaling == LLAMA_ROPE_LLAMA3) {
+      const double wl = 2.0 * M_PI / v;
+      const double orig = c.rope_original_max_pos;
+      const double lo = c.rope_low_freq_factor, hi = c.rope_high_freq_factor;
+      if (wl < orig / hi) {
+        // high frequency: unchanged
+      } else if (wl > orig / lo) {
+        v = v / c.rope_factor;
+      } else {
+        const double s = (orig / wl - lo) / (hi - lo);
+        v = (1.0 - s) * v / c.rope_factor + s * v;
+      }
+    }
+    f[i] = v;
+  }
+}
+
+struct WsLayout {
+  size_t pos, r1, ss2, qkv, attn, h, act, total;
+};
+
+WsLayout ws_layout(const llama_layer_config& c, int tokens) {
+  size_t es = c.dtype == LLAMA_DTYPE_BF16 ? 2 : 4;
+  size_t T = (size_t)(tokens > 0 ? tokens : 0);
+  size_t nqkv = (size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  WsLayout w;
+  size_t o = 0;
+  w.pos = o; o = align_up(o + T * 4);
+  w.r1 = o; o = align_up(o + T * 4);
+  w.ss2 = o; o = align_up(o + T * 4);
+  w.qkv = o; o = align_up(o + T * nqkv * es);
+  w.attn = o; o = align_up(o + T * c.n_heads * c.head_dim * es);
+  w.h = o; o = align_up(o + T * c.hidden * es);
+  w.act = o; o = align_up(o + T * c.intermediate * es);
+  w.total = o;
+  return w;
+}
+
+}  // namespace
+
+struct llama_layer {
+  llama_layer_config cfg;
+  Dims dm;
+  bool bf16;
+  char* packed;
+  PackedLayout pl;
+  int* status;
+  int sm_count;
+  CUtensorMap tm_wqkv, tm_wo, tm_wgu, tm_wd;  // bf16 weights, box 256 rows
+};
+
+namespace {
+
+int cuda_err(cudaError_t e) { return e == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA; }
+
+template <typename P>
+char* at(P* base, size_t off) {
+  return reinterpret_cast<char*>(const_cast<void*>(static_cast<const void*>(base))) + off;
+}
+
+int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in,
+                 const int32_t* cu, int n_seq, int seq_len, int T, char* ws,
+                 cudaStream_t s) {
+  const llama_layer_config& c = L->cfg;
+  const Dims& dm = L->dm;
+  const bool b16 = L->bf16;
+  WsLayout w = ws_layout(c, T);
+  int32_t* pos = pos_in ? const_cast<int32_t*>(pos_in)
+                        : reinterpret_cast<int32_t*>(ws + w.pos);
+  float* r1 = reinterpret_cast<float*>(ws + w.r1);
+  float* ss2 = reinterpret_cast<float*>(ws + w.ss2);
+  void* qkv = ws + w.qkv;
+  void* attn = ws + w.attn;
+  void* h = ws + w.h;
+  void* act = ws + w.act;
+  const char* P = L->packed;
+  const float* cos_t = reinterpret_cast<const float*>(P + L->pl.cos_t);
+  const float* sin_t = reinterpret_cast<const float*>(P + L->pl.sin_t);
+
+  launch_positions(cu, n_seq, seq_len, T, reinterpret_cast<int32_t*>(ws + w.pos),
+                   pos_in == nullptr, L->status, s);
+  simt_row_rms(b16, x, T, dm.H, dm.eps, r1, s);
+  if (b16) {
+    cudaError_t e;
+    CUtensorMap ta;
+    TcEpiArgs ep;
+    ep.status = L->status;
+    // a2 + a3: QKV projection, row scale 1/RMS, RoPE on q and k.
+    if (!tc_encode_bf16(&ta, x, T, dm.H, 128)) return LLAMA_ERR_CUDA;
+    ep.out = qkv; ep.ldo = dm.Nqkv; ep.rowscale = r1; ep.pos = pos;
+    ep.cos_t = cos_t; ep.sin_t = sin_t; ep.head_dim = dm.d;
+    ep.rope_cols = (dm.Hq + dm.Hkv) * dm.d; ep.max_pos = dm.max_pos;
+    e = tc_gemm(TC_QKV, 256, ta, L->tm_wqkv, T, dm.Nqkv, dm.H, 1, ep, L->sm_count, s);
+    if (e != cudaSuccess) return LLAMA_ERR_CUDA;
+    // a4 / a5: causal GQA attention.
+    simt_attention_prefill(b16, qkv, attn, T, dm, cu, n_seq, seq_len, seq_len, s);
+    // a7: o_proj + residual, row sums of h^2 for the second RMSNorm.
+    cudaMemsetAsync(ss2, 0, (size_t)T * 4, s);
+    if (!tc_encode_bf16(&ta, attn, T, dm.Hq * dm.d, 128)) return LLAMA_ERR_CUDA;
+    ep = TcEpiArgs();
+    ep.status = L->status;
+    ep.out = h; ep.ldo = dm.H; ep.residual = x; ep.ss_out = ss2;
+    e = tc_gemm(TC_RESID_SS, 256, ta, L->tm_wo, T, dm.H, dm.Hq * dm.d, 1, ep, L->sm_count, s);
+    if (e != cudaSuccess) return LLAMA_ERR_CUDA;
+    // a8: gate_up with the RMSNorm row scale, silu(gate) * up.
+    if (!tc_encode_bf16(&ta, h, T, dm.H, 128)) return LLAMA_ERR_CUDA;
+    ep = TcEpiArgs();
+    ep.status = L->status;
+    ep.out = act; ep.ldo = dm.I; ep.ss_in = ss2; ep.inv_h = 1.0f / dm.H; ep.eps = dm.eps;
+    e = tc_gemm(TC_SWIGLU, 256, ta, L->tm_wgu, T, 2 * dm.I, dm.H, 1, ep, L->sm_count, s);
+    if (e != cudaSuccess) return LLAMA_ERR_CUDA;
+    // a9: down_proj + residual.
+    if (!tc_encode_bf16(&ta, act, T, dm.I, 128)) return LLAMA_ERR_CUDA;
+    ep = TcEpiArgs();
+    ep.status = L->status;
+    ep.out = out; ep.ldo = dm.H; ep.residual = h;
+    e = tc_gemm(TC_RESID, 256, ta, L->tm_wd, T, dm.H, dm.I, 1, ep, L->sm_count, s);
+    if (e != cudaSuccess) return LLAMA_ERR_CUDA;
+  } else {
+    simt_gemm(b16, EPI_ROWSCALE, x, P + L->pl.wqkv, qkv, T, dm.Nqkv, dm.H, r1,
+              nullptr, s);
+    simt_rope(b16, qkv, T, dm, pos, cos_t, sin_t, L->status, s);
+    simt_attention_prefill(b16, qkv, attn, T, dm, cu, n_seq, seq_len, seq_len, s);
+    simt_gemm(b16, EPI_RESIDUAL, attn, P + L->pl.wo, h, T, dm.H, dm.Hq * dm.d,
+              nullptr, x, s);
+    simt_row_rms(b16, h, T, dm.H, dm.eps, ss2, s);
+    simt_gemm(b16, EPI_SWIGLU, h, P + L->pl.wgu, act, T, dm.I, dm.H, ss2,
+              nullptr, s);
+    simt_gemm(b16, EPI_RESIDUAL, act, P + L->pl.wd, out, T, dm.H, dm.I,
+              nullptr, h, s);
+  }
+  return cuda_err(cudaGetLastError());
+}
+
+int decode_impl(llama_layer* L, const void* x, void* out, void* ck, void* cv,
+                const int32_t* start_pos, int B, int max_seq, char* ws,
+                cudaStream_t s) {
+  const llama_layer_config& c = L->cfg;
+  const Dims& dm = L->dm;
+  const bool b16 = L->bf16;
+  WsLayout w = ws_layout(c, B);
+  float* r1 = reinterpret_cast<float*>(ws + w.r1);
+  float* r2 = reinterpret_cast<float*>(ws + w.ss2);
+  void* qkv = ws + w.qkv;
+  void* attn = ws + w.attn;
+  void* h = ws + w.h;
+  void* act = ws + w.act;
+  const char* P = L->packed;
+  const float* cos_t = reinterpret_cast<const float*>(P + L->pl.cos_t);
+  const float* sin_t = reinterpret_cast<const float*>(P + L->pl.sin_t);
+
+  simt_row_rms(b16, x, B, dm.H, dm.eps, r1, s);
+  simt_gemm(b16, EPI_ROWSCALE, x, P + L->pl.wqkv, qkv, B, dm.Nqkv, dm.H, r1,
+            nullptr, s);
+  simt_rope(b16, qkv, B, dm, start_pos, cos_t, sin_t, L->status, s);
+  simt_cache_append(b16, qkv, ck, cv, start_pos, B, max_seq, dm, L->status, s);
+  simt_attention_decode(b16, qkv, ck, cv, attn, start_pos, B, max_seq, dm, s);
+  simt_gemm(b16, EPI_RESIDUAL, attn, P + L->pl.wo, h, B, dm.H, dm.Hq * dm.d,
+            nullptr, x, s);
+  simt_row_rms(b16, h, B, dm.H, dm.eps, r2, s);
+  simt_gemm(b16, EPI_SWIGLU, h, P + L->pl.wgu, act, B, dm.I, dm.H, r2, nullptr,
+            s);
+  simt_gemm(b16, EPI_RESIDUAL, act, P + L->pl.wd, out, B, dm.H, dm.I, nullptr,
+            h, s);
+  return cuda_err(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" {
+
+int llama_layer_packed_bytes(const llama_layer_config* cfg, size_t* bytes) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!bytes) return LLAMA_ERR_INVALID_ARG;
+  *bytes = packed_layout(*cfg).total;
+  return LLAMA_OK;
+}
+
+int llama_layer_init(const llama_layer_config* cfg,
+                     const llama_layer_weights* wts, void* packed,
+                     size_t packed_bytes, void* stream, llama_layer_t** out) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!wts || !packed || !out) return LLAMA_ERR_INVALID_ARG;
+  const void* ptrs[6] = {wts->w_qkv, wts->w_o, wts->w_gate_up,
+                         wts->w_down, wts->g_in, wts->g_post};
+  for (const void* p : ptrs)
+    if (!p || !aligned(p, 16)) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned(packed, kAlign)) return LLAMA_ERR_INVALID_ARG;
+  PackedLayout pl = packed_layout(*cfg);
+  if (packed_bytes < pl.total) return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LLAMA_ERR_CUDA;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || minor != 3) return LLAMA_ERR_UNSUPPORTED_DEVICE;
+
+  llama_layer* L = new (std::nothrow) llama_layer();
+  if (!L) return LLAMA_ERR_INVALID_ARG;
+  L->cfg = *cfg;
+  const llama_layer_config& c = *cfg;
+  L->dm.H = c.hidden; L->dm.Hq = c.n_heads; L->dm.Hkv = c.n_kv_heads;
+  L->dm.d = c.head_dim; L->dm.I = c.intermediate;
+  L->dm.Nqkv = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  L->dm.max_pos = c.max_position; L->dm.eps = c.rms_eps;
+  L->bf16 = c.dtype == LLAMA_DTYPE_BF16;
+  L->packed = static_cast<char*>(packed);
+  L->pl = pl;
+  L->status = reinterpret_cast<int*>(L->packed + pl.status);
+  L->sm_count = sms;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Dims& dm = L->dm;
+
+  launch_pack(L->bf16, wts->w_qkv, wts->g_in, L->packed + pl.wqkv, dm.Nqkv,
+              dm.H, 0, s);
+  launch_pack(L->bf16, wts->w_o, nullptr, L->packed + pl.wo, dm.H,
+              dm.Hq * dm.d, 0, s);
+  launch_pack(L->bf16, wts->w_gate_up, wts->g_post, L->packed + pl.wgu,
+              2 * dm.I, dm.H, dm.I, s);
+  launch_pack(L->bf16, wts->w_down, nullptr, L->packed + pl.wd, dm.H, dm.I, 0, s);
+
+  // RoPE table: cos / sin of p * inv_freq_i in double, stored as fp32.
+  const int half = c.head_dim / 2;
+  size_t n = (size_t)c.max_position * half;
+  float* host = new (std::nothrow) float[2 * n];
+  double* f = new (std::nothrow) double[half];
+  if (!host || !f) {
+    delete[] host;
+    delete[] f;
+    delete L;
+    return LLAMA_ERR_INVALID_ARG;
+  }
+  rope_inv_freq(c, f);
+  for (int p = 0; p < c.max_position; ++p)
+    for (int i = 0; i < half; ++i) {
+      double a = (double)p * f[i];
+      host[(size_t)p * half + i] = (float)cos(a);
+      host[n + (size_t)p * half + i] = (float)sin(a);
+    }
+  cudaError_t e = cudaMemcpyAsync(L->packed + pl.cos_t, host, n * 4,
+                                  cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(L->packed + pl.sin_t, host + n, n * 4,
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(L->status, 0, 64, s);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  delete[] host;
+  delete[] f;
+  if (e != cudaSuccess) {
+    delete L;
+    return LLAMA_ERR_CUDA;
+  }
+  if (L->bf16) {
+    bool ok = tc_encode_bf16(&L->tm_wqkv, L->packed + pl.wqkv, dm.Nqkv, dm.H, 256) &&
+              tc_encode_bf16(&L->tm_wo, L->packed + pl.wo, dm.H, dm.Hq * dm.d, 256) &&
+              tc_encode_bf16(&L->tm_wgu, L->packed + pl.wgu, 2 * dm.I, dm.H, 256) &&
+              tc_encode_bf16(&L->tm_wd, L->packed + pl.wd, dm.H, dm.I, 256);
+    if (!ok) {
+      delete L;
+      return LLAMA_ERR_CUDA;
+    }
+  }
+  *out = L;
+  return LLAMA_OK;
+}
+
+int llama_layer_workspace_bytes(const llama_layer_t* L, int max_tokens,
+                                int decode_batch, int decode_max_seq,
+                                size_t* bytes) {
+  if (!L || !bytes || max_tokens < 0 || decode_batch < 0 || decode_max_seq < 0)
+    return LLAMA_ERR_INVALID_ARG;
+  size_t a = ws_layout(L->cfg, max_tokens).total;
+  size_t b = ws_layout(L->cfg, decode_batch).total;
+  *bytes = a > b ? a : b;
+  return LLAMA_OK;
+}
+
+int llama_layer_workspace_offsets(const llama_layer_t* L, int tokens, int decode,
+                                  size_t offsets[LLAMA_WS_NUM]) {
+  if (!L || !offsets || tokens < 0) return LLAMA_ERR_INVALID_ARG;
+  (void)decode;
+  WsLayout w = ws_layout(L->cfg, tokens);
+  offsets[0] = w.qkv;
+  offsets[1] = w.attn;
+  offsets[2] = w.h;
+  offsets[3] = w.act;
+  return LLAMA_OK;
+}
+
+int llama_layer_forward(llama_layer_t* L, const void* x, void* out,
+                        const int32_t* position_ids, const int32_t* cu_seqlens,
+                        int n_seq, int seq_len, int total_tokens,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  if (!L || !x || !out || total_tokens < 0) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || x == out) return LLAMA_ERR_INVALID_ARG;
+  if (position_ids && !aligned(position_ids, 4)) return LLAMA_ERR_INVALID_ARG;
+  if (cu_seqlens && !aligned(cu_seqlens, 4)) return LLAMA_ERR_INVALID_ARG;
+  if (total_tokens == 0) return LLAMA_OK;
+  if (n_seq <= 0 || seq_len <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!cu_seqlens && (long)n_seq * seq_len != total_tokens)
+    return LLAMA_ERR_INVALID_ARG;
+  if (cu_seqlens && (long)n_seq > total_tokens) return LLAMA_ERR_INVALID_ARG;
+  if (!position_ids && seq_len > L->cfg.max_position) return LLAMA_ERR_INVALID_ARG;
+  if ((size_t)seq_len * sizeof(float) > 200 * 1024) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
+  if (workspace_bytes < ws_layout(L->cfg, total_tokens).total)
+    return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+  return forward_impl(L, x, out, position_ids, cu_seqlens, n_seq, seq_len,
+                      total_tokens, static_cast<char*>(workspace),
+                      static_cast<cudaStream_t>(stream));
+}
+
+int llama_layer_decode(llama_layer_t* L, const void* x, void* out,
+                       void* cache_k, void* cache_v, const int32_t* start_pos,
+                       int batch, int max_seq, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (!L || !x || !out || batch < 0) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || x == out) return LLAMA_ERR_INVALID_ARG;
+  if (batch == 0) return LLAMA_OK;
+  if (!cache_k || !cache_v || !start_pos || max_seq <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned(cache_k, 16) || !aligned(cache_v, 16) || !aligned(start_pos, 4) ||
+      cache_k == cache_v)
+    return LLAMA_ERR_INVALID_ARG;
+  if ((size_t)max_seq * sizeof(float) > 200 * 1024) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
+  if (workspace_bytes < ws_layout(L->cfg, batch).total)
+    return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+  return decode_impl(L, x, out, cache_k, cache_v, start_pos, batch, max_seq,
+                     static_cast<char*>(workspace),
+                     static_cast<cudaStream_t>(stream));
+}
+
+int llama_layer_status(llama_layer_t* L, void* stream) {
+  if (!L) return LLAMA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (cudaMemcpy(&word, L->status, sizeof(int), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return LLAMA_ERR_CUDA;
+  if (cudaMemset(L->status, 0, sizeof(int)) != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (word & ST_TIMEOUT) return LLAMA_ERR_DEVICE_TIMEOUT;
+  if (word) return LLAMA_ERR_DEVICE_BAD_INPUT;
+  return LLAMA_OK;
+}
+
+void llama_layer_destroy(llama_layer_t* L) { delete L; }
+
+const char* llama_layer_strerror(int code) {
+  switch (code) {
+    case LLAMA_OK: return "ok";
+    case LLAMA_ERR_INVALID_ARG: return "invalid argument";
+    case LLAMA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case LLAMA_ERR_WORKSPACE_TOO_SMALL: return "buffer too small";
+    case LLAMA_ERR_CUDA: return "CUDA runtime error";
+    case LLAMA_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+    case LLAMA_ERR_DEVICE_BAD_INPUT: return "bad cu_seqlens / positions / start_pos";
+    case LLAMA_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103";
+  }
+  return "unknown error";
+}
+
+int llama_gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K,
+                    void* stream) {
+  if (!A || !B || !D || M < 0 || N < 0 || K <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16))
+    return LLAMA_ERR_INVALID_ARG;
+  if (K % 8 != 0 || N % 32 != 0) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || N == 0) return LLAMA_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LLAMA_ERR_CUDA;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  CUtensorMap ta, tb;
+  if (!tc_encode_bf16(&ta, A, M, K, 128) || !tc_encode_bf16(&tb, B, N, K, 256))
+    return LLAMA_ERR_CUDA;
+  TcEpiArgs ep;
+  ep.out = D;
+  ep.ldo = N;
+  return cuda_err(tc_gemm(TC_STORE, 256, ta, tb, M, N, K, 1, ep, sms,
+                          static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

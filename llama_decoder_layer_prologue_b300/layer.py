@@ -1,0 +1,142 @@
+"""Torch-side plumbing around the C ABI: allocates the caller-owned device
+buffers (packed weights, workspace) with torch and passes raw pointers and the
+current stream to ``binding``.  No arithmetic of the layer happens here.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+
+def make_config(shape) -> B.llama_layer_config:
+    """llama_layer_config from an object with the LayerShape fields."""
+    return B.llama_layer_config(
+        hidden=shape.hidden, n_heads=shape.n_heads,
+        n_kv_heads=shape.n_kv_heads, head_dim=shape.head_dim,
+        intermediate=shape.intermediate, rms_eps=shape.rms_eps,
+        rope_base=shape.rope_base, rope_scaling=shape.rope_scaling,
+        rope_factor=shape.rope_factor,
+        rope_low_freq_factor=shape.rope_low_freq_factor,
+        rope_high_freq_factor=shape.rope_high_freq_factor,
+        rope_original_max_pos=shape.rope_original_max_pos,
+        max_position=shape.max_position,
+        dtype=B.LLAMA_DTYPE_BF16 if shape.dtype == "bf16" else B.LLAMA_DTYPE_F32)
+
+
+def torch_dtype(shape) -> torch.dtype:
+    return torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+
+
+def to_device(arr: np.ndarray, device="cuda", pin: bool = False) -> torch.Tensor:
+    """A stored workload array (bf16 bits as uint16, float32, int32) as a
+    torch tensor of the matching dtype, on `device` (or pinned host memory)."""
+    if arr.dtype == np.uint16:
+        t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(
+            torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(arr))
+    if pin:
+        return t.pin_memory()
+    return t.to(device)
+
+
+def stream_ptr() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+class LlamaLayer:
+    """One decoder layer whose weights were packed by llama_layer_init."""
+
+    def __init__(self, shape, w_qkv, w_o, w_gate_up, w_down, g_in, g_post):
+        self.shape = shape
+        self.cfg = make_config(shape)
+        self.dtype = torch_dtype(shape)
+        dev = w_qkv.device
+        self.device = dev
+        nbytes = B.llama_layer_packed_bytes(self.cfg)
+        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        ws = [w_qkv, w_o, w_gate_up, w_down, g_in, g_post]
+        for t in ws:
+            assert t.is_contiguous() and t.dtype == self.dtype and t.is_cuda
+        wts = B.llama_layer_weights(*[t.data_ptr() for t in ws])
+        self.handle = B.llama_layer_init(self.cfg, wts, self.packed.data_ptr(),
+                                         nbytes, stream_ptr())
+        self.workspace = torch.empty(0, dtype=torch.uint8, device=dev)
+
+    @classmethod
+    def from_numpy(cls, shape, weights, device="cuda") -> "LlamaLayer":
+        d = {k: to_device(getattr(weights, k), device) for k in
+             ("w_qkv", "w_o", "w_gate_up", "w_down", "g_in", "g_post")}
+        return cls(shape, **d)
+
+    def ensure_workspace(self, tokens=0, decode_batch=0, max_seq=0) -> None:
+        n = B.llama_layer_workspace_bytes(self.handle, tokens, decode_batch,
+                                          max_seq)
+        if self.workspace.numel() < n:
+            self.workspace = torch.empty(n, dtype=torch.uint8,
+                                         device=self.device)
+
+    def forward(self, x, position_ids=None, cu_seqlens=None, n_seq=None,
+                seq_len=None, out=None):
+        """Padded batch when cu_seqlens is None (x: [n_seq * seq_len, H])."""
+        T = x.shape[0]
+        if cu_seqlens is None:
+            seq_len = seq_len or T
+            n_seq = n_seq or (T // seq_len)
+        else:
+            n_seq = cu_seqlens.numel() - 1
+            assert seq_len is not None, "varlen needs max_seqlen"
+        self.ensure_workspace(T)
+        if out is None:
+            out = torch.empty_like(x)
+        B.llama_layer_forward(
+            self.handle, x.data_ptr(), out.data_ptr(),
+            position_ids.data_ptr() if position_ids is not None else None,
+            cu_seqlens.data_ptr() if cu_seqlens is not None else None,
+            n_seq, seq_len, T, self.workspace.data_ptr(),
+            self.workspace.numel(), stream_ptr())
+        return out
+
+    def decode(self, x, cache_k, cache_v, start_pos, out=None):
+        Bt = x.shape[0]
+        max_seq = cache_k.shape[1]
+        self.ensure_workspace(0, Bt, max_seq)
+        if out is None:
+            out = torch.empty_like(x)
+        B.llama_layer_decode(self.handle, x.data_ptr(), out.data_ptr(),
+                             cache_k.data_ptr(), cache_v.data_ptr(),
+                             start_pos.data_ptr(), Bt, max_seq,
+                             self.workspace.data_ptr(), self.workspace.numel(),
+                             stream_ptr())
+        return out
+
+    def status(self) -> int:
+        return B.llama_layer_status(self.handle, stream_ptr())
+
+    def stages(self, tokens: int, decode: bool = False) -> dict:
+        """Views of the intermediates of the last call with `tokens` rows."""
+        off = B.llama_layer_workspace_offsets(self.handle, tokens, int(decode))
+        s = self.shape
+        widths = {"qkv": s.n_qkv, "attn": s.q_size, "h": s.hidden,
+                  "act": s.intermediate}
+        es = 2 if self.dtype == torch.bfloat16 else 4
+        views = {}
+        for (name, width), o in zip(widths.items(), off):
+            n = tokens * width * es
+            views[name] = self.workspace[o:o + n].view(self.dtype).view(
+                tokens, width)
+        return views
+
+    def close(self) -> None:
+        if self.handle:
+            B.llama_layer_destroy(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,110 @@
+"""Shared helpers of the GPU parity tests: run the library on a workload, run
+the oracle on the same bytes, and compare with the stated tolerances.
+
+Tolerances (fixed for this layer):
+  * fp32 workloads: max |gpu - oracle| <= 1e-4.
+  * bf16 workloads (fp32 accumulation): max |gpu - oracle| <= 2e-2 * RMS(oracle)
+    and mean relative error sum|gpu - oracle| / sum|oracle| <= 5e-3.
+"""
+
+from __future__ import annotations
+
+import types
+
+import numpy as np
+import torch
+
+import oracle
+from llama_decoder_layer_prologue_b300 import synth
+from llama_decoder_layer_prologue_b300.layer import LlamaLayer, to_device
+
+FP32_MAX_ABS = 1e-4
+BF16_MAX_ABS_REL_RMS = 2e-2
+BF16_MEAN_REL = 5e-3
+
+
+def weights_f64(w: synth.LayerWeights):
+    return types.SimpleNamespace(**{
+        k: synth.to_f64(getattr(w, k)) for k in
+        ("w_qkv", "w_o", "w_gate_up", "w_down", "g_in", "g_post")})
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def errors(got: np.ndarray, ref: np.ndarray) -> dict:
+    diff = np.abs(got - ref)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    return dict(max_abs=float(diff.max()) if diff.size else 0.0, rms_ref=rms,
+                mean_rel=float(diff.sum() / max(np.abs(ref).sum(), 1e-300)),
+                finite=bool(np.all(np.isfinite(got))))
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str):
+    e = errors(got, ref)
+    assert e["finite"], f"{what}: non-finite output"
+    if dtype == "fp32":
+        assert e["max_abs"] <= FP32_MAX_ABS, f"{what}: {e}"
+    else:
+        assert e["max_abs"] <= BF16_MAX_ABS_REL_RMS * e["rms_ref"], f"{what}: {e}"
+        assert e["mean_rel"] <= BF16_MEAN_REL, f"{what}: {e}"
+    return e
+
+
+def oracle_qkv(ref: dict, rows=None) -> np.ndarray:
+    q, k, v = ref["q"], ref["k"], ref["v"]
+    if rows is not None:
+        q, k, v = q[rows], k[rows], v[rows]
+    n = q.shape[0]
+    return np.concatenate([q.reshape(n, -1), k.reshape(n, -1),
+                           v.reshape(n, -1)], axis=1)
+
+
+def build_layer(inp: synth.LayerInputs) -> LlamaLayer:
+    return LlamaLayer.from_numpy(inp.workload.shape, inp.weights)
+
+
+def run_forward(layer: LlamaLayer, inp: synth.LayerInputs, varlen: bool,
+                with_positions: bool = False):
+    x = to_device(inp.x)
+    pos = to_device(inp.positions) if with_positions else None
+    w = inp.workload
+    if varlen:
+        cu = to_device(inp.cu_seqlens)
+        L = int(np.diff(inp.cu_seqlens).max())
+        out = layer.forward(x, position_ids=pos, cu_seqlens=cu, seq_len=L)
+    else:
+        S = int(inp.cu_seqlens[1] - inp.cu_seqlens[0])
+        out = layer.forward(x, position_ids=pos, n_seq=len(inp.cu_seqlens) - 1,
+                            seq_len=S)
+    torch.cuda.synchronize()
+    return out
+
+
+def sample_rows(cu: np.ndarray, per_seq: int, seed: int,
+                max_seqs: int | None = None) -> np.ndarray:
+    """First, last and random rows of (some of) the sequences."""
+    rng = np.random.default_rng(seed)
+    n = len(cu) - 1
+    seqs = np.arange(n)
+    if max_seqs is not None and n > max_seqs:
+        seqs = np.unique(np.concatenate(
+            [[0, n - 1], rng.choice(n, max_seqs - 2, replace=False)]))
+    rows = []
+    for s in seqs:
+        a, b = int(cu[s]), int(cu[s + 1])
+        rows += [a, b - 1]
+        if b - a > 2:
+            rows += list(rng.integers(a, b, size=per_seq))
+    return np.unique(np.asarray(rows, dtype=np.int64))
+
+
+def poison_cache(cache: np.ndarray, start_pos: np.ndarray) -> np.ndarray:
+    """Rows >= start_pos become NaN: the layer must write row start_pos and
+    never read beyond it."""
+    c = cache.copy()
+    nan = np.uint16(0x7FC0) if c.dtype == np.uint16 else np.float32(np.nan)
+    for b, sp in enumerate(start_pos):
+        c[b, sp:] = nan
+    return c

@@ -1,0 +1,214 @@
+"""GPU vs oracle parity through the C ABI on small shapes that still span
+several tiles and ragged tails, plus the edge cases and the device-side input
+checks.  Full-size workloads are in test_workloads_gpu.py."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from llama_decoder_layer_prologue_b300 import binding as B
+from llama_decoder_layer_prologue_b300 import synth
+from llama_decoder_layer_prologue_b300.layer import to_device
+
+from parity import (assert_close, build_layer, oracle_qkv, poison_cache,
+                    run_forward, to_f64, weights_f64)
+
+pytestmark = pytest.mark.gpu
+
+L3 = dict(rope_scaling=1, rope_factor=8.0, rope_low_freq_factor=1.0,
+          rope_high_freq_factor=4.0, rope_original_max_pos=8192)
+
+
+def shape(H, hq, hkv, d, I, dtype="bf16", max_position=4096, **kw):
+    args = dict(rms_eps=1e-5, rope_base=500000.0, rope_scaling=0)
+    args.update(kw)
+    return synth.LayerShape(hidden=H, n_heads=hq, n_kv_heads=hkv, head_dim=d,
+                            intermediate=I, max_position=max_position,
+                            dtype=dtype, **args)
+
+
+def check_forward(inp, varlen, with_positions=False, stages=True):
+    s = inp.workload.shape
+    layer = build_layer(inp)
+    out = run_forward(layer, inp, varlen, with_positions)
+    assert layer.status() == B.LLAMA_OK
+    ref = oracle.decoder_layer(synth.to_f64(inp.x), weights_f64(inp.weights),
+                               s, inp.positions, inp.cu_seqlens)
+    T = inp.tokens
+    if stages:
+        st = layer.stages(T)
+        assert_close(to_f64(st["qkv"]), oracle_qkv(ref), s.dtype, "qkv")
+        assert_close(to_f64(st["attn"]), ref["attn"], s.dtype, "attn")
+        assert_close(to_f64(st["h"]), ref["h"], s.dtype, "h")
+        assert_close(to_f64(st["act"]), ref["act"], s.dtype, "act")
+    assert_close(to_f64(out), ref["out"], s.dtype, "out")
+    layer.close()
+
+
+def test_tiny_fp32_workload():
+    check_forward(synth.make_inputs("tiny"), varlen=False)
+
+
+@pytest.mark.parametrize("case", [
+    # (name, shape, kind, kwargs)
+    ("padded_ragged_llama3", shape(256, 4, 2, 64, 384, **L3), "padded",
+     dict(batch=3, seq=100)),
+    ("padded_d128_one_kv", shape(512, 4, 1, 128, 256), "padded",
+     dict(batch=2, seq=129)),
+    ("mha", shape(256, 4, 4, 64, 256), "padded", dict(batch=2, seq=65)),
+    ("single_token", shape(256, 4, 2, 64, 256), "padded", dict(batch=1, seq=1)),
+    ("varlen_with_len1", shape(512, 8, 2, 64, 512, **L3), "varlen",
+     dict(total_tokens=700, min_len=1, max_len=300)),
+])
+def test_small_bf16_forward(case):
+    name, s, kind, kw = case
+    w = synth.custom_workload(name, s, kind, **kw)
+    check_forward(synth.make_inputs(w), varlen=(kind == "varlen"))
+
+
+def test_explicit_position_ids():
+    s = shape(256, 4, 2, 64, 256, **L3)
+    w = synth.custom_workload("pos", s, "padded", batch=2, seq=64)
+    inp = synth.make_inputs(w)
+    inp.positions = (inp.positions * 7 + 3).astype(np.int32)  # any positions
+    check_forward(inp, varlen=False, with_positions=True)
+
+
+def test_varlen_equals_padded_on_the_gpu():
+    s = shape(256, 4, 2, 64, 256)
+    w = synth.custom_workload("vp", s, "padded", batch=3, seq=96)
+    inp = synth.make_inputs(w)
+    layer = build_layer(inp)
+    padded = run_forward(layer, inp, varlen=False).clone()
+    varlen = run_forward(layer, inp, varlen=True)
+    # same tokens, same sequences: the two launch paths agree exactly
+    assert torch.equal(padded, varlen)
+    layer.close()
+
+
+def check_decode(s, batch, max_seq, start_pos):
+    w = synth.custom_workload("dec", s, "decode", batch=batch, max_seq=max_seq,
+                              min_start=0)
+    inp = synth.make_inputs(w)
+    inp.start_pos = np.asarray(start_pos, dtype=np.int32)
+    inp.cache_k = synth._make_cache(np.random.SeedSequence(5), w, inp.start_pos)
+    inp.cache_v = synth._make_cache(np.random.SeedSequence(6), w, inp.start_pos)
+    layer = build_layer(inp)
+    ck = to_device(poison_cache(inp.cache_k, inp.start_pos))
+    cv = to_device(poison_cache(inp.cache_v, inp.start_pos))
+    ck0, cv0 = ck.clone(), cv.clone()
+    x = to_device(inp.x)
+    sp = to_device(inp.start_pos)
+    out = layer.decode(x, ck, cv, sp)
+    torch.cuda.synchronize()
+    assert layer.status() == B.LLAMA_OK
+    rows = lambda b, n: (synth.to_f64(inp.cache_k[b, :n]),
+                         synth.to_f64(inp.cache_v[b, :n]))
+    ref = oracle.decoder_layer_decode(synth.to_f64(inp.x),
+                                      weights_f64(inp.weights), s, rows,
+                                      inp.start_pos)
+    assert_close(to_f64(out), ref["out"], s.dtype, "decode out")
+    st = layer.stages(batch, decode=True)
+    assert_close(to_f64(st["attn"]), ref["attn"], s.dtype, "decode attn")
+    for b, p in enumerate(inp.start_pos):
+        assert_close(to_f64(ck[b, p]), ref["k_new"][b], s.dtype, "k row")
+        assert_close(to_f64(cv[b, p]), ref["v_new"][b], s.dtype, "v row")
+        # nothing else in the cache changed (NaN rows stay NaN)
+        assert torch.equal(ck[b, :p], ck0[b, :p])
+        assert torch.equal(cv[b, :p], cv0[b, :p])
+        assert torch.isnan(ck[b, p + 1:].float()).all()
+        assert torch.isnan(cv[b, p + 1:].float()).all()
+    layer.close()
+
+
+def test_decode_small_bf16_edges():
+    s = shape(256, 4, 2, 64, 256, **L3)
+    check_decode(s, batch=5, max_seq=300, start_pos=[0, 299, 1, 150, 257])
+
+
+def test_decode_small_d128():
+    s = shape(512, 8, 2, 128, 384)
+    check_decode(s, batch=3, max_seq=520, start_pos=[513, 7, 64])
+
+
+def test_decode_tiny_fp32():
+    s = synth.WORKLOADS["tiny"].shape
+    s = synth.LayerShape(**{**s.__dict__, "max_position": 128})
+    check_decode(s, batch=2, max_seq=100, start_pos=[63, 0])
+
+
+def test_bad_cu_seqlens_are_flagged():
+    s = shape(256, 4, 2, 64, 256)
+    w = synth.custom_workload("bad", s, "varlen", total_tokens=300, min_len=50,
+                              max_len=150)
+    inp = synth.make_inputs(w)
+    layer = build_layer(inp)
+    cu = inp.cu_seqlens.copy()
+    cu[1], cu[2] = cu[2], cu[1]  # not monotone
+    out = layer.forward(to_device(inp.x), cu_seqlens=to_device(cu),
+                        seq_len=300)
+    torch.cuda.synchronize()
+    assert layer.status() == B.LLAMA_ERR_DEVICE_BAD_INPUT
+    assert layer.status() == B.LLAMA_OK  # the word was cleared
+    layer.close()
+
+
+def test_bad_start_pos_is_flagged():
+    s = shape(256, 4, 2, 64, 256)
+    w = synth.custom_workload("dec", s, "decode", batch=2, max_seq=64,
+                              min_start=0)
+    inp = synth.make_inputs(w, with_cache=False)
+    layer = build_layer(inp)
+    ck = torch.zeros(2, 64, 2, 64, dtype=torch.bfloat16, device="cuda")
+    cv = torch.zeros_like(ck)
+    sp = torch.tensor([64, -1], dtype=torch.int32, device="cuda")
+    layer.decode(to_device(inp.x), ck, cv, sp)
+    torch.cuda.synchronize()
+    assert layer.status() == B.LLAMA_ERR_DEVICE_BAD_INPUT
+    assert torch.count_nonzero(ck) == 0 and torch.count_nonzero(cv) == 0
+    layer.close()
+
+
+def test_positions_beyond_the_table_are_flagged():
+    s = shape(256, 4, 2, 64, 256, max_position=64)
+    w = synth.custom_workload("pos", s, "padded", batch=1, seq=32)
+    inp = synth.make_inputs(w)
+    layer = build_layer(inp)
+    pos = torch.full((32,), 64, dtype=torch.int32, device="cuda")
+    layer.forward(to_device(inp.x), position_ids=pos, seq_len=32)
+    torch.cuda.synchronize()
+    assert layer.status() == B.LLAMA_ERR_DEVICE_BAD_INPUT
+    layer.close()
+
+
+def test_host_checks_launch_nothing():
+    s = shape(256, 4, 2, 64, 256)
+    w = synth.custom_workload("chk", s, "padded", batch=1, seq=8)
+    inp = synth.make_inputs(w)
+    layer = build_layer(inp)
+    x = to_device(inp.x)
+    out = torch.zeros_like(x)
+    layer.ensure_workspace(8)
+    ws = layer.workspace
+    st = torch.cuda.current_stream().cuda_stream
+    with pytest.raises(B.LlamaError) as e:  # workspace too small
+        B.llama_layer_forward(layer.handle, x.data_ptr(), out.data_ptr(), None,
+                              None, 1, 8, 8, ws.data_ptr(), 100, st)
+    assert e.value.code == B.LLAMA_ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(B.LlamaError) as e:  # n_seq * seq_len != T
+        B.llama_layer_forward(layer.handle, x.data_ptr(), out.data_ptr(), None,
+                              None, 2, 8, 8, ws.data_ptr(), ws.numel(), st)
+    assert e.value.code == B.LLAMA_ERR_INVALID_ARG
+    with pytest.raises(B.LlamaError) as e:  # x aliases out
+        B.llama_layer_forward(layer.handle, x.data_ptr(), x.data_ptr(), None,
+                              None, 1, 8, 8, ws.data_ptr(), ws.numel(), st)
+    assert e.value.code == B.LLAMA_ERR_INVALID_ARG
+    with pytest.raises(B.LlamaError) as e:  # misaligned output
+        B.llama_layer_forward(layer.handle, x.data_ptr(), out.data_ptr() + 2,
+                              None, None, 1, 8, 8, ws.data_ptr(), ws.numel(),
+                              st)
+    assert e.value.code == B.LLAMA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0
+    layer.close()
