@@ -1,0 +1,48 @@
+// Decode-step kernels: stream-K partial finalizers and split-KV attention.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gemm_tc.cuh"
+
+namespace llama {
+
+enum DecStage : int { DEC_QKV = 0, DEC_O = 1, DEC_GU = 2, DEC_DOWN = 3 };
+
+struct DecodeArgs {
+  int batch, bn;  // tokens; column stride of the GEMM partials
+  int hidden, n_heads, n_kv_heads, head_dim, inter, nqkv;
+  int max_seq, max_pos;
+  float eps;
+  const float* part;  // stream-K partials of the current projection
+  const __nv_bfloat16* x;  // [B, H] layer input
+  const float* r1;         // [B] 1/RMS(x)
+  float* ss2;              // [B] sum of h^2 (zeroed before DEC_O)
+  const int32_t* start_pos;
+  const float *cos_t, *sin_t;
+  __nv_bfloat16* qkv;      // [B, nqkv]
+  __nv_bfloat16 *cache_k, *cache_v;  // [B, max_seq, Hkv, D]
+  __nv_bfloat16* attn;     // [B, Hq * D]
+  float* attn_part;        // split-KV records
+  int max_chunks, n_rep_rec;
+  float* h32;              // [B, H]
+  __nv_bfloat16* h16;      // [B, H]
+  __nv_bfloat16* act;      // [B, I]
+  __nv_bfloat16* out;      // [B, H]
+  int* status;
+};
+
+// Reduces the partials of projection `stage` and applies its epilogue.
+cudaError_t decode_finalize(int stage, const DecodeArgs& a,
+                            const TcStreamK& plan, cudaStream_t s);
+
+// Split-KV attention of every new token over cache rows 0..start_pos[b],
+// then the log-sum-exp combine into a.attn.
+cudaError_t decode_attention(const DecodeArgs& a, cudaStream_t s);
+
+size_t attn_decode_smem(int head_dim);
+int attn_decode_chunks(int max_seq);
+
+}  // namespace llama

@@ -39,11 +39,8 @@ struct Layout {
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles,
-                                            int& m, int& n, int& split) {
-  int per_split = m_tiles * n_tiles;
-  split = tile / per_split;
-  int t = tile - split * per_split;
+__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles,
+                                            int& m, int& n) {
   int group = GROUP_M * n_tiles;
   int g = t / group;
   int first_m = g * GROUP_M;
@@ -79,23 +76,11 @@ __device__ __forceinline__ void store_bf16x32(void* p, const float* v) {
   }
 }
 
-// Rounds v to bf16 in place and returns the sum of squares of the rounded
-// values.
-__device__ __forceinline__ float round_bf16_ss(float* v) {
-  float ss = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    v[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
-    ss = fmaf(v[j], v[j], ss);
-  }
-  return ss;
-}
-
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool valid,
-                                              int n0, int M, int N, int split,
+                                              int n0, int M, int N,
                                               const TcEpiArgs& ep) {
   if constexpr (EPI == TC_STORE || EPI == TC_RESID || EPI == TC_RESID_SS) {
     float ss = 0.f;
@@ -111,8 +96,23 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
           load_bf16x32(static_cast<const __nv_bfloat16*>(ep.residual) + off, r);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] += r[j];
+          if constexpr (EPI == TC_RESID) {
+            if (ep.residual2) {
+              load_bf16x32(static_cast<const __nv_bfloat16*>(ep.residual2) + off, r);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += r[j];
+            }
+          }
         }
-        if constexpr (EPI == TC_RESID_SS) ss += round_bf16_ss(v);
+        if constexpr (EPI == TC_RESID_SS) {
+          float lo[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            ss = fmaf(v[j], v[j], ss);
+            lo[j] = v[j] - __bfloat162float(__float2bfloat16_rn(v[j]));
+          }
+          store_bf16x32(static_cast<__nv_bfloat16*>(ep.out2) + off, lo);
+        }
         store_bf16x32(static_cast<__nv_bfloat16*>(ep.out) + off, v);
       }
     }
@@ -189,34 +189,70 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
                           col, g);
       }
     }
-  } else if constexpr (EPI == TC_PARTIAL) {
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      tmem_ld32(t_row + c * 32, v);
-      int col = n0 + c * 32;
-      if (valid && col < N) {
-        float* o = static_cast<float*>(ep.out) +
-                   ((size_t)split * M + row) * ep.ldo + col;
-        if (col + 32 <= N) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(o)[q] =
-                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
-          for (int j = 0; j < N - col; ++j) o[j] = v[j];
-        }
-      }
-    }
   }
 }
+
+// Work of one CTA as a sequence of segments (tile, K-blocks [kb0, kb1), slot).
+//   tile-stride mode: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...,
+//                     visited in bands of GROUP_M M-tiles.
+//   stream-K mode:    the CTA owns the global K-block range
+//                     [c W / G, (c + 1) W / G) of W = tiles * kb_total; each
+//                     run inside one tile is a segment whose fp32 partial goes
+//                     to slot (c - first CTA of that tile).
+struct Sched {
+  int m_tiles, n_tiles, kb_total, num_tiles, grid, cta;
+  bool stream_k;
+  long long W, g, g_end;
+  int next_tile;
+
+  __device__ Sched(int M, int N, int K, int bn, bool sk) {
+    m_tiles = (M + BM - 1) / BM;
+    n_tiles = (N + bn - 1) / bn;
+    kb_total = (K + BK - 1) / BK;
+    num_tiles = m_tiles * n_tiles;
+    grid = gridDim.x;
+    cta = blockIdx.x;
+    stream_k = sk;
+    W = (long long)num_tiles * kb_total;
+    g = (long long)cta * W / grid;
+    g_end = (long long)(cta + 1) * W / grid;
+    next_tile = cta;
+  }
+
+  __device__ bool next(int& mt, int& nt, int& kb0, int& kb1, int& tile,
+                       int& slot) {
+    if (!stream_k) {
+      if (next_tile >= num_tiles) return false;
+      tile = next_tile;
+      tile_coords(tile, m_tiles, n_tiles, mt, nt);
+      kb0 = 0;
+      kb1 = kb_total;
+      slot = 0;
+      next_tile += grid;
+      return true;
+    }
+    if (g >= g_end) return false;
+    tile = (int)(g / kb_total);
+    kb0 = (int)(g - (long long)tile * kb_total);
+    long long left = g_end - g;
+    kb1 = (int)(kb0 + left < kb_total ? kb0 + left : kb_total);
+    long long gs = (long long)tile * kb_total;
+    int first = (int)(((gs + 1) * grid - 1) / W);
+    slot = cta - first;
+    mt = tile / n_tiles;
+    nt = tile - mt * n_tiles;
+    g += kb1 - kb0;
+    return true;
+  }
+};
 
 template <int BN, int STAGES, int EPI>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
-                   int splits, TcEpiArgs ep) {
+                   TcEpiArgs ep) {
   using L = Layout<BN, STAGES>;
+  constexpr bool kStreamK = EPI == TC_PARTIAL;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -252,10 +288,8 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
-  const int num_tiles = m_tiles * n_tiles * splits;
-  const int kb_total = (K + BK - 1) / BK;
-  const int kb_per = (kb_total + splits - 1) / splits;
+  Sched sched(M, N, K, BN, kStreamK);
+  int mt, nt, kb0, kb1, tile, slot;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -263,10 +297,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       uint32_t issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        int mt, nt, sp;
-        tile_coords(tile, m_tiles, n_tiles, mt, nt, sp);
-        const int kb0 = sp * kb_per, kb1 = min(kb_total, kb0 + kb_per);
+      while (ok && sched.next(mt, nt, kb0, kb1, tile, slot)) {
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, ep.status, abort_flag)) {
             ok = false;
@@ -300,12 +331,9 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t local = 0;
       bool ok = true;
       bool issued_any = false;
-      for (int tile = blockIdx.x; tile < num_tiles && ok;
-           tile += gridDim.x, ++local) {
-        int mt, nt, sp;
-        tile_coords(tile, m_tiles, n_tiles, mt, nt, sp);
-        const int kb0 = sp * kb_per, kb1 = min(kb_total, kb0 + kb_per);
+      while (ok && sched.next(mt, nt, kb0, kb1, tile, slot)) {
         const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
+        ++local;
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, ep.status, abort_flag)) {
           ok = false;
           break;
@@ -343,17 +371,31 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     const int quad = warp & 3;
     uint32_t local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-      int mt, nt, sp;
-      tile_coords(tile, m_tiles, n_tiles, mt, nt, sp);
+    while (sched.next(mt, nt, kb0, kb1, tile, slot)) {
       const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
+      ++local;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_phase, ep.status, abort_flag);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       tc_fence_after();
-      const int row = mt * BM + quad * 32 + lane;
+      const int r = quad * 32 + lane;
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
-      epilogue_tile<BN, EPI>(t_row, row, row < M, nt * BN, M, N, sp, ep);
+      if constexpr (EPI == TC_PARTIAL) {
+        float* o = static_cast<float*>(ep.out) +
+                   (((size_t)tile * ep.part_slots + slot) * BM + r) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(t_row + c * 32, v);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(o + c * 32)[q] =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      } else {
+        const int row = mt * BM + r;
+        epilogue_tile<BN, EPI>(t_row, row, row < M, nt * BN, M, N, ep);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -370,8 +412,7 @@ __global__ void __launch_bounds__(192, 1)
 
 template <int BN, int STAGES, int EPI>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
-                   int K, int splits, const TcEpiArgs& ep, int grid_limit,
-                   cudaStream_t s) {
+                   int K, const TcEpiArgs& ep, int grid, cudaStream_t s) {
   using L = Layout<BN, STAGES>;
   auto kern = gemm_tc_kernel<BN, STAGES, EPI>;
   static bool attr_set = false;
@@ -381,15 +422,13 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  long tiles = (long)((M + BM - 1) / BM) * ((N + BN - 1) / BN) * splits;
-  if (tiles <= 0) return cudaSuccess;
-  int grid = (int)(tiles < grid_limit ? tiles : grid_limit);
+  if (grid <= 0) return cudaSuccess;
   TcEpiArgs e = ep;
   if (!e.status) {
     cudaError_t err = cudaGetSymbolAddress((void**)&e.status, g_tc_status);
     if (err != cudaSuccess) return err;
   }
-  kern<<<grid, 192, L::TOTAL, s>>>(ta, tb, M, N, K, splits, e);
+  kern<<<grid, 192, L::TOTAL, s>>>(ta, tb, M, N, K, e);
   return cudaGetLastError();
 }
 
@@ -431,19 +470,39 @@ bool tc_encode_bf16(CUtensorMap* map, const void* ptr, uint64_t rows,
   return r == CUDA_SUCCESS;
 }
 
+TcStreamK tc_streamk_plan(int M, int N, int K, int bn, int grid_limit) {
+  TcStreamK p;
+  p.tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  p.kb_total = (K + BK - 1) / BK;
+  long long W = (long long)p.tiles * p.kb_total;
+  p.grid = (int)(W < grid_limit ? W : grid_limit);
+  p.slots = 0;
+  for (int t = 0; t < p.tiles; ++t) {
+    int n = tc_streamk_segments(p, t);
+    if (n > p.slots) p.slots = n;
+  }
+  return p;
+}
+
 cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
-                    const CUtensorMap& tb, int M, int N, int K, int splits,
+                    const CUtensorMap& tb, int M, int N, int K,
                     const TcEpiArgs& ep, int grid_limit, cudaStream_t s) {
+  int tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  int grid = tiles < grid_limit ? tiles : grid_limit;
   switch (epi) {
-    case TC_STORE: return launch<256, 4, TC_STORE>(ta, tb, M, N, K, 1, ep, grid_limit, s);
-    case TC_QKV: return launch<256, 4, TC_QKV>(ta, tb, M, N, K, 1, ep, grid_limit, s);
-    case TC_RESID_SS: return launch<256, 4, TC_RESID_SS>(ta, tb, M, N, K, 1, ep, grid_limit, s);
-    case TC_SWIGLU: return launch<256, 4, TC_SWIGLU>(ta, tb, M, N, K, 1, ep, grid_limit, s);
-    case TC_RESID: return launch<256, 4, TC_RESID>(ta, tb, M, N, K, 1, ep, grid_limit, s);
-    case TC_PARTIAL:
-      if (bn == 64) return launch<64, 8, TC_PARTIAL>(ta, tb, M, N, K, splits, ep, grid_limit, s);
-      if (bn == 128) return launch<128, 6, TC_PARTIAL>(ta, tb, M, N, K, splits, ep, grid_limit, s);
-      return launch<256, 4, TC_PARTIAL>(ta, tb, M, N, K, splits, ep, grid_limit, s);
+    case TC_STORE: return launch<256, 4, TC_STORE>(ta, tb, M, N, K, ep, grid, s);
+    case TC_QKV: return launch<256, 4, TC_QKV>(ta, tb, M, N, K, ep, grid, s);
+    case TC_RESID_SS: return launch<256, 4, TC_RESID_SS>(ta, tb, M, N, K, ep, grid, s);
+    case TC_SWIGLU: return launch<256, 4, TC_SWIGLU>(ta, tb, M, N, K, ep, grid, s);
+    case TC_RESID: return launch<256, 4, TC_RESID>(ta, tb, M, N, K, ep, grid, s);
+    case TC_PARTIAL: {
+      TcStreamK p = tc_streamk_plan(M, N, K, bn, grid_limit);
+      if (p.slots != ep.part_slots) return cudaErrorInvalidValue;
+      if (bn == 64) return launch<64, 8, TC_PARTIAL>(ta, tb, M, N, K, ep, p.grid, s);
+      if (bn == 128) return launch<128, 6, TC_PARTIAL>(ta, tb, M, N, K, ep, p.grid, s);
+      if (bn == 256) return launch<256, 4, TC_PARTIAL>(ta, tb, M, N, K, ep, p.grid, s);
+      return cudaErrorInvalidValue;
+    }
   }
   return cudaErrorInvalidValue;
 }

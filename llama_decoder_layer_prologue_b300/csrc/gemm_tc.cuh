@@ -11,16 +11,19 @@ namespace llama {
 enum TcEpi : int {
   TC_STORE = 0,     // out = acc (bf16)
   TC_QKV = 1,       // out = r1[m] * acc, RoPE on q / k head columns
-  TC_RESID_SS = 2,  // out = res + acc; ss_out[m] += sum over row of out^2
+  TC_RESID_SS = 2,  // h = res + acc: out = bf16(h), out2 = bf16(h - out),
+                    // ss_out[m] += sum over the row of h^2
   TC_SWIGLU = 3,    // gate|up interleaved by 128: out = silu(r2 g) * (r2 u)
-  TC_RESID = 4,     // out = res + acc
-  TC_PARTIAL = 5,   // fp32 split-K partial: part[split][m][n] = acc
+  TC_RESID = 4,     // out = res (+ res2) + acc
+  TC_PARTIAL = 5,   // stream-K fp32 partials: part[tile][slot][128][bn]
 };
 
 struct TcEpiArgs {
   void* out = nullptr;  // bf16 [M, ldo] (TC_SWIGLU: [M, N/2]); fp32 partials
   int ldo = 0;
+  void* out2 = nullptr;            // TC_RESID_SS: rounding remainder of h
   const void* residual = nullptr;  // bf16 [M, ldo]
+  const void* residual2 = nullptr; // TC_RESID: optional second addend
   const float* rowscale = nullptr; // r1 [M]
   const float* ss_in = nullptr;    // sum of squares of h [M] (TC_SWIGLU)
   float* ss_out = nullptr;         // TC_RESID_SS
@@ -29,6 +32,7 @@ struct TcEpiArgs {
   const float* cos_t = nullptr;    // [max_pos, d/2]
   const float* sin_t = nullptr;
   int head_dim = 0, rope_cols = 0, max_pos = 0;  // rope on columns < rope_cols
+  int part_slots = 0;              // TC_PARTIAL: slots per tile (plan.slots)
   int* status = nullptr;
 };
 
@@ -37,10 +41,29 @@ struct TcEpiArgs {
 bool tc_encode_bf16(CUtensorMap* map, const void* ptr, uint64_t rows,
                     uint64_t cols, uint32_t box_rows);
 
-// Launches the persistent GEMM.  bn in {64, 128, 256}; splits >= 1 splits K
-// (TC_PARTIAL only).  Returns cudaSuccess or the launch error.
+// Stream-K plan of a TC_PARTIAL GEMM: `grid` CTAs share the
+// tiles * kb_total K-blocks evenly; tile t's partial sums land in
+// tc_streamk_segments(plan, t) consecutive slots of part[t][slot][128][bn]
+// (fp32; row r of the slot is output row 128 t + r, column c is output
+// column c), slots <= plan.slots.
+struct TcStreamK {
+  int grid, tiles, kb_total, slots;
+};
+TcStreamK tc_streamk_plan(int M, int N, int K, int bn, int grid_limit);
+
+__host__ __device__ inline int tc_streamk_segments(const TcStreamK& p, int t) {
+  long long W = (long long)p.tiles * p.kb_total;
+  long long g0 = (long long)t * p.kb_total, g1 = g0 + p.kb_total - 1;
+  long long c0 = ((g0 + 1) * p.grid - 1) / W, c1 = ((g1 + 1) * p.grid - 1) / W;
+  return (int)(c1 - c0 + 1);
+}
+
+// Launches the persistent GEMM.  TC_PARTIAL: bn in {64, 128, 256} (N <= bn
+// tokens), stream-K over min(grid_limit, K-blocks) CTAs, ep.part_slots must
+// equal tc_streamk_plan(...).slots.  Other epilogues: bn = 256, whole tiles
+// over min(grid_limit, tiles) CTAs.
 cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
-                    const CUtensorMap& tb, int M, int N, int K, int splits,
+                    const CUtensorMap& tb, int M, int N, int K,
                     const TcEpiArgs& ep, int grid_limit, cudaStream_t s);
 
 }  // namespace llama

@@ -15,9 +15,10 @@ struct Dims {
 
 // ----------------------------------------------------------------- simt.cu
 // Element type T is float or __nv_bfloat16 (tag: is_bf16).
-// r[row] = 1 / sqrt(mean(x[row]^2) + eps) for `rows` rows of width H.
+// r[row] = 1 / sqrt(mean(x[row]^2) + eps) for `rows` rows of width H; also
+// zeroes zero[row] when zero is not null.
 void simt_row_rms(bool is_bf16, const void* x, int rows, int H, float eps,
-                  float* r, cudaStream_t s);
+                  float* r, float* zero, cudaStream_t s);
 
 // Positions and sequence checks: pos[t] = t - start of t's sequence (when
 // fill_pos), validates cu_seqlens (device) when given, else padded seq_len.

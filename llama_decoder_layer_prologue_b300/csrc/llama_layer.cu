@@ -11,6 +11,7 @@
 
 #include "../../include/llama_layer.h"
 #include "common.cuh"
+#include "decode.cuh"
 #include "gemm_tc.cuh"
 #include "kernels.h"
 
@@ -56,7 +57,8 @@ int check_config(const llama_layer_config* c) {
       c->intermediate <= 0 || c->max_position <= 0)
     return LLAMA_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return LLAMA_ERR_UNSUPPORTED_SHAPE;
-  if (c->n_heads % c->n_kv_heads != 0) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (c->n_heads % c->n_kv_heads != 0 || c->n_heads / c->n_kv_heads > 16)
+    return LLAMA_ERR_UNSUPPORTED_SHAPE;
   if (c->hidden % 128 != 0 || c->intermediate % 128 != 0)
     return LLAMA_ERR_UNSUPPORTED_SHAPE;
   if (!(c->rms_eps > 0.f) || !(c->rope_base > 1.0)) return LLAMA_ERR_INVALID_ARG;
@@ -96,7 +98,7 @@ void rope_inv_freq(const llama_layer_config& c, double* f) {
 }
 
 struct WsLayout {
-  size_t pos, r1, ss2, qkv, attn, h, act, total;
+  size_t pos, r1, ss2, qkv, attn, h, h_lo, act, total;
 };
 
 WsLayout ws_layout(const llama_layer_config& c, int tokens) {
@@ -111,6 +113,7 @@ WsLayout ws_layout(const llama_layer_config& c, int tokens) {
   w.qkv = o; o = align_up(o + T * nqkv * es);
   w.attn = o; o = align_up(o + T * c.n_heads * c.head_dim * es);
   w.h = o; o = align_up(o + T * c.hidden * es);
+  w.h_lo = o; o = align_up(o + T * c.hidden * es);
   w.act = o; o = align_up(o + T * c.intermediate * es);
   w.total = o;
   return w;
@@ -126,17 +129,13 @@ struct llama_layer {
   PackedLayout pl;
   int* status;
   int sm_count;
-  CUtensorMap tm_wqkv, tm_wo, tm_wgu, tm_wd;  // bf16 weights, box 256 rows
+  CUtensorMap tm_wqkv, tm_wo, tm_wgu, tm_wd;  // bf16 weights as B, 256 rows
+  CUtensorMap ta_wqkv, ta_wo, ta_wgu, ta_wd;  // bf16 weights as A, 128 rows
 };
 
 namespace {
 
 int cuda_err(cudaError_t e) { return e == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA; }
-
-template <typename P>
-char* at(P* base, size_t off) {
-  return reinterpret_cast<char*>(const_cast<void*>(static_cast<const void*>(base))) + off;
-}
 
 int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in,
                  const int32_t* cu, int n_seq, int seq_len, int T, char* ws,
@@ -159,7 +158,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
 
   launch_positions(cu, n_seq, seq_len, T, reinterpret_cast<int32_t*>(ws + w.pos),
                    pos_in == nullptr, L->status, s);
-  simt_row_rms(b16, x, T, dm.H, dm.eps, r1, s);
+  simt_row_rms(b16, x, T, dm.H, dm.eps, r1, ss2, s);
   if (b16) {
     cudaError_t e;
     CUtensorMap ta;
@@ -170,31 +169,31 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.out = qkv; ep.ldo = dm.Nqkv; ep.rowscale = r1; ep.pos = pos;
     ep.cos_t = cos_t; ep.sin_t = sin_t; ep.head_dim = dm.d;
     ep.rope_cols = (dm.Hq + dm.Hkv) * dm.d; ep.max_pos = dm.max_pos;
-    e = tc_gemm(TC_QKV, 256, ta, L->tm_wqkv, T, dm.Nqkv, dm.H, 1, ep, L->sm_count, s);
+    e = tc_gemm(TC_QKV, 256, ta, L->tm_wqkv, T, dm.Nqkv, dm.H, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
     // a4 / a5: causal GQA attention.
     simt_attention_prefill(b16, qkv, attn, T, dm, cu, n_seq, seq_len, seq_len, s);
     // a7: o_proj + residual, row sums of h^2 for the second RMSNorm.
-    cudaMemsetAsync(ss2, 0, (size_t)T * 4, s);
     if (!tc_encode_bf16(&ta, attn, T, dm.Hq * dm.d, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
-    ep.out = h; ep.ldo = dm.H; ep.residual = x; ep.ss_out = ss2;
-    e = tc_gemm(TC_RESID_SS, 256, ta, L->tm_wo, T, dm.H, dm.Hq * dm.d, 1, ep, L->sm_count, s);
+    ep.out = h; ep.out2 = ws + w.h_lo; ep.ldo = dm.H; ep.residual = x;
+    ep.ss_out = ss2;
+    e = tc_gemm(TC_RESID_SS, 256, ta, L->tm_wo, T, dm.H, dm.Hq * dm.d, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
     // a8: gate_up with the RMSNorm row scale, silu(gate) * up.
     if (!tc_encode_bf16(&ta, h, T, dm.H, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
     ep.out = act; ep.ldo = dm.I; ep.ss_in = ss2; ep.inv_h = 1.0f / dm.H; ep.eps = dm.eps;
-    e = tc_gemm(TC_SWIGLU, 256, ta, L->tm_wgu, T, 2 * dm.I, dm.H, 1, ep, L->sm_count, s);
+    e = tc_gemm(TC_SWIGLU, 256, ta, L->tm_wgu, T, 2 * dm.I, dm.H, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
     // a9: down_proj + residual.
     if (!tc_encode_bf16(&ta, act, T, dm.I, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
-    ep.out = out; ep.ldo = dm.H; ep.residual = h;
-    e = tc_gemm(TC_RESID, 256, ta, L->tm_wd, T, dm.H, dm.I, 1, ep, L->sm_count, s);
+    ep.out = out; ep.ldo = dm.H; ep.residual = h; ep.residual2 = ws + w.h_lo;
+    e = tc_gemm(TC_RESID, 256, ta, L->tm_wd, T, dm.H, dm.I, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
   } else {
     simt_gemm(b16, EPI_ROWSCALE, x, P + L->pl.wqkv, qkv, T, dm.Nqkv, dm.H, r1,
@@ -203,12 +202,119 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     simt_attention_prefill(b16, qkv, attn, T, dm, cu, n_seq, seq_len, seq_len, s);
     simt_gemm(b16, EPI_RESIDUAL, attn, P + L->pl.wo, h, T, dm.H, dm.Hq * dm.d,
               nullptr, x, s);
-    simt_row_rms(b16, h, T, dm.H, dm.eps, ss2, s);
+    simt_row_rms(b16, h, T, dm.H, dm.eps, ss2, nullptr, s);
     simt_gemm(b16, EPI_SWIGLU, h, P + L->pl.wgu, act, T, dm.I, dm.H, ss2,
               nullptr, s);
     simt_gemm(b16, EPI_RESIDUAL, act, P + L->pl.wd, out, T, dm.H, dm.I,
               nullptr, h, s);
   }
+  return cuda_err(cudaGetLastError());
+}
+
+constexpr int kDecodeChunk = 256;  // tokens per decode pass (<= GEMM bn)
+
+int decode_bn(int B) { return B <= 64 ? 64 : (B <= 128 ? 128 : 256); }
+
+struct DecLayout {
+  size_t r1, ss2, qkv, attn, h16, h32, act, part, attn_part, total;
+  int bn, max_chunks, rec;
+  TcStreamK plan[4];  // QKV, O, GU, DOWN
+};
+
+// Decode workspace for B (<= kDecodeChunk) tokens and caches of max_seq rows.
+DecLayout dec_layout(const llama_layer* L, int B, int max_seq) {
+  const Dims& dm = L->dm;
+  const size_t T = (size_t)(B > 0 ? B : 0);
+  const size_t es = L->bf16 ? 2 : 4;
+  DecLayout w;
+  w.bn = decode_bn(B);
+  w.plan[DEC_QKV] = tc_streamk_plan(dm.Nqkv, B, dm.H, w.bn, L->sm_count);
+  w.plan[DEC_O] = tc_streamk_plan(dm.H, B, dm.Hq * dm.d, w.bn, L->sm_count);
+  w.plan[DEC_GU] = tc_streamk_plan(2 * dm.I, B, dm.H, w.bn, L->sm_count);
+  w.plan[DEC_DOWN] = tc_streamk_plan(dm.H, B, dm.I, w.bn, L->sm_count);
+  size_t part = 0;
+  for (const TcStreamK& p : w.plan) {
+    size_t n = (size_t)p.tiles * p.slots * 128 * w.bn * sizeof(float);
+    if (n > part) part = n;
+  }
+  w.max_chunks = attn_decode_chunks(max_seq > 0 ? max_seq : 1);
+  const int n_rep = dm.Hq / dm.Hkv;
+  w.rec = n_rep * (dm.d + 2);
+  size_t o = 0;
+  w.r1 = o; o = align_up(o + T * 4);
+  w.ss2 = o; o = align_up(o + T * 4);
+  w.qkv = o; o = align_up(o + T * dm.Nqkv * es);
+  w.attn = o; o = align_up(o + T * dm.Hq * dm.d * es);
+  w.h16 = o; o = align_up(o + T * dm.H * es);
+  w.h32 = o; o = align_up(o + T * dm.H * 4);
+  w.act = o; o = align_up(o + T * dm.I * es);
+  w.part = o; o = align_up(o + part);
+  w.attn_part = o;
+  o = align_up(o + T * dm.Hkv * (size_t)w.max_chunks * w.rec * sizeof(float));
+  w.total = o;
+  return w;
+}
+
+int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
+                 const int32_t* start_pos, int B, int max_seq, char* ws,
+                 cudaStream_t s) {
+  const Dims& dm = L->dm;
+  const DecLayout w = dec_layout(L, B, max_seq);
+  const char* P = L->packed;
+  DecodeArgs a;
+  a.batch = B; a.bn = w.bn;
+  a.hidden = dm.H; a.n_heads = dm.Hq; a.n_kv_heads = dm.Hkv;
+  a.head_dim = dm.d; a.inter = dm.I; a.nqkv = dm.Nqkv;
+  a.max_seq = max_seq; a.max_pos = dm.max_pos; a.eps = dm.eps;
+  a.part = reinterpret_cast<const float*>(ws + w.part);
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.r1 = reinterpret_cast<const float*>(ws + w.r1);
+  a.ss2 = reinterpret_cast<float*>(ws + w.ss2);
+  a.start_pos = start_pos;
+  a.cos_t = reinterpret_cast<const float*>(P + L->pl.cos_t);
+  a.sin_t = reinterpret_cast<const float*>(P + L->pl.sin_t);
+  a.qkv = reinterpret_cast<__nv_bfloat16*>(ws + w.qkv);
+  a.cache_k = static_cast<__nv_bfloat16*>(ck);
+  a.cache_v = static_cast<__nv_bfloat16*>(cv);
+  a.attn = reinterpret_cast<__nv_bfloat16*>(ws + w.attn);
+  a.attn_part = reinterpret_cast<float*>(ws + w.attn_part);
+  a.max_chunks = w.max_chunks; a.n_rep_rec = w.rec;
+  a.h32 = reinterpret_cast<float*>(ws + w.h32);
+  a.h16 = reinterpret_cast<__nv_bfloat16*>(ws + w.h16);
+  a.act = reinterpret_cast<__nv_bfloat16*>(ws + w.act);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.status = L->status;
+
+  // One projection: stream-K swap-AB GEMM into the partials, then its
+  // finalize kernel.
+  auto project = [&](int stage, const CUtensorMap& wmap, const void* act_in,
+                     int N_out, int K) -> int {
+    CUtensorMap tb;
+    if (!tc_encode_bf16(&tb, act_in, B, K, w.bn)) return LLAMA_ERR_CUDA;
+    TcEpiArgs ep;
+    ep.out = ws + w.part;
+    ep.part_slots = w.plan[stage].slots;
+    ep.status = L->status;
+    if (tc_gemm(TC_PARTIAL, w.bn, wmap, tb, N_out, B, K, ep, L->sm_count, s) !=
+        cudaSuccess)
+      return LLAMA_ERR_CUDA;
+    return decode_finalize(stage, a, w.plan[stage], s) == cudaSuccess
+               ? LLAMA_OK : LLAMA_ERR_CUDA;
+  };
+
+  // a1: 1/RMS of every new token (and zero the sums of h^2).
+  simt_row_rms(true, x, B, dm.H, dm.eps, const_cast<float*>(a.r1), a.ss2, s);
+  // a2 + a3 + cache append.
+  int rc = project(DEC_QKV, L->ta_wqkv, x, dm.Nqkv, dm.H);
+  if (rc) return rc;
+  // a6: split-KV attention over rows 0..start_pos[b].
+  if (decode_attention(a, s) != cudaSuccess) return LLAMA_ERR_CUDA;
+  // a7: o_proj + residual (+ sums of h^2).
+  if ((rc = project(DEC_O, L->ta_wo, a.attn, dm.H, dm.Hq * dm.d))) return rc;
+  // a8: gate_up + SiLU * up.
+  if ((rc = project(DEC_GU, L->ta_wgu, a.h16, 2 * dm.I, dm.H))) return rc;
+  // a9: down_proj + residual.
+  if ((rc = project(DEC_DOWN, L->ta_wd, a.act, dm.H, dm.I))) return rc;
   return cuda_err(cudaGetLastError());
 }
 
@@ -218,6 +324,20 @@ int decode_impl(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   const llama_layer_config& c = L->cfg;
   const Dims& dm = L->dm;
   const bool b16 = L->bf16;
+  if (b16) {
+    const size_t es = 2, row = (size_t)dm.H * es;
+    const size_t cache_seq = (size_t)max_seq * dm.Hkv * dm.d * es;
+    for (int b0 = 0; b0 < B; b0 += kDecodeChunk) {
+      const int nb = B - b0 < kDecodeChunk ? B - b0 : kDecodeChunk;
+      int rc = decode_chunk(L, static_cast<const char*>(x) + b0 * row,
+                            static_cast<char*>(out) + b0 * row,
+                            static_cast<char*>(ck) + b0 * cache_seq,
+                            static_cast<char*>(cv) + b0 * cache_seq,
+                            start_pos + b0, nb, max_seq, ws, s);
+      if (rc) return rc;
+    }
+    return LLAMA_OK;
+  }
   WsLayout w = ws_layout(c, B);
   float* r1 = reinterpret_cast<float*>(ws + w.r1);
   float* r2 = reinterpret_cast<float*>(ws + w.ss2);
@@ -229,7 +349,7 @@ int decode_impl(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   const float* cos_t = reinterpret_cast<const float*>(P + L->pl.cos_t);
   const float* sin_t = reinterpret_cast<const float*>(P + L->pl.sin_t);
 
-  simt_row_rms(b16, x, B, dm.H, dm.eps, r1, s);
+  simt_row_rms(b16, x, B, dm.H, dm.eps, r1, nullptr, s);
   simt_gemm(b16, EPI_ROWSCALE, x, P + L->pl.wqkv, qkv, B, dm.Nqkv, dm.H, r1,
             nullptr, s);
   simt_rope(b16, qkv, B, dm, start_pos, cos_t, sin_t, L->status, s);
@@ -237,12 +357,18 @@ int decode_impl(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   simt_attention_decode(b16, qkv, ck, cv, attn, start_pos, B, max_seq, dm, s);
   simt_gemm(b16, EPI_RESIDUAL, attn, P + L->pl.wo, h, B, dm.H, dm.Hq * dm.d,
             nullptr, x, s);
-  simt_row_rms(b16, h, B, dm.H, dm.eps, r2, s);
+  simt_row_rms(b16, h, B, dm.H, dm.eps, r2, nullptr, s);
   simt_gemm(b16, EPI_SWIGLU, h, P + L->pl.wgu, act, B, dm.I, dm.H, r2, nullptr,
             s);
   simt_gemm(b16, EPI_RESIDUAL, act, P + L->pl.wd, out, B, dm.H, dm.I, nullptr,
             h, s);
   return cuda_err(cudaGetLastError());
+}
+
+size_t decode_ws_bytes(const llama_layer* L, int batch, int max_seq) {
+  if (batch <= 0) return 0;
+  if (!L->bf16) return ws_layout(L->cfg, batch).total;
+  return dec_layout(L, batch < kDecodeChunk ? batch : kDecodeChunk, max_seq).total;
 }
 
 }  // namespace
@@ -338,7 +464,11 @@ int llama_layer_init(const llama_layer_config* cfg,
     bool ok = tc_encode_bf16(&L->tm_wqkv, L->packed + pl.wqkv, dm.Nqkv, dm.H, 256) &&
               tc_encode_bf16(&L->tm_wo, L->packed + pl.wo, dm.H, dm.Hq * dm.d, 256) &&
               tc_encode_bf16(&L->tm_wgu, L->packed + pl.wgu, 2 * dm.I, dm.H, 256) &&
-              tc_encode_bf16(&L->tm_wd, L->packed + pl.wd, dm.H, dm.I, 256);
+              tc_encode_bf16(&L->tm_wd, L->packed + pl.wd, dm.H, dm.I, 256) &&
+              tc_encode_bf16(&L->ta_wqkv, L->packed + pl.wqkv, dm.Nqkv, dm.H, 128) &&
+              tc_encode_bf16(&L->ta_wo, L->packed + pl.wo, dm.H, dm.Hq * dm.d, 128) &&
+              tc_encode_bf16(&L->ta_wgu, L->packed + pl.wgu, 2 * dm.I, dm.H, 128) &&
+              tc_encode_bf16(&L->ta_wd, L->packed + pl.wd, dm.H, dm.I, 128);
     if (!ok) {
       delete L;
       return LLAMA_ERR_CUDA;
@@ -353,16 +483,25 @@ int llama_layer_workspace_bytes(const llama_layer_t* L, int max_tokens,
                                 size_t* bytes) {
   if (!L || !bytes || max_tokens < 0 || decode_batch < 0 || decode_max_seq < 0)
     return LLAMA_ERR_INVALID_ARG;
-  size_t a = ws_layout(L->cfg, max_tokens).total;
-  size_t b = ws_layout(L->cfg, decode_batch).total;
+  size_t a = max_tokens > 0 ? ws_layout(L->cfg, max_tokens).total : 0;
+  size_t b = decode_ws_bytes(L, decode_batch, decode_max_seq);
   *bytes = a > b ? a : b;
+  if (*bytes == 0) *bytes = kAlign;
   return LLAMA_OK;
 }
 
 int llama_layer_workspace_offsets(const llama_layer_t* L, int tokens, int decode,
                                   size_t offsets[LLAMA_WS_NUM]) {
   if (!L || !offsets || tokens < 0) return LLAMA_ERR_INVALID_ARG;
-  (void)decode;
+  if (decode && L->bf16) {
+    if (tokens > kDecodeChunk) return LLAMA_ERR_INVALID_ARG;
+    DecLayout w = dec_layout(L, tokens, 1);
+    offsets[0] = w.qkv;
+    offsets[1] = w.attn;
+    offsets[2] = w.h16;
+    offsets[3] = w.act;
+    return LLAMA_OK;
+  }
   WsLayout w = ws_layout(L->cfg, tokens);
   offsets[0] = w.qkv;
   offsets[1] = w.attn;
@@ -405,9 +544,10 @@ int llama_layer_decode(llama_layer_t* L, const void* x, void* out,
   if (!aligned(cache_k, 16) || !aligned(cache_v, 16) || !aligned(start_pos, 4) ||
       cache_k == cache_v)
     return LLAMA_ERR_INVALID_ARG;
-  if ((size_t)max_seq * sizeof(float) > 200 * 1024) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (!L->bf16 && (size_t)max_seq * sizeof(float) > 200 * 1024)
+    return LLAMA_ERR_UNSUPPORTED_SHAPE;
   if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
-  if (workspace_bytes < ws_layout(L->cfg, batch).total)
+  if (workspace_bytes < decode_ws_bytes(L, batch, max_seq))
     return LLAMA_ERR_WORKSPACE_TOO_SMALL;
   return decode_impl(L, x, out, cache_k, cache_v, start_pos, batch, max_seq,
                      static_cast<char*>(workspace),
@@ -460,7 +600,7 @@ int llama_gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K,
   TcEpiArgs ep;
   ep.out = D;
   ep.ldo = N;
-  return cuda_err(tc_gemm(TC_STORE, 256, ta, tb, M, N, K, 1, ep, sms,
+  return cuda_err(tc_gemm(TC_STORE, 256, ta, tb, M, N, K, ep, sms,
                           static_cast<cudaStream_t>(stream)));
 }
 

@@ -16,7 +16,8 @@ using bf16 = __nv_bfloat16;
 // "llama3 结构详解" 3.1: RMS(a) = sqrt(mean(a^2) + eps); one warp per row.
 template <typename T>
 __global__ void row_rms_kernel(const T* __restrict__ x, int rows, int H,
-                               float eps, float* __restrict__ r) {
+                               float eps, float* __restrict__ r,
+                               float* __restrict__ zero) {
   int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -27,7 +28,10 @@ __global__ void row_rms_kernel(const T* __restrict__ x, int rows, int H,
     ss = fmaf(v, v, ss);
   }
   ss = warp_sum(ss);
-  if (lane == 0) r[row] = rsqrtf(ss / (float)H + eps);
+  if (lane == 0) {
+    r[row] = rsqrtf(ss / (float)H + eps);
+    if (zero) zero[row] = 0.f;
+  }
 }
 
 // ----------------------------------------------------------------- positions
@@ -285,10 +289,10 @@ void set_smem(const void* fn, size_t bytes) {
   } while (0)
 
 void simt_row_rms(bool is_bf16, const void* x, int rows, int H, float eps,
-                  float* r, cudaStream_t s) {
+                  float* r, float* zero, cudaStream_t s) {
   if (rows <= 0) return;
   DISPATCH(is_bf16, row_rms_kernel<T><<<(rows + 7) / 8, 256, 0, s>>>(
-                        (const T*)x, rows, H, eps, r));
+                        (const T*)x, rows, H, eps, r, zero));
 }
 
 void launch_positions(const int32_t* cu, int n_seq, int seq_len, int T,

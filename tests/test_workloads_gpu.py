@@ -12,7 +12,7 @@ from llama_decoder_layer_prologue_b300 import binding as B
 from llama_decoder_layer_prologue_b300 import synth
 from llama_decoder_layer_prologue_b300.layer import to_device
 
-from parity import (assert_close, build_layer, poison_cache, run_forward,
+from parity import (assert_close, assert_stage_close, build_layer, poison_cache, run_forward,
                     sample_rows, to_f64, weights_f64)
 
 pytestmark = pytest.mark.gpu
@@ -34,9 +34,9 @@ def test_prefill_workload_sampled_rows(name, per_seq, max_seqs):
                                     inp.positions, inp.cu_seqlens, rows)
     st = layer.stages(inp.tokens)
     idx = torch.as_tensor(rows, device="cuda")
-    assert_close(to_f64(st["attn"][idx]), ref["attn"], s.dtype, "attn")
-    assert_close(to_f64(st["h"][idx]), ref["h"], s.dtype, "h")
-    assert_close(to_f64(st["act"][idx]), ref["act"], s.dtype, "act")
+    assert_stage_close(to_f64(st["attn"][idx]), ref["attn"], s.dtype, "attn")
+    assert_stage_close(to_f64(st["h"][idx]), ref["h"], s.dtype, "h")
+    assert_stage_close(to_f64(st["act"][idx]), ref["act"], s.dtype, "act")
     assert_close(to_f64(out[idx]), ref["out"], s.dtype, "out")
     # every output row is finite (rows the oracle did not recompute included)
     assert torch.isfinite(out.float()).all()
@@ -59,9 +59,9 @@ def test_decode_workload():
                                       inp.start_pos)
     assert_close(to_f64(out), ref["out"], s.dtype, "out")
     st = layer.stages(inp.tokens, decode=True)
-    assert_close(to_f64(st["attn"]), ref["attn"], s.dtype, "attn")
+    assert_stage_close(to_f64(st["attn"]), ref["attn"], s.dtype, "attn")
     b_idx = torch.arange(len(inp.start_pos), device="cuda")
     sp = torch.as_tensor(inp.start_pos, device="cuda").long()
-    assert_close(to_f64(ck[b_idx, sp]), ref["k_new"], s.dtype, "k rows")
-    assert_close(to_f64(cv[b_idx, sp]), ref["v_new"], s.dtype, "v rows")
+    assert_stage_close(to_f64(ck[b_idx, sp]), ref["k_new"], s.dtype, "k rows")
+    assert_stage_close(to_f64(cv[b_idx, sp]), ref["v_new"], s.dtype, "v rows")
     layer.close()
