@@ -80,7 +80,8 @@ extern "C" {
 #define LLAMA_ROPE_LLAMA3 1
 
 /* Layer shape and RoPE settings.
- * Supported: head_dim in {64, 128}; n_heads % n_kv_heads == 0;
+ * Supported: head_dim in {64, 128}; n_heads % n_kv_heads == 0 and
+ * n_heads / n_kv_heads <= 16;
  * hidden % 128 == 0; intermediate % 128 == 0; rms_eps > 0; rope_base > 1;
  * max_position >= 1 (length of the RoPE table: every position used must be
  * < max_position).  Llama3 scaling (see "parallel_attention.py" section 1 and
@@ -129,9 +130,9 @@ LLAMA_API int llama_layer_packed_bytes(const llama_layer_config* cfg, size_t* by
  * untouched until llama_layer_destroy), builds the RoPE cos/sin table in
  * double precision on the host and uploads it as fp32, and returns a host
  * handle in *out.  Synchronises `stream` before returning.  Repacking folds
- * g_in into the columns of W_qkv and g_post into those of W_gate_up
- * (x_n W^T = r * x (g . W)^T with r the row's 1/RMS) and interleaves the
- * gate and up rows in blocks of 128. */
+ * g_in into the columns of W_qkv (x_n W^T = r * x (g . W)^T with r the row's
+ * 1/RMS), keeps a copy of g_post (the MLP input is h * g_post, scaled by r in
+ * the epilogue) and interleaves the gate and up rows in blocks of 128. */
 LLAMA_API int llama_layer_init(const llama_layer_config* cfg,
                      const llama_layer_weights* weights, void* packed,
                      size_t packed_bytes, void* stream, llama_layer_t** out);
@@ -183,11 +184,11 @@ LLAMA_API int llama_layer_status(llama_layer_t* layer, void* stream);
 
 /* Byte offsets inside the workspace of the intermediates of the last call
  * with these sizes, for checking individual stages:
- *   [0] q|k|v after RoPE   [tokens, n_heads*d + 2*n_kv_heads*d]
- *   [1] attention output    [tokens, n_heads*d]
- *   [2] h (after o_proj + residual) [tokens, hidden]
- *   [3] act = silu(gate)*up [tokens, intermediate]
- * all of the config's dtype.  decode == 1 gives the decode layout. */
+ *   [0] q|k|v after RoPE   [tokens, n_heads*d + 2*n_kv_heads*d]  dtype
+ *   [1] attention output    [tokens, n_heads*d]                   dtype
+ *   [2] h (after o_proj + residual) [tokens, hidden]              fp32
+ *   [3] act = silu(gate)*up [tokens, intermediate]                dtype
+ * decode == 1 gives the decode layout (tokens <= 256). */
 #define LLAMA_WS_NUM 4
 LLAMA_API int llama_layer_workspace_offsets(const llama_layer_t* layer, int tokens,
                                   int decode, size_t offsets[LLAMA_WS_NUM]);

@@ -1,0 +1,22 @@
+// Prefill causal GQA attention (padded batch or packed varlen).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace llama {
+
+struct AttnArgs {
+  const __nv_bfloat16* qkv;  // [tokens, nqkv]: q | k | v, q and k rotated
+  __nv_bfloat16* out;        // [tokens, n_heads * head_dim]
+  const int32_t* cu;         // [n_seq + 1] or null (padded: seq_len each)
+  int tokens, seq_len, nqkv, n_heads, n_kv_heads, head_dim;
+  int hpc;                   // query heads per CTA (set by attn_prefill)
+};
+
+// max_len: longest sequence (padded: seq_len).
+cudaError_t attn_prefill(const AttnArgs& a, int n_seq, int max_len,
+                         cudaStream_t s);
+
+}  // namespace llama

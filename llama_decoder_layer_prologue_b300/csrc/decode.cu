@@ -67,8 +67,8 @@ __global__ void __launch_bounds__(128) finalize_qkv_kernel(DecodeArgs a,
   }
 }
 
-// h = x + o_proj: fp32 copy (residual of the down projection), bf16 copy
-// (operand of gate_up) and the row sums of h^2.
+// h = x + o_proj: fp32 copy (residual of the down projection), bf16 copy of
+// h * g_post (operand of gate_up) and the row sums of h^2.
 __global__ void __launch_bounds__(128) finalize_o_kernel(DecodeArgs a,
                                                          TcStreamK plan) {
   const int t = blockIdx.x, r = threadIdx.x, n = t * 128 + r;
@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(128) finalize_o_kernel(DecodeArgs a,
   for (int b = 0; b < a.batch; ++b) {
     const float h = __bfloat162float(a.x[(size_t)b * H + n]) + P(r, b);
     a.h32[(size_t)b * H + n] = h;
-    a.h16[(size_t)b * H + n] = __float2bfloat16_rn(h);
+    a.hg[(size_t)b * H + n] =
+        __float2bfloat16_rn(h * __bfloat162float(a.g_post[n]));
     const float ss = warp_sum(h * h);
     if ((threadIdx.x & 31) == 0) atomicAdd(a.ss2 + b, ss);
   }

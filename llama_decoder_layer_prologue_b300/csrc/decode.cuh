@@ -27,8 +27,9 @@ struct DecodeArgs {
   __nv_bfloat16* attn;     // [B, Hq * D]
   float* attn_part;        // split-KV records
   int max_chunks, n_rep_rec;
-  float* h32;              // [B, H]
-  __nv_bfloat16* h16;      // [B, H]
+  float* h32;              // [B, H] h in fp32
+  __nv_bfloat16* hg;       // [B, H] bf16(h * g_post), operand of gate_up
+  const __nv_bfloat16* g_post;  // [H] RMSNorm weight of the MLP
   __nv_bfloat16* act;      // [B, I]
   __nv_bfloat16* out;      // [B, H]
   int* status;

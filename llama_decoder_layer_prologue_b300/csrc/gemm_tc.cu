@@ -76,6 +76,13 @@ __device__ __forceinline__ void store_bf16x32(void* p, const float* v) {
   }
 }
 
+__device__ __forceinline__ void store_f32x32(float* p, const float* v) {
+  float4* q = reinterpret_cast<float4*>(p);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
 template <int BN, int EPI>
@@ -91,29 +98,32 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
       int col = n0 + c * 32;
       if (valid && col < N) {
         size_t off = (size_t)row * ep.ldo + col;
-        if constexpr (EPI != TC_STORE) {
+        if constexpr (EPI == TC_RESID_SS) {
           float r[32];
           load_bf16x32(static_cast<const __nv_bfloat16*>(ep.residual) + off, r);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] += r[j];
-          if constexpr (EPI == TC_RESID) {
-            if (ep.residual2) {
-              load_bf16x32(static_cast<const __nv_bfloat16*>(ep.residual2) + off, r);
+          for (int j = 0; j < 32; ++j) {
+            v[j] += r[j];
+            ss = fmaf(v[j], v[j], ss);
+          }
+          store_f32x32(static_cast<float*>(ep.out) + off, v);
+          load_bf16x32(static_cast<const __nv_bfloat16*>(ep.colscale) + col, r);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] += r[j];
+          for (int j = 0; j < 32; ++j) r[j] *= v[j];
+          store_bf16x32(static_cast<__nv_bfloat16*>(ep.out2) + off, r);
+        } else {
+          if constexpr (EPI == TC_RESID) {
+            const float4* r4 =
+                reinterpret_cast<const float4*>(static_cast<const float*>(ep.residual) + off);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float4 rr = r4[q];
+              v[4 * q] += rr.x; v[4 * q + 1] += rr.y;
+              v[4 * q + 2] += rr.z; v[4 * q + 3] += rr.w;
             }
           }
+          store_bf16x32(static_cast<__nv_bfloat16*>(ep.out) + off, v);
         }
-        if constexpr (EPI == TC_RESID_SS) {
-          float lo[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            ss = fmaf(v[j], v[j], ss);
-            lo[j] = v[j] - __bfloat162float(__float2bfloat16_rn(v[j]));
-          }
-          store_bf16x32(static_cast<__nv_bfloat16*>(ep.out2) + off, lo);
-        }
-        store_bf16x32(static_cast<__nv_bfloat16*>(ep.out) + off, v);
       }
     }
     if constexpr (EPI == TC_RESID_SS) {

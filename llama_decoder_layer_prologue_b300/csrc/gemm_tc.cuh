@@ -11,19 +11,19 @@ namespace llama {
 enum TcEpi : int {
   TC_STORE = 0,     // out = acc (bf16)
   TC_QKV = 1,       // out = r1[m] * acc, RoPE on q / k head columns
-  TC_RESID_SS = 2,  // h = res + acc: out = bf16(h), out2 = bf16(h - out),
+  TC_RESID_SS = 2,  // h = res + acc: out = h (fp32), out2 = bf16(h * colscale),
                     // ss_out[m] += sum over the row of h^2
   TC_SWIGLU = 3,    // gate|up interleaved by 128: out = silu(r2 g) * (r2 u)
-  TC_RESID = 4,     // out = res (+ res2) + acc
+  TC_RESID = 4,     // out = res (fp32) + acc
   TC_PARTIAL = 5,   // stream-K fp32 partials: part[tile][slot][128][bn]
 };
 
 struct TcEpiArgs {
   void* out = nullptr;  // bf16 [M, ldo] (TC_SWIGLU: [M, N/2]); fp32 partials
   int ldo = 0;
-  void* out2 = nullptr;            // TC_RESID_SS: rounding remainder of h
-  const void* residual = nullptr;  // bf16 [M, ldo]
-  const void* residual2 = nullptr; // TC_RESID: optional second addend
+  void* out2 = nullptr;            // TC_RESID_SS: bf16(h * colscale)
+  const void* residual = nullptr;  // TC_RESID_SS: bf16; TC_RESID: fp32 [M, ldo]
+  const void* colscale = nullptr;  // TC_RESID_SS: bf16 [ldo] (RMSNorm weight)
   const float* rowscale = nullptr; // r1 [M]
   const float* ss_in = nullptr;    // sum of squares of h [M] (TC_SWIGLU)
   float* ss_out = nullptr;         // TC_RESID_SS

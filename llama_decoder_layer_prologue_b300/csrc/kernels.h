@@ -37,6 +37,10 @@ void simt_gemm(bool is_bf16, int epi, const void* A, const void* B, void* out,
                int M, int N, int K, const float* rowscale,
                const void* residual, cudaStream_t s);
 
+// out[r, c] = in[r, c] * g[c] for `rows` rows of width `cols` (fp32 path).
+void simt_scale_cols(const float* in, const float* g, float* out, int rows,
+                     int cols, cudaStream_t s);
+
 // In-place RoPE on the q and k heads of qkv rows [T, Nqkv].
 void simt_rope(bool is_bf16, void* qkv, int T, const Dims& dm,
                const int32_t* pos, const float* cos_t, const float* sin_t,

@@ -11,6 +11,7 @@
 
 #include "../../include/llama_layer.h"
 #include "common.cuh"
+#include "attn_prefill.cuh"
 #include "decode.cuh"
 #include "gemm_tc.cuh"
 #include "kernels.h"
@@ -28,7 +29,7 @@ bool aligned(const void* p, size_t a) {
 }
 
 struct PackedLayout {
-  size_t wqkv, wo, wgu, wd, cos_t, sin_t, status, total;
+  size_t wqkv, wo, wgu, wd, gpost, cos_t, sin_t, status, total;
 };
 
 PackedLayout packed_layout(const llama_layer_config& c) {
@@ -41,6 +42,7 @@ PackedLayout packed_layout(const llama_layer_config& c) {
   p.wo = o; o = align_up(o + (size_t)c.hidden * qs * es);
   p.wgu = o; o = align_up(o + 2 * (size_t)c.intermediate * c.hidden * es);
   p.wd = o; o = align_up(o + (size_t)c.hidden * c.intermediate * es);
+  p.gpost = o; o = align_up(o + (size_t)c.hidden * es);
   size_t table = (size_t)c.max_position * (c.head_dim / 2) * sizeof(float);
   p.cos_t = o; o = align_up(o + table);
   p.sin_t = o; o = align_up(o + table);
@@ -98,7 +100,7 @@ void rope_inv_freq(const llama_layer_config& c, double* f) {
 }
 
 struct WsLayout {
-  size_t pos, r1, ss2, qkv, attn, h, h_lo, act, total;
+  size_t pos, r1, ss2, qkv, attn, h, hg, act, total;
 };
 
 WsLayout ws_layout(const llama_layer_config& c, int tokens) {
@@ -112,8 +114,8 @@ WsLayout ws_layout(const llama_layer_config& c, int tokens) {
   w.ss2 = o; o = align_up(o + T * 4);
   w.qkv = o; o = align_up(o + T * nqkv * es);
   w.attn = o; o = align_up(o + T * c.n_heads * c.head_dim * es);
-  w.h = o; o = align_up(o + T * c.hidden * es);
-  w.h_lo = o; o = align_up(o + T * c.hidden * es);
+  w.h = o; o = align_up(o + T * c.hidden * 4);     // fp32
+  w.hg = o; o = align_up(o + T * c.hidden * es);   // h * g_post
   w.act = o; o = align_up(o + T * c.intermediate * es);
   w.total = o;
   return w;
@@ -171,18 +173,23 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.rope_cols = (dm.Hq + dm.Hkv) * dm.d; ep.max_pos = dm.max_pos;
     e = tc_gemm(TC_QKV, 256, ta, L->tm_wqkv, T, dm.Nqkv, dm.H, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
-    // a4 / a5: causal GQA attention.
-    simt_attention_prefill(b16, qkv, attn, T, dm, cu, n_seq, seq_len, seq_len, s);
+    // a4 / a5: causal GQA attention (padded or varlen).
+    AttnArgs aa;
+    aa.qkv = static_cast<const __nv_bfloat16*>(qkv);
+    aa.out = static_cast<__nv_bfloat16*>(attn);
+    aa.cu = cu; aa.tokens = T; aa.seq_len = seq_len; aa.nqkv = dm.Nqkv;
+    aa.n_heads = dm.Hq; aa.n_kv_heads = dm.Hkv; aa.head_dim = dm.d;
+    if (attn_prefill(aa, n_seq, seq_len, s) != cudaSuccess) return LLAMA_ERR_CUDA;
     // a7: o_proj + residual, row sums of h^2 for the second RMSNorm.
     if (!tc_encode_bf16(&ta, attn, T, dm.Hq * dm.d, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
-    ep.out = h; ep.out2 = ws + w.h_lo; ep.ldo = dm.H; ep.residual = x;
-    ep.ss_out = ss2;
+    ep.out = h; ep.out2 = ws + w.hg; ep.ldo = dm.H; ep.residual = x;
+    ep.colscale = P + L->pl.gpost; ep.ss_out = ss2;
     e = tc_gemm(TC_RESID_SS, 256, ta, L->tm_wo, T, dm.H, dm.Hq * dm.d, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
-    // a8: gate_up with the RMSNorm row scale, silu(gate) * up.
-    if (!tc_encode_bf16(&ta, h, T, dm.H, 128)) return LLAMA_ERR_CUDA;
+    // a8: gate_up on h * g_post with the RMSNorm row scale, silu(gate) * up.
+    if (!tc_encode_bf16(&ta, ws + w.hg, T, dm.H, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
     ep.out = act; ep.ldo = dm.I; ep.ss_in = ss2; ep.inv_h = 1.0f / dm.H; ep.eps = dm.eps;
@@ -192,7 +199,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     if (!tc_encode_bf16(&ta, act, T, dm.I, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
-    ep.out = out; ep.ldo = dm.H; ep.residual = h; ep.residual2 = ws + w.h_lo;
+    ep.out = out; ep.ldo = dm.H; ep.residual = h;
     e = tc_gemm(TC_RESID, 256, ta, L->tm_wd, T, dm.H, dm.I, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
   } else {
@@ -203,8 +210,11 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     simt_gemm(b16, EPI_RESIDUAL, attn, P + L->pl.wo, h, T, dm.H, dm.Hq * dm.d,
               nullptr, x, s);
     simt_row_rms(b16, h, T, dm.H, dm.eps, ss2, nullptr, s);
-    simt_gemm(b16, EPI_SWIGLU, h, P + L->pl.wgu, act, T, dm.I, dm.H, ss2,
-              nullptr, s);
+    simt_scale_cols(static_cast<const float*>(h),
+                    reinterpret_cast<const float*>(P + L->pl.gpost),
+                    reinterpret_cast<float*>(ws + w.hg), T, dm.H, s);
+    simt_gemm(b16, EPI_SWIGLU, ws + w.hg, P + L->pl.wgu, act, T, dm.I, dm.H,
+              ss2, nullptr, s);
     simt_gemm(b16, EPI_RESIDUAL, act, P + L->pl.wd, out, T, dm.H, dm.I,
               nullptr, h, s);
   }
@@ -216,7 +226,7 @@ constexpr int kDecodeChunk = 256;  // tokens per decode pass (<= GEMM bn)
 int decode_bn(int B) { return B <= 64 ? 64 : (B <= 128 ? 128 : 256); }
 
 struct DecLayout {
-  size_t r1, ss2, qkv, attn, h16, h32, act, part, attn_part, total;
+  size_t r1, ss2, qkv, attn, hg, h32, act, part, attn_part, total;
   int bn, max_chunks, rec;
   TcStreamK plan[4];  // QKV, O, GU, DOWN
 };
@@ -245,8 +255,8 @@ DecLayout dec_layout(const llama_layer* L, int B, int max_seq) {
   w.ss2 = o; o = align_up(o + T * 4);
   w.qkv = o; o = align_up(o + T * dm.Nqkv * es);
   w.attn = o; o = align_up(o + T * dm.Hq * dm.d * es);
-  w.h16 = o; o = align_up(o + T * dm.H * es);
   w.h32 = o; o = align_up(o + T * dm.H * 4);
+  w.hg = o; o = align_up(o + T * dm.H * es);
   w.act = o; o = align_up(o + T * dm.I * es);
   w.part = o; o = align_up(o + part);
   w.attn_part = o;
@@ -280,7 +290,8 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   a.attn_part = reinterpret_cast<float*>(ws + w.attn_part);
   a.max_chunks = w.max_chunks; a.n_rep_rec = w.rec;
   a.h32 = reinterpret_cast<float*>(ws + w.h32);
-  a.h16 = reinterpret_cast<__nv_bfloat16*>(ws + w.h16);
+  a.hg = reinterpret_cast<__nv_bfloat16*>(ws + w.hg);
+  a.g_post = reinterpret_cast<const __nv_bfloat16*>(P + L->pl.gpost);
   a.act = reinterpret_cast<__nv_bfloat16*>(ws + w.act);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.status = L->status;
@@ -312,7 +323,7 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   // a7: o_proj + residual (+ sums of h^2).
   if ((rc = project(DEC_O, L->ta_wo, a.attn, dm.H, dm.Hq * dm.d))) return rc;
   // a8: gate_up + SiLU * up.
-  if ((rc = project(DEC_GU, L->ta_wgu, a.h16, 2 * dm.I, dm.H))) return rc;
+  if ((rc = project(DEC_GU, L->ta_wgu, a.hg, 2 * dm.I, dm.H))) return rc;
   // a9: down_proj + residual.
   if ((rc = project(DEC_DOWN, L->ta_wd, a.act, dm.H, dm.I))) return rc;
   return cuda_err(cudaGetLastError());
@@ -358,8 +369,11 @@ int decode_impl(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   simt_gemm(b16, EPI_RESIDUAL, attn, P + L->pl.wo, h, B, dm.H, dm.Hq * dm.d,
             nullptr, x, s);
   simt_row_rms(b16, h, B, dm.H, dm.eps, r2, nullptr, s);
-  simt_gemm(b16, EPI_SWIGLU, h, P + L->pl.wgu, act, B, dm.I, dm.H, r2, nullptr,
-            s);
+  simt_scale_cols(static_cast<const float*>(h),
+                  reinterpret_cast<const float*>(P + L->pl.gpost),
+                  reinterpret_cast<float*>(ws + w.hg), B, dm.H, s);
+  simt_gemm(b16, EPI_SWIGLU, ws + w.hg, P + L->pl.wgu, act, B, dm.I, dm.H, r2,
+            nullptr, s);
   simt_gemm(b16, EPI_RESIDUAL, act, P + L->pl.wd, out, B, dm.H, dm.I, nullptr,
             h, s);
   return cuda_err(cudaGetLastError());
@@ -424,7 +438,9 @@ int llama_layer_init(const llama_layer_config* cfg,
               dm.H, 0, s);
   launch_pack(L->bf16, wts->w_o, nullptr, L->packed + pl.wo, dm.H,
               dm.Hq * dm.d, 0, s);
-  launch_pack(L->bf16, wts->w_gate_up, wts->g_post, L->packed + pl.wgu,
+  launch_pack(L->bf16, wts->g_post, nullptr, L->packed + pl.gpost, 1, dm.H, 0,
+              s);
+  launch_pack(L->bf16, wts->w_gate_up, nullptr, L->packed + pl.wgu,
               2 * dm.I, dm.H, dm.I, s);
   launch_pack(L->bf16, wts->w_down, nullptr, L->packed + pl.wd, dm.H, dm.I, 0, s);
 
@@ -498,7 +514,7 @@ int llama_layer_workspace_offsets(const llama_layer_t* L, int tokens, int decode
     DecLayout w = dec_layout(L, tokens, 1);
     offsets[0] = w.qkv;
     offsets[1] = w.attn;
-    offsets[2] = w.h16;
+    offsets[2] = w.h32;
     offsets[3] = w.act;
     return LLAMA_OK;
   }

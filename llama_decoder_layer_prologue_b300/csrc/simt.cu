@@ -132,6 +132,14 @@ __global__ void __launch_bounds__(256) gemm_kernel(
   }
 }
 
+__global__ void scale_cols_kernel(const float* __restrict__ in,
+                                  const float* __restrict__ g,
+                                  float* __restrict__ out, size_t n, int cols) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    out[i] = in[i] * g[i % cols];
+}
+
 // ----------------------------------------------------------------- RoPE
 // "RoPE高效实现": y = x cos + rotate_half(x) sin on the (i, i + d/2) pairs.
 template <typename T>
@@ -322,6 +330,13 @@ void simt_gemm(bool is_bf16, int epi, const void* A, const void* B, void* out,
           (const T*)A, (const T*)B, (T*)out, M, N, K, rowscale,
           (const T*)residual);
   });
+}
+
+void simt_scale_cols(const float* in, const float* g, float* out, int rows,
+                     int cols, cudaStream_t s) {
+  if (rows <= 0) return;
+  scale_cols_kernel<<<148 * 4, 256, 0, s>>>(in, g, out, (size_t)rows * cols,
+                                            cols);
 }
 
 void simt_rope(bool is_bf16, void* qkv, int ntok, const Dims& dm,

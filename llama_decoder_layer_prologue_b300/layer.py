@@ -122,12 +122,11 @@ class LlamaLayer:
         s = self.shape
         widths = {"qkv": s.n_qkv, "attn": s.q_size, "h": s.hidden,
                   "act": s.intermediate}
-        es = 2 if self.dtype == torch.bfloat16 else 4
         views = {}
         for (name, width), o in zip(widths.items(), off):
-            n = tokens * width * es
-            views[name] = self.workspace[o:o + n].view(self.dtype).view(
-                tokens, width)
+            dt = torch.float32 if name == "h" else self.dtype
+            n = tokens * width * (4 if dt == torch.float32 else 2)
+            views[name] = self.workspace[o:o + n].view(dt).view(tokens, width)
         return views
 
     def close(self) -> None:
