@@ -1,0 +1,678 @@
+"""Throughput of one Llama-style decoder layer on B300: tokens/s plus the
+fraction of the roofline reached by the dominant kernel.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one call of the layer (``llama_layer_forward`` for the prefill
+workloads, ``llama_layer_decode`` for the decode workload) over one batch of
+seeded synthetic input that already sits in HBM.  Between timed steps L2 is
+flushed by writing a 256 MiB buffer (outside the step's events).  Each step is
+timed with CUDA events on the launching stream; the library's own stage
+events (``llama_layer_set_timing``) time every kernel stage of the same steps.
+
+N > 1 (under torchrun): every rank runs an independent replica of the layer
+on its own GPU with its own copy of the workload (the path has no exchange
+step); timing is bracketed by a barrier and a synchronize, and the value is
+the tokens of all ranks over the slowest rank's time (weak scaling).
+
+``--impl reference`` times the fp64 CPU oracle instead (rank 0 only), on a
+bounded prefix of the same workload per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decoder-layer tokens/sec on 1 B300 (bf16) + % of TC-peak / HBM roofline"
+UNIT = "tokens/s"
+FLUSH_BYTES = 256 << 20  # > 126 MB of L2
+
+DESCRIPTIONS = {
+    "tiny": "tiny fp32 layer prefill: batch 1 x seq 64, hidden 256, 4 q / 2 kv "
+            "heads, head_dim 64, intermediate 512, RoPE base 1e4",
+    "1b": "Llama-3.2-1B-shaped layer prefill bf16: batch 4 x seq 2048, hidden "
+          "2048, 32 q / 8 kv heads, head_dim 64, intermediate 8192, Llama3 RoPE "
+          "(base 5e5, factor 32), causal",
+    "8b": "Llama-3-8B-shaped layer prefill bf16: batch 2 x seq 4096, hidden "
+          "4096, 32 q / 8 kv heads, head_dim 128, intermediate 14336, Llama3 "
+          "RoPE (base 5e5, factor 8), causal",
+    "varlen": "packed varlen 8B-shaped layer prefill bf16: 16384 tokens, "
+              "sequence lengths U{128..1024} (seeded), cu_seqlens int32, "
+              "causal within each sequence",
+    "decode": "KV-cache decode 8B-shaped layer bf16: batch 64 x 1 new token, "
+              "start_pos U{512..8191} (seeded), cache [64, 8192, 8, 128] bf16",
+}
+
+# Kernel sources behind each stage: a recorded DRAM traffic figure is only
+# reported while these files are unchanged.
+STAGE_SOURCES = {
+    "gate_up_swiglu": ["gemm_tc.cu", "gemm_tc.cuh", "common.cuh"],
+    "qkv_rope": ["gemm_tc.cu", "gemm_tc.cuh", "common.cuh"],
+    "o_proj_residual": ["gemm_tc.cu", "gemm_tc.cuh", "common.cuh"],
+    "down_residual": ["gemm_tc.cu", "gemm_tc.cuh", "common.cuh"],
+    "attention": ["attn_prefill.cu", "decode.cu", "common.cuh"],
+}
+
+
+# ----------------------------------------------------------------- helpers
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about 2 s of work)")
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="1b", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0,
+                    help="CPU work of the oracle baseline (0: leave it out)")
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps of the host-buffer measurement (0: leave it out)")
+    ap.add_argument("--stages", action="store_true",
+                    help="print the per-stage table to stderr")
+    return ap.parse_args()
+
+
+DEFAULT_STEPS = {"tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
+                 "decode": 3000}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def src_sha(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "llama_decoder_layer_prologue_b300", "csrc",
+                               f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, stage: str):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel
+    sources are unchanged since (profiles/dram_traffic.md)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    want = src_sha(STAGE_SOURCES.get(stage, []))
+    with open(path) as fh:
+        for line in fh:
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) >= 4 and cells[0] == workload and cells[1] == stage:
+                try:
+                    value = float(cells[2])
+                except ValueError:
+                    continue
+                return value if cells[3] == want else None
+    return None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained",
+                                                      p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0,
+                source="fallback")
+
+
+# ----------------------------------------------------------------- work
+def algorithmic_work(inp) -> dict:
+    """Per-stage algorithmic FLOPs (prefill) or bytes (decode) of one step."""
+    import numpy as np
+
+    w = inp.workload
+    s = w.shape
+    H, I, d, Hq, Hkv = s.hidden, s.intermediate, s.head_dim, s.n_heads, s.n_kv_heads
+    q, nqkv = s.q_size, s.n_qkv
+    es = 2 if s.dtype == "bf16" else 4
+    T = inp.tokens
+    weights = es * (nqkv * H + H * q + 2 * I * H + I * H)
+    if w.kind != "decode":
+        lens = np.diff(inp.cu_seqlens).astype(np.float64)
+        attn = float(np.sum(2.0 * d * Hq * lens * (lens + 1)))
+        flops = {"qkv_rope": 2.0 * T * H * nqkv, "attention": attn,
+                 "o_proj_residual": 2.0 * T * q * H,
+                 "gate_up_swiglu": 2.0 * T * H * 2 * I,
+                 "down_residual": 2.0 * T * I * H}
+        # the row statistics pass reads x once
+        return dict(kind="prefill", flops=flops, total_flops=sum(flops.values()),
+                    bytes={"rmsnorm_stats": float(T * H * es)}, weight_bytes=weights)
+    sp = inp.start_pos.astype(np.float64)
+    kv_read = float(np.sum(2.0 * sp * Hkv * d * es))
+    append = 2.0 * T * Hkv * d * es
+    act = T * es * (2 * H + nqkv + q + H + 2 * I + I + H)  # x, qkv, o, h, act, out
+    total = kv_read + append + weights + act
+    # per stage: the bytes a stage has to move at the least (weights once,
+    # activations in and out; the stream-K partials are not counted)
+    stage = {
+        "rmsnorm_stats": T * H * es,
+        "qkv_gemm": es * nqkv * H + T * H * es,
+        "qkv_rope_cache_append": T * nqkv * es + append,
+        "attention": kv_read + T * nqkv * es + T * q * es,
+        "o_proj_gemm": es * H * q + T * q * es,
+        "o_residual": T * H * es + T * H * (4 + es),
+        "gate_up_gemm": es * 2 * I * H + T * H * es,
+        "swiglu": T * I * es,
+        "down_gemm": es * I * H + T * I * es,
+        "down_residual": T * H * (4 + es),
+    }
+    return dict(kind="decode", bytes={k: float(v) for k, v in stage.items()},
+                total_bytes=total, kv_read=kv_read, weight_bytes=weights, flops={})
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples the SM clock, power and clock-event reasons of one GPU while
+    running (read only): NVML every 20 ms when pynvml imports, else an
+    ``nvidia-smi -lms 100`` child process."""
+
+    BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+            0x2: "applications_clocks_setting"}
+    QUERY = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active"
+
+    def __init__(self, device_index: int, pci_bus_id: str | None = None):
+        self.samples = []  # (sm MHz, power W, reason bits)
+        self.error = None
+        self.max_mhz = None
+        self.source = None
+        self.nv = None
+        self.proc = None
+        self._stop = threading.Event()
+        self._t = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = (pynvml.nvmlDeviceGetHandleByPciBusId(pci_bus_id) if pci_bus_id
+                      else pynvml.nvmlDeviceGetHandleByIndex(device_index))
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.source = "nvml, 20 ms"
+        except Exception as e:  # noqa: BLE001
+            self.nv = None
+            self.error = f"nvml: {e}"
+            self.target = pci_bus_id or str(device_index)
+
+    def _reasons(self):
+        nv = self.nv
+        for fn in ("nvmlDeviceGetCurrentClocksEventReasons",
+                   "nvmlDeviceGetCurrentClocksThrottleReasons"):
+            if hasattr(nv, fn):
+                return int(getattr(nv, fn)(self.h))
+        return 0
+
+    def _nvml_sample(self):
+        nv = self.nv
+        try:
+            self.samples.append((nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM),
+                                 nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0,
+                                 self._reasons()))
+        except Exception as e:  # noqa: BLE001
+            self.error = str(e)
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._nvml_sample()
+            time.sleep(0.02)
+
+    def __enter__(self):
+        if self.nv is not None:
+            self._nvml_sample()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+            return self
+        import subprocess
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.target, f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi, 100 ms"
+            time.sleep(0.3)  # let the first sample land before the timed work
+        except Exception as e:  # noqa: BLE001
+            self.error = f"{self.error}; nvidia-smi: {e}"
+        return self
+
+    def __exit__(self, *a):
+        if self._t is not None:
+            self._stop.set()
+            self._t.join()
+            self._nvml_sample()
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            for line in out.splitlines():
+                f = [c.strip() for c in line.split(",")]
+                try:
+                    self.max_mhz = float(f[1])
+                    self.samples.append((float(f[0]), float(f[2]), int(f[3], 16)))
+                except (ValueError, IndexError):
+                    continue
+
+    def summary(self) -> dict:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "samples": 0, "note": self.error or "no samples"}
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for s in self.samples:
+            bits |= s[2]
+        reasons = [n for b, n in sorted(self.BITS.items()) if bits & b]
+        return {"sm_mhz": float(statistics.median(mhz)), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(mhz), "power_w_max": max(s[1] for s in self.samples),
+                "reasons": reasons, "samples": len(self.samples), "source": self.source}
+
+
+# ----------------------------------------------------------------- oracle
+def _f64_weights(inp):
+    import types
+
+    from llama_decoder_layer_prologue_b300 import synth
+    return types.SimpleNamespace(**{k: synth.to_f64(getattr(inp.weights, k)) for k in
+                                    ("w_qkv", "w_o", "w_gate_up", "w_down", "g_in",
+                                     "g_post")})
+
+
+class OracleRunner:
+    """Runs the fp64 oracle on a sample of the workload: a prefix of the
+    token stream cut at whole sequences when it spans more than one, or the
+    first b sequences of a decode batch.  Prefixes of a causal sequence are
+    exact sub-problems (their outputs do not depend on later tokens)."""
+
+    def __init__(self, inp):
+        import numpy as np
+
+        import oracle
+        from llama_decoder_layer_prologue_b300 import synth
+
+        self.np, self.oracle, self.synth = np, oracle, synth
+        self.inp = inp
+        self.w = _f64_weights(inp)
+
+    def units(self, n: int):
+        """A sample of n tokens: (callable, tokens, description)."""
+        np, inp, synth = self.np, self.inp, self.synth
+        s = inp.workload.shape
+        if inp.workload.kind == "decode":
+            b = max(1, min(n, inp.tokens))
+            x = synth.to_f64(inp.x[:b])
+            sp = inp.start_pos[:b]
+
+            def rows(i, k):
+                return (synth.to_f64(inp.cache_k[i, :k]), synth.to_f64(inp.cache_v[i, :k]))
+
+            def run():
+                self.oracle.decoder_layer_decode(x, self.w, s, rows, sp)
+            return run, b, f"first {b} of {inp.tokens} decode sequences"
+        cu = inp.cu_seqlens.astype(np.int64)
+        n = max(1, min(n, inp.tokens))
+        whole = int(np.searchsorted(cu, n, side="right") - 1)
+        if whole >= 1:
+            n = int(cu[whole])
+            cut = cu[: whole + 1]
+            what = f"first {whole} of {len(cu) - 1} sequences ({n} tokens)"
+        else:
+            cut = np.array([0, n], dtype=np.int64)
+            what = f"prefix of {n} tokens of sequence 0 (length {int(cu[1])})"
+        x = synth.to_f64(inp.x[:n])
+        pos = inp.positions[:n]
+
+        def run():
+            self.oracle.decoder_layer(x, self.w, s, pos, cut)
+        return run, n, what
+
+    def calibrate(self, budget_s: float) -> int:
+        """Sample size (tokens) taking about budget_s seconds."""
+        small = 16 if self.inp.workload.kind == "decode" else 128
+        run, n, _ = self.units(small)
+        t = time.perf_counter()
+        run()
+        dt = max(time.perf_counter() - t, 1e-6)
+        return max(1, int(n * budget_s / dt))
+
+
+def oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        info = [p.get("num_threads", 1) for p in threadpool_info()
+                if p.get("user_api") == "blas"]
+        if info:
+            return int(max(info))
+    except Exception:  # noqa: BLE001
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(inp, budget_s: float) -> dict:
+    r = OracleRunner(inp)
+    n = r.calibrate(min(budget_s, 2.0) / 4)
+    n = max(1, int(n * budget_s / (min(budget_s, 2.0) / 4)))
+    run, tokens, what = r.units(n)
+    t = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t
+    return {"value": tokens / dt, "unit": UNIT, "cores": oracle_threads(),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"{what} of the workload, fp64 numpy oracle, one pass"}
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args, rank, local_rank, world):
+    import numpy as np
+    import torch
+
+    from llama_decoder_layer_prologue_b300 import synth
+    from llama_decoder_layer_prologue_b300.layer import LlamaLayer, to_device
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    inp = synth.make_inputs(args.workload)
+    w = inp.workload
+    s = w.shape
+    layer = LlamaLayer.from_numpy(s, inp.weights)
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
+    W = args.warmup
+    x = to_device(inp.x)
+    out = torch.empty_like(x)
+    decode = w.kind == "decode"
+    if decode:
+        ck, cv = to_device(inp.cache_k), to_device(inp.cache_v)
+        sp = to_device(inp.start_pos)
+
+        def step(o=out):
+            layer.decode(x, ck, cv, sp, out=o)
+    else:
+        varlen = w.kind == "varlen"
+        cu = to_device(inp.cu_seqlens) if varlen else None
+        seq = int(np.diff(inp.cu_seqlens).max())
+        n_seq = len(inp.cu_seqlens) - 1
+
+        def step(o=out):
+            if varlen:
+                layer.forward(x, cu_seqlens=cu, seq_len=seq, out=o)
+            else:
+                layer.forward(x, n_seq=n_seq, seq_len=seq, out=o)
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(W):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    rc = layer.status()
+    if rc != 0:
+        raise RuntimeError(f"layer status after warm-up: {rc}")
+    launches_per_step = layer.launch_count()
+
+    layer.set_timing(min(K, 4096))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sampler = None
+    if rank == 0:
+        p = torch.cuda.get_device_properties(torch.cuda.current_device())
+        bus = None
+        if hasattr(p, "pci_bus_id"):
+            bus = "%08X:%02X:%02X.0" % (getattr(p, "pci_domain_id", 0), p.pci_bus_id,
+                                        getattr(p, "pci_device_id", 0))
+        sampler = ClockSampler(torch.cuda.current_device(), bus)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    if sampler:
+        sampler.__enter__()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.__exit__()
+    region_s = time.perf_counter() - t0
+    if dist is not None:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = float(sum(step_ms))
+    # stage times of the recorded steps (the last min(K, 4096))
+    stages = {}
+    for c in range(min(K, 4096)):
+        for name, ms in layer.stage_times(c):
+            stages.setdefault(name, []).append(ms)
+    layer.set_timing(0)
+    rc = layer.status()
+    if rc != 0:
+        raise RuntimeError(f"layer status after the timed steps: {rc}")
+
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    tokens = inp.tokens
+    value = world * K * tokens / (total_ms / 1e3)
+    work = algorithmic_work(inp)
+    pk = peaks()
+
+    # ---- end to end: host input -> layer -> host output, copies timed
+    e2e = None
+    n_e2e = args.e2e_steps if args.e2e_steps is not None else min(K, 200)
+    if n_e2e > 0:
+        x_h = to_device(inp.x, pin=True)
+        out_h = torch.empty_like(x_h).pin_memory()
+        extra_h, extra_d = [], []
+        if decode:
+            extra_h.append(to_device(inp.start_pos, pin=True))
+            extra_d.append(sp)
+        elif w.kind == "varlen":
+            extra_h.append(to_device(inp.cu_seqlens, pin=True))
+            extra_d.append(cu)
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_e2e)]
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(n_e2e):
+            flush.fill_(i & 0xFF)
+            ev2[i][0].record(stream)
+            for h_, d_ in zip(extra_h, extra_d):
+                d_.copy_(h_, non_blocking=True)
+            if decode:
+                layer.decode_from_host(x_h, out_h, x, out, ck, cv, sp)
+            elif w.kind == "varlen":
+                layer.forward_from_host(x_h, out_h, x, out, cu_seqlens=cu, seq_len=seq)
+            else:
+                layer.forward_from_host(x_h, out_h, x, out, n_seq=n_seq, seq_len=seq)
+            ev2[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = float(sum(a.elapsed_time(b) for a, b in ev2))
+        if dist is not None:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        bi = x_h.numel() * x_h.element_size() + sum(
+            h_.numel() * h_.element_size() for h_ in extra_h)
+        bo = out_h.numel() * out_h.element_size()
+        e2e = {"value": world * n_e2e * tokens / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+               "steps": n_e2e, "ms_per_step": e2e_ms / n_e2e,
+               "api": "LlamaLayer.%s_from_host (pinned host buffers, "
+                      "cudaMemcpyAsync on the layer's stream)"
+                      % ("decode" if decode else "forward")}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    stage_ms = {k: statistics.mean(v) for k, v in stages.items()}
+    # the dominant kernel: the stage with the largest share of the step
+    dom = max(stage_ms, key=stage_ms.get) if stage_ms else None
+    roofline = None
+    if dom:
+        dom_ms = stage_ms[dom]
+        launches = "2 launches: split-KV + combine" if (
+            dom == "attention" and work["kind"] == "decode") else "1 launch"
+        share = dom_ms / (sum(stage_ms.values()) or 1.0)
+        if dom in work["flops"]:
+            achieved = work["flops"][dom] / (dom_ms / 1e3) / 1e12
+            roofline = {"bound": "tensor", "kernel": f"{dom} ({launches})",
+                        "achieved": achieved, "peak": pk["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                        "peak_source": f"{pk['source']} bf16 burst",
+                        "frac_of_sustained": achieved / pk["bf16_tflops_sustained"],
+                        "algorithmic_per_launch": work["flops"][dom],
+                        "launch_ms": dom_ms, "share_of_step": share}
+        else:
+            achieved = work["bytes"][dom] / (dom_ms / 1e3) / 1e9
+            roofline = {"bound": "hbm", "kernel": f"{dom} ({launches})",
+                        "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / pk["hbm_gbs"],
+                        "peak_source": f"{pk['source']} HBM copy",
+                        "algorithmic_per_launch": work["bytes"][dom],
+                        "launch_ms": dom_ms, "share_of_step": share}
+        roofline["traffic"] = recorded_traffic(args.workload, dom)
+    ms_step = total_ms / K
+    if work["kind"] == "prefill":
+        achieved = work["total_flops"] / (ms_step / 1e3) / 1e12
+        layer_roof = {"bound": "tensor", "achieved": achieved, "unit": "TFLOP/s",
+                      "frac": achieved / pk["bf16_tflops"],
+                      "frac_of_sustained": achieved / pk["bf16_tflops_sustained"],
+                      "algorithmic_per_step": work["total_flops"]}
+    else:
+        achieved = work["total_bytes"] / (ms_step / 1e3) / 1e9
+        layer_roof = {"bound": "hbm", "achieved": achieved, "unit": "GB/s",
+                      "frac": achieved / pk["hbm_gbs"],
+                      "frac_of_8tbs": achieved / 8000.0,
+                      "algorithmic_per_step": work["total_bytes"]}
+
+    stage_roof = {}
+    for name, ms in stage_ms.items():
+        e = {"ms": ms}
+        if name in work["flops"]:
+            tf = work["flops"][name] / (ms / 1e3) / 1e12
+            e.update(tflops=tf, frac=tf / pk["bf16_tflops"])
+        if name in work.get("bytes", {}):
+            gb = work["bytes"][name] / (ms / 1e3) / 1e9
+            e.update(gbs=gb, frac=gb / pk["hbm_gbs"])
+        stage_roof[name] = e
+
+    cpu = None
+    if args.cpu_baseline_seconds > 0:
+        cpu = cpu_baseline(inp, args.cpu_baseline_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if s.dtype == "bf16" else "f32",
+        "data": "synthetic: seeded x ~ N(0,1), weights ~ N(0,0.02), RMSNorm "
+                "weights ~ 1+N(0,0.1), no trained weights",
+        "config": {"workload": DESCRIPTIONS[args.workload], "name": args.workload,
+                   "tokens_per_step": tokens, "parallelism": f"replicas x{world}",
+                   "l2": "flushed between timed steps (256 MiB write, outside "
+                         "the step's events)",
+                   "region_s": round(region_s, 3)},
+        "roofline": roofline,
+        "layer_roofline": layer_roof,
+        "stages": stage_roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(K * launches_per_step),
+        "launches_per_step": launches_per_step,
+        "clocks": sampler.summary() if sampler else None,
+    }
+    if args.stages:
+        for name, e in stage_roof.items():
+            print(f"{name:>24s} {e['ms']:9.4f} ms  "
+                  + (f"{e['tflops']:8.1f} TF/s " if "tflops" in e else "")
+                  + (f"{e['gbs']:8.1f} GB/s " if "gbs" in e else "")
+                  + (f"frac {e['frac']:.3f}" if "frac" in e else ""),
+                  file=sys.stderr)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+# ----------------------------------------------------------------- reference
+def run_reference(args, rank, world):
+    """The fp64 oracle on the host cores, K timed steps of a bounded sample."""
+    if rank != 0:
+        return None
+    from llama_decoder_layer_prologue_b300 import synth
+
+    inp = synth.make_inputs(args.workload)
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
+    W = args.warmup
+    r = OracleRunner(inp)
+    per_step = min(4.0, 150.0 / max(1, K + W))  # whole run within minutes
+    n = r.calibrate(per_step)
+    run, tokens, what = r.units(n)
+    for _ in range(min(W, 1)):
+        run()
+    times = []
+    for _ in range(K):
+        t = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    value = K * tokens / total
+    s = inp.workload.shape
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": min(W, 1), "ms_per_step": 1e3 * total / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (same seeded inputs as the CUDA arm)",
+        "config": {"workload": DESCRIPTIONS[args.workload], "name": args.workload,
+                   "tokens_per_step": tokens, "parallelism": "host cores, rank 0"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(),
+                         "kind": "oracle",
+                         "sample": f"{what} per step (bounded so the run ends "
+                                   f"within minutes), fp64 numpy oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+        "note": f"dtype of the workload is {s.dtype}; the oracle computes in fp64",
+    }
+
+
+def main():
+    args = parse_args()
+    rank, local_rank, world = dist_env()
+    if args.gpus != world and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, local_rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

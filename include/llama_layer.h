@@ -193,6 +193,34 @@ LLAMA_API int llama_layer_status(llama_layer_t* layer, void* stream);
 LLAMA_API int llama_layer_workspace_offsets(const llama_layer_t* layer, int tokens,
                                   int decode, size_t offsets[LLAMA_WS_NUM]);
 
+/* Stage timing.  With timing on, every forward / decode call records a CUDA
+ * event on its stream where each of its stages begins and one where the call
+ * ends, into the next record of a ring of `ring_calls` records (events are
+ * driver objects, not device memory).  ring_calls = 0 switches timing off
+ * (the default); 1 <= ring_calls <= LLAMA_MAX_TIMED_CALLS switches it on and
+ * forgets earlier records.  Returns LLAMA_ERR_CUDA if the events cannot be
+ * created. */
+#define LLAMA_MAX_STAGES 16
+#define LLAMA_MAX_TIMED_CALLS 4096
+LLAMA_API int llama_layer_set_timing(llama_layer_t* layer, int ring_calls);
+
+/* Stage durations of a recorded call, in milliseconds
+ * (cudaEventElapsedTime between consecutive events; waits for that call's
+ * last event).  call = 0 is the most recent forward / decode call, 1 the one
+ * before, ... (< ring_calls).  Writes up to max_stages entries of ms[] and of
+ * names[] (static strings; names may be NULL) and the number of stages in
+ * *n_stages (may be NULL): 0 when timing is off or the call was not recorded,
+ * at most LLAMA_MAX_STAGES (the first ones of a call that has more).  Stages
+ * of a prefill: "rmsnorm_stats", "qkv_rope", "attention", "o_proj_residual",
+ * "gate_up_swiglu", "down_residual". */
+LLAMA_API int llama_layer_stage_times(llama_layer_t* layer, int call,
+                                      int max_stages, float* ms,
+                                      const char** names, int* n_stages);
+
+/* Number of kernels the last forward / decode call launched (timing on or
+ * off), or LLAMA_ERR_INVALID_ARG for a null handle. */
+LLAMA_API int llama_layer_launch_count(const llama_layer_t* layer);
+
 /* Frees the host handle only (packed memory stays the caller's). */
 LLAMA_API void llama_layer_destroy(llama_layer_t* layer);
 

@@ -29,6 +29,8 @@ LLAMA_DTYPE_BF16 = 1
 LLAMA_ROPE_NONE = 0
 LLAMA_ROPE_LLAMA3 = 1
 LLAMA_WS_NUM = 4
+LLAMA_MAX_STAGES = 16
+LLAMA_MAX_TIMED_CALLS = 4096
 
 # Every symbol include/llama_layer.h declares.
 EXPORTS = (
@@ -36,6 +38,8 @@ EXPORTS = (
     "llama_layer_workspace_bytes", "llama_layer_forward", "llama_layer_decode",
     "llama_layer_status", "llama_layer_workspace_offsets",
     "llama_layer_destroy", "llama_layer_strerror", "llama_gemm_bf16",
+    "llama_layer_set_timing", "llama_layer_stage_times",
+    "llama_layer_launch_count",
 )
 
 
@@ -98,6 +102,12 @@ def lib() -> ctypes.CDLL:
         "llama_layer_destroy": (None, [_P]),
         "llama_layer_strerror": (ctypes.c_char_p, [_I]),
         "llama_gemm_bf16": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+        "llama_layer_set_timing": (_I, [_P, _I]),
+        "llama_layer_stage_times": (_I, [_P, _I, _I,
+                                         ctypes.POINTER(ctypes.c_float),
+                                         ctypes.POINTER(ctypes.c_char_p),
+                                         ctypes.POINTER(_I)]),
+        "llama_layer_launch_count": (_I, [_P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -180,6 +190,29 @@ def llama_layer_workspace_offsets(layer: int, tokens: int,
 
 def llama_layer_destroy(layer: int) -> None:
     lib().llama_layer_destroy(layer)
+
+
+def llama_layer_set_timing(layer: int, ring_calls: int) -> None:
+    _check("llama_layer_set_timing",
+           lib().llama_layer_set_timing(layer, int(ring_calls)))
+
+
+def llama_layer_stage_times(layer: int, call: int = 0) -> list[tuple[str, float]]:
+    """[(stage name, ms)] of recorded call ``call`` (0 = the most recent)."""
+    ms = (ctypes.c_float * LLAMA_MAX_STAGES)()
+    names = (ctypes.c_char_p * LLAMA_MAX_STAGES)()
+    n = _I()
+    _check("llama_layer_stage_times",
+           lib().llama_layer_stage_times(layer, call, LLAMA_MAX_STAGES, ms,
+                                         names, ctypes.byref(n)))
+    return [(names[i].decode(), float(ms[i])) for i in range(n.value)]
+
+
+def llama_layer_launch_count(layer: int) -> int:
+    rc = lib().llama_layer_launch_count(layer)
+    if rc < 0:
+        raise LlamaError("llama_layer_launch_count", rc)
+    return rc
 
 
 def llama_gemm_bf16(A: int, B: int, D: int, M: int, N: int, K: int,

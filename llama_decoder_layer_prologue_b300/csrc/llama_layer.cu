@@ -133,11 +133,55 @@ struct llama_layer {
   int sm_count;
   CUtensorMap tm_wqkv, tm_wo, tm_wgu, tm_wd;  // bf16 weights as B, 256 rows
   CUtensorMap ta_wqkv, ta_wo, ta_wgu, ta_wd;  // bf16 weights as A, 128 rows
+  // Stage timing (llama_layer_set_timing): a ring of `ring` call records.
+  // In record c, event i is recorded on the call's stream where stage i
+  // begins and the last one where the call ends.
+  int ring;                  // 0 = timing off
+  int calls;                 // calls recorded since timing was switched on
+  cudaEvent_t* ev;           // [ring][LLAMA_MAX_STAGES + 1]
+  const char** stage_name;   // [ring][LLAMA_MAX_STAGES]
+  int* n_marks;              // [ring]
+  int launches;  // kernels launched by the last forward / decode call
 };
 
 namespace {
 
 int cuda_err(cudaError_t e) { return e == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA; }
+
+// Starts stage `name` (or ends the call when name is null) on stream s.
+void mark(llama_layer* L, cudaStream_t s, const char* name) {
+  if (!L->ring) return;
+  const int c = (L->calls - 1) % L->ring;
+  int& n = L->n_marks[c];
+  if (n > LLAMA_MAX_STAGES) return;
+  if (!name && n == LLAMA_MAX_STAGES + 1) return;
+  if (name && n == LLAMA_MAX_STAGES) return;  // keep the last event for the end
+  cudaEventRecord(L->ev[(size_t)c * (LLAMA_MAX_STAGES + 1) + n], s);
+  if (name) L->stage_name[(size_t)c * LLAMA_MAX_STAGES + n] = name;
+  ++n;
+}
+
+void begin_call(llama_layer* L) {
+  L->launches = 0;
+  if (!L->ring) return;
+  ++L->calls;
+  L->n_marks[(L->calls - 1) % L->ring] = 0;
+}
+
+void free_timing(llama_layer* L) {
+  if (L->ev) {
+    for (size_t i = 0; i < (size_t)L->ring * (LLAMA_MAX_STAGES + 1); ++i)
+      if (L->ev[i]) cudaEventDestroy(L->ev[i]);
+  }
+  delete[] L->ev;
+  delete[] L->stage_name;
+  delete[] L->n_marks;
+  L->ev = nullptr;
+  L->stage_name = nullptr;
+  L->n_marks = nullptr;
+  L->ring = 0;
+  L->calls = 0;
+}
 
 int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in,
                  const int32_t* cu, int n_seq, int seq_len, int T, char* ws,
@@ -158,9 +202,12 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
   const float* cos_t = reinterpret_cast<const float*>(P + L->pl.cos_t);
   const float* sin_t = reinterpret_cast<const float*>(P + L->pl.sin_t);
 
+  begin_call(L);
+  mark(L, s, "rmsnorm_stats");
   launch_positions(cu, n_seq, seq_len, T, reinterpret_cast<int32_t*>(ws + w.pos),
                    pos_in == nullptr, L->status, s);
   simt_row_rms(b16, x, T, dm.H, dm.eps, r1, ss2, s);
+  L->launches += 2;
   if (b16) {
     cudaError_t e;
     CUtensorMap ta;
@@ -171,37 +218,47 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.out = qkv; ep.ldo = dm.Nqkv; ep.rowscale = r1; ep.pos = pos;
     ep.cos_t = cos_t; ep.sin_t = sin_t; ep.head_dim = dm.d;
     ep.rope_cols = (dm.Hq + dm.Hkv) * dm.d; ep.max_pos = dm.max_pos;
+    mark(L, s, "qkv_rope");
     e = tc_gemm(TC_QKV, 256, ta, L->tm_wqkv, T, dm.Nqkv, dm.H, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
+    ++L->launches;
     // a4 / a5: causal GQA attention (padded or varlen).
     AttnArgs aa;
     aa.qkv = static_cast<const __nv_bfloat16*>(qkv);
     aa.out = static_cast<__nv_bfloat16*>(attn);
     aa.cu = cu; aa.tokens = T; aa.seq_len = seq_len; aa.nqkv = dm.Nqkv;
     aa.n_heads = dm.Hq; aa.n_kv_heads = dm.Hkv; aa.head_dim = dm.d;
+    mark(L, s, "attention");
     if (attn_prefill(aa, n_seq, seq_len, s) != cudaSuccess) return LLAMA_ERR_CUDA;
+    ++L->launches;
     // a7: o_proj + residual, row sums of h^2 for the second RMSNorm.
     if (!tc_encode_bf16(&ta, attn, T, dm.Hq * dm.d, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
     ep.out = h; ep.out2 = ws + w.hg; ep.ldo = dm.H; ep.residual = x;
     ep.colscale = P + L->pl.gpost; ep.ss_out = ss2;
+    mark(L, s, "o_proj_residual");
     e = tc_gemm(TC_RESID_SS, 256, ta, L->tm_wo, T, dm.H, dm.Hq * dm.d, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
+    ++L->launches;
     // a8: gate_up on h * g_post with the RMSNorm row scale, silu(gate) * up.
     if (!tc_encode_bf16(&ta, ws + w.hg, T, dm.H, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
     ep.out = act; ep.ldo = dm.I; ep.ss_in = ss2; ep.inv_h = 1.0f / dm.H; ep.eps = dm.eps;
+    mark(L, s, "gate_up_swiglu");
     e = tc_gemm(TC_SWIGLU, 256, ta, L->tm_wgu, T, 2 * dm.I, dm.H, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
+    ++L->launches;
     // a9: down_proj + residual.
     if (!tc_encode_bf16(&ta, act, T, dm.I, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
     ep.out = out; ep.ldo = dm.H; ep.residual = h;
+    mark(L, s, "down_residual");
     e = tc_gemm(TC_RESID, 256, ta, L->tm_wd, T, dm.H, dm.I, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
+    ++L->launches;
   } else {
     simt_gemm(b16, EPI_ROWSCALE, x, P + L->pl.wqkv, qkv, T, dm.Nqkv, dm.H, r1,
               nullptr, s);
@@ -217,7 +274,9 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
               ss2, nullptr, s);
     simt_gemm(b16, EPI_RESIDUAL, act, P + L->pl.wd, out, T, dm.H, dm.I,
               nullptr, h, s);
+    L->launches += 8;
   }
+  mark(L, s, nullptr);
   return cuda_err(cudaGetLastError());
 }
 
@@ -298,6 +357,11 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
 
   // One projection: stream-K swap-AB GEMM into the partials, then its
   // finalize kernel.
+  static const char* const kGemmName[4] = {"qkv_gemm", "o_proj_gemm",
+                                            "gate_up_gemm", "down_gemm"};
+  static const char* const kFinName[4] = {"qkv_rope_cache_append",
+                                          "o_residual", "swiglu",
+                                          "down_residual"};
   auto project = [&](int stage, const CUtensorMap& wmap, const void* act_in,
                      int N_out, int K) -> int {
     CUtensorMap tb;
@@ -306,20 +370,27 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
     ep.out = ws + w.part;
     ep.part_slots = w.plan[stage].slots;
     ep.status = L->status;
+    mark(L, s, kGemmName[stage]);
     if (tc_gemm(TC_PARTIAL, w.bn, wmap, tb, N_out, B, K, ep, L->sm_count, s) !=
         cudaSuccess)
       return LLAMA_ERR_CUDA;
+    mark(L, s, kFinName[stage]);
+    L->launches += 2;
     return decode_finalize(stage, a, w.plan[stage], s) == cudaSuccess
                ? LLAMA_OK : LLAMA_ERR_CUDA;
   };
 
   // a1: 1/RMS of every new token (and zero the sums of h^2).
+  mark(L, s, "rmsnorm_stats");
   simt_row_rms(true, x, B, dm.H, dm.eps, const_cast<float*>(a.r1), a.ss2, s);
+  ++L->launches;
   // a2 + a3 + cache append.
   int rc = project(DEC_QKV, L->ta_wqkv, x, dm.Nqkv, dm.H);
   if (rc) return rc;
   // a6: split-KV attention over rows 0..start_pos[b].
+  mark(L, s, "attention");
   if (decode_attention(a, s) != cudaSuccess) return LLAMA_ERR_CUDA;
+  L->launches += 2;
   // a7: o_proj + residual (+ sums of h^2).
   if ((rc = project(DEC_O, L->ta_wo, a.attn, dm.H, dm.Hq * dm.d))) return rc;
   // a8: gate_up + SiLU * up.
@@ -335,6 +406,7 @@ int decode_impl(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   const llama_layer_config& c = L->cfg;
   const Dims& dm = L->dm;
   const bool b16 = L->bf16;
+  begin_call(L);
   if (b16) {
     const size_t es = 2, row = (size_t)dm.H * es;
     const size_t cache_seq = (size_t)max_seq * dm.Hkv * dm.d * es;
@@ -347,6 +419,7 @@ int decode_impl(llama_layer* L, const void* x, void* out, void* ck, void* cv,
                             start_pos + b0, nb, max_seq, ws, s);
       if (rc) return rc;
     }
+    mark(L, s, nullptr);
     return LLAMA_OK;
   }
   WsLayout w = ws_layout(c, B);
@@ -360,6 +433,7 @@ int decode_impl(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   const float* cos_t = reinterpret_cast<const float*>(P + L->pl.cos_t);
   const float* sin_t = reinterpret_cast<const float*>(P + L->pl.sin_t);
 
+  mark(L, s, "decode_fp32");
   simt_row_rms(b16, x, B, dm.H, dm.eps, r1, nullptr, s);
   simt_gemm(b16, EPI_ROWSCALE, x, P + L->pl.wqkv, qkv, B, dm.Nqkv, dm.H, r1,
             nullptr, s);
@@ -376,6 +450,8 @@ int decode_impl(llama_layer* L, const void* x, void* out, void* ck, void* cv,
             nullptr, s);
   simt_gemm(b16, EPI_RESIDUAL, act, P + L->pl.wd, out, B, dm.H, dm.I, nullptr,
             h, s);
+  L->launches += 10;
+  mark(L, s, nullptr);
   return cuda_err(cudaGetLastError());
 }
 
@@ -584,7 +660,56 @@ int llama_layer_status(llama_layer_t* L, void* stream) {
   return LLAMA_OK;
 }
 
-void llama_layer_destroy(llama_layer_t* L) { delete L; }
+int llama_layer_set_timing(llama_layer_t* L, int ring) {
+  if (!L || ring < 0 || ring > LLAMA_MAX_TIMED_CALLS) return LLAMA_ERR_INVALID_ARG;
+  free_timing(L);
+  if (ring == 0) return LLAMA_OK;
+  const size_t n_ev = (size_t)ring * (LLAMA_MAX_STAGES + 1);
+  L->ev = new (std::nothrow) cudaEvent_t[n_ev]();
+  L->stage_name = new (std::nothrow) const char*[(size_t)ring * LLAMA_MAX_STAGES]();
+  L->n_marks = new (std::nothrow) int[ring]();
+  L->ring = ring;
+  if (!L->ev || !L->stage_name || !L->n_marks) {
+    free_timing(L);
+    return LLAMA_ERR_INVALID_ARG;
+  }
+  for (size_t i = 0; i < n_ev; ++i) {
+    if (cudaEventCreate(&L->ev[i]) != cudaSuccess) {
+      free_timing(L);
+      return LLAMA_ERR_CUDA;
+    }
+  }
+  return LLAMA_OK;
+}
+
+int llama_layer_stage_times(llama_layer_t* L, int call, int max_stages,
+                            float* ms, const char** names, int* n_stages) {
+  if (!L || call < 0 || max_stages < 0 || (max_stages > 0 && !ms))
+    return LLAMA_ERR_INVALID_ARG;
+  if (n_stages) *n_stages = 0;
+  if (!L->ring || call >= L->ring || call >= L->calls) return LLAMA_OK;
+  const int c = (L->calls - 1 - call) % L->ring;
+  const int n = L->n_marks[c] > 1 ? L->n_marks[c] - 1 : 0;
+  if (n_stages) *n_stages = n;
+  if (n == 0) return LLAMA_OK;
+  const cudaEvent_t* e = L->ev + (size_t)c * (LLAMA_MAX_STAGES + 1);
+  if (cudaEventSynchronize(e[n]) != cudaSuccess) return LLAMA_ERR_CUDA;
+  for (int i = 0; i < n && i < max_stages; ++i) {
+    if (cudaEventElapsedTime(&ms[i], e[i], e[i + 1]) != cudaSuccess)
+      return LLAMA_ERR_CUDA;
+    if (names) names[i] = L->stage_name[(size_t)c * LLAMA_MAX_STAGES + i];
+  }
+  return LLAMA_OK;
+}
+
+int llama_layer_launch_count(const llama_layer_t* L) {
+  return L ? L->launches : LLAMA_ERR_INVALID_ARG;
+}
+
+void llama_layer_destroy(llama_layer_t* L) {
+  if (L) free_timing(L);
+  delete L;
+}
 
 const char* llama_layer_strerror(int code) {
   switch (code) {

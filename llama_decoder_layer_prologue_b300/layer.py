@@ -113,6 +113,35 @@ class LlamaLayer:
                              stream_ptr())
         return out
 
+    def forward_from_host(self, x_host, out_host, x_dev, out_dev, **kw):
+        """One forward whose input and output live in (pinned) host memory:
+        copy x in, run the layer, copy out back, all on the current stream.
+        ``x_dev`` / ``out_dev`` are device buffers of the same shape."""
+        x_dev.copy_(x_host, non_blocking=True)
+        self.forward(x_dev, out=out_dev, **kw)
+        out_host.copy_(out_dev, non_blocking=True)
+        return out_host
+
+    def decode_from_host(self, x_host, out_host, x_dev, out_dev, cache_k,
+                         cache_v, start_pos):
+        """One decode step with host input / output (see forward_from_host);
+        the KV cache stays resident on the device."""
+        x_dev.copy_(x_host, non_blocking=True)
+        self.decode(x_dev, cache_k, cache_v, start_pos, out=out_dev)
+        out_host.copy_(out_dev, non_blocking=True)
+        return out_host
+
+    def set_timing(self, ring_calls: int) -> None:
+        """Record stage events for the last ``ring_calls`` calls (0: off)."""
+        B.llama_layer_set_timing(self.handle, ring_calls)
+
+    def stage_times(self, call: int = 0):
+        """[(stage, ms)] of recorded call ``call`` (0 = the most recent)."""
+        return B.llama_layer_stage_times(self.handle, call)
+
+    def launch_count(self) -> int:
+        return B.llama_layer_launch_count(self.handle)
+
     def status(self) -> int:
         return B.llama_layer_status(self.handle, stream_ptr())
 
