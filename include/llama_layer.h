@@ -234,6 +234,34 @@ LLAMA_API const char* llama_layer_strerror(int code);
 LLAMA_API int llama_gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K,
                     void* stream);
 
+/* D[M, N] = A[M, K] . B[N, K]^T in bf16 with fp32 accumulation, without any
+ * device memory from the caller beyond A, B and D.  The pages this library
+ * follows have no counterpart of this entry point: it exists for callers that
+ * cannot allocate device memory where they run the GEMM (an engine that has
+ * reserved all device memory for its own pool, or a latency-critical loop in
+ * which cudaMalloc / cudaFree could synchronise the device) and have no
+ * workspace to hand over.
+ *
+ * It runs the stream-K tcgen05 GEMM of the decode projections (A is the
+ * large side, e.g. a weight matrix; B holds up to 256 rows, e.g. tokens; K
+ * is split evenly over all SMs) and keeps the fp32 partial sums in a 16 MiB
+ * array of device memory that the library defines at file scope: every GPU
+ * that loads the library holds those 16 MiB until the process exits.  The
+ * partials of tile t fill slots x 128 x bn floats (bn = 64, 128 or 256, the
+ * smallest >= N); a call whose partials need more than 16 MiB returns
+ * LLAMA_ERR_WORKSPACE_TOO_SMALL and launches nothing.
+ *   A [M, K], B [N, K], D [M, N]: device, row-major, 16-byte aligned;
+ *   K % 8 == 0, N % 8 == 0, N <= 256 (else LLAMA_ERR_UNSUPPORTED_SHAPE).
+ * The first call on a device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress; make that first call
+ * before any stream capture.  The call never calls cudaMalloc, cudaFree or
+ * an allocating library routine.  Every call shares the one array, which
+ * keeps the last call's partials; a call writes every partial it reads, so
+ * nothing has to start at zero.  Calls that overlap on the GPU (other
+ * streams, other host threads) race on the array: order them on one stream. */
+LLAMA_API int llama_gemm_bf16_streamk_static(const void* A, const void* B, void* D,
+                                             int M, int N, int K, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

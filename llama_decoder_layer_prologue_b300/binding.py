@@ -39,7 +39,7 @@ EXPORTS = (
     "llama_layer_status", "llama_layer_workspace_offsets",
     "llama_layer_destroy", "llama_layer_strerror", "llama_gemm_bf16",
     "llama_layer_set_timing", "llama_layer_stage_times",
-    "llama_layer_launch_count",
+    "llama_layer_launch_count", "llama_gemm_bf16_streamk_static",
 )
 
 
@@ -108,6 +108,7 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(ctypes.c_char_p),
                                          ctypes.POINTER(_I)]),
         "llama_layer_launch_count": (_I, [_P]),
+        "llama_gemm_bf16_streamk_static": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -218,3 +219,11 @@ def llama_layer_launch_count(layer: int) -> int:
 def llama_gemm_bf16(A: int, B: int, D: int, M: int, N: int, K: int,
                     stream: int) -> None:
     _check("llama_gemm_bf16", lib().llama_gemm_bf16(A, B, D, M, N, K, stream))
+
+
+def llama_gemm_bf16_streamk_static(A: int, B: int, D: int, M: int, N: int,
+                                   K: int, stream: int) -> None:
+    """Stream-K GEMM whose partial sums live in the library's own fixed
+    device array (no caller workspace, no allocation)."""
+    _check("llama_gemm_bf16_streamk_static",
+           lib().llama_gemm_bf16_streamk_static(A, B, D, M, N, K, stream))
