@@ -58,6 +58,9 @@ def test_tiny_fp32_workload():
      dict(batch=2, seq=129)),
     ("mha", shape(256, 4, 4, 64, 256), "padded", dict(batch=2, seq=65)),
     ("single_token", shape(256, 4, 2, 64, 256), "padded", dict(batch=1, seq=1)),
+    # q|k|v width 320: not a multiple of the 128-row / 256-column tiles
+    ("three_heads_one_kv", shape(256, 3, 1, 64, 256), "padded",
+     dict(batch=2, seq=70)),
     ("varlen_with_len1", shape(512, 8, 2, 64, 512, **L3), "varlen",
      dict(total_tokens=700, min_len=1, max_len=300)),
 ])
@@ -130,6 +133,11 @@ def test_decode_small_bf16_edges():
 def test_decode_small_d128():
     s = shape(512, 8, 2, 128, 384)
     check_decode(s, batch=3, max_seq=520, start_pos=[513, 7, 64])
+
+
+def test_decode_qkv_width_not_tile_aligned():
+    s = shape(256, 3, 1, 64, 256, **L3)
+    check_decode(s, batch=33, max_seq=200, start_pos=list(range(0, 198, 6)))
 
 
 def test_decode_tiny_fp32():
