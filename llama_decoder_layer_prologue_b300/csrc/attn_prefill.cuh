@@ -12,11 +12,13 @@ struct AttnArgs {
   __nv_bfloat16* out;        // [tokens, n_heads * head_dim]
   const int32_t* cu;         // [n_seq + 1] or null (padded: seq_len each)
   int tokens, seq_len, nqkv, n_heads, n_kv_heads, head_dim;
-  int hpc;                   // query heads per CTA (set by attn_prefill)
+  int hpc;                   // query heads per tile (set by attn_prefill)
+  int* status;               // device status word (bounded waits)
 };
 
-// max_len: longest sequence (padded: seq_len).
+// max_len: longest sequence (padded: seq_len).  Persistent over
+// min(work items, sm_count) CTAs.
 cudaError_t attn_prefill(const AttnArgs& a, int n_seq, int max_len,
-                         cudaStream_t s);
+                         int sm_count, cudaStream_t s);
 
 }  // namespace llama

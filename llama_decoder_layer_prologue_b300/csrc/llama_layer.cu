@@ -228,8 +228,10 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     aa.out = static_cast<__nv_bfloat16*>(attn);
     aa.cu = cu; aa.tokens = T; aa.seq_len = seq_len; aa.nqkv = dm.Nqkv;
     aa.n_heads = dm.Hq; aa.n_kv_heads = dm.Hkv; aa.head_dim = dm.d;
+    aa.status = L->status;
     mark(L, s, "attention");
-    if (attn_prefill(aa, n_seq, seq_len, s) != cudaSuccess) return LLAMA_ERR_CUDA;
+    if (attn_prefill(aa, n_seq, seq_len, L->sm_count, s) != cudaSuccess)
+      return LLAMA_ERR_CUDA;
     ++L->launches;
     // a7: o_proj + residual, row sums of h^2 for the second RMSNorm.
     if (!tc_encode_bf16(&ta, attn, T, dm.Hq * dm.d, 128)) return LLAMA_ERR_CUDA;
