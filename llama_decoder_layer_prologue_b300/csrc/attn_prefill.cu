@@ -4,28 +4,29 @@
 // each sequence, query head h reading kv head h / n_rep.  q and k arrive
 // already rotated by the QKV GEMM epilogue.
 //
-// tcgen05 / TMEM flash attention, persistent (one CTA per SM), 10 warps:
-//   warps 0..7  softmax + epilogue: query row r of the tile (TMEM lane r) is
-//               shared by warp r / 32 (keys 0..63 of each S tile, the first
-//               half of O) and warp 4 + r / 32 (keys 64..127, second half of
-//               O); the two threads swap their partial row maxima through
-//               shared memory.  Each thread masks its scores, keeps the
-//               running max m and its partial sum l, writes its half of
-//               P = 2^(s - m) as bf16 into a 128-byte swizzled smem tile (the
-//               A operand of P V), and at the end reads its half of O,
-//               divides by the row's l and stores bf16.
-//   warp 8      TMA producer: the Q tile once per work item, K / V tiles of
-//               128 keys into a ring of stages.
-//   warp 9      one thread issues tcgen05.mma: S = Q K^T into one of two TMEM
-//               S buffers, O += P V into the TMEM O buffer (V is read as an
-//               MN-major operand straight from its TMA tile).
-// A tile of 128 query rows holds `hpc` query heads of one kv group times
-// 128 / hpc positions, so each K / V tile feeds every head of the group
-// (repeat_kv is never materialised).  Rescaling of O is lazy: a row's
-// reference max only moves (and O is rescaled in TMEM) when the new max
-// exceeds it by more than 8 in the log2 domain, so P stays <= 2^8.
-// Work items (query block, head group, sequence) run longest causal range
-// first.  Every wait is bounded (2 s -> status bit, abort, drain, free TMEM).
+// tcgen05 / TMEM flash attention, persistent (one CTA per SM), 12 warps.  A
+// work item is two query tiles A and B of 128 rows each: `hpc` query heads of
+// one kv group times BP = 128 / hpc positions, B holding the BP positions
+// after A's, so every K / V tile feeds 256 query rows (repeat_kv is never
+// materialised).
+//   warps 0..3  softmax of tile A, warps 4..7 softmax of tile B: thread r of
+//               a warpgroup owns query row r (TMEM lane r).  Per K / V tile
+//               it loads its S row, masks, keeps the running max m and sum l,
+//               and writes P = 2^(s - m) as bf16 into the 128-byte swizzled
+//               P tile (the A operand of P V); at the end it reads its O row,
+//               divides by l and stores bf16.
+//   warp 8      TMA producer: the two Q tiles once per item, then K(j), V(j)
+//               into a ring of single-tile slots.
+//   warp 9      one thread issues tcgen05.mma in the order
+//               S_A(j+1), PV_A(j), S_B(j+1), PV_B(j): S = Q K^T into the
+//               tile's TMEM S buffer, O += P V into its TMEM O buffer (V read
+//               as an MN-major operand straight from its TMA tile).  While one
+//               warpgroup computes its softmax the tensor core works on the
+//               other's products; the two share one P buffer, written in turn.
+// Rescaling of O is lazy: a row's reference max only moves (and O is
+// rescaled in TMEM) when the new max exceeds it by more than 8 in the log2
+// domain, so P stays <= 2^8.  Items run longest causal range first.  Every
+// wait is bounded (2 s -> status bit, abort, drain, free TMEM).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -40,23 +41,30 @@ using bf16 = __nv_bfloat16;
 constexpr int AM = 128;  // query rows per tile (MMA M)
 constexpr int AN = 128;  // keys per K / V tile
 constexpr float kRescaleLog2 = 8.0f;
+// 12 warps = 3 warpgroups: the register file is shared out per warpgroup,
+// so the block launches at 168 registers a thread (384 x 168 = 64512) and
+// then moves registers with setmaxnreg: the two softmax warpgroups go up to
+// kSoftmaxRegs, the producer / MMA warpgroup (warps 8..11, 10 and 11 idle)
+// down to kControlRegs; 2 x 128 x 200 + 128 x 104 = 64512.
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kSoftmaxRegs = 200, kControlRegs = 104;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168,
+              "register split exceeds the launch allocation");
 
 template <int D>
 struct AttnLayout {
   static constexpr int ATOMS = D / 64;  // 128-byte swizzle atoms per row
-  static constexpr uint32_t Q_BYTES = AM * D * 2;
-  static constexpr uint32_t KV_BYTES = AN * D * 2;  // K or V tile
+  static constexpr uint32_t Q_BYTES = AM * D * 2;   // one query tile
+  static constexpr uint32_t KV_BYTES = AN * D * 2;  // one K or V tile (a slot)
   static constexpr uint32_t P_BYTES = AM * AN * 2;
-  static constexpr int STAGES = D == 64 ? 4 : 2;
-  static constexpr uint32_t STAGE = 2 * KV_BYTES;
-  static constexpr uint32_t Q_OFF = 0;
-  static constexpr uint32_t P_OFF = Q_OFF + Q_BYTES;
+  static constexpr int SLOTS = D == 64 ? 8 : 4;
+  static constexpr uint32_t Q_OFF = 0;              // Q_A, Q_B
+  static constexpr uint32_t P_OFF = Q_OFF + 2 * Q_BYTES;
   static constexpr uint32_t KV_OFF = P_OFF + P_BYTES;
-  static constexpr uint32_t BAR_OFF = KV_OFF + STAGES * STAGE;
-  static constexpr uint32_t RED_OFF = BAR_OFF + 256;  // [2][2][128] maxima, [2][128] sums
-  static constexpr uint32_t TOTAL = RED_OFF + 6 * 128 * 4 + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;  // S0 [0,128) S1 [128,256) O [256,256+D)
-  static constexpr uint32_t O_COL = 256;
+  static constexpr uint32_t BAR_OFF = KV_OFF + SLOTS * KV_BYTES;
+  static constexpr uint32_t TOTAL = BAR_OFF + 512 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;  // S_A S_B [0,256), O_A O_B [256, 256+2D)
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
 
@@ -66,7 +74,7 @@ struct Item {
 };
 
 // Work item i: query block from the top (longest causal range first), then
-// head group, then sequence.
+// head group, then sequence.  A block is 2 BP positions.
 __device__ __forceinline__ Item get_item(const AttnArgs& a, int i, int n_hg,
                                          int n_seq, int n_qb, int BP) {
   Item it;
@@ -77,7 +85,7 @@ __device__ __forceinline__ Item get_item(const AttnArgs& a, int i, int n_hg,
   const int n_rep = a.n_heads / a.n_kv_heads;
   it.h0 = hg * a.hpc;
   it.g = it.h0 / n_rep;
-  it.q0 = qb * BP;
+  it.q0 = qb * 2 * BP;
   if (a.cu) {
     const int s0 = a.cu[s], s1 = a.cu[s + 1];
     if (s0 < 0 || s1 < s0 || s1 > a.tokens) {  // flagged by the positions kernel
@@ -89,14 +97,10 @@ __device__ __forceinline__ Item get_item(const AttnArgs& a, int i, int n_hg,
     it.a0 = s * a.seq_len;
     it.L = a.seq_len;
   }
-  const int hi = min(it.q0 + BP, it.L);
+  const int hi = min(it.q0 + 2 * BP, it.L);
   it.n_tiles = it.q0 < it.L ? (hi + AN - 1) / AN : 0;
   return it;
 }
-
-constexpr int kSoftmaxThreads = 256;
-constexpr int kThreads = kSoftmaxThreads + 64;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -114,42 +118,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  uint64_t* kv_full = bar;                     // [STAGES]
-  uint64_t* kv_empty = kv_full + L::STAGES;    // [STAGES]
-  uint64_t* s_full = kv_empty + L::STAGES;     // [2]
-  uint64_t* s_free = s_full + 2;               // [2]
-  uint64_t* q_full = s_free + 2;
+  uint64_t* kv_full = bar;                    // [SLOTS]
+  uint64_t* kv_empty = kv_full + L::SLOTS;    // [SLOTS]
+  uint64_t* s_full = kv_empty + L::SLOTS;     // [2] per query tile
+  uint64_t* s_free = s_full + 2;              // [2]
+  uint64_t* p_full = s_free + 2;              // [2]
+  uint64_t* pv_done = p_full + 2;             // [2]
+  uint64_t* o_free = pv_done + 2;             // [2]
+  uint64_t* q_full = o_free + 2;
   uint64_t* q_empty = q_full + 1;
-  uint64_t* p_full = q_empty + 1;
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* o_free = pv_done + 1;
-  uint64_t* drain = o_free + 1;
-  uint64_t* mx_bar = drain + 1;                // [2] row-max exchange
-  uint64_t* l_bar = mx_bar + 2;                // row-sum exchange
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(l_bar + 1);
-  float* red_max = reinterpret_cast<float*>(smem + L::RED_OFF);  // [2][2][128]
-  float* red_l = red_max + 4 * 128;                               // [2][128]
+  uint64_t* drain = q_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  const int BP = AM / a.hpc;  // positions per tile
+  const int BP = AM / a.hpc;  // positions per query tile
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::STAGES; ++s) {
+    for (int s = 0; s < L::SLOTS; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], kSoftmaxThreads);
-      mbar_init(&mx_bar[b], kSoftmaxThreads);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], 128);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&pv_done[t], 1);
+      mbar_init(&o_free[t], 128);
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    mbar_init(p_full, kSoftmaxThreads);
-    mbar_init(pv_done, 1);
-    mbar_init(o_free, kSoftmaxThreads);
     mbar_init(drain, 1);
-    mbar_init(l_bar, kSoftmaxThreads);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -163,10 +161,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == kProducerWarp) {
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
+    if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t kvc = 0, k = 0, issued = 0;
+      uint32_t n = 0, k = 0;  // K / V tiles loaded, items started
       bool ok = true;
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
         const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP);
@@ -175,40 +175,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(q_full, L::Q_BYTES);
-        for (int hh = 0; hh < a.hpc; ++hh)
-          for (int at = 0; at < L::ATOMS; ++at)
-            tma_load_2d(smem + L::Q_OFF + at * (AM * 128) + hh * BP * 128, &tmQ,
-                        q_full, (it.h0 + hh) * D + at * 64, it.a0 + it.q0);
-        ++issued;
+        mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
+        for (int t = 0; t < 2; ++t)
+          for (int hh = 0; hh < a.hpc; ++hh)
+            for (int at = 0; at < L::ATOMS; ++at)
+              tma_load_2d(smem + L::Q_OFF + t * L::Q_BYTES + at * (AM * 128) +
+                              hh * BP * 128,
+                          &tmQ, q_full, (it.h0 + hh) * D + at * 64,
+                          it.a0 + it.q0 + t * BP);
         ++k;
-        const int kcol = (a.n_heads + it.g) * D;
-        const int vcol = (a.n_heads + a.n_kv_heads + it.g) * D;
-        for (int j = 0; j < it.n_tiles; ++j, ++kvc) {
-          const int st = kvc % L::STAGES;
-          if (!mbar_wait(&kv_empty[st], ((kvc / L::STAGES) & 1) ^ 1, a.status,
-                         abort_flag)) {
-            ok = false;
-            break;
+        const int col[2] = {(a.n_heads + it.g) * D,
+                            (a.n_heads + a.n_kv_heads + it.g) * D};
+        for (int j = 0; ok && j < it.n_tiles; ++j) {
+          for (int kv = 0; kv < 2; ++kv, ++n) {  // K(j), then V(j)
+            const int sl = n % L::SLOTS;
+            if (!mbar_wait(&kv_empty[sl], ((n / L::SLOTS) & 1) ^ 1, a.status,
+                           abort_flag)) {
+              ok = false;
+              break;
+            }
+            uint8_t* dst = smem + L::KV_OFF + sl * L::KV_BYTES;
+            mbar_arrive_expect_tx(&kv_full[sl], L::KV_BYTES);
+            for (int at = 0; at < L::ATOMS; ++at)
+              tma_load_2d(dst + at * (AN * 128), &tmKV, &kv_full[sl],
+                          col[kv] + at * 64, it.a0 + j * AN);
           }
-          uint8_t* base = smem + L::KV_OFF + st * L::STAGE;
-          mbar_arrive_expect_tx(&kv_full[st], L::STAGE);
-          for (int at = 0; at < L::ATOMS; ++at) {
-            tma_load_2d(base + at * (AN * 128), &tmKV, &kv_full[st], kcol + at * 64,
-                        it.a0 + j * AN);
-            tma_load_2d(base + L::KV_BYTES + at * (AN * 128), &tmKV, &kv_full[st],
-                        vcol + at * 64, it.a0 + j * AN);
-          }
-          ++issued;
         }
       }
-      (void)issued;
       if (!ok) {  // let the copies already issued land (bounded)
         volatile int own = 0;
-        const uint32_t n = kvc < (uint32_t)L::STAGES ? kvc : (uint32_t)L::STAGES;
-        for (uint32_t j = 1; j <= n; ++j) {
-          const uint32_t idx = kvc - j;
-          mbar_wait(&kv_full[idx % L::STAGES], (idx / L::STAGES) & 1, a.status, &own);
+        const uint32_t m = n < (uint32_t)L::SLOTS ? n : (uint32_t)L::SLOTS;
+        for (uint32_t j = 1; j <= m; ++j) {
+          const uint32_t idx = n - j;
+          mbar_wait(&kv_full[idx % L::SLOTS], (idx / L::SLOTS) & 1, a.status, &own);
         }
       }
     }
@@ -219,26 +218,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = idesc_bf16(AM, D) | (1u << 16);  // B MN-major
       const uint32_t q_addr = smem_u32(smem + L::Q_OFF);
       const uint32_t p_addr = smem_u32(smem + L::P_OFF);
-      const uint32_t o_tmem = tmem_base + L::O_COL;
-      uint32_t g = 0, kvc = 0, k = 0;
+      const uint32_t kv_addr = smem_u32(smem + L::KV_OFF);
+      uint32_t g = 0, n = 0, k = 0;  // tiles, K / V loads consumed, items
       bool ok = true, issued_any = false;
-      auto pv = [&](uint32_t gi, uint32_t kvi, bool first) -> bool {
-        if (!mbar_wait(p_full, gi & 1, a.status, abort_flag)) return false;
-        if (first && k > 1 && !mbar_wait(o_free, (k - 2) & 1, a.status, abort_flag))
+      // S_t(gi) = Q_t K^T with K in ring slot `sl`
+      auto mma_s = [&](int t, uint32_t gi, uint32_t sl) -> bool {
+        if (!mbar_wait(&s_free[t], (gi & 1) ^ 1, a.status, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t qa = q_addr + t * L::Q_BYTES;
+        const uint32_t ka = kv_addr + sl * L::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * (AM * 128) + (kk % 4) * 32;
+          const uint32_t koff = (kk / 4) * (AN * 128) + (kk % 4) * 32;
+          tc_mma_bf16(tmem_base + t * AN, sdesc_k128(qa + off), sdesc_k128(ka + koff),
+                      idesc_s, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[t]);
+        issued_any = true;
+        return true;
+      };
+      // O_t (+)= P V with V in ring slot `sl`
+      auto mma_pv = [&](int t, uint32_t gi, uint32_t sl, bool first) -> bool {
+        if (!mbar_wait(&p_full[t], gi & 1, a.status, abort_flag)) return false;
+        if (first && k > 1 && !mbar_wait(&o_free[t], (k - 2) & 1, a.status, abort_flag))
           return false;
         tc_fence_after();
-        const int st = kvi % L::STAGES;
-        const uint32_t v_addr =
-            smem_u32(smem + L::KV_OFF + st * L::STAGE + L::KV_BYTES);
+        const uint32_t va = kv_addr + sl * L::KV_BYTES;
+        const uint32_t o_tmem = tmem_base + 2 * AN + t * D;
 #pragma unroll
         for (int kk = 0; kk < AN / 16; ++kk) {
           const uint64_t ad = sdesc_k128(p_addr + (kk / 4) * (AM * 128) + (kk % 4) * 32);
-          const uint64_t bd = sdesc_mn128(v_addr + kk * 2048, AN * 128);
+          const uint64_t bd = sdesc_mn128(va + kk * 2048, AN * 128);
           tc_mma_bf16(o_tmem, ad, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
         }
-        tc_commit(pv_done);
-        tc_commit(&kv_empty[st]);
+        tc_commit(&pv_done[t]);
         return true;
+      };
+      auto wait_kv = [&](uint32_t idx) -> bool {
+        return mbar_wait(&kv_full[idx % L::SLOTS], (idx / L::SLOTS) & 1, a.status,
+                         abort_flag);
       };
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
         const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP);
@@ -248,39 +267,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ++k;
-        for (int j = 0; j < it.n_tiles; ++j) {
-          const int st = (kvc + j) % L::STAGES;
-          const uint32_t sb = (g + j) & 1;
-          if (!mbar_wait(&kv_full[st], ((kvc + j) / L::STAGES) & 1, a.status,
-                         abort_flag) ||
-              !mbar_wait(&s_free[sb], (((g + j) >> 1) & 1) ^ 1, a.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + L::KV_OFF + st * L::STAGE);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * (AM * 128) + (kk % 4) * 32;
-            const uint32_t koff = (kk / 4) * (AN * 128) + (kk % 4) * 32;
-            tc_mma_bf16(tmem_base + sb * AN, sdesc_k128(q_addr + off),
-                        sdesc_k128(k_addr + koff), idesc_s, kk > 0 ? 1u : 0u);
-          }
-          issued_any = true;
-          tc_commit(&s_full[sb]);
-          if (j == it.n_tiles - 1) tc_commit(q_empty);
-          if (j >= 1 && !pv(g + j - 1, kvc + j - 1, j == 1)) {
-            ok = false;
-            break;
-          }
-        }
+        const int nt = it.n_tiles;
+        // K(j) is K / V load number n + 2 j, V(j) number n + 2 j + 1
+        ok = wait_kv(n) && mma_s(0, g, n % L::SLOTS) && mma_s(1, g, n % L::SLOTS);
         if (!ok) break;
-        if (!pv(g + it.n_tiles - 1, kvc + it.n_tiles - 1, it.n_tiles == 1)) {
-          ok = false;
-          break;
+        tc_commit(&kv_empty[n % L::SLOTS]);  // K(0) no longer needed
+        if (nt == 1) tc_commit(q_empty);
+        for (int j = 0; j < nt; ++j) {
+          const uint32_t kn = n + 2 * (j + 1), vn = n + 2 * j + 1;
+          const bool more = j + 1 < nt;
+          if (more && !(wait_kv(kn) && mma_s(0, g + j + 1, kn % L::SLOTS))) {
+            ok = false;
+            break;
+          }
+          if (!(wait_kv(vn) && mma_pv(0, g + j, vn % L::SLOTS, j == 0))) {
+            ok = false;
+            break;
+          }
+          if (more) {
+            if (!mma_s(1, g + j + 1, kn % L::SLOTS)) {
+              ok = false;
+              break;
+            }
+            tc_commit(&kv_empty[kn % L::SLOTS]);  // K(j+1) no longer needed
+            if (j + 2 == nt) tc_commit(q_empty);
+          }
+          if (!mma_pv(1, g + j, vn % L::SLOTS, j == 0)) {
+            ok = false;
+            break;
+          }
+          tc_commit(&kv_empty[vn % L::SLOTS]);  // V(j) no longer needed
         }
-        g += it.n_tiles;
-        kvc += it.n_tiles;
+        g += nt;
+        n += 2 * nt;
       }
       if (!ok && issued_any) {  // wait for the MMAs in flight
         volatile int own = 0;
@@ -288,69 +307,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(drain, 0, a.status, &own);
       }
     }
+    }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ------------------------------------------------------------ softmax
-    const int quad = warp & 3, half = warp >> 2;
-    const int r = quad * 32 + lane;  // row of the tile == TMEM lane
-    const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-    constexpr int HN = AN / 2, HD = D / 2;  // this thread's keys / O columns
-    uint8_t* prow = smem + L::P_OFF + half * (AM * 128) + r * 128;
+    const int t = warp >> 2;               // query tile: 0 = A, 1 = B
+    const int r = (warp & 3) * 32 + lane;  // row of the tile == TMEM lane
+    const uint32_t lane_base = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_col = t * AN, o_col = 2 * AN + t * D;
+    uint8_t* prow = smem + L::P_OFF + r * 128;
     const float scale = 1.4426950408889634f * rsqrtf((float)D);  // log2(e)/sqrt(d)
-    uint32_t g = 0, k = 0;
+    uint32_t g = 0;
     bool ok = true;
     auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
       int w_ok = 1;
       if (lane == 0) w_ok = mbar_wait(b, parity, a.status, abort_flag);
       return __shfl_sync(0xffffffffu, w_ok, 0) != 0;
     };
-    // every lane acquires: the exchanged values were written by other warps
-    auto all_wait = [&](uint64_t* b, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(b, parity, a.status, abort_flag));
-    };
     for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
       const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP);
       if (it.n_tiles == 0) continue;
-      ++k;
-      const int pos = it.q0 + (r % BP);
+      const int q0 = it.q0 + t * BP;  // first position of this tile
+      const int pos = q0 + (r % BP);
       const int head = it.h0 + r / BP;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < it.n_tiles; ++j, ++g) {
-        const uint32_t sb = g & 1;
-        if (!warp_wait(&s_full[sb], (g >> 1) & 1)) {
+        if (!warp_wait(&s_full[t], g & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float s[HN];
+        float s[AN];
 #pragma unroll
-        for (int c = 0; c < HN / 32; ++c)
-          tmem_ld32(lane_base + sb * AN + half * HN + c * 32, s + c * 32);
+        for (int c = 0; c < AN / 32; ++c) tmem_ld32(lane_base + s_col + c * 32, s + c * 32);
         tc_fence_before();
-        mbar_arrive(&s_free[sb]);
-        // causal mask (keys after the row's position), partial max of the
-        // raw scores (8 independent chains)
-        const int kb = j * AN + half * HN;
-        if (kb + HN - 1 > it.q0) {
+        mbar_arrive(&s_free[t]);
+        // causal mask (keys after the row's position), tile max of the raw
+        // scores (8 independent chains)
+        const int kb = j * AN;
+        if (kb + AN - 1 > q0) {
           const int lim = pos - kb;
 #pragma unroll
-          for (int c = 0; c < HN; ++c) s[c] = c > lim ? -INFINITY : s[c];
+          for (int c = 0; c < AN; ++c) s[c] = c > lim ? -INFINITY : s[c];
         }
         float pm[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) pm[e] = s[e];
 #pragma unroll
-        for (int c = 8; c < HN; ++c) pm[c & 7] = fmaxf(pm[c & 7], s[c]);
-        float hmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                           fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-        // swap partial maxima with the thread holding the row's other half
-        float* rm = red_max + sb * 256;
-        rm[half * 128 + r] = hmax;
-        mbar_arrive(&mx_bar[sb]);
-        if (!all_wait(&mx_bar[sb], (g >> 1) & 1)) {
-          ok = false;
-          break;
-        }
-        const float tmax = fmaxf(hmax, rm[(half ^ 1) * 128 + r]) * scale;
+        for (int c = 8; c < AN; ++c) pm[c & 7] = fmaxf(pm[c & 7], s[c]);
+        const float tmax =
+            fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                  fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale;
         float alpha = 1.f;
         bool rescale = false;
         if (j == 0) {
@@ -365,62 +372,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         // p = 2^(s * scale - m), 8 independent partial sums
         float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < HN; ++c) {
+        for (int c = 0; c < AN; ++c) {
           s[c] = ex2(fmaf(s[c], scale, -mref));
           ps[c & 7] += s[c];
         }
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-        // the P buffer and O are free once P V of the previous tile is done
-        if (j > 0) {
-          if (!warp_wait(pv_done, (g - 1) & 1)) {
+        // The shared P buffer is free once the P V before ours is done:
+        // tile A of step g follows P V_B of step g - 1, tile B follows
+        // P V_A of step g.  Either also means our own previous P V is done,
+        // so O can be rescaled.
+        if (t == 1 || g > 0) {
+          if (!warp_wait(&pv_done[t ^ 1], t == 1 ? (g & 1) : ((g - 1) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, rescale)) {
+        }
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-            for (int c = 0; c < HD / 32; ++c) {
-              float o[32];
-              const uint32_t t = lane_base + L::O_COL + half * HD + c * 32;
-              tmem_ld32(t, o);
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            const uint32_t ta = lane_base + o_col + c * 32;
+            tmem_ld32(ta, o);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] *= alpha;
-              tmem_st32(t, o);
-            }
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(ta, o);
           }
         }
-        // this thread's 64 keys of P as bf16: one 128-byte swizzle atom row
+        // P as bf16 into the 128-byte swizzled A tile
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
+        for (int c16 = 0; c16 < AN / 8; ++c16) {
           uint4 u;
-          u.x = pack_bf16x2(s[cc * 8 + 0], s[cc * 8 + 1]);
-          u.y = pack_bf16x2(s[cc * 8 + 2], s[cc * 8 + 3]);
-          u.z = pack_bf16x2(s[cc * 8 + 4], s[cc * 8 + 5]);
-          u.w = pack_bf16x2(s[cc * 8 + 6], s[cc * 8 + 7]);
-          *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = u;
+          u.x = pack_bf16x2(s[c16 * 8 + 0], s[c16 * 8 + 1]);
+          u.y = pack_bf16x2(s[c16 * 8 + 2], s[c16 * 8 + 3]);
+          u.z = pack_bf16x2(s[c16 * 8 + 4], s[c16 * 8 + 5]);
+          u.w = pack_bf16x2(s[c16 * 8 + 6], s[c16 * 8 + 7]);
+          const int atom = c16 / 8, cc = c16 % 8;
+          *reinterpret_cast<uint4*>(prow + atom * (AM * 128) + ((cc ^ (r & 7)) << 4)) = u;
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(p_full);
+        mbar_arrive(&p_full[t]);
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, rows inside the sequence only
-      red_l[half * 128 + r] = l;
-      mbar_arrive(l_bar);
-      if (!all_wait(l_bar, (k - 1) & 1) || !warp_wait(pv_done, (g - 1) & 1)) {
+      if (!warp_wait(&pv_done[t], (g - 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float lsum = l + red_l[(half ^ 1) * 128 + r];
       const bool valid = pos < it.L;
-      const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
-      bf16* out = a.out + (size_t)(it.a0 + (valid ? pos : 0)) * a.n_heads * D +
-                  head * D + half * HD;
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      bf16* out = a.out + (size_t)(it.a0 + (valid ? pos : 0)) * a.n_heads * D + head * D;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         float o[32];
-        tmem_ld32(lane_base + L::O_COL + half * HD + c * 32, o);
+        tmem_ld32(lane_base + o_col + c * 32, o);
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
 #pragma unroll
@@ -435,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(o_free);
+      mbar_arrive(&o_free[t]);
     }
   }
 
@@ -462,7 +469,7 @@ cudaError_t launch(const AttnArgs& a, int n_seq, int max_len, int sm_count,
   if (!tc_encode_bf16(&tq, a.qkv, a.tokens, a.nqkv, BP) ||
       !tc_encode_bf16(&tkv, a.qkv, a.tokens, a.nqkv, AN))
     return cudaErrorInvalidValue;
-  const int n_qb = (max_len + BP - 1) / BP;
+  const int n_qb = (max_len + 2 * BP - 1) / (2 * BP);
   const int n_hg = a.n_heads / a.hpc;
   const long long items = (long long)n_qb * n_hg * n_seq;
   if (items <= 0) return cudaSuccess;
