@@ -2,7 +2,8 @@
 // ("模型层" 9.3 CausalSelfAttention; "parallel_attention.py" 2 step 4 and 3
 // flash_attn_varlen_func): o = softmax(q k^T / sqrt(d) + causal mask) v within
 // each sequence, query head h reading kv head h / n_rep.  q and k arrive
-// already rotated by the QKV GEMM epilogue.
+// already rotated by the QKV GEMM epilogue; q, k, v, P and the output are
+// fp16 (fp16 x fp16 -> fp32 on the tensor cores).
 //
 // tcgen05 / TMEM flash attention, persistent (one CTA per SM), 12 warps.  A
 // work item is two query tiles A and B of 128 rows each: `hpc` query heads of
@@ -12,9 +13,9 @@
 //   warps 0..3  softmax of tile A, warps 4..7 softmax of tile B: thread r of
 //               a warpgroup owns query row r (TMEM lane r).  Per K / V tile
 //               it loads its S row, masks, keeps the running max m and sum l,
-//               and writes P = 2^(s - m) as bf16 into the 128-byte swizzled
+//               and writes P = 2^(s - m) as fp16 into the 128-byte swizzled
 //               P tile (the A operand of P V); at the end it reads its O row,
-//               divides by l and stores bf16.
+//               divides by l and stores fp16.
 //   warp 8      TMA producer: the two Q tiles once per item, then K(j), V(j)
 //               into a ring of single-tile slots.
 //   warp 9      one thread issues tcgen05.mma in the order
@@ -22,7 +23,7 @@
 //               tile's TMEM S buffer, O += P V into its TMEM O buffer (V read
 //               as an MN-major operand straight from its TMA tile).  While one
 //               warpgroup computes its softmax the tensor core works on the
-//               other's products; the two share one P buffer, written in turn.
+//               other's products (P buffers: see AttnLayout).
 // Rescaling of O is lazy: a row's reference max only moves (and O is
 // rescaled in TMEM) when the new max exceeds it by more than 8 in the log2
 // domain, so P stays <= 2^8.  Items run longest causal range first.  Every
@@ -39,7 +40,6 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 constexpr int AM = 128;  // query rows per tile (MMA M)
-constexpr int AN = 128;  // keys per K / V tile
 constexpr float kRescaleLog2 = 8.0f;
 // 12 warps = 3 warpgroups: the register file is shared out per warpgroup,
 // so the block launches at 168 registers a thread (384 x 168 = 64512) and
@@ -52,19 +52,29 @@ constexpr int kSoftmaxRegs = 200, kControlRegs = 104;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168,
               "register split exceeds the launch allocation");
 
+// Shared memory, 224 KB either way: two query tiles, the P tiles and 8
+// (head_dim 64) or 4 (head_dim 128) single-tile K / V slots.  For head_dim 64
+// each query tile has its own P tile (SEP_P): a warpgroup then only waits for
+// its own previous P V.  For head_dim 128 the two query tiles share one P
+// tile, written in turn (tile A of step j after P V_B of step j - 1, tile B
+// after P V_A of step j), which keeps room for 4 slots of 32 KB.
 template <int D>
 struct AttnLayout {
+  static constexpr int AN = 128;                    // keys per K / V tile
+  static constexpr bool SEP_P = D == 64;
   static constexpr int ATOMS = D / 64;  // 128-byte swizzle atoms per row
   static constexpr uint32_t Q_BYTES = AM * D * 2;   // one query tile
   static constexpr uint32_t KV_BYTES = AN * D * 2;  // one K or V tile (a slot)
-  static constexpr uint32_t P_BYTES = AM * AN * 2;
+  static constexpr uint32_t P_BYTES = AM * AN * 2;  // one P tile
   static constexpr int SLOTS = D == 64 ? 8 : 4;
   static constexpr uint32_t Q_OFF = 0;              // Q_A, Q_B
   static constexpr uint32_t P_OFF = Q_OFF + 2 * Q_BYTES;
-  static constexpr uint32_t KV_OFF = P_OFF + P_BYTES;
+  static constexpr uint32_t KV_OFF = P_OFF + (SEP_P ? 2 : 1) * P_BYTES;
   static constexpr uint32_t BAR_OFF = KV_OFF + SLOTS * KV_BYTES;
   static constexpr uint32_t TOTAL = BAR_OFF + 512 + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;  // S_A S_B [0,256), O_A O_B [256, 256+2D)
+  // S_A [0, AN), S_B [AN, 2 AN), O_A [2 AN, 2 AN + D), O_B [2 AN + D, 2 AN + 2 D)
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(2 * AN + 2 * D <= (int)TMEM_COLS, "tensor memory budget");
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
 
@@ -76,7 +86,7 @@ struct Item {
 // Work item i: query block from the top (longest causal range first), then
 // head group, then sequence.  A block is 2 BP positions.
 __device__ __forceinline__ Item get_item(const AttnArgs& a, int i, int n_hg,
-                                         int n_seq, int n_qb, int BP) {
+                                         int n_seq, int n_qb, int BP, int AN) {
   Item it;
   const int per_qb = n_hg * n_seq;
   const int qb = n_qb - 1 - i / per_qb;
@@ -108,12 +118,38 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (a0, a1) * (b, b) + (c, c) on the paired fp32 pipe.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float b, float c) {
+  uint64_t x, y, z;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(b));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(z) : "f"(c));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x) : "l"(x), "l"(y), "l"(z));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(x));
+}
+
+// (s0, s1) += (a0, a1)
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+  uint64_t x, y;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(a0), "f"(a1));
+  asm("add.f32x2 %0, %1, %2;" : "=l"(x) : "l"(x), "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(x));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmKV, AttnArgs a,
                    int n_items, int n_hg, int n_seq, int n_qb) {
   using L = AttnLayout<D>;
+  constexpr int AN = L::AN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -169,9 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t n = 0, k = 0;  // K / V tiles loaded, items started
       bool ok = true;
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
-        const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP);
+        const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP, L::AN);
         if (it.n_tiles == 0) continue;
-        if (k > 0 && !mbar_wait(q_empty, (k - 1) & 1, a.status, abort_flag)) {
+        if (k > 0 && !mbar_wait_sleep(q_empty, (k - 1) & 1, a.status, abort_flag)) {
           ok = false;
           break;
         }
@@ -189,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j < it.n_tiles; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++n) {  // K(j), then V(j)
             const int sl = n % L::SLOTS;
-            if (!mbar_wait(&kv_empty[sl], ((n / L::SLOTS) & 1) ^ 1, a.status,
+            if (!mbar_wait_sleep(&kv_empty[sl], ((n / L::SLOTS) & 1) ^ 1, a.status,
                            abort_flag)) {
               ok = false;
               break;
@@ -207,105 +243,111 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t m = n < (uint32_t)L::SLOTS ? n : (uint32_t)L::SLOTS;
         for (uint32_t j = 1; j <= m; ++j) {
           const uint32_t idx = n - j;
-          mbar_wait(&kv_full[idx % L::SLOTS], (idx / L::SLOTS) & 1, a.status, &own);
+          mbar_wait_sleep(&kv_full[idx % L::SLOTS], (idx / L::SLOTS) & 1, a.status, &own);
         }
       }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(AM, AN);
-      constexpr uint32_t idesc_pv = idesc_bf16(AM, D) | (1u << 16);  // B MN-major
-      const uint32_t q_addr = smem_u32(smem + L::Q_OFF);
-      const uint32_t p_addr = smem_u32(smem + L::P_OFF);
-      const uint32_t kv_addr = smem_u32(smem + L::KV_OFF);
-      uint32_t g = 0, n = 0, k = 0;  // tiles, K / V loads consumed, items
-      bool ok = true, issued_any = false;
-      // S_t(gi) = Q_t K^T with K in ring slot `sl`
-      auto mma_s = [&](int t, uint32_t gi, uint32_t sl) -> bool {
-        if (!mbar_wait(&s_free[t], (gi & 1) ^ 1, a.status, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t qa = q_addr + t * L::Q_BYTES;
-        const uint32_t ka = kv_addr + sl * L::KV_BYTES;
+    // The whole warp runs the loop (its values stay warp-uniform); one
+    // elected lane issues each MMA / commit.
+    constexpr uint32_t idesc_s = idesc_f16(AM, AN);
+    constexpr uint32_t idesc_pv = idesc_f16(AM, D) | (1u << 16);  // B MN-major
+    // descriptor bases; a K step adds its byte offset >> 4 to the address
+    const uint64_t q_desc = sdesc_k128(smem_u32(smem + L::Q_OFF));
+    const uint64_t p_desc = sdesc_k128(smem_u32(smem + L::P_OFF));
+    const uint64_t k_desc = sdesc_k128(smem_u32(smem + L::KV_OFF));
+    const uint64_t v_desc = sdesc_mn128(smem_u32(smem + L::KV_OFF), AN * 128);
+    constexpr uint32_t SLOT16 = L::KV_BYTES >> 4, Q16 = L::Q_BYTES >> 4;
+    auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait_sleep(b, parity, a.status, abort_flag));
+    };
+    uint32_t g = 0, n = 0, k = 0;  // tiles, K / V loads consumed, items
+    bool ok = true, issued_any = false;
+    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+      const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP, L::AN);
+      if (it.n_tiles == 0) continue;
+      if (!wait_all(q_full, k & 1)) {
+        ok = false;
+        break;
+      }
+      ++k;
+      const int nt = it.n_tiles;
+      // K(j) is K / V load number n + 2 j, V(j) number n + 2 j + 1.
+      // Issue order: S_A(0) S_B(0), then per j: S_A(j+1) PV_A(j) S_B(j+1) PV_B(j).
+      for (int step = -1; step < 2 * nt && ok; ++step) {
+        // step -1: S_A(0), S_B(0); step 2j: S_A(j+1), PV_A(j);
+        // step 2j+1: S_B(j+1), PV_B(j)
+        const int j = step < 0 ? -1 : step >> 1;
+        const int tt = step < 0 ? 0 : step & 1;
+        for (int t = 0; t < 2; ++t) {
+          if (step >= 0 && t != tt) continue;
+          const int js = j + 1;  // tile of the S product
+          if (js >= nt) break;
+          const uint32_t kn = n + 2 * js;
+          if (t == 0 && !wait_all(&kv_full[kn % L::SLOTS], (kn / L::SLOTS) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t gs = g + js;
+          if (!wait_all(&s_free[t], (gs & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t qd = q_desc + t * Q16;
+          const uint64_t kd = k_desc + (kn % L::SLOTS) * SLOT16;
+          const uint32_t d_tmem = tmem_base + t * AN;
+          if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * (AM * 128) + (kk % 4) * 32;
-          const uint32_t koff = (kk / 4) * (AN * 128) + (kk % 4) * 32;
-          tc_mma_bf16(tmem_base + t * AN, sdesc_k128(qa + off), sdesc_k128(ka + koff),
-                      idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t qo = ((kk / 4) * (AM * 128) + (kk % 4) * 32) >> 4;
+              const uint32_t ko = ((kk / 4) * (AN * 128) + (kk % 4) * 32) >> 4;
+              tc_mma_bf16_nc(d_tmem, qd + qo, kd + ko, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(&s_full[t]);
+            if (t == 1) {
+              tc_commit(&kv_empty[kn % L::SLOTS]);  // K(js) no longer needed
+              if (js == nt - 1) tc_commit(q_empty);
+            }
+          }
+          __syncwarp();
+          issued_any = true;
         }
-        tc_commit(&s_full[t]);
-        issued_any = true;
-        return true;
-      };
-      // O_t (+)= P V with V in ring slot `sl`
-      auto mma_pv = [&](int t, uint32_t gi, uint32_t sl, bool first) -> bool {
-        if (!mbar_wait(&p_full[t], gi & 1, a.status, abort_flag)) return false;
-        if (first && k > 1 && !mbar_wait(&o_free[t], (k - 2) & 1, a.status, abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t va = kv_addr + sl * L::KV_BYTES;
-        const uint32_t o_tmem = tmem_base + 2 * AN + t * D;
-#pragma unroll
-        for (int kk = 0; kk < AN / 16; ++kk) {
-          const uint64_t ad = sdesc_k128(p_addr + (kk / 4) * (AM * 128) + (kk % 4) * 32);
-          const uint64_t bd = sdesc_mn128(va + kk * 2048, AN * 128);
-          tc_mma_bf16(o_tmem, ad, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(&pv_done[t]);
-        return true;
-      };
-      auto wait_kv = [&](uint32_t idx) -> bool {
-        return mbar_wait(&kv_full[idx % L::SLOTS], (idx / L::SLOTS) & 1, a.status,
-                         abort_flag);
-      };
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
-        const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP);
-        if (it.n_tiles == 0) continue;
-        if (!mbar_wait(q_full, k & 1, a.status, abort_flag)) {
+        if (!ok || step < 0) continue;
+        // PV_tt(j)
+        const uint32_t vn = n + 2 * j + 1, gp = g + j;
+        const bool first = j == 0;
+        if ((tt == 0 && !wait_all(&kv_full[vn % L::SLOTS], (vn / L::SLOTS) & 1)) ||
+            !wait_all(&p_full[tt], gp & 1) ||
+            (first && k > 1 && !wait_all(&o_free[tt], (k - 2) & 1))) {
           ok = false;
           break;
         }
-        ++k;
-        const int nt = it.n_tiles;
-        // K(j) is K / V load number n + 2 j, V(j) number n + 2 j + 1
-        ok = wait_kv(n) && mma_s(0, g, n % L::SLOTS) && mma_s(1, g, n % L::SLOTS);
-        if (!ok) break;
-        tc_commit(&kv_empty[n % L::SLOTS]);  // K(0) no longer needed
-        if (nt == 1) tc_commit(q_empty);
-        for (int j = 0; j < nt; ++j) {
-          const uint32_t kn = n + 2 * (j + 1), vn = n + 2 * j + 1;
-          const bool more = j + 1 < nt;
-          if (more && !(wait_kv(kn) && mma_s(0, g + j + 1, kn % L::SLOTS))) {
-            ok = false;
-            break;
+        tc_fence_after();
+        const uint64_t vd = v_desc + (vn % L::SLOTS) * SLOT16;
+        const uint64_t pd = p_desc + (L::SEP_P ? tt * (L::P_BYTES >> 4) : 0);
+        const uint32_t o_tmem = tmem_base + 2 * AN + tt * D;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < AN / 16; ++kk) {
+            const uint32_t po = ((kk / 4) * (AM * 128) + (kk % 4) * 32) >> 4;
+            tc_mma_bf16_nc(o_tmem, pd + po, vd + kk * (2048 >> 4), idesc_pv,
+                           (!first || kk > 0) ? 1u : 0u);
           }
-          if (!(wait_kv(vn) && mma_pv(0, g + j, vn % L::SLOTS, j == 0))) {
-            ok = false;
-            break;
-          }
-          if (more) {
-            if (!mma_s(1, g + j + 1, kn % L::SLOTS)) {
-              ok = false;
-              break;
-            }
-            tc_commit(&kv_empty[kn % L::SLOTS]);  // K(j+1) no longer needed
-            if (j + 2 == nt) tc_commit(q_empty);
-          }
-          if (!mma_pv(1, g + j, vn % L::SLOTS, j == 0)) {
-            ok = false;
-            break;
-          }
-          tc_commit(&kv_empty[vn % L::SLOTS]);  // V(j) no longer needed
+          tc_commit(&pv_done[tt]);
+          if (tt == 1) tc_commit(&kv_empty[vn % L::SLOTS]);  // V(j) no longer needed
         }
-        g += nt;
-        n += 2 * nt;
+        __syncwarp();
       }
-      if (!ok && issued_any) {  // wait for the MMAs in flight
-        volatile int own = 0;
-        tc_commit(drain);
-        mbar_wait(drain, 0, a.status, &own);
-      }
+      g += nt;
+      n += 2 * nt;
+    }
+    if (!ok && issued_any) {  // wait for the MMAs in flight
+      volatile int own = 0;
+      if (elect_one()) tc_commit(drain);
+      __syncwarp();
+      mbar_wait_sleep(drain, 0, a.status, &own);
     }
     }
   } else {
@@ -315,17 +357,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;  // row of the tile == TMEM lane
     const uint32_t lane_base = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = t * AN, o_col = 2 * AN + t * D;
-    uint8_t* prow = smem + L::P_OFF + r * 128;
+    uint8_t* prow = smem + L::P_OFF + (L::SEP_P ? t * L::P_BYTES : 0) + r * 128;
     const float scale = 1.4426950408889634f * rsqrtf((float)D);  // log2(e)/sqrt(d)
     uint32_t g = 0;
     bool ok = true;
     auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
       int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait(b, parity, a.status, abort_flag);
+      if (lane == 0) w_ok = mbar_wait_sleep(b, parity, a.status, abort_flag);
       return __shfl_sync(0xffffffffu, w_ok, 0) != 0;
     };
     for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
-      const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP);
+      const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP, L::AN);
       if (it.n_tiles == 0) continue;
       const int q0 = it.q0 + t * BP;  // first position of this tile
       const int pos = q0 + (r % BP);
@@ -339,7 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         float s[AN];
 #pragma unroll
-        for (int c = 0; c < AN / 32; ++c) tmem_ld32(lane_base + s_col + c * 32, s + c * 32);
+        for (int c = 0; c < AN / 32; ++c)
+          tmem_ld32_nowait(lane_base + s_col + c * 32, s + c * 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < AN; ++c) tmem_pin(s[c]);
         tc_fence_before();
         mbar_arrive(&s_free[t]);
         // causal mask (keys after the row's position), tile max of the raw
@@ -352,12 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float pm[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) pm[e] = s[e];
+        for (int e = 0; e < 8; ++e) pm[e] = fmaxf(s[e], s[e + 8]);
 #pragma unroll
-        for (int c = 8; c < AN; ++c) pm[c & 7] = fmaxf(pm[c & 7], s[c]);
+        for (int c = 16; c < AN; c += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) pm[e] = max3(pm[e], s[c + e], s[c + 8 + e]);
         const float tmax =
-            fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                  fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale;
+            max3(max3(pm[0], pm[1], pm[2]), max3(pm[3], pm[4], pm[5]),
+                 fmaxf(pm[6], pm[7])) * scale;
         float alpha = 1.f;
         bool rescale = false;
         if (j == 0) {
@@ -369,24 +417,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
         }
         const float mref = m == -INFINITY ? 0.f : m;
-        // p = 2^(s * scale - m), 8 independent partial sums
+        // p = 2^(s * scale - m) (paired fp32 FMA), 8 independent partial sums
         float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < AN; ++c) {
-          s[c] = ex2(fmaf(s[c], scale, -mref));
-          ps[c & 7] += s[c];
+        for (int c = 0; c < AN; c += 2) {
+          fma2(s[c], s[c + 1], scale, -mref);
+          s[c] = ex2(s[c]);
+          s[c + 1] = ex2(s[c + 1]);
+          add2(ps[c & 7], ps[(c & 7) + 1], s[c], s[c + 1]);
         }
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-        // The shared P buffer is free once the P V before ours is done:
-        // tile A of step g follows P V_B of step g - 1, tile B follows
-        // P V_A of step g.  Either also means our own previous P V is done,
-        // so O can be rescaled.
-        if (t == 1 || g > 0) {
-          if (!warp_wait(&pv_done[t ^ 1], t == 1 ? (g & 1) : ((g - 1) & 1))) {
-            ok = false;
-            break;
+        if constexpr (L::SEP_P) {
+          // This tile's P buffer and O are free once its previous P V is
+          // done (for the first tile of an item the epilogue already waited).
+          if (j > 0) {
+            if (!warp_wait(&pv_done[t], (g - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
-          tc_fence_after();
+        } else {
+          // The shared P buffer is free once the P V before ours is done:
+          // tile A of step g follows P V_B of step g - 1, tile B follows P
+          // V_A of step g.  Either also means our own previous P V is done,
+          // so O can be rescaled.
+          if (t == 1 || g > 0) {
+            if (!warp_wait(&pv_done[t ^ 1], t == 1 ? (g & 1) : ((g - 1) & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
         }
         if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
@@ -399,14 +461,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(ta, o);
           }
         }
-        // P as bf16 into the 128-byte swizzled A tile
+        // P as fp16 into the 128-byte swizzled A tile
 #pragma unroll
         for (int c16 = 0; c16 < AN / 8; ++c16) {
           uint4 u;
-          u.x = pack_bf16x2(s[c16 * 8 + 0], s[c16 * 8 + 1]);
-          u.y = pack_bf16x2(s[c16 * 8 + 2], s[c16 * 8 + 3]);
-          u.z = pack_bf16x2(s[c16 * 8 + 4], s[c16 * 8 + 5]);
-          u.w = pack_bf16x2(s[c16 * 8 + 6], s[c16 * 8 + 7]);
+          u.x = pack_f16x2(s[c16 * 8 + 0], s[c16 * 8 + 1]);
+          u.y = pack_f16x2(s[c16 * 8 + 2], s[c16 * 8 + 3]);
+          u.z = pack_f16x2(s[c16 * 8 + 4], s[c16 * 8 + 5]);
+          u.w = pack_f16x2(s[c16 * 8 + 6], s[c16 * 8 + 7]);
           const int atom = c16 / 8, cc = c16 % 8;
           *reinterpret_cast<uint4*>(prow + atom * (AM * 128) + ((cc ^ (r & 7)) << 4)) = u;
         }
@@ -415,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&p_full[t]);
       }
       if (!ok) break;
-      // ---- epilogue: O / l -> bf16, rows inside the sequence only
+      // ---- epilogue: O / l -> fp16, rows inside the sequence only
       if (!warp_wait(&pv_done[t], (g - 1) & 1)) {
         ok = false;
         break;
@@ -423,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool valid = pos < it.L;
       const float inv = l > 0.f ? 1.0f / l : 0.f;
-      bf16* out = a.out + (size_t)(it.a0 + (valid ? pos : 0)) * a.n_heads * D + head * D;
+      __half* out = a.out + (size_t)(it.a0 + (valid ? pos : 0)) * a.n_heads * D + head * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
@@ -433,10 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 u;
-            u.x = pack_bf16x2(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
-            u.y = pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
-            u.z = pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
-            u.w = pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+            u.x = pack_f16x2(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
+            u.y = pack_f16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+            u.z = pack_f16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+            u.w = pack_f16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
             dst[q] = u;
           }
         }
@@ -464,6 +526,7 @@ template <int D>
 cudaError_t launch(const AttnArgs& a, int n_seq, int max_len, int sm_count,
                    cudaStream_t s) {
   using L = AttnLayout<D>;
+  constexpr int AN = L::AN;
   const int BP = AM / a.hpc;
   CUtensorMap tq, tkv;
   if (!tc_encode_bf16(&tq, a.qkv, a.tokens, a.nqkv, BP) ||

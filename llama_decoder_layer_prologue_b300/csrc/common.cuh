@@ -5,6 +5,7 @@
 
 #include <cuda.h>  // CUtensorMap (type only; the driver entry is looked up)
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -31,6 +32,15 @@ struct Elem<float> {
   static __device__ __forceinline__ void store(float* p, float v) { *p = v; }
 };
 template <>
+struct Elem<__half> {
+  static __device__ __forceinline__ float load(const __half* p) {
+    return __half2float(*p);
+  }
+  static __device__ __forceinline__ void store(__half* p, float v) {
+    *p = __float2half_rn(v);
+  }
+};
+template <>
 struct Elem<__nv_bfloat16> {
   static __device__ __forceinline__ float load(const __nv_bfloat16* p) {
     return __bfloat162float(*p);
@@ -43,6 +53,16 @@ struct Elem<__nv_bfloat16> {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
+  __half2 v = *reinterpret_cast<__half2*>(&u);
+  return __half22float2(v);
 }
 
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
@@ -109,6 +129,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread (instead of spinning) for up to about
+// `hint_ns` while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], "
+      "%2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Default limit of a bounded wait: 2 s of wall time.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -130,6 +164,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
         *abort_flag = 1;
         return false;
       }
+    }
+  }
+}
+
+// The same bounded wait, but a waiting thread is suspended in hardware (up
+// to ~20 us per try) instead of spinning: for waits that share their SM
+// sub-partition with busy compute warps.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                int* status,
+                                                volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      set_status(status, ST_TIMEOUT);
+      *abort_flag = 1;
+      return false;
     }
   }
 }
@@ -203,6 +256,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
          ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with fp16 A and B (format 0): fp16 x fp16 -> fp32.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -240,6 +298,28 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc,
       : "memory");
 }
 
+// The same MMA without a memory clobber: for issue loops whose ordering
+// against other asm volatile statements (waits, fences, commits) is all that
+// matters, so that the compiler keeps loop state in registers.
+__device__ __forceinline__ void tc_mma_bf16_nc(uint32_t d_tmem, uint64_t adesc,
+                                               uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// True in exactly one lane of the (fully active) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
@@ -268,6 +348,34 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+
+// tcgen05.ld of 32 columns without the wait: call tmem_wait_ld() before
+// using any of v, then tmem_pin() on every value read (keeps the uses after
+// the wait).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, "
+      "%8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, "
+      "%23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]),
+        "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// An empty volatile asm that "rewrites" x: uses of x cannot move above it.
+__device__ __forceinline__ void tmem_pin(float& x) { asm volatile("" : "+f"(x)); }
 
 // Each thread of the warp writes 32 consecutive fp32 columns of its TMEM
 // lane, then waits for the stores to land.

@@ -8,6 +8,7 @@
 
 #include "common.cuh"
 #include "decode.cuh"
+#include "kernels.h"
 
 namespace llama {
 namespace {
@@ -110,7 +111,8 @@ __global__ void __launch_bounds__(FT) finalize_o_kernel(DecodeArgs a,
     const int b = b0 + j, n = t * 128 + r;
     const float h = __bfloat162float(a.x[(size_t)b * H + n]) + s[r * FS + j];
     a.h32[(size_t)b * H + n] = h;
-    a.hg[(size_t)b * H + n] = __float2bfloat16_rn(h * __bfloat162float(a.g_post[n]));
+    a.hg[(size_t)b * H + n] =
+        __float2half_rn(h * __bfloat162float(a.g_post[n]) * kHgScale);
     const float ss = warp_sum(h * h);
     if ((threadIdx.x & 31) == 0) atomicAdd(a.ss2 + b, ss);
   }
@@ -132,10 +134,10 @@ __global__ void __launch_bounds__(FT) finalize_gu_kernel(DecodeArgs a,
     const int r = e & 127, j = e >> 7;
     if (j >= nb) continue;
     const int b = b0 + j;
-    const float r2 = rsqrtf(a.ss2[b] * inv_h + a.eps);
+    const float r2 = rsqrtf(a.ss2[b] * inv_h + a.eps) / kHgScale;
     const float g = r2 * sg[r * FS + j], u = r2 * su[r * FS + j];
     a.act[(size_t)b * a.inter + k * 128 + r] =
-        __float2bfloat16_rn(g / (1.0f + __expf(-g)) * u);
+        __float2half_rn(g / (1.0f + __expf(-g)) * u * kActScale);
   }
 }
 
@@ -152,8 +154,8 @@ __global__ void __launch_bounds__(FT) finalize_down_kernel(DecodeArgs a,
     const int r = e & 127, j = e >> 7;
     if (j >= nb) continue;
     const int b = b0 + j, n = t * 128 + r;
-    a.out[(size_t)b * H + n] =
-        __float2bfloat16_rn(a.h32[(size_t)b * H + n] + s[r * FS + j]);
+    a.out[(size_t)b * H + n] = __float2bfloat16_rn(
+        fmaf(s[r * FS + j], 1.0f / kActScale, a.h32[(size_t)b * H + n]));
   }
 }
 
@@ -352,10 +354,10 @@ __global__ void attn_combine_kernel(DecodeArgs a) {
   const int D = a.head_dim;
   const int n_rep = a.n_heads / a.n_kv_heads;
   const int g = h / n_rep, row = h % n_rep;
-  bf16* o = a.attn + (size_t)b * a.n_heads * D + h * D;
+  __half* o = a.attn + (size_t)b * a.n_heads * D + h * D;
   const int sp = a.start_pos[b];
   if (!start_ok(sp, a)) {
-    for (int i = threadIdx.x; i < D; i += blockDim.x) o[i] = __float2bfloat16_rn(0.f);
+    for (int i = threadIdx.x; i < D; i += blockDim.x) o[i] = __float2half_rn(0.f);
     return;
   }
   const int nc = (sp + 1 + KS - 1) / KS;
@@ -372,7 +374,7 @@ __global__ void attn_combine_kernel(DecodeArgs a) {
       num += w * rec[row * D + i];
       den += w * rec[n_rep * D + n_rep + row];
     }
-    o[i] = __float2bfloat16_rn(num / den);
+    o[i] = __float2half_rn(num / den);
   }
 }
 

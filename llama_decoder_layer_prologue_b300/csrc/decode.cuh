@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,13 +25,13 @@ struct DecodeArgs {
   const float *cos_t, *sin_t;
   __nv_bfloat16* qkv;      // [B, nqkv]
   __nv_bfloat16 *cache_k, *cache_v;  // [B, max_seq, Hkv, D]
-  __nv_bfloat16* attn;     // [B, Hq * D]
+  __half* attn;            // [B, Hq * D] fp16
   float* attn_part;        // split-KV records
   int max_chunks, n_rep_rec;
   float* h32;              // [B, H] h in fp32
-  __nv_bfloat16* hg;       // [B, H] bf16(h * g_post), operand of gate_up
+  __half* hg;              // [B, H] fp16(h * g_post * kHgScale), gate_up operand
   const __nv_bfloat16* g_post;  // [H] RMSNorm weight of the MLP
-  __nv_bfloat16* act;      // [B, I]
+  __half* act;             // [B, I] fp16(act * kActScale)
   __nv_bfloat16* out;      // [B, H]
   int* status;
 };

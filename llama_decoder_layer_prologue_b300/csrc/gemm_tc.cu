@@ -76,6 +76,28 @@ __device__ __forceinline__ void store_bf16x32(void* p, const float* v) {
   }
 }
 
+__device__ __forceinline__ void store_f16x32(void* p, const float* v) {
+  uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u;
+    u.x = pack_f16x2(v[8 * i + 0], v[8 * i + 1]);
+    u.y = pack_f16x2(v[8 * i + 2], v[8 * i + 3]);
+    u.z = pack_f16x2(v[8 * i + 4], v[8 * i + 5]);
+    u.w = pack_f16x2(v[8 * i + 6], v[8 * i + 7]);
+    q[i] = u;
+  }
+}
+
+// bf16 or fp16 (16-bit elements) at element offset `off` of p.
+__device__ __forceinline__ void store_16x32(void* p, size_t off, const float* v,
+                                            bool f16) {
+  if (f16)
+    store_f16x32(static_cast<__half*>(p) + off, v);
+  else
+    store_bf16x32(static_cast<__nv_bfloat16*>(p) + off, v);
+}
+
 __device__ __forceinline__ void store_f32x32(float* p, const float* v) {
   float4* q = reinterpret_cast<float4*>(p);
 #pragma unroll
@@ -109,17 +131,20 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
           store_f32x32(static_cast<float*>(ep.out) + off, v);
           load_bf16x32(static_cast<const __nv_bfloat16*>(ep.colscale) + col, r);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] *= v[j];
-          store_bf16x32(static_cast<__nv_bfloat16*>(ep.out2) + off, r);
+          for (int j = 0; j < 32; ++j) r[j] *= v[j] * ep.out_scale;
+          store_16x32(ep.out2, off, r, ep.out_f16);
         } else {
           if constexpr (EPI == TC_RESID) {
             const float4* r4 =
                 reinterpret_cast<const float4*>(static_cast<const float*>(ep.residual) + off);
+            const float sc = ep.in_scale;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               float4 rr = r4[q];
-              v[4 * q] += rr.x; v[4 * q + 1] += rr.y;
-              v[4 * q + 2] += rr.z; v[4 * q + 3] += rr.w;
+              v[4 * q] = fmaf(sc, v[4 * q], rr.x);
+              v[4 * q + 1] = fmaf(sc, v[4 * q + 1], rr.y);
+              v[4 * q + 2] = fmaf(sc, v[4 * q + 2], rr.z);
+              v[4 * q + 3] = fmaf(sc, v[4 * q + 3], rr.w);
             }
           }
           store_bf16x32(static_cast<__nv_bfloat16*>(ep.out) + off, v);
@@ -176,16 +201,16 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
               x2[j] *= rs;
             }
           }
-          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(ep.out) +
-                             (size_t)row * ep.ldo + hc + c;
-          store_bf16x32(o, x1);
-          store_bf16x32(o + half, x2);
+          const size_t o = (size_t)row * ep.ldo + hc + c;
+          store_16x32(ep.out, o, x1, ep.out_f16);
+          store_16x32(ep.out, o + half, x2, ep.out_f16);
         }
       }
     }
   } else if constexpr (EPI == TC_SWIGLU) {
     static_assert(BN == 256, "gate/up interleave is 128 + 128");
-    float r2 = valid ? rsqrtf(ep.ss_in[row] * ep.inv_h + ep.eps) : 0.f;
+    const float r2 =
+        valid ? ep.in_scale * rsqrtf(ep.ss_in[row] * ep.inv_h + ep.eps) : 0.f;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       float g[32], u[32];
@@ -194,9 +219,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
       int col = n0 / 2 + c * 32;
       if (valid && n0 < N) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) g[j] = silu(r2 * g[j]) * (r2 * u[j]);
-        store_bf16x32(static_cast<__nv_bfloat16*>(ep.out) + (size_t)row * ep.ldo +
-                          col, g);
+        for (int j = 0; j < 32; ++j)
+          g[j] = silu(r2 * g[j]) * (r2 * u[j]) * ep.out_scale;
+        store_16x32(ep.out, (size_t)row * ep.ldo + col, g, ep.out_f16);
       }
     }
   }
@@ -335,7 +360,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      const uint32_t idesc = ep.ab_f16 ? idesc_f16(BM, BN) : idesc_bf16(BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t local = 0;
@@ -357,11 +382,11 @@ __global__ void __launch_bounds__(192, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * L::STAGE);
-          const uint32_t sb = sa + L::A_BYTES;
+          const uint64_t ad = sdesc_k128(sa), bd = sdesc_k128(sa + L::A_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            tc_mma_bf16(d_tmem, sdesc_k128(sa + k * 32), sdesc_k128(sb + k * 32),
-                        idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < BK / 16; ++k) {  // a K step of 16 is 32 bytes
+            tc_mma_bf16_nc(d_tmem, ad + 2 * k, bd + 2 * k, idesc,
+                           (kb > kb0 || k > 0) ? 1u : 0u);
           }
           issued_any = true;
           tc_commit(&empty[stage]);

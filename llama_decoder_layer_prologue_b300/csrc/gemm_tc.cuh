@@ -34,6 +34,12 @@ struct TcEpiArgs {
   int head_dim = 0, rope_cols = 0, max_pos = 0;  // rope on columns < rope_cols
   int part_slots = 0;              // TC_PARTIAL: slots per tile (plan.slots)
   int* status = nullptr;
+  // operand / output types and power-of-two scales of the fp16 path
+  int ab_f16 = 0;        // A and B are fp16 (else bf16)
+  int out_f16 = 0;       // TC_QKV / TC_SWIGLU output (out2 for TC_RESID_SS) is fp16
+  float in_scale = 1.f;  // TC_SWIGLU: gate / up = in_scale * r2 * acc;
+                         // TC_RESID: out = res + in_scale * acc
+  float out_scale = 1.f; // TC_SWIGLU: act stored * out_scale; TC_RESID_SS: out2 * out_scale
 };
 
 // Encodes a 2-D bf16 tensor map over a row-major [rows, cols] matrix with a

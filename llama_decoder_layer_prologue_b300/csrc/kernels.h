@@ -8,6 +8,13 @@
 
 namespace llama {
 
+// Scales of the fp16 intermediates of the bf16 layer (powers of two, so
+// exact): the gate_up operand h * g_post is stored times kHgScale and the
+// SwiGLU output act times kActScale, leaving fp16 headroom for large hidden
+// states; the consuming epilogues multiply back.
+constexpr float kHgScale = 1.0f / 256.0f;
+constexpr float kActScale = 1.0f / 16.0f;
+
 struct Dims {
   int H, Hq, Hkv, d, I, Nqkv, max_pos;
   float eps;
@@ -65,8 +72,11 @@ void simt_attention_decode(bool is_bf16, const void* qkv, const void* cache_k,
 
 // ----------------------------------------------------------------- pack.cu
 // out[n, k] = W[src(n), k] * (g ? g[k] : 1), src(n) = n, or the gate/up
-// interleave in blocks of 128 when interleave_inter > 0.
+// interleave in blocks of 128 when interleave_inter > 0.  out_f16 (bf16
+// input only): the packed copy is fp16 (exact for bf16 values in fp16's
+// normal range).
 void launch_pack(bool is_bf16, const void* W, const void* g, void* out,
-                 int rows, int cols, int interleave_inter, cudaStream_t s);
+                 int rows, int cols, int interleave_inter, bool out_f16,
+                 cudaStream_t s);
 
 }  // namespace llama

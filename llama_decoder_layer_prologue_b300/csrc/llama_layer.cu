@@ -218,14 +218,15 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.out = qkv; ep.ldo = dm.Nqkv; ep.rowscale = r1; ep.pos = pos;
     ep.cos_t = cos_t; ep.sin_t = sin_t; ep.head_dim = dm.d;
     ep.rope_cols = (dm.Hq + dm.Hkv) * dm.d; ep.max_pos = dm.max_pos;
+    ep.out_f16 = 1;  // q | k | v in fp16 for the attention
     mark(L, s, "qkv_rope");
     e = tc_gemm(TC_QKV, 256, ta, L->tm_wqkv, T, dm.Nqkv, dm.H, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
     ++L->launches;
     // a4 / a5: causal GQA attention (padded or varlen).
     AttnArgs aa;
-    aa.qkv = static_cast<const __nv_bfloat16*>(qkv);
-    aa.out = static_cast<__nv_bfloat16*>(attn);
+    aa.qkv = static_cast<const __half*>(qkv);
+    aa.out = static_cast<__half*>(attn);
     aa.cu = cu; aa.tokens = T; aa.seq_len = seq_len; aa.nqkv = dm.Nqkv;
     aa.n_heads = dm.Hq; aa.n_kv_heads = dm.Hkv; aa.head_dim = dm.d;
     aa.status = L->status;
@@ -239,6 +240,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.status = L->status;
     ep.out = h; ep.out2 = ws + w.hg; ep.ldo = dm.H; ep.residual = x;
     ep.colscale = P + L->pl.gpost; ep.ss_out = ss2;
+    ep.ab_f16 = 1; ep.out_f16 = 1; ep.out_scale = kHgScale;
     mark(L, s, "o_proj_residual");
     e = tc_gemm(TC_RESID_SS, 256, ta, L->tm_wo, T, dm.H, dm.Hq * dm.d, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
@@ -248,6 +250,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep = TcEpiArgs();
     ep.status = L->status;
     ep.out = act; ep.ldo = dm.I; ep.ss_in = ss2; ep.inv_h = 1.0f / dm.H; ep.eps = dm.eps;
+    ep.ab_f16 = 1; ep.in_scale = 1.0f / kHgScale; ep.out_f16 = 1; ep.out_scale = kActScale;
     mark(L, s, "gate_up_swiglu");
     e = tc_gemm(TC_SWIGLU, 256, ta, L->tm_wgu, T, 2 * dm.I, dm.H, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
@@ -257,6 +260,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep = TcEpiArgs();
     ep.status = L->status;
     ep.out = out; ep.ldo = dm.H; ep.residual = h;
+    ep.ab_f16 = 1; ep.in_scale = 1.0f / kActScale;
     mark(L, s, "down_residual");
     e = tc_gemm(TC_RESID, 256, ta, L->tm_wd, T, dm.H, dm.I, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
@@ -347,13 +351,13 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   a.qkv = reinterpret_cast<__nv_bfloat16*>(ws + w.qkv);
   a.cache_k = static_cast<__nv_bfloat16*>(ck);
   a.cache_v = static_cast<__nv_bfloat16*>(cv);
-  a.attn = reinterpret_cast<__nv_bfloat16*>(ws + w.attn);
+  a.attn = reinterpret_cast<__half*>(ws + w.attn);
   a.attn_part = reinterpret_cast<float*>(ws + w.attn_part);
   a.max_chunks = w.max_chunks; a.n_rep_rec = w.rec;
   a.h32 = reinterpret_cast<float*>(ws + w.h32);
-  a.hg = reinterpret_cast<__nv_bfloat16*>(ws + w.hg);
+  a.hg = reinterpret_cast<__half*>(ws + w.hg);
   a.g_post = reinterpret_cast<const __nv_bfloat16*>(P + L->pl.gpost);
-  a.act = reinterpret_cast<__nv_bfloat16*>(ws + w.act);
+  a.act = reinterpret_cast<__half*>(ws + w.act);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.status = L->status;
 
@@ -372,6 +376,7 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
     ep.out = ws + w.part;
     ep.part_slots = w.plan[stage].slots;
     ep.status = L->status;
+    ep.ab_f16 = stage != DEC_QKV;  // fp16 weights and activations after QKV
     mark(L, s, kGemmName[stage]);
     if (tc_gemm(TC_PARTIAL, w.bn, wmap, tb, N_out, B, K, ep, L->sm_count, s) !=
         cudaSuccess)
@@ -512,15 +517,20 @@ int llama_layer_init(const llama_layer_config* cfg,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& dm = L->dm;
 
+  // bf16 layers: W_qkv (times g_in) stays bf16 (its A operand is the bf16
+  // input x); W_o, W_gate_up and W_down become fp16, the type of the
+  // intermediates they multiply.
+  const bool f16 = L->bf16;
   launch_pack(L->bf16, wts->w_qkv, wts->g_in, L->packed + pl.wqkv, dm.Nqkv,
-              dm.H, 0, s);
+              dm.H, 0, false, s);
   launch_pack(L->bf16, wts->w_o, nullptr, L->packed + pl.wo, dm.H,
-              dm.Hq * dm.d, 0, s);
+              dm.Hq * dm.d, 0, f16, s);
   launch_pack(L->bf16, wts->g_post, nullptr, L->packed + pl.gpost, 1, dm.H, 0,
-              s);
+              false, s);
   launch_pack(L->bf16, wts->w_gate_up, nullptr, L->packed + pl.wgu,
-              2 * dm.I, dm.H, dm.I, s);
-  launch_pack(L->bf16, wts->w_down, nullptr, L->packed + pl.wd, dm.H, dm.I, 0, s);
+              2 * dm.I, dm.H, dm.I, f16, s);
+  launch_pack(L->bf16, wts->w_down, nullptr, L->packed + pl.wd, dm.H, dm.I, 0,
+              f16, s);
 
   // RoPE table: cos / sin of p * inv_freq_i in double, stored as fp32.
   const int half = c.head_dim / 2;

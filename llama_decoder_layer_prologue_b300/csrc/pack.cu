@@ -2,6 +2,7 @@
 // following projection and interleave gate / up rows for the fused SwiGLU
 // epilogue.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -16,9 +17,9 @@ __device__ __forceinline__ int gate_up_source_row(int n, int inter) {
   return w < 128 ? blk * 128 + w : inter + blk * 128 + (w - 128);
 }
 
-template <typename T>
+template <typename T, typename TO>
 __global__ void pack_kernel(const T* __restrict__ W, const T* __restrict__ g,
-                            T* __restrict__ out, int rows, int cols,
+                            TO* __restrict__ out, int rows, int cols,
                             int inter) {
   size_t total = (size_t)rows * cols;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
@@ -27,23 +28,28 @@ __global__ void pack_kernel(const T* __restrict__ W, const T* __restrict__ g,
     int src = inter > 0 ? gate_up_source_row(n, inter) : n;
     float v = Elem<T>::load(W + (size_t)src * cols + k);
     if (g) v *= Elem<T>::load(g + k);
-    Elem<T>::store(out + i, v);
+    Elem<TO>::store(out + i, v);
   }
 }
 
 }  // namespace
 
 void launch_pack(bool is_bf16, const void* W, const void* g, void* out,
-                 int rows, int cols, int interleave_inter, cudaStream_t s) {
+                 int rows, int cols, int interleave_inter, bool out_f16,
+                 cudaStream_t s) {
   int blocks = 148 * 8;
-  if (is_bf16)
-    pack_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+  if (is_bf16 && out_f16)
+    pack_kernel<__nv_bfloat16, __half><<<blocks, 256, 0, s>>>(
+        (const __nv_bfloat16*)W, (const __nv_bfloat16*)g, (__half*)out, rows,
+        cols, interleave_inter);
+  else if (is_bf16)
+    pack_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks, 256, 0, s>>>(
         (const __nv_bfloat16*)W, (const __nv_bfloat16*)g,
         (__nv_bfloat16*)out, rows, cols, interleave_inter);
   else
-    pack_kernel<float><<<blocks, 256, 0, s>>>((const float*)W, (const float*)g,
-                                              (float*)out, rows, cols,
-                                              interleave_inter);
+    pack_kernel<float, float><<<blocks, 256, 0, s>>>(
+        (const float*)W, (const float*)g, (float*)out, rows, cols,
+        interleave_inter);
 }
 
 }  // namespace llama

@@ -146,16 +146,22 @@ class LlamaLayer:
         return B.llama_layer_status(self.handle, stream_ptr())
 
     def stages(self, tokens: int, decode: bool = False) -> dict:
-        """Views of the intermediates of the last call with `tokens` rows."""
+        """The intermediates of the last call with `tokens` rows (element
+        types as llama_layer_workspace_offsets documents; act is returned
+        already multiplied back by 16 for bf16 layers)."""
         off = B.llama_layer_workspace_offsets(self.handle, tokens, int(decode))
         s = self.shape
-        widths = {"qkv": s.n_qkv, "attn": s.q_size, "h": s.hidden,
-                  "act": s.intermediate}
+        bf = self.dtype == torch.bfloat16
+        f16 = torch.float16 if bf else torch.float32
+        types = {"qkv": (s.n_qkv, torch.bfloat16 if (bf and decode) else f16),
+                 "attn": (s.q_size, f16), "h": (s.hidden, torch.float32),
+                 "act": (s.intermediate, f16)}
         views = {}
-        for (name, width), o in zip(widths.items(), off):
-            dt = torch.float32 if name == "h" else self.dtype
-            n = tokens * width * (4 if dt == torch.float32 else 2)
+        for (name, (width, dt)), o in zip(types.items(), off):
+            n = tokens * width * torch.tensor([], dtype=dt).element_size()
             views[name] = self.workspace[o:o + n].view(dt).view(tokens, width)
+        if bf:
+            views["act"] = views["act"].float() * 16.0
         return views
 
     def close(self) -> None:
