@@ -1,14 +1,15 @@
 // Persistent tcgen05 GEMM for sm_103a.
 //
-// One CTA per SM, 6 warps:
+// One CTA per SM, 10 warps:
 //   warp 0      TMA producer: A / B K-slices (64 bf16 = one 128-byte swizzle
 //               row) into a STAGES-deep shared-memory ring (mbarrier full /
 //               empty pairs).
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma
 //               (M = 128, N = BN, K = 16) into one of two TMEM accumulators
 //               and commits each ring slot back to the producer.
-//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (one output row
-//               per thread), fused epilogue, bf16 stores.  The two
+//   warps 2..9  epilogue: tcgen05.ld of their 32 TMEM lanes (one output row
+//               per thread; two warps per lane quadrant, each taking half of
+//               the tile's columns), fused epilogue, stores.  The two
 //               accumulators let the epilogue of tile i overlap the main loop
 //               of tile i + 1.
 // Tiles are visited in bands of 16 M-tiles so that a wave of CTAs shares A
@@ -23,6 +24,9 @@ namespace llama {
 namespace {
 
 constexpr int BM = 128, BK = 64, GROUP_M = 16;
+// warp 0 producer, warp 1 MMA, warps 2..9 epilogue (two per TMEM lane
+// quadrant, each on half of the tile's columns)
+constexpr int kEpiWarps = 8, kGemmThreads = 64 + 32 * kEpiWarps;
 
 // Status word for GEMMs launched without a layer (llama_gemm_bf16).
 __device__ int g_tc_status;
@@ -107,14 +111,16 @@ __device__ __forceinline__ void store_f32x32(float* p, const float* v) {
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
+// Epilogue of one accumulator row (TMEM lane) over column half `part` (0 or
+// 1) of the tile (two warps share each lane quadrant, one per half).
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool valid,
-                                              int n0, int M, int N,
+                                              int n0, int M, int N, int part,
                                               const TcEpiArgs& ep) {
   if constexpr (EPI == TC_STORE || EPI == TC_RESID || EPI == TC_RESID_SS) {
     float ss = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = part * (BN / 64); c < (part + 1) * (BN / 64); ++c) {
       float v[32];
       tmem_ld32(t_row + c * 32, v);
       int col = n0 + c * 32;
@@ -169,7 +175,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
     const float* cs = ep.cos_t + (size_t)p * half;
     const float* sn = ep.sin_t + (size_t)p * half;
 #pragma unroll 1
-    for (int hb = 0; hb < BN; hb += d) {
+    for (int hb = part * (BN / 2); hb < (part + 1) * (BN / 2); hb += d) {
       const int hc = n0 + hb;
       const bool rope = hc < ep.rope_cols;
 #pragma unroll 1
@@ -212,7 +218,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
     const float r2 =
         valid ? ep.in_scale * rsqrtf(ep.ss_in[row] * ep.inv_h + ep.eps) : 0.f;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = part * 2; c < part * 2 + 2; ++c) {
       float g[32], u[32];
       tmem_ld32(t_row + c * 32, g);
       tmem_ld32(t_row + 128 + c * 32, u);
@@ -282,7 +288,7 @@ struct Sched {
 };
 
 template <int BN, int STAGES, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
                    TcEpiArgs ep) {
@@ -307,7 +313,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);
+      mbar_init(&acc_empty[a], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -404,7 +410,8 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
-    const int quad = warp & 3;
+    const int quad = warp & 3;            // TMEM lane quadrant of this warp
+    const int part = (warp - 2) / 4;      // column half of the tile
     uint32_t local = 0;
     while (sched.next(mt, nt, kb0, kb1, tile, slot)) {
       const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
@@ -419,7 +426,7 @@ __global__ void __launch_bounds__(192, 1)
         float* o = static_cast<float*>(ep.out) +
                    (((size_t)tile * ep.part_slots + slot) * BM + r) * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = part * (BN / 64); c < (part + 1) * (BN / 64); ++c) {
           float v[32];
           tmem_ld32(t_row + c * 32, v);
 #pragma unroll
@@ -429,7 +436,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       } else {
         const int row = mt * BM + r;
-        epilogue_tile<BN, EPI>(t_row, row, row < M, nt * BN, M, N, ep);
+        epilogue_tile<BN, EPI>(t_row, row, row < M, nt * BN, M, N, part, ep);
       }
       tc_fence_before();
       __syncwarp();
@@ -463,7 +470,7 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
     cudaError_t err = cudaGetSymbolAddress((void**)&e.status, g_tc_status);
     if (err != cudaSuccess) return err;
   }
-  kern<<<grid, 192, L::TOTAL, s>>>(ta, tb, M, N, K, e);
+  kern<<<grid, kGemmThreads, L::TOTAL, s>>>(ta, tb, M, N, K, e);
   return cudaGetLastError();
 }
 
