@@ -196,6 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // q|k|v come from the previous kernel
 
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
@@ -546,8 +548,8 @@ cudaError_t launch(const AttnArgs& a, int n_seq, int max_len, int sm_count,
     attr_set = true;
   }
   const int grid = (int)(items < sm_count ? items : sm_count);
-  kern<<<grid, kThreads, L::TOTAL, s>>>(tq, tkv, a, (int)items, n_hg, n_seq, n_qb);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), L::TOTAL, s, tq, tkv, a,
+                    (int)items, n_hg, n_seq, n_qb);
 }
 
 }  // namespace

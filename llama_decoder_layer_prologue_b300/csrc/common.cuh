@@ -11,6 +11,36 @@
 
 namespace llama {
 
+// ------------------------------------------------------------------ PDL
+// Programmatic dependent launch: a kernel launched with launch_pdl may start
+// while its predecessor in the stream is still running.  pdl_trigger() lets
+// the next kernel start; pdl_wait() blocks until the predecessor has
+// completed and its writes are visible -- every kernel calls it before it
+// touches global memory other than the (immutable) weights.  Both are no-ops
+// for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Bits of the device status word.
 enum : int {
   ST_TIMEOUT = 1,        // a bounded wait ran out

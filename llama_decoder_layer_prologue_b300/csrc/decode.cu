@@ -58,6 +58,8 @@ __device__ __forceinline__ void gather_tile(const DecodeArgs& a,
 // all three -> qkv[b, :], k and v also -> cache row start_pos[b].
 __global__ void __launch_bounds__(FT) finalize_qkv_kernel(DecodeArgs a,
                                                           TcStreamK plan) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float s[128 * FS];
   const int t = blockIdx.x, b0 = blockIdx.y * FB;
   gather_tile(a, plan, t, b0, s);
@@ -99,6 +101,8 @@ __global__ void __launch_bounds__(FT) finalize_qkv_kernel(DecodeArgs a,
 // h * g_post (operand of gate_up) and the row sums of h^2.
 __global__ void __launch_bounds__(FT) finalize_o_kernel(DecodeArgs a,
                                                         TcStreamK plan) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float s[128 * FS];
   const int t = blockIdx.x, b0 = blockIdx.y * FB;
   gather_tile(a, plan, t, b0, s);
@@ -122,6 +126,8 @@ __global__ void __launch_bounds__(FT) finalize_o_kernel(DecodeArgs a,
 // rows of act columns [128 k, 128 k + 128).
 __global__ void __launch_bounds__(FT) finalize_gu_kernel(DecodeArgs a,
                                                          TcStreamK plan) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sg[128 * FS];
   __shared__ float su[128 * FS];
   const int k = blockIdx.x, b0 = blockIdx.y * FB;
@@ -144,6 +150,8 @@ __global__ void __launch_bounds__(FT) finalize_gu_kernel(DecodeArgs a,
 // out = h + down_proj.
 __global__ void __launch_bounds__(FT) finalize_down_kernel(DecodeArgs a,
                                                            TcStreamK plan) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float s[128 * FS];
   const int t = blockIdx.x, b0 = blockIdx.y * FB;
   gather_tile(a, plan, t, b0, s);
@@ -172,6 +180,8 @@ constexpr int NST = 3;   // ring stages
 
 template <int D>
 __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int P = D + 8;  // padded row (bf16 elements): conflict-free ldmatrix
   constexpr int CH = D / 8;  // 16-byte chunks per row
   extern __shared__ __align__(16) uint8_t smem[];
@@ -350,6 +360,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
 
 // attn[b, h] = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c over the splits.
 __global__ void attn_combine_kernel(DecodeArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y;
   const int D = a.head_dim;
   const int n_rep = a.n_heads / a.n_kv_heads;
@@ -394,17 +406,15 @@ cudaError_t decode_finalize(int stage, const DecodeArgs& a,
   const int chunks = (a.batch + FB - 1) / FB;
   switch (stage) {
     case DEC_QKV:
-      finalize_qkv_kernel<<<dim3(plan.tiles, chunks), FT, 0, s>>>(a, plan);
-      break;
+      return launch_pdl(finalize_qkv_kernel, dim3(plan.tiles, chunks), dim3(FT), 0, s, a, plan);
     case DEC_O:
-      finalize_o_kernel<<<dim3(plan.tiles, chunks), FT, 0, s>>>(a, plan);
-      break;
+      return launch_pdl(finalize_o_kernel, dim3(plan.tiles, chunks), dim3(FT), 0, s, a, plan);
     case DEC_GU:
-      finalize_gu_kernel<<<dim3(plan.tiles / 2, chunks), FT, 0, s>>>(a, plan);
-      break;
+      return launch_pdl(finalize_gu_kernel, dim3(plan.tiles / 2, chunks), dim3(FT), 0, s, a,
+                        plan);
     case DEC_DOWN:
-      finalize_down_kernel<<<dim3(plan.tiles, chunks), FT, 0, s>>>(a, plan);
-      break;
+      return launch_pdl(finalize_down_kernel, dim3(plan.tiles, chunks), dim3(FT), 0, s, a,
+                        plan);
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -420,7 +430,8 @@ cudaError_t decode_attention(const DecodeArgs& a, cudaStream_t s) {
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       set = true;
     }
-    attn_decode_kernel<128><<<grid, 128, smem, s>>>(a);
+    cudaError_t e = launch_pdl(attn_decode_kernel<128>, grid, dim3(128), smem, s, a);
+    if (e != cudaSuccess) return e;
   } else {
     static bool set = false;
     if (!set) {
@@ -428,12 +439,12 @@ cudaError_t decode_attention(const DecodeArgs& a, cudaStream_t s) {
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       set = true;
     }
-    attn_decode_kernel<64><<<grid, 128, smem, s>>>(a);
+    cudaError_t e = launch_pdl(attn_decode_kernel<64>, grid, dim3(128), smem, s, a);
+    if (e != cudaSuccess) return e;
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3(a.n_heads, a.batch), 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(attn_combine_kernel, dim3(a.n_heads, a.batch), dim3(128), 0, s, a);
 }
 
 }  // namespace llama

@@ -332,12 +332,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   Sched sched(M, N, K, BN, kStreamK);
   int mt, nt, kb0, kb1, tile, slot;
 
+  pdl_trigger();
   if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
       bool ok = true;
+      // The weights (A of the swap-AB stream-K GEMM, B otherwise) never
+      // depend on the previous kernel: their first STAGES K-slices are
+      // requested before waiting for it.
+      constexpr bool kWeightsA = EPI == TC_PARTIAL;
+      uint32_t pre = 0;
+      {
+        Sched s2 = sched;
+        int pm, pn, pk0, pk1, pt, ps;
+        if (s2.next(pm, pn, pk0, pk1, pt, ps)) {
+          for (int kb = pk0; kb < pk1 && pre < (uint32_t)STAGES; ++kb, ++pre) {
+            uint8_t* sa = smem + pre * L::STAGE;
+            mbar_arrive_expect_tx(&full[pre], L::STAGE);
+            if (kWeightsA)
+              tma_load_2d(sa, &tmA, &full[pre], kb * BK, pm * BM);
+            else
+              tma_load_2d(sa + L::A_BYTES, &tmB, &full[pre], kb * BK, pn * BN);
+          }
+        }
+      }
+      pdl_wait();
       while (ok && sched.next(mt, nt, kb0, kb1, tile, slot)) {
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, ep.status, abort_flag)) {
@@ -345,9 +366,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           uint8_t* sa = smem + stage * L::STAGE;
-          mbar_arrive_expect_tx(&full[stage], L::STAGE);
-          tma_load_2d(sa, &tmA, &full[stage], kb * BK, mt * BM);
-          tma_load_2d(sa + L::A_BYTES, &tmB, &full[stage], kb * BK, nt * BN);
+          if (issued < pre) {  // weights already requested, tx already armed
+            if (kWeightsA)
+              tma_load_2d(sa + L::A_BYTES, &tmB, &full[stage], kb * BK, nt * BN);
+            else
+              tma_load_2d(sa, &tmA, &full[stage], kb * BK, mt * BM);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], L::STAGE);
+            tma_load_2d(sa, &tmA, &full[stage], kb * BK, mt * BM);
+            tma_load_2d(sa + L::A_BYTES, &tmB, &full[stage], kb * BK, nt * BN);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -357,6 +385,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok) {  // let the copies already issued land before leaving
         volatile int own = 0;
+        if (issued < pre) issued = pre;  // prefetched stages are in flight too
         uint32_t n = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
         for (uint32_t j = 1; j <= n; ++j) {
           uint32_t idx = issued - j;
@@ -365,6 +394,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp == 1) {
+    pdl_wait();
     if (lane == 0) {
       const uint32_t idesc = ep.ab_f16 ? idesc_f16(BM, BN) : idesc_bf16(BM, BN);
       int stage = 0;
@@ -410,6 +440,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else {
+    pdl_wait();
     const int quad = warp & 3;            // TMEM lane quadrant of this warp
     const int part = (warp - 2) / 4;      // column half of the tile
     uint32_t local = 0;
@@ -470,6 +501,7 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
     cudaError_t err = cudaGetSymbolAddress((void**)&e.status, g_tc_status);
     if (err != cudaSuccess) return err;
   }
+  if (e.pdl) return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), L::TOTAL, s, ta, tb, M, N, K, e);
   kern<<<grid, kGemmThreads, L::TOTAL, s>>>(ta, tb, M, N, K, e);
   return cudaGetLastError();
 }

@@ -40,6 +40,7 @@ struct TcEpiArgs {
   float in_scale = 1.f;  // TC_SWIGLU: gate / up = in_scale * r2 * acc;
                          // TC_RESID: out = res + in_scale * acc
   float out_scale = 1.f; // TC_SWIGLU: act stored * out_scale; TC_RESID_SS: out2 * out_scale
+  int pdl = 0;           // launch with programmatic dependent launch
 };
 
 // Encodes a 2-D bf16 tensor map over a row-major [rows, cols] matrix with a

@@ -213,6 +213,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     CUtensorMap ta;
     TcEpiArgs ep;
     ep.status = L->status;
+    ep.pdl = 1;
     // a2 + a3: QKV projection, row scale 1/RMS, RoPE on q and k.
     if (!tc_encode_bf16(&ta, x, T, dm.H, 128)) return LLAMA_ERR_CUDA;
     ep.out = qkv; ep.ldo = dm.Nqkv; ep.rowscale = r1; ep.pos = pos;
@@ -238,6 +239,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     if (!tc_encode_bf16(&ta, attn, T, dm.Hq * dm.d, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
+    ep.pdl = 1;
     ep.out = h; ep.out2 = ws + w.hg; ep.ldo = dm.H; ep.residual = x;
     ep.colscale = P + L->pl.gpost; ep.ss_out = ss2;
     ep.ab_f16 = 1; ep.out_f16 = 1; ep.out_scale = kHgScale;
@@ -249,6 +251,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     if (!tc_encode_bf16(&ta, ws + w.hg, T, dm.H, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
+    ep.pdl = 1;
     ep.out = act; ep.ldo = dm.I; ep.ss_in = ss2; ep.inv_h = 1.0f / dm.H; ep.eps = dm.eps;
     ep.ab_f16 = 1; ep.in_scale = 1.0f / kHgScale; ep.out_f16 = 1; ep.out_scale = kActScale;
     mark(L, s, "gate_up_swiglu");
@@ -259,6 +262,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     if (!tc_encode_bf16(&ta, act, T, dm.I, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
+    ep.pdl = 1;
     ep.out = out; ep.ldo = dm.H; ep.residual = h;
     ep.ab_f16 = 1; ep.in_scale = 1.0f / kActScale;
     mark(L, s, "down_residual");
@@ -374,6 +378,7 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
     if (!tc_encode_bf16(&tb, act_in, B, K, w.bn)) return LLAMA_ERR_CUDA;
     TcEpiArgs ep;
     ep.out = ws + w.part;
+    ep.pdl = 1;
     ep.part_slots = w.plan[stage].slots;
     ep.status = L->status;
     ep.ab_f16 = stage != DEC_QKV;  // fp16 weights and activations after QKV

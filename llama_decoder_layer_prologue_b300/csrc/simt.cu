@@ -30,6 +30,8 @@ template <typename T>
 __global__ void row_rms_kernel(const T* __restrict__ x, int rows, int H,
                                float eps, float* __restrict__ r,
                                float* __restrict__ zero) {
+  pdl_trigger();
+  pdl_wait();
   int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -54,6 +56,8 @@ __global__ void row_rms_kernel(const T* __restrict__ x, int rows, int H,
 __global__ void positions_kernel(const int32_t* __restrict__ cu, int n_seq,
                                  int seq_len, int T, int32_t* __restrict__ pos,
                                  int fill_pos, int* status) {
+  pdl_trigger();
+  pdl_wait();
   int s = blockIdx.x;
   int a, b;
   if (cu) {
@@ -314,16 +318,16 @@ void set_smem(const void* fn, size_t bytes) {
 void simt_row_rms(bool is_bf16, const void* x, int rows, int H, float eps,
                   float* r, float* zero, cudaStream_t s) {
   if (rows <= 0) return;
-  DISPATCH(is_bf16, row_rms_kernel<T><<<(rows + 7) / 8, 256, 0, s>>>(
-                        (const T*)x, rows, H, eps, r, zero));
+  DISPATCH(is_bf16, launch_pdl(row_rms_kernel<T>, dim3((rows + 7) / 8), dim3(256), 0,
+                               s, (const T*)x, rows, H, eps, r, zero));
 }
 
 void launch_positions(const int32_t* cu, int n_seq, int seq_len, int T,
                       int32_t* pos, bool fill_pos, int* status,
                       cudaStream_t s) {
   if (n_seq <= 0) return;
-  positions_kernel<<<n_seq, 256, 0, s>>>(cu, n_seq, seq_len, T, pos,
-                                         fill_pos ? 1 : 0, status);
+  launch_pdl(positions_kernel, dim3(n_seq), dim3(256), 0, s, cu, n_seq, seq_len, T,
+             pos, fill_pos ? 1 : 0, status);
 }
 
 void simt_gemm(bool is_bf16, int epi, const void* A, const void* B, void* out,
