@@ -63,6 +63,13 @@ def test_tiny_fp32_workload():
      dict(batch=2, seq=70)),
     ("varlen_with_len1", shape(512, 8, 2, 64, 512, **L3), "varlen",
      dict(total_tokens=700, min_len=1, max_len=300)),
+    # 8 query heads per kv head: 16 positions per 128-row attention tile
+    ("gqa8", shape(512, 8, 1, 64, 256, **L3), "padded", dict(batch=2, seq=90)),
+    # 16 query heads per kv head (the largest ratio the library takes)
+    ("gqa16", shape(1024, 16, 1, 64, 256), "padded", dict(batch=1, seq=77)),
+    # head_dim 128 packed sequences, many shorter than a query tile
+    ("varlen_d128_short", shape(512, 4, 2, 128, 256, **L3), "varlen",
+     dict(total_tokens=400, min_len=1, max_len=40)),
 ])
 def test_small_bf16_forward(case):
     name, s, kind, kw = case
@@ -90,7 +97,7 @@ def test_varlen_equals_padded_on_the_gpu():
     layer.close()
 
 
-def check_decode(s, batch, max_seq, start_pos):
+def check_decode(s, batch, max_seq, start_pos, stages=True):
     w = synth.custom_workload("dec", s, "decode", batch=batch, max_seq=max_seq,
                               min_start=0)
     inp = synth.make_inputs(w)
@@ -112,8 +119,9 @@ def check_decode(s, batch, max_seq, start_pos):
                                       weights_f64(inp.weights), s, rows,
                                       inp.start_pos)
     assert_close(to_f64(out), ref["out"], s.dtype, "decode out")
-    st = layer.stages(batch, decode=True)
-    assert_stage_close(to_f64(st["attn"]), ref["attn"], s.dtype, "decode attn")
+    if stages:  # the workspace holds one pass of at most 256 tokens
+        st = layer.stages(batch, decode=True)
+        assert_stage_close(to_f64(st["attn"]), ref["attn"], s.dtype, "decode attn")
     for b, p in enumerate(inp.start_pos):
         assert_stage_close(to_f64(ck[b, p]), ref["k_new"][b], s.dtype, "k row")
         assert_stage_close(to_f64(cv[b, p]), ref["v_new"][b], s.dtype, "v row")
@@ -138,6 +146,20 @@ def test_decode_small_d128():
 def test_decode_qkv_width_not_tile_aligned():
     s = shape(256, 3, 1, 64, 256, **L3)
     check_decode(s, batch=33, max_seq=200, start_pos=list(range(0, 198, 6)))
+
+
+def test_decode_batch_128_wide_token_tile():
+    # 65..128 tokens: the decode GEMMs use 128-wide token tiles
+    s = shape(256, 4, 2, 64, 256, **L3)
+    sp = [(7 * b) % 190 for b in range(100)]
+    check_decode(s, batch=100, max_seq=192, start_pos=sp)
+
+
+def test_decode_batch_above_256_is_chunked():
+    # more than 256 tokens: two decode passes (256 + 44), 256-wide tiles
+    s = shape(256, 4, 2, 64, 256)
+    sp = [(13 * b) % 60 for b in range(300)]
+    check_decode(s, batch=300, max_seq=64, start_pos=sp, stages=False)
 
 
 def test_decode_tiny_fp32():
