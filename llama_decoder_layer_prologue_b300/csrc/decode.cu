@@ -15,111 +15,136 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-// The finalizers reduce the stream-K partials of one 128-row tile for a chunk
-// of FB tokens into shared memory (reads run along the tokens of one row,
-// i.e. along memory), then apply the stage's epilogue with the output row as
-// the fastest thread index (writes run along the token-major outputs).
-constexpr int FB = 16;   // tokens per block
-constexpr int FT = 256;  // threads per block
-constexpr int FS = FB + 1;  // padded smem row: conflict-free column reads
-constexpr int EPT = 128 * FB / FT;  // elements per thread
+// The finalizers read the stream-K partials token-major (part[tile][slot]
+// [token][128]): a warp takes one token and the 128 rows of a tile, a lane
+// rows 4 lane .. 4 lane + 3, so every partial load is a 512-byte warp-wide
+// float4 read and every output store runs along the token's row.  All loads
+// of a thread (up to FMAXS slots, plus the epilogue's inputs) are issued
+// before the first use: the kernels are latency-bound, and this keeps them
+// at one or two memory round trips.
+constexpr int FT = 256;            // threads per block
+constexpr int FB = FT / 32;        // tokens per block (one per warp)
+constexpr int FMAXS = 8;           // slots loaded per round trip
 
 __device__ __forceinline__ bool start_ok(int sp, const DecodeArgs& a) {
   return sp >= 0 && sp < a.max_seq && sp < a.max_pos;
 }
 
-// s[r * FS + j] = sum over tile t's slots of partial (row r, token b0 + j).
-// Slot-outer so that every thread has EPT independent loads in flight.
-__device__ __forceinline__ void gather_tile(const DecodeArgs& a,
-                                            const TcStreamK& plan, int t, int b0,
-                                            float* s) {
-  const float* base = a.part + (size_t)t * plan.slots * 128 * a.bn + b0;
+// Sum over tile t's slots of rows 4 lane .. 4 lane + 3 of token b.
+__device__ __forceinline__ float4 gather_rows(const DecodeArgs& a,
+                                              const TcStreamK& plan, int t,
+                                              int b) {
   const int nseg = tc_streamk_segments(plan, t);
-  const int nb = min(FB, a.batch - b0);
-  float acc[EPT];
+  const float* src = a.part + ((size_t)t * plan.slots * a.bn + b) * 128 +
+                     (threadIdx.x & 31) * 4;
+  const size_t slot_stride = (size_t)a.bn * 128;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < nseg; k0 += FMAXS) {
+    float4 v[FMAXS];
 #pragma unroll
-  for (int i = 0; i < EPT; ++i) acc[i] = 0.f;
-  for (int k = 0; k < nseg; ++k) {
-    const float* src = base + (size_t)k * 128 * a.bn;
+    for (int k = 0; k < FMAXS; ++k)
+      v[k] = k0 + k < nseg
+                 ? __ldcg(reinterpret_cast<const float4*>(src + (k0 + k) * slot_stride))
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < EPT; ++i) {
-      const int e = threadIdx.x + i * FT, r = e / FB, j = e - r * FB;
-      if (j < nb) acc[i] += src[(size_t)r * a.bn + j];
+    for (int k = 0; k < FMAXS; ++k) {
+      acc.x += v[k].x; acc.y += v[k].y; acc.z += v[k].z; acc.w += v[k].w;
     }
   }
-#pragma unroll
-  for (int i = 0; i < EPT; ++i) {
-    const int e = threadIdx.x + i * FT, r = e / FB, j = e - r * FB;
-    s[r * FS + j] = acc[i];
-  }
+  return acc;
+}
+
+__device__ __forceinline__ float4 ld_bf16x4(const __nv_bfloat16* p) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+__device__ __forceinline__ void st_bf16x4(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo);
+  u.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+__device__ __forceinline__ void st_f16x4(__half* p, float4 v) {
+  __half2 lo = __floats2half2_rn(v.x, v.y);
+  __half2 hi = __floats2half2_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo);
+  u.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
 }
 
 // q, k, v of the new tokens: row scale 1/RMS, RoPE at start_pos on q and k,
-// all three -> qkv[b, :], k and v also -> cache row start_pos[b].
+// all three -> qkv[b, :], k and v also -> cache row start_pos[b].  Head
+// boundaries fall on 4-row groups and head_dim divides 128, so the RoPE
+// partner rows i +- D/2 sit D/8 lanes away in the same warp.
 __global__ void __launch_bounds__(FT) finalize_qkv_kernel(DecodeArgs a,
                                                           TcStreamK plan) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float s[128 * FS];
-  const int t = blockIdx.x, b0 = blockIdx.y * FB;
-  gather_tile(a, plan, t, b0, s);
-  __syncthreads();
+  const int t = blockIdx.x, b = blockIdx.y * FB + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (b >= a.batch) return;
+  const int sp = a.start_pos[b];
+  const float r1 = a.r1[b];
+  float4 x = gather_rows(a, plan, t, b);
+  if (!start_ok(sp, a)) {
+    if (lane == 0) set_status(a.status, ST_BAD_START_POS);
+    return;
+  }
   const int D = a.head_dim, half = D / 2;
   const int hq = a.n_heads, hkv = a.n_kv_heads;
-  const int nb = min(FB, a.batch - b0);
-  for (int e = threadIdx.x; e < 128 * FB; e += FT) {
-    const int r = e & 127, j = e >> 7;
-    if (j >= nb) continue;
-    const int b = b0 + j, n = t * 128 + r;
-    if (n >= a.nqkv) continue;  // last tile of a width that is not 128-aligned
-    const int head = n / D, i = n - head * D;
-    const int sp = a.start_pos[b];
-    if (!start_ok(sp, a)) {
-      if (t == 0 && r == 0) set_status(a.status, ST_BAD_START_POS);
-      continue;
-    }
-    const float r1 = a.r1[b];
-    float x = r1 * s[r * FS + j];
-    if (head < hq + hkv) {
-      const int pr = i < half ? r + half : r - half;
-      const float y = r1 * s[pr * FS + j];
-      const float c = a.cos_t[(size_t)sp * half + (i % half)];
-      const float sn = a.sin_t[(size_t)sp * half + (i % half)];
-      x = i < half ? x * c - y * sn : x * c + y * sn;
-    }
-    const bf16 v = __float2bfloat16_rn(x);
-    a.qkv[(size_t)b * a.nqkv + n] = v;
-    if (head >= hq) {
-      const int g = head < hq + hkv ? head - hq : head - hq - hkv;
-      bf16* cache = head < hq + hkv ? a.cache_k : a.cache_v;
-      cache[(((size_t)b * a.max_seq + sp) * hkv + g) * D + i] = v;
-    }
+  const int n = t * 128 + lane * 4;
+  const int head = n / D, i = n - head * D;
+  x.x *= r1; x.y *= r1; x.z *= r1; x.w *= r1;
+  const int dl = half / 4;  // partner lane offset
+  float4 y;
+  y.x = __shfl_xor_sync(0xffffffffu, x.x, dl);
+  y.y = __shfl_xor_sync(0xffffffffu, x.y, dl);
+  y.z = __shfl_xor_sync(0xffffffffu, x.z, dl);
+  y.w = __shfl_xor_sync(0xffffffffu, x.w, dl);
+  if (n >= a.nqkv) return;  // last tile of a width that is not 128-aligned
+  if (head < hq + hkv) {
+    const int ci = i < half ? i : i - half;
+    const float4 c = __ldg(reinterpret_cast<const float4*>(a.cos_t + (size_t)sp * half + ci));
+    const float4 sn = __ldg(reinterpret_cast<const float4*>(a.sin_t + (size_t)sp * half + ci));
+    const float sg = i < half ? -1.f : 1.f;  // x c - y s (first half), x c + y s
+    x = make_float4(fmaf(sg * y.x, sn.x, x.x * c.x), fmaf(sg * y.y, sn.y, x.y * c.y),
+                    fmaf(sg * y.z, sn.z, x.z * c.z), fmaf(sg * y.w, sn.w, x.w * c.w));
+  }
+  st_bf16x4(a.qkv + (size_t)b * a.nqkv + n, x);
+  if (head >= hq) {
+    const int g = head < hq + hkv ? head - hq : head - hq - hkv;
+    __nv_bfloat16* cache = head < hq + hkv ? a.cache_k : a.cache_v;
+    st_bf16x4(cache + (((size_t)b * a.max_seq + sp) * hkv + g) * D + i, x);
   }
 }
 
-// h = x + o_proj: fp32 copy (residual of the down projection), bf16 copy of
+// h = x + o_proj: fp32 copy (residual of the down projection), fp16 copy of
 // h * g_post (operand of gate_up) and the row sums of h^2.
 __global__ void __launch_bounds__(FT) finalize_o_kernel(DecodeArgs a,
                                                         TcStreamK plan) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float s[128 * FS];
-  const int t = blockIdx.x, b0 = blockIdx.y * FB;
-  gather_tile(a, plan, t, b0, s);
-  __syncthreads();
-  const int H = a.hidden;
-  const int nb = min(FB, a.batch - b0);
-  for (int e = threadIdx.x; e < 128 * FB; e += FT) {
-    const int r = e & 127, j = e >> 7;  // a warp: 32 rows of one token
-    if (j >= nb) continue;
-    const int b = b0 + j, n = t * 128 + r;
-    const float h = __bfloat162float(a.x[(size_t)b * H + n]) + s[r * FS + j];
-    a.h32[(size_t)b * H + n] = h;
-    a.hg[(size_t)b * H + n] =
-        __float2half_rn(h * __bfloat162float(a.g_post[n]) * kHgScale);
-    const float ss = warp_sum(h * h);
-    if ((threadIdx.x & 31) == 0) atomicAdd(a.ss2 + b, ss);
-  }
+  const int t = blockIdx.x, b = blockIdx.y * FB + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (b >= a.batch) return;
+  const int H = a.hidden, n = t * 128 + lane * 4;
+  const float4 xv = ld_bf16x4(a.x + (size_t)b * H + n);
+  const float4 gp = ld_bf16x4(a.g_post + n);
+  const float4 o = gather_rows(a, plan, t, b);
+  const float4 h = make_float4(xv.x + o.x, xv.y + o.y, xv.z + o.z, xv.w + o.w);
+  *reinterpret_cast<float4*>(a.h32 + (size_t)b * H + n) = h;
+  st_f16x4(a.hg + (size_t)b * H + n,
+           make_float4(h.x * gp.x * kHgScale, h.y * gp.y * kHgScale,
+                       h.z * gp.z * kHgScale, h.w * gp.w * kHgScale));
+  const float ss = warp_sum(h.x * h.x + h.y * h.y + h.z * h.z + h.w * h.w);
+  if (lane == 0) atomicAdd(a.ss2 + b, ss);
 }
 
 // act = silu(r2 gate) * (r2 up); packed tiles 2k / 2k+1 are the gate / up
@@ -128,23 +153,22 @@ __global__ void __launch_bounds__(FT) finalize_gu_kernel(DecodeArgs a,
                                                          TcStreamK plan) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float sg[128 * FS];
-  __shared__ float su[128 * FS];
-  const int k = blockIdx.x, b0 = blockIdx.y * FB;
-  gather_tile(a, plan, 2 * k, b0, sg);
-  gather_tile(a, plan, 2 * k + 1, b0, su);
-  __syncthreads();
-  const float inv_h = 1.0f / a.hidden;
-  const int nb = min(FB, a.batch - b0);
-  for (int e = threadIdx.x; e < 128 * FB; e += FT) {
-    const int r = e & 127, j = e >> 7;
-    if (j >= nb) continue;
-    const int b = b0 + j;
-    const float r2 = rsqrtf(a.ss2[b] * inv_h + a.eps) / kHgScale;
-    const float g = r2 * sg[r * FS + j], u = r2 * su[r * FS + j];
-    a.act[(size_t)b * a.inter + k * 128 + r] =
-        __float2half_rn(g / (1.0f + __expf(-g)) * u * kActScale);
+  const int k = blockIdx.x, b = blockIdx.y * FB + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (b >= a.batch) return;
+  const float ss = a.ss2[b];
+  const float4 gs = gather_rows(a, plan, 2 * k, b);
+  const float4 us = gather_rows(a, plan, 2 * k + 1, b);
+  const float r2 = rsqrtf(ss * (1.0f / a.hidden) + a.eps) / kHgScale;
+  float gv[4] = {gs.x, gs.y, gs.z, gs.w}, uv[4] = {us.x, us.y, us.z, us.w};
+  float av[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float g = r2 * gv[q], u = r2 * uv[q];
+    av[q] = g / (1.0f + __expf(-g)) * u * kActScale;
   }
+  st_f16x4(a.act + (size_t)b * a.inter + k * 128 + lane * 4,
+           make_float4(av[0], av[1], av[2], av[3]));
 }
 
 // out = h + down_proj.
@@ -152,19 +176,16 @@ __global__ void __launch_bounds__(FT) finalize_down_kernel(DecodeArgs a,
                                                            TcStreamK plan) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float s[128 * FS];
-  const int t = blockIdx.x, b0 = blockIdx.y * FB;
-  gather_tile(a, plan, t, b0, s);
-  __syncthreads();
-  const int H = a.hidden;
-  const int nb = min(FB, a.batch - b0);
-  for (int e = threadIdx.x; e < 128 * FB; e += FT) {
-    const int r = e & 127, j = e >> 7;
-    if (j >= nb) continue;
-    const int b = b0 + j, n = t * 128 + r;
-    a.out[(size_t)b * H + n] = __float2bfloat16_rn(
-        fmaf(s[r * FS + j], 1.0f / kActScale, a.h32[(size_t)b * H + n]));
-  }
+  const int t = blockIdx.x, b = blockIdx.y * FB + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (b >= a.batch) return;
+  const int H = a.hidden, n = t * 128 + lane * 4;
+  const float4 h = __ldcg(reinterpret_cast<const float4*>(a.h32 + (size_t)b * H + n));
+  const float4 d = gather_rows(a, plan, t, b);
+  constexpr float is = 1.0f / kActScale;
+  st_bf16x4(a.out + (size_t)b * H + n,
+            make_float4(fmaf(d.x, is, h.x), fmaf(d.y, is, h.y), fmaf(d.z, is, h.z),
+                        fmaf(d.w, is, h.w)));
 }
 
 // ------------------------------------------------------------ attention
@@ -359,34 +380,69 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
 }
 
 // attn[b, h] = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c over the splits.
-__global__ void attn_combine_kernel(DecodeArgs a) {
+// The split weights go through shared memory (one load of every (m, l) by
+// the block), then each thread's O loads over the splits are issued
+// together, so the kernel costs two memory round trips for up to 8 splits.
+constexpr int CT = 128;  // combine threads
+__global__ void __launch_bounds__(CT) attn_combine_kernel(DecodeArgs a) {
+  extern __shared__ float wsplit[];  // a.max_chunks split weights
+  __shared__ float red[CT / 32];
   pdl_trigger();
   pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y;
   const int D = a.head_dim;
   const int n_rep = a.n_heads / a.n_kv_heads;
   const int g = h / n_rep, row = h % n_rep;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __half* o = a.attn + (size_t)b * a.n_heads * D + h * D;
   const int sp = a.start_pos[b];
   if (!start_ok(sp, a)) {
-    for (int i = threadIdx.x; i < D; i += blockDim.x) o[i] = __float2half_rn(0.f);
+    for (int i = threadIdx.x; i < D; i += CT) o[i] = __float2half_rn(0.f);
     return;
   }
   const int nc = (sp + 1 + KS - 1) / KS;
   const float* base =
       a.attn_part + ((size_t)b * a.n_kv_heads + g) * a.max_chunks * a.n_rep_rec;
-  float M = -INFINITY;
-  for (int c = 0; c < nc; ++c)
-    M = fmaxf(M, base[(size_t)c * a.n_rep_rec + n_rep * D + row]);
-  for (int i = threadIdx.x; i < D; i += blockDim.x) {
-    float num = 0.f, den = 0.f;
-    for (int c = 0; c < nc; ++c) {
-      const float* rec = base + (size_t)c * a.n_rep_rec;
-      const float w = exp2f(rec[n_rep * D + row] - M);
-      num += w * rec[row * D + i];
-      den += w * rec[n_rep * D + n_rep + row];
+  const int moff = n_rep * D + row, loff = n_rep * D + n_rep + row;
+  float mx = -INFINITY;
+  for (int c = threadIdx.x; c < nc; c += CT)
+    mx = fmaxf(mx, __ldcg(base + (size_t)c * a.n_rep_rec + moff));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int w = 1; w < CT / 32; ++w) M = fmaxf(M, red[w]);
+  float den = 0.f;
+  for (int c = threadIdx.x; c < nc; c += CT) {
+    const float* rec = base + (size_t)c * a.n_rep_rec;
+    const float w = exp2f(__ldcg(rec + moff) - M);
+    wsplit[c] = w;
+    den += w * __ldcg(rec + loff);
+  }
+  den = warp_sum(den);
+  __syncthreads();  // every warp has read red[] (M) and written wsplit[]
+  if (lane == 0) red[warp] = den;
+  __syncthreads();
+  den = red[0];
+#pragma unroll
+  for (int w = 1; w < CT / 32; ++w) den += red[w];
+  const float inv = 1.0f / den;
+  for (int i = threadIdx.x; i < D; i += CT) {
+    const float* src = base + row * D + i;
+    float num = 0.f;
+    for (int c0 = 0; c0 < nc; c0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        v[c] = c0 + c < nc ? __ldcg(src + (size_t)(c0 + c) * a.n_rep_rec) : 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        if (c0 + c < nc) num = fmaf(wsplit[c0 + c], v[c], num);
     }
-    o[i] = __float2half_rn(num / den);
+    o[i] = __float2half_rn(num * inv);
   }
 }
 
@@ -444,7 +500,8 @@ cudaError_t decode_attention(const DecodeArgs& a, cudaStream_t s) {
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_combine_kernel, dim3(a.n_heads, a.batch), dim3(128), 0, s, a);
+  return launch_pdl(attn_combine_kernel, dim3(a.n_heads, a.batch), dim3(CT),
+                    (size_t)a.max_chunks * sizeof(float), s, a);
 }
 
 }  // namespace llama

@@ -47,22 +47,29 @@ float* scratch_on_current_device() {
   return g_scratch_ptr[dev];
 }
 
-// D[m, n] = bf16(sum over the tile's stream-K slots of part[tile][slot][r][n])
-// with m = 128 tile + r.  One CTA per 128-row tile; thread i walks the
-// tile's (r, n) elements in memory order so the partial reads coalesce.
+// D[m, n] = bf16(sum over the tile's stream-K slots of part[tile][slot][n][r])
+// with m = 128 tile + r.  CTA (tile, group of 32 columns): the partials are
+// read along r (their memory order), summed into shared memory and written
+// along n, D's memory order.
 __global__ void __launch_bounds__(256)
     streamk_reduce_kernel(const float* __restrict__ part, TcStreamK plan, int bn,
                           __nv_bfloat16* __restrict__ D, int M, int N) {
-  const int t = blockIdx.x;
+  __shared__ float s[32][129];
+  const int t = blockIdx.x, n0 = blockIdx.y * 32;
   const int nseg = tc_streamk_segments(plan, t);
-  const float* base = part + (size_t)t * plan.slots * 128 * bn;
-  for (int e = threadIdx.x; e < 128 * bn; e += blockDim.x) {
-    const int r = e / bn, n = e - r * bn;
-    const int m = t * 128 + r;
-    if (m >= M || n >= N) continue;
+  const float* base = part + ((size_t)t * plan.slots * bn + n0) * 128;
+  for (int e = threadIdx.x; e < 32 * 128; e += blockDim.x) {
+    const int c = e >> 7, r = e & 127;
     float acc = 0.f;
-    for (int j = 0; j < nseg; ++j) acc += base[(size_t)j * 128 * bn + e];
-    D[(size_t)m * N + n] = __float2bfloat16_rn(acc);
+    if (n0 + c < N)
+      for (int j = 0; j < nseg; ++j) acc += base[(size_t)j * bn * 128 + e];
+    s[c][r] = acc;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < 128 * 32; e += blockDim.x) {
+    const int r = e >> 5, c = e & 31;
+    const int m = t * 128 + r, n = n0 + c;
+    if (m < M && n < N) D[(size_t)m * N + n] = __float2bfloat16_rn(s[c][r]);
   }
 }
 
@@ -103,7 +110,7 @@ extern "C" int llama_gemm_bf16_streamk_static(const void* A, const void* B,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (tc_gemm(TC_PARTIAL, bn, ta, tb, M, N, K, ep, sms, s) != cudaSuccess)
     return LLAMA_ERR_CUDA;
-  streamk_reduce_kernel<<<plan.tiles, 256, 0, s>>>(
+  streamk_reduce_kernel<<<dim3(plan.tiles, (N + 31) / 32), 256, 0, s>>>(
       part, plan, bn, static_cast<__nv_bfloat16*>(D), M, N);
   return cudaGetLastError() == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA;
 }

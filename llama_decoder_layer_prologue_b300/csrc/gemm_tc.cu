@@ -454,16 +454,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int r = quad * 32 + lane;
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
       if constexpr (EPI == TC_PARTIAL) {
+        // token-major slot: column c of the tile is 128 consecutive floats,
+        // so a warp's 32 rows of one column are one 128-byte store
         float* o = static_cast<float*>(ep.out) +
-                   (((size_t)tile * ep.part_slots + slot) * BM + r) * BN;
+                   ((size_t)tile * ep.part_slots + slot) * BN * BM + r;
 #pragma unroll 1
         for (int c = part * (BN / 64); c < (part + 1) * (BN / 64); ++c) {
           float v[32];
           tmem_ld32(t_row + c * 32, v);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(o + c * 32)[q] =
-                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          for (int q = 0; q < 32; ++q) o[(size_t)(c * 32 + q) * BM] = v[q];
         }
       } else {
         const int row = mt * BM + r;

@@ -15,7 +15,7 @@ enum TcEpi : int {
                     // ss_out[m] += sum over the row of h^2
   TC_SWIGLU = 3,    // gate|up interleaved by 128: out = silu(r2 g) * (r2 u)
   TC_RESID = 4,     // out = res (fp32) + acc
-  TC_PARTIAL = 5,   // stream-K fp32 partials: part[tile][slot][128][bn]
+  TC_PARTIAL = 5,   // stream-K fp32 partials: part[tile][slot][bn][128]
 };
 
 struct TcEpiArgs {
@@ -50,9 +50,9 @@ bool tc_encode_bf16(CUtensorMap* map, const void* ptr, uint64_t rows,
 
 // Stream-K plan of a TC_PARTIAL GEMM: `grid` CTAs share the
 // tiles * kb_total K-blocks evenly; tile t's partial sums land in
-// tc_streamk_segments(plan, t) consecutive slots of part[t][slot][128][bn]
-// (fp32; row r of the slot is output row 128 t + r, column c is output
-// column c), slots <= plan.slots.
+// tc_streamk_segments(plan, t) consecutive slots of part[t][slot][bn][128]
+// (fp32, token-major: element [c][r] is output row 128 t + r, column c),
+// slots <= plan.slots.
 struct TcStreamK {
   int grid, tiles, kb_total, slots;
 };
