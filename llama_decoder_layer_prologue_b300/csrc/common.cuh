@@ -217,6 +217,34 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Flags between CTAs of one grid (gpu scope).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until *flag == want, with the limits of mbar_wait.
+__device__ __forceinline__ bool flag_wait(const uint32_t* flag, uint32_t want,
+                                          int* status, volatile int* abort_flag) {
+  if (ld_acquire_gpu(flag) == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(100);
+    if (ld_acquire_gpu(flag) == want) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      set_status(status, ST_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m))

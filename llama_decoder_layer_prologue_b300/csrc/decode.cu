@@ -126,7 +126,8 @@ __global__ void __launch_bounds__(FT) finalize_qkv_kernel(DecodeArgs a,
 }
 
 // h = x + o_proj: fp32 copy (residual of the down projection), fp16 copy of
-// h * g_post (operand of gate_up) and the row sums of h^2.
+// h (operand of gate_up, whose packed weights hold g_post) and the row sums
+// of h^2.
 __global__ void __launch_bounds__(FT) finalize_o_kernel(DecodeArgs a,
                                                         TcStreamK plan) {
   pdl_trigger();
@@ -136,13 +137,11 @@ __global__ void __launch_bounds__(FT) finalize_o_kernel(DecodeArgs a,
   if (b >= a.batch) return;
   const int H = a.hidden, n = t * 128 + lane * 4;
   const float4 xv = ld_bf16x4(a.x + (size_t)b * H + n);
-  const float4 gp = ld_bf16x4(a.g_post + n);
   const float4 o = gather_rows(a, plan, t, b);
   const float4 h = make_float4(xv.x + o.x, xv.y + o.y, xv.z + o.z, xv.w + o.w);
   *reinterpret_cast<float4*>(a.h32 + (size_t)b * H + n) = h;
   st_f16x4(a.hg + (size_t)b * H + n,
-           make_float4(h.x * gp.x * kHgScale, h.y * gp.y * kHgScale,
-                       h.z * gp.z * kHgScale, h.w * gp.w * kHgScale));
+           make_float4(h.x * kHgScale, h.y * kHgScale, h.z * kHgScale, h.w * kHgScale));
   const float ss = warp_sum(h.x * h.x + h.y * h.y + h.z * h.z + h.w * h.w);
   if (lane == 0) atomicAdd(a.ss2 + b, ss);
 }

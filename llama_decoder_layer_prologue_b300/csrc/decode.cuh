@@ -29,8 +29,7 @@ struct DecodeArgs {
   float* attn_part;        // split-KV records
   int max_chunks, n_rep_rec;
   float* h32;              // [B, H] h in fp32
-  __half* hg;              // [B, H] fp16(h * g_post * kHgScale), gate_up operand
-  const __nv_bfloat16* g_post;  // [H] RMSNorm weight of the MLP
+  __half* hg;              // [B, H] fp16(h * kHgScale), gate_up operand
   __half* act;             // [B, I] fp16(act * kActScale)
   __nv_bfloat16* out;      // [B, H]
   int* status;

@@ -54,106 +54,211 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles,
   n = w / gm;
 }
 
-__device__ __forceinline__ void load_bf16x32(const void* p, float* v) {
-  const uint4* q = reinterpret_cast<const uint4*>(p);
+// 256-bit global accesses (sm_100 and later): a lane moves one whole
+// 32-byte sector, so a warp's 32 row-accesses of one chunk are 32 full
+// sectors.  The 128-bit forms serve pointers that are only 16-byte aligned.
+// Both are volatile so that they keep their place relative to the mbarrier
+// waits and TMEM loads (a load issued before a wait overlaps it).
+__device__ __forceinline__ void ld_v8(const void* p, uint32_t* u) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]),
+                 "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void ld_v4(const void* p, uint32_t* u) {
+  asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void st_v8(void* p, const uint32_t* u) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+               "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]),
+               "r"(u[6]), "r"(u[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void st_v4(void* p, const uint32_t* u) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(u[0]),
+               "r"(u[1]), "r"(u[2]), "r"(u[3])
+               : "memory");
+}
+
+// `words` (a multiple of 8) 32-bit words at p, 32-byte or 16-byte accesses.
+template <int WORDS>
+__device__ __forceinline__ void ld_words(const void* p, uint32_t* u, bool v8) {
+  const char* c = static_cast<const char*>(p);
+  if (v8) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 u = q[i];
-    float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y),
-           c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
-    v[8 * i + 0] = a.x; v[8 * i + 1] = a.y; v[8 * i + 2] = b.x;
-    v[8 * i + 3] = b.y; v[8 * i + 4] = c.x; v[8 * i + 5] = c.y;
-    v[8 * i + 6] = d.x; v[8 * i + 7] = d.y;
+    for (int i = 0; i < WORDS / 8; ++i) ld_v8(c + 32 * i, u + 8 * i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < WORDS / 4; ++i) ld_v4(c + 16 * i, u + 4 * i);
   }
 }
 
-__device__ __forceinline__ void store_bf16x32(void* p, const float* v) {
-  uint4* q = reinterpret_cast<uint4*>(p);
+template <int WORDS>
+__device__ __forceinline__ void st_words(void* p, const uint32_t* u, bool v8) {
+  char* c = static_cast<char*>(p);
+  if (v8) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 u;
-    u.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-    u.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-    u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-    u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-    q[i] = u;
+    for (int i = 0; i < WORDS / 8; ++i) st_v8(c + 32 * i, u + 8 * i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < WORDS / 4; ++i) st_v4(c + 16 * i, u + 4 * i);
   }
 }
 
-__device__ __forceinline__ void store_f16x32(void* p, const float* v) {
-  uint4* q = reinterpret_cast<uint4*>(p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 u;
-    u.x = pack_f16x2(v[8 * i + 0], v[8 * i + 1]);
-    u.y = pack_f16x2(v[8 * i + 2], v[8 * i + 3]);
-    u.z = pack_f16x2(v[8 * i + 4], v[8 * i + 5]);
-    u.w = pack_f16x2(v[8 * i + 6], v[8 * i + 7]);
-    q[i] = u;
-  }
-}
-
-// bf16 or fp16 (16-bit elements) at element offset `off` of p.
+// 32 values as 16-bit elements (fp16 or bf16) at element offset `off` of p.
 __device__ __forceinline__ void store_16x32(void* p, size_t off, const float* v,
-                                            bool f16) {
-  if (f16)
-    store_f16x32(static_cast<__half*>(p) + off, v);
-  else
-    store_bf16x32(static_cast<__nv_bfloat16*>(p) + off, v);
-}
-
-__device__ __forceinline__ void store_f32x32(float* p, const float* v) {
-  float4* q = reinterpret_cast<float4*>(p);
+                                            bool f16, bool v8) {
+  uint32_t u[16];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  for (int i = 0; i < 16; ++i)
+    u[i] = f16 ? pack_f16x2(v[2 * i], v[2 * i + 1]) : pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  st_words<16>(static_cast<char*>(p) + 2 * off, u, v8);
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Residual words per 32-column chunk and chunks held in registers ahead of
+// use (the rest of TC_RESID's fp32 residual is requested into L2 first).
+template <int EPI>
+constexpr int kResidWords = EPI == TC_RESID_SS ? 16 : 32;
+template <int BN, int EPI>
+constexpr int kResidAhead = EPI == TC_RESID_SS ? BN / 64 : 2;
+
+// Inputs of one tile's epilogue that do not depend on the accumulator,
+// loaded before waiting for it: the residual of the first column chunk, the
+// row's RMS statistics, its RoPE position and cos / sin of the first chunk.
+struct EpiPre {
+  uint32_t w[64];           // residual chunks (bf16 pairs or fp32 bits)
+  uint32_t cs[32], sn[32];  // TC_QKV: cos / sin (fp32 bits) of frequencies 0..31
+  float f;               // TC_QKV: 1/RMS; TC_SWIGLU: sum of h^2
+  int p;                 // TC_QKV: position
+};
+
+// Column chunks of 32 that this epilogue warp covers: [c_begin, c_end).
+template <int BN>
+__device__ __forceinline__ int chunk_begin(int part) { return part * (BN / 64); }
+
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_prefetch(EpiPre& pre, int row, bool valid,
+                                                  int n0, int N, int part,
+                                                  const TcEpiArgs& ep) {
+  if (!valid) return;
+  if constexpr (EPI == TC_RESID_SS || EPI == TC_RESID) {
+    // TC_RESID_SS: every chunk of the bf16 residual (16 words each);
+    // TC_RESID: the first two fp32 chunks, the rest requested into L2
+    constexpr int RW = kResidWords<EPI>, AHEAD = kResidAhead<BN, EPI>;
+    const int cb = chunk_begin<BN>(part);
+#pragma unroll
+    for (int k = 0; k < BN / 64; ++k) {
+      const int col = n0 + (cb + k) * 32;
+      if (col >= N) break;
+      const size_t off = (size_t)row * ep.ldo + col;
+      if (k < AHEAD) {
+        if constexpr (EPI == TC_RESID_SS)
+          ld_words<RW>(static_cast<const __nv_bfloat16*>(ep.residual) + off,
+                       pre.w + k * RW, ep.vec32);
+        else
+          ld_words<RW>(static_cast<const float*>(ep.residual) + off, pre.w + k * RW, true);
+      } else {
+        prefetch_l2(static_cast<const float*>(ep.residual) + off);
+      }
+    }
+  } else if constexpr (EPI == TC_QKV) {
+    pre.f = ep.rowscale[row];
+    int p = ep.pos[row];
+    if (p < 0 || p >= ep.max_pos) {
+      set_status(ep.status, ST_BAD_POSITION);
+      p = 0;
+    }
+    pre.p = p;
+    const int half = ep.head_dim / 2;
+    ld_words<32>(ep.cos_t + (size_t)p * half, pre.cs, true);
+    ld_words<32>(ep.sin_t + (size_t)p * half, pre.sn, true);
+  } else if constexpr (EPI == TC_SWIGLU) {
+    pre.f = ep.ss_in[row];
+  }
+}
+
+// Adds the other piece of a split tile (fp32 row `fin`) into this thread's
+// TMEM row before the epilogue reads it: exactly the 32-column chunks that
+// this warp's epilogue reads (TC_SWIGLU: gate chunks 2 part, 2 part + 1 and
+// the matching up chunks 4 + 2 part, 5 + 2 part; otherwise the part's four
+// chunks), so no other warp's reads depend on it.
+template <int BN, int EPI>
+__device__ __forceinline__ void add_partial_tmem(uint32_t t_row, const float* fin,
+                                                 int part) {
+#pragma unroll 1
+  for (int k = 0; k < BN / 64; ++k) {
+    const int c = EPI == TC_SWIGLU ? (k < 2 ? 2 * part + k : 4 + 2 * part + (k - 2))
+                                   : part * (BN / 64) + k;
+    uint32_t u[32];
+    ld_words<32>(fin + c * 32, u, true);
+    float v[32];
+    tmem_ld32(t_row + c * 32, v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(u[j]);
+    tmem_st32(t_row + c * 32, v);  // waits for the store
+  }
+}
 
 // Epilogue of one accumulator row (TMEM lane) over column half `part` (0 or
 // 1) of the tile (two warps share each lane quadrant, one per half).
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool valid,
                                               int n0, int M, int N, int part,
-                                              const TcEpiArgs& ep) {
+                                              const TcEpiArgs& ep, EpiPre& pre) {
   if constexpr (EPI == TC_STORE || EPI == TC_RESID || EPI == TC_RESID_SS) {
+    // unrolled over the part's chunks so that the residual registers of
+    // every chunk stay in place (no copies that would wait on the loads)
+    constexpr int RW = kResidWords<EPI>, AHEAD = kResidAhead<BN, EPI>;
     float ss = 0.f;
-#pragma unroll 1
-    for (int c = part * (BN / 64); c < (part + 1) * (BN / 64); ++c) {
+    const int cb = chunk_begin<BN>(part);
+#pragma unroll
+    for (int k = 0; k < BN / 64; ++k) {
+      const int c = cb + k;
+      const int col = n0 + c * 32;
+      const bool live = valid && col < N;
+      const size_t off = (size_t)row * ep.ldo + col;
       float v[32];
       tmem_ld32(t_row + c * 32, v);
-      int col = n0 + c * 32;
-      if (valid && col < N) {
-        size_t off = (size_t)row * ep.ldo + col;
+      if (live) {
         if constexpr (EPI == TC_RESID_SS) {
-          float r[32];
-          load_bf16x32(static_cast<const __nv_bfloat16*>(ep.residual) + off, r);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v[j] += r[j];
-            ss = fmaf(v[j], v[j], ss);
+          for (int j = 0; j < 16; ++j) {
+            const float2 r = unpack_bf16x2(pre.w[k * RW + j]);
+            v[2 * j] += r.x;
+            v[2 * j + 1] += r.y;
           }
-          store_f32x32(static_cast<float*>(ep.out) + off, v);
-          load_bf16x32(static_cast<const __nv_bfloat16*>(ep.colscale) + col, r);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] *= v[j] * ep.out_scale;
-          store_16x32(ep.out2, off, r, ep.out_f16);
+          for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+          uint32_t hb[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) hb[j] = __float_as_uint(v[j]);
+          st_words<32>(static_cast<float*>(ep.out) + off, hb, true);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= ep.out_scale;
+          store_16x32(ep.out2, off, v, ep.out_f16, true);
+        } else if constexpr (EPI == TC_RESID) {
+          const float sc = ep.in_scale;
+          const int slot = (k % AHEAD) * RW;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = fmaf(sc, v[j], __uint_as_float(pre.w[slot + j]));
+          store_16x32(ep.out, off, v, false, ep.vec32);
+          // refill the slot with the chunk AHEAD further on (now in L2)
+          if (k + AHEAD < BN / 64 && col + AHEAD * 32 < N)
+            ld_words<RW>(static_cast<const float*>(ep.residual) + off + AHEAD * 32,
+                         pre.w + slot, true);
         } else {
-          if constexpr (EPI == TC_RESID) {
-            const float4* r4 =
-                reinterpret_cast<const float4*>(static_cast<const float*>(ep.residual) + off);
-            const float sc = ep.in_scale;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              float4 rr = r4[q];
-              v[4 * q] = fmaf(sc, v[4 * q], rr.x);
-              v[4 * q + 1] = fmaf(sc, v[4 * q + 1], rr.y);
-              v[4 * q + 2] = fmaf(sc, v[4 * q + 2], rr.z);
-              v[4 * q + 3] = fmaf(sc, v[4 * q + 3], rr.w);
-            }
-          }
-          store_bf16x32(static_cast<__nv_bfloat16*>(ep.out) + off, v);
+          store_16x32(ep.out, off, v, false, ep.vec32);
         }
       }
     }
@@ -162,43 +267,36 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
     }
   } else if constexpr (EPI == TC_QKV) {
     const int d = ep.head_dim, half = d / 2;
-    float rs = 0.f;
-    int p = 0;
-    if (valid) {
-      rs = ep.rowscale[row];
-      p = ep.pos[row];
-      if (p < 0 || p >= ep.max_pos) {
-        set_status(ep.status, ST_BAD_POSITION);
-        p = 0;
-      }
-    }
-    const float* cs = ep.cos_t + (size_t)p * half;
-    const float* sn = ep.sin_t + (size_t)p * half;
+    const float rs = valid ? pre.f : 0.f;
 #pragma unroll 1
     for (int hb = part * (BN / 2); hb < (part + 1) * (BN / 2); hb += d) {
       const int hc = n0 + hb;
       const bool rope = hc < ep.rope_cols;
 #pragma unroll 1
       for (int c = 0; c < half; c += 32) {
+        // frequencies 32..63 (head_dim 128: one head block per part, so
+        // the prefetched 0..31 are not needed again)
+        if (c > 0 && valid) {
+          ld_words<32>(ep.cos_t + (size_t)pre.p * half + c, pre.cs, true);
+          ld_words<32>(ep.sin_t + (size_t)pre.p * half + c, pre.sn, true);
+        }
         float x1[32], x2[32];
-        tmem_ld32(t_row + hb + c, x1);
-        tmem_ld32(t_row + hb + half + c, x2);
+        tmem_ld32_nowait(t_row + hb + c, x1);
+        tmem_ld32_nowait(t_row + hb + half + c, x2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          tmem_pin(x1[j]);
+          tmem_pin(x2[j]);
+        }
         if (valid && hc < N) {
           if (rope) {
-            const float4* c4 = reinterpret_cast<const float4*>(cs + c);
-            const float4* s4 = reinterpret_cast<const float4*>(sn + c);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              float4 cc = c4[q], ss = s4[q];
-              float cv[4] = {cc.x, cc.y, cc.z, cc.w};
-              float sv[4] = {ss.x, ss.y, ss.z, ss.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                int j = 4 * q + e;
-                float a = rs * x1[j], b = rs * x2[j];
-                x1[j] = a * cv[e] - b * sv[e];
-                x2[j] = b * cv[e] + a * sv[e];
-              }
+            for (int j = 0; j < 32; ++j) {
+              const float a = rs * x1[j], b = rs * x2[j];
+              const float cj = __uint_as_float(pre.cs[j]), sj = __uint_as_float(pre.sn[j]);
+              x1[j] = a * cj - b * sj;
+              x2[j] = b * cj + a * sj;
             }
           } else {
 #pragma unroll
@@ -208,26 +306,31 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
             }
           }
           const size_t o = (size_t)row * ep.ldo + hc + c;
-          store_16x32(ep.out, o, x1, ep.out_f16);
-          store_16x32(ep.out, o + half, x2, ep.out_f16);
+          store_16x32(ep.out, o, x1, ep.out_f16, true);
+          store_16x32(ep.out, o + half, x2, ep.out_f16, true);
         }
       }
     }
   } else if constexpr (EPI == TC_SWIGLU) {
     static_assert(BN == 256, "gate/up interleave is 128 + 128");
-    const float r2 =
-        valid ? ep.in_scale * rsqrtf(ep.ss_in[row] * ep.inv_h + ep.eps) : 0.f;
+    const float r2 = valid ? ep.in_scale * rsqrtf(pre.f * ep.inv_h + ep.eps) : 0.f;
 #pragma unroll 1
     for (int c = part * 2; c < part * 2 + 2; ++c) {
       float g[32], u[32];
-      tmem_ld32(t_row + c * 32, g);
-      tmem_ld32(t_row + 128 + c * 32, u);
+      tmem_ld32_nowait(t_row + c * 32, g);
+      tmem_ld32_nowait(t_row + 128 + c * 32, u);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        tmem_pin(g[j]);
+        tmem_pin(u[j]);
+      }
       int col = n0 / 2 + c * 32;
       if (valid && n0 < N) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           g[j] = silu(r2 * g[j]) * (r2 * u[j]) * ep.out_scale;
-        store_16x32(ep.out, (size_t)row * ep.ldo + col, g, ep.out_f16);
+        store_16x32(ep.out, (size_t)row * ep.ldo + col, g, ep.out_f16, true);
       }
     }
   }
@@ -236,7 +339,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
 // Work of one CTA as a sequence of segments (tile, K-blocks [kb0, kb1), slot).
 //   tile-stride mode: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...,
 //                     visited in bands of GROUP_M M-tiles.
-//   stream-K mode:    the CTA owns the global K-block range
+//   split phase:      before those, the first sk_tiles tiles (in the same
+//                     order) are shared by K-block: the CTA owns units
+//                     [c W / G, (c + 1) W / G) of W = sk_tiles * kb_total, at
+//                     least one tile's worth, so a tile is cut at most once;
+//                     the tile-stride tiles then start at sk_tiles.
+//   stream-K mode:    (TC_PARTIAL) the CTA owns the global K-block range
 //                     [c W / G, (c + 1) W / G) of W = tiles * kb_total; each
 //                     run inside one tile is a segment whose fp32 partial goes
 //                     to slot (c - first CTA of that tile).
@@ -246,7 +354,7 @@ struct Sched {
   long long W, g, g_end;
   int next_tile;
 
-  __device__ Sched(int M, int N, int K, int bn, bool sk) {
+  __device__ Sched(int M, int N, int K, int bn, bool sk, int sk_tiles) {
     m_tiles = (M + BM - 1) / BM;
     n_tiles = (N + bn - 1) / bn;
     kb_total = (K + BK - 1) / BK;
@@ -254,35 +362,40 @@ struct Sched {
     grid = gridDim.x;
     cta = blockIdx.x;
     stream_k = sk;
-    W = (long long)num_tiles * kb_total;
+    const int split = sk ? num_tiles : sk_tiles;
+    W = (long long)split * kb_total;
     g = (long long)cta * W / grid;
     g_end = (long long)(cta + 1) * W / grid;
-    next_tile = cta;
+    next_tile = sk ? num_tiles : split + cta;
   }
 
   __device__ bool next(int& mt, int& nt, int& kb0, int& kb1, int& tile,
                        int& slot) {
-    if (!stream_k) {
-      if (next_tile >= num_tiles) return false;
-      tile = next_tile;
-      tile_coords(tile, m_tiles, n_tiles, mt, nt);
-      kb0 = 0;
-      kb1 = kb_total;
-      slot = 0;
-      next_tile += grid;
+    if (g < g_end) {
+      tile = (int)(g / kb_total);
+      kb0 = (int)(g - (long long)tile * kb_total);
+      long long left = g_end - g;
+      kb1 = (int)(kb0 + left < kb_total ? kb0 + left : kb_total);
+      g += kb1 - kb0;
+      if (stream_k) {
+        long long gs = (long long)tile * kb_total;
+        int first = (int)(((gs + 1) * grid - 1) / W);
+        slot = cta - first;
+        mt = tile / n_tiles;
+        nt = tile - mt * n_tiles;
+      } else {
+        slot = 0;
+        tile_coords(tile, m_tiles, n_tiles, mt, nt);
+      }
       return true;
     }
-    if (g >= g_end) return false;
-    tile = (int)(g / kb_total);
-    kb0 = (int)(g - (long long)tile * kb_total);
-    long long left = g_end - g;
-    kb1 = (int)(kb0 + left < kb_total ? kb0 + left : kb_total);
-    long long gs = (long long)tile * kb_total;
-    int first = (int)(((gs + 1) * grid - 1) / W);
-    slot = cta - first;
-    mt = tile / n_tiles;
-    nt = tile - mt * n_tiles;
-    g += kb1 - kb0;
+    if (next_tile >= num_tiles) return false;
+    tile = next_tile;
+    tile_coords(tile, m_tiles, n_tiles, mt, nt);
+    kb0 = 0;
+    kb1 = kb_total;
+    slot = 0;
+    next_tile += grid;
     return true;
   }
 };
@@ -304,6 +417,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // arrivals of the epilogue threads at the split tiles' flags
+  int* sk_count = const_cast<int*>(abort_flag) + 1;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -317,6 +432,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    sk_count[0] = sk_count[1] = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -329,7 +445,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  Sched sched(M, N, K, BN, kStreamK);
+  Sched sched(M, N, K, BN, kStreamK, ep.sk_tiles);
   int mt, nt, kb0, kb1, tile, slot;
 
   pdl_trigger();
@@ -447,11 +563,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     while (sched.next(mt, nt, kb0, kb1, tile, slot)) {
       const uint32_t acc = local & 1, acc_phase = (local >> 1) & 1;
       ++local;
+      const int r = quad * 32 + lane;
+      EpiPre pre;
+      if constexpr (EPI != TC_PARTIAL)
+        epilogue_prefetch<BN, EPI>(pre, mt * BM + r, mt * BM + r < M, nt * BN, N, part, ep);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_phase, ep.status, abort_flag);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       tc_fence_after();
-      const int r = quad * 32 + lane;
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
       if constexpr (EPI == TC_PARTIAL) {
         // token-major slot: column c of the tile is 128 consecutive floats,
@@ -465,9 +584,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int q = 0; q < 32; ++q) o[(size_t)(c * 32 + q) * BM] = v[q];
         }
+      } else if (kb0 > 0) {
+        // the later K-blocks of a split tile, computed first: hand the fp32
+        // sums to the CTA that finishes the tile (blockIdx.x - 1)
+        float* dst = ep.sk_part + ((size_t)blockIdx.x * BM + r) * BN;
+#pragma unroll 1
+        for (int c = part * (BN / 64); c < (part + 1) * (BN / 64); ++c) {
+          float v[32];
+          tmem_ld32(t_row + c * 32, v);
+          uint32_t u[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(v[j]);
+          st_words<32>(dst + c * 32, u, true);
+        }
+        __threadfence();
+        if (atomicAdd(&sk_count[0], 1) == kEpiWarps * 32 - 1)
+          st_release_gpu(ep.sk_flag + blockIdx.x, ep.sk_epoch);
       } else {
         const int row = mt * BM + r;
-        epilogue_tile<BN, EPI>(t_row, row, row < M, nt * BN, M, N, part, ep);
+        const bool split = kb1 < sched.kb_total;  // the rest comes from CTA + 1
+        if (split && flag_wait(ep.sk_flag + blockIdx.x + 1, ep.sk_epoch, ep.status,
+                               abort_flag))
+          add_partial_tmem<BN, EPI>(t_row, ep.sk_part + ((size_t)(blockIdx.x + 1) * BM + r) * BN,
+                               part);
+        epilogue_tile<BN, EPI>(t_row, row, row < M, nt * BN, M, N, part, ep, pre);
+        // every thread has read its rows: clear the flag for the next launch
+        if (split && atomicAdd(&sk_count[1], 1) == kEpiWarps * 32 - 1)
+          ep.sk_flag[blockIdx.x + 1] = 0;
       }
       tc_fence_before();
       __syncwarp();
@@ -497,6 +640,10 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
   }
   if (grid <= 0) return cudaSuccess;
   TcEpiArgs e = ep;
+  const uintptr_t al = reinterpret_cast<uintptr_t>(e.out) |
+                       reinterpret_cast<uintptr_t>(e.out2) |
+                       reinterpret_cast<uintptr_t>(e.residual);
+  e.vec32 = (al & 31) == 0 && e.ldo % 16 == 0;
   if (!e.status) {
     cudaError_t err = cudaGetSymbolAddress((void**)&e.status, g_tc_status);
     if (err != cudaSuccess) return err;
@@ -558,17 +705,32 @@ TcStreamK tc_streamk_plan(int M, int N, int K, int bn, int grid_limit) {
   return p;
 }
 
+int tc_split_tiles(int tiles, int grid, int kb_total) {
+  // a split costs a 128 KB store and reload per cut tile and one more
+  // epilogue pass: worth it only behind a long main loop
+  if (kb_total < 64) return 0;
+  if (grid <= 0 || tiles <= grid || tiles % grid == 0) return 0;
+  const int rounds = (tiles + grid - 1) / grid;
+  const double idle = rounds - (double)tiles / grid;  // in rounds
+  if (idle <= 0.03 * rounds) return 0;
+  return grid + tiles % grid;
+}
+
 cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
                     const CUtensorMap& tb, int M, int N, int K,
                     const TcEpiArgs& ep, int grid_limit, cudaStream_t s) {
   int tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
   int grid = tiles < grid_limit ? tiles : grid_limit;
+  TcEpiArgs e = ep;
+  e.sk_tiles = 0;
+  if (epi != TC_PARTIAL && ep.sk_part && ep.sk_flag && ep.sk_epoch != 0)
+    e.sk_tiles = tc_split_tiles(tiles, grid, (K + BK - 1) / BK);
   switch (epi) {
-    case TC_STORE: return launch<256, 4, TC_STORE>(ta, tb, M, N, K, ep, grid, s);
-    case TC_QKV: return launch<256, 4, TC_QKV>(ta, tb, M, N, K, ep, grid, s);
-    case TC_RESID_SS: return launch<256, 4, TC_RESID_SS>(ta, tb, M, N, K, ep, grid, s);
-    case TC_SWIGLU: return launch<256, 4, TC_SWIGLU>(ta, tb, M, N, K, ep, grid, s);
-    case TC_RESID: return launch<256, 4, TC_RESID>(ta, tb, M, N, K, ep, grid, s);
+    case TC_STORE: return launch<256, 4, TC_STORE>(ta, tb, M, N, K, e, grid, s);
+    case TC_QKV: return launch<256, 4, TC_QKV>(ta, tb, M, N, K, e, grid, s);
+    case TC_RESID_SS: return launch<256, 4, TC_RESID_SS>(ta, tb, M, N, K, e, grid, s);
+    case TC_SWIGLU: return launch<256, 4, TC_SWIGLU>(ta, tb, M, N, K, e, grid, s);
+    case TC_RESID: return launch<256, 4, TC_RESID>(ta, tb, M, N, K, e, grid, s);
     case TC_PARTIAL: {
       TcStreamK p = tc_streamk_plan(M, N, K, bn, grid_limit);
       if (p.slots != ep.part_slots) return cudaErrorInvalidValue;

@@ -11,7 +11,7 @@ namespace llama {
 enum TcEpi : int {
   TC_STORE = 0,     // out = acc (bf16)
   TC_QKV = 1,       // out = r1[m] * acc, RoPE on q / k head columns
-  TC_RESID_SS = 2,  // h = res + acc: out = h (fp32), out2 = bf16(h * colscale),
+  TC_RESID_SS = 2,  // h = res + acc: out = h (fp32), out2 = 16-bit(h * out_scale),
                     // ss_out[m] += sum over the row of h^2
   TC_SWIGLU = 3,    // gate|up interleaved by 128: out = silu(r2 g) * (r2 u)
   TC_RESID = 4,     // out = res (fp32) + acc
@@ -21,9 +21,8 @@ enum TcEpi : int {
 struct TcEpiArgs {
   void* out = nullptr;  // bf16 [M, ldo] (TC_SWIGLU: [M, N/2]); fp32 partials
   int ldo = 0;
-  void* out2 = nullptr;            // TC_RESID_SS: bf16(h * colscale)
+  void* out2 = nullptr;            // TC_RESID_SS: 16-bit h * out_scale
   const void* residual = nullptr;  // TC_RESID_SS: bf16; TC_RESID: fp32 [M, ldo]
-  const void* colscale = nullptr;  // TC_RESID_SS: bf16 [ldo] (RMSNorm weight)
   const float* rowscale = nullptr; // r1 [M]
   const float* ss_in = nullptr;    // sum of squares of h [M] (TC_SWIGLU)
   float* ss_out = nullptr;         // TC_RESID_SS
@@ -41,6 +40,20 @@ struct TcEpiArgs {
                          // TC_RESID: out = res + in_scale * acc
   float out_scale = 1.f; // TC_SWIGLU: act stored * out_scale; TC_RESID_SS: out2 * out_scale
   int pdl = 0;           // launch with programmatic dependent launch
+  // Split tiles (whole-tile epilogues): when sk_part is set and the tiles do
+  // not fill whole rounds of the grid, tc_gemm spreads the first
+  // grid + (tiles % grid) tiles evenly over the CTAs by K-block.  A tile cut
+  // between CTAs c and c + 1 is finished by c: c + 1 computes its K-blocks
+  // first, stores the fp32 sums in sk_part[c + 1][128][bn] and sets
+  // sk_flag[c + 1] = sk_epoch; c adds them in its epilogue and clears the
+  // flag.  sk_part holds grid slots; sk_flag grid + 1 words, zero when no
+  // launch is in flight; sk_epoch must be nonzero and differ from the
+  // previous launch that used the same flags.
+  float* sk_part = nullptr;
+  uint32_t* sk_flag = nullptr;
+  uint32_t sk_epoch = 0;
+  int sk_tiles = 0;      // set by tc_gemm: tiles of the split phase
+  int vec32 = 0;         // set by tc_gemm: out / residual rows are 32-byte aligned
 };
 
 // Encodes a 2-D bf16 tensor map over a row-major [rows, cols] matrix with a
@@ -68,9 +81,16 @@ __host__ __device__ inline int tc_streamk_segments(const TcStreamK& p, int t) {
 // Launches the persistent GEMM.  TC_PARTIAL: bn in {64, 128, 256} (N <= bn
 // tokens), stream-K over min(grid_limit, K-blocks) CTAs, ep.part_slots must
 // equal tc_streamk_plan(...).slots.  Other epilogues: bn = 256, whole tiles
-// over min(grid_limit, tiles) CTAs.
+// over min(grid_limit, tiles) CTAs, with the split-tile phase when
+// tc_split_tiles() is nonzero and ep.sk_part is set.
 cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
                     const CUtensorMap& tb, int M, int N, int K,
                     const TcEpiArgs& ep, int grid_limit, cudaStream_t s);
+
+// Tiles of the split phase for a whole-tile GEMM of `tiles` tiles of
+// kb_total K-blocks on `grid` CTAs: grid + tiles % grid when the last round
+// of plain tile rounds would leave more than 3 % of the rounds' time idle
+// and a tile has at least 64 K-blocks, else 0.
+int tc_split_tiles(int tiles, int grid, int kb_total);
 
 }  // namespace llama

@@ -9,9 +9,10 @@
 namespace llama {
 
 // Scales of the fp16 intermediates of the bf16 layer (powers of two, so
-// exact): the gate_up operand h * g_post is stored times kHgScale and the
-// SwiGLU output act times kActScale, leaving fp16 headroom for large hidden
-// states; the consuming epilogues multiply back.
+// exact): the gate_up operand h (g_post lives in the packed W_gate_up) is
+// stored times kHgScale and the SwiGLU output act times kActScale, leaving
+// fp16 headroom for large hidden states; the consuming epilogues multiply
+// back.
 constexpr float kHgScale = 1.0f / 256.0f;
 constexpr float kActScale = 1.0f / 16.0f;
 

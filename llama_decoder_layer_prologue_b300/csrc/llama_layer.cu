@@ -21,6 +21,10 @@ using namespace llama;
 namespace {
 
 constexpr size_t kAlign = 256;
+// Split-tile phase of the prefill GEMMs: CTAs (one per SM) it supports, and
+// the fp32 slot of one 128 x 256 tile piece.
+constexpr int kMaxSkCtas = 160;
+constexpr size_t kSkSlotBytes = 128 * 256 * sizeof(float);
 
 size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
@@ -29,7 +33,7 @@ bool aligned(const void* p, size_t a) {
 }
 
 struct PackedLayout {
-  size_t wqkv, wo, wgu, wd, gpost, cos_t, sin_t, status, total;
+  size_t wqkv, wo, wgu, wd, gpost, cos_t, sin_t, status, skflag, total;
 };
 
 PackedLayout packed_layout(const llama_layer_config& c) {
@@ -47,6 +51,7 @@ PackedLayout packed_layout(const llama_layer_config& c) {
   p.cos_t = o; o = align_up(o + table);
   p.sin_t = o; o = align_up(o + table);
   p.status = o; o = align_up(o + 64);
+  p.skflag = o; o = align_up(o + (kMaxSkCtas + 1) * sizeof(uint32_t));
   p.total = o;
   return p;
 }
@@ -100,7 +105,7 @@ void rope_inv_freq(const llama_layer_config& c, double* f) {
 }
 
 struct WsLayout {
-  size_t pos, r1, ss2, qkv, attn, h, hg, act, total;
+  size_t pos, r1, ss2, qkv, attn, h, hg, act, sk, total;
 };
 
 WsLayout ws_layout(const llama_layer_config& c, int tokens) {
@@ -115,8 +120,10 @@ WsLayout ws_layout(const llama_layer_config& c, int tokens) {
   w.qkv = o; o = align_up(o + T * nqkv * es);
   w.attn = o; o = align_up(o + T * c.n_heads * c.head_dim * es);
   w.h = o; o = align_up(o + T * c.hidden * 4);     // fp32
-  w.hg = o; o = align_up(o + T * c.hidden * es);   // h * g_post
+  w.hg = o; o = align_up(o + T * c.hidden * es);   // MLP input
   w.act = o; o = align_up(o + T * c.intermediate * es);
+  w.sk = o;  // split-tile pieces of the tensor-core GEMMs (bf16 layers)
+  if (c.dtype == LLAMA_DTYPE_BF16 && T > 0) o = align_up(o + kMaxSkCtas * kSkSlotBytes);
   w.total = o;
   return w;
 }
@@ -142,6 +149,8 @@ struct llama_layer {
   const char** stage_name;   // [ring][LLAMA_MAX_STAGES]
   int* n_marks;              // [ring]
   int launches;  // kernels launched by the last forward / decode call
+  uint32_t* sk_flag;  // split-tile flags (packed buffer, zeroed at init)
+  uint32_t sk_epoch;  // value of the last split-tile launch's flags
 };
 
 namespace {
@@ -211,6 +220,15 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
   if (b16) {
     cudaError_t e;
     CUtensorMap ta;
+    // Split-tile phase: pieces in the workspace, flags in the packed buffer,
+    // a new nonzero epoch per launch.
+    auto split = [&](TcEpiArgs& a) {
+      if (L->sm_count > kMaxSkCtas) return;
+      a.sk_part = reinterpret_cast<float*>(ws + w.sk);
+      a.sk_flag = L->sk_flag;
+      if (++L->sk_epoch == 0) ++L->sk_epoch;
+      a.sk_epoch = L->sk_epoch;
+    };
     TcEpiArgs ep;
     ep.status = L->status;
     ep.pdl = 1;
@@ -221,6 +239,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.rope_cols = (dm.Hq + dm.Hkv) * dm.d; ep.max_pos = dm.max_pos;
     ep.out_f16 = 1;  // q | k | v in fp16 for the attention
     mark(L, s, "qkv_rope");
+    split(ep);
     e = tc_gemm(TC_QKV, 256, ta, L->tm_wqkv, T, dm.Nqkv, dm.H, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
     ++L->launches;
@@ -241,13 +260,15 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.status = L->status;
     ep.pdl = 1;
     ep.out = h; ep.out2 = ws + w.hg; ep.ldo = dm.H; ep.residual = x;
-    ep.colscale = P + L->pl.gpost; ep.ss_out = ss2;
+    ep.ss_out = ss2;
     ep.ab_f16 = 1; ep.out_f16 = 1; ep.out_scale = kHgScale;
     mark(L, s, "o_proj_residual");
+    split(ep);
     e = tc_gemm(TC_RESID_SS, 256, ta, L->tm_wo, T, dm.H, dm.Hq * dm.d, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
     ++L->launches;
-    // a8: gate_up on h * g_post with the RMSNorm row scale, silu(gate) * up.
+    // a8: gate_up (g_post folded into its packed weights) on h with the
+    // RMSNorm row scale, silu(gate) * up.
     if (!tc_encode_bf16(&ta, ws + w.hg, T, dm.H, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
     ep.status = L->status;
@@ -255,6 +276,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.out = act; ep.ldo = dm.I; ep.ss_in = ss2; ep.inv_h = 1.0f / dm.H; ep.eps = dm.eps;
     ep.ab_f16 = 1; ep.in_scale = 1.0f / kHgScale; ep.out_f16 = 1; ep.out_scale = kActScale;
     mark(L, s, "gate_up_swiglu");
+    split(ep);
     e = tc_gemm(TC_SWIGLU, 256, ta, L->tm_wgu, T, 2 * dm.I, dm.H, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
     ++L->launches;
@@ -266,6 +288,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.out = out; ep.ldo = dm.H; ep.residual = h;
     ep.ab_f16 = 1; ep.in_scale = 1.0f / kActScale;
     mark(L, s, "down_residual");
+    split(ep);
     e = tc_gemm(TC_RESID, 256, ta, L->tm_wd, T, dm.H, dm.I, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
     ++L->launches;
@@ -360,7 +383,6 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   a.max_chunks = w.max_chunks; a.n_rep_rec = w.rec;
   a.h32 = reinterpret_cast<float*>(ws + w.h32);
   a.hg = reinterpret_cast<__half*>(ws + w.hg);
-  a.g_post = reinterpret_cast<const __nv_bfloat16*>(P + L->pl.gpost);
   a.act = reinterpret_cast<__half*>(ws + w.act);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.status = L->status;
@@ -518,6 +540,8 @@ int llama_layer_init(const llama_layer_config* cfg,
   L->packed = static_cast<char*>(packed);
   L->pl = pl;
   L->status = reinterpret_cast<int*>(L->packed + pl.status);
+  L->sk_flag = reinterpret_cast<uint32_t*>(L->packed + pl.skflag);
+  L->sk_epoch = 0;
   L->sm_count = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& dm = L->dm;
@@ -532,8 +556,11 @@ int llama_layer_init(const llama_layer_config* cfg,
               dm.Hq * dm.d, 0, f16, s);
   launch_pack(L->bf16, wts->g_post, nullptr, L->packed + pl.gpost, 1, dm.H, 0,
               false, s);
-  launch_pack(L->bf16, wts->w_gate_up, nullptr, L->packed + pl.wgu,
-              2 * dm.I, dm.H, dm.I, f16, s);
+  // bf16 layers also fold g_post into the columns of W_gate_up (the fp16
+  // product of two bf16 values is within 2^-12 of exact), so the MLP input
+  // is h itself; the fp32 layer scales h by g_post instead.
+  launch_pack(L->bf16, wts->w_gate_up, f16 ? wts->g_post : nullptr,
+              L->packed + pl.wgu, 2 * dm.I, dm.H, dm.I, f16, s);
   launch_pack(L->bf16, wts->w_down, nullptr, L->packed + pl.wd, dm.H, dm.I, 0,
               f16, s);
 
@@ -560,7 +587,9 @@ int llama_layer_init(const llama_layer_config* cfg,
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(L->packed + pl.sin_t, host + n, n * 4,
                         cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(L->status, 0, 64, s);
+  // status word and split-tile flags start at zero
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(L->packed + pl.status, 0, pl.total - pl.status, s);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   delete[] host;

@@ -70,11 +70,35 @@ def test_tiny_fp32_workload():
     # head_dim 128 packed sequences, many shorter than a query tile
     ("varlen_d128_short", shape(512, 4, 2, 128, 256, **L3), "varlen",
      dict(total_tokens=400, min_len=1, max_len=40)),
+    # GEMMs with 64 K-blocks whose tiles leave the last round of 148 SMs
+    # partly idle run the split-tile phase (tiles cut between two CTAs):
+    # here QKV (384 tiles), o_proj (256) and gate_up (304) ...
+    ("split_tiles_wide", shape(4096, 32, 8, 128, 2432), "padded",
+     dict(batch=2, seq=1024)),
+    # ... and down_proj (200 tiles, ragged last row tile, packed sequences)
+    ("split_tiles_down_varlen", shape(512, 8, 2, 64, 4096, **L3), "varlen",
+     dict(total_tokens=12700, min_len=1, max_len=1000)),
 ])
 def test_small_bf16_forward(case):
     name, s, kind, kw = case
     w = synth.custom_workload(name, s, kind, **kw)
     check_forward(synth.make_inputs(w), varlen=(kind == "varlen"))
+
+
+def test_split_tiles_repeated_calls():
+    # every launch must find the split-tile flags cleared by the previous one
+    # and wait for its own pieces (a new epoch), call after call
+    s = shape(512, 8, 2, 64, 4096, **L3)
+    w = synth.custom_workload("split_rep", s, "padded", batch=4, seq=3200)
+    inp = synth.make_inputs(w)
+    layer = build_layer(inp)
+    ref = oracle.decoder_layer(synth.to_f64(inp.x), weights_f64(inp.weights),
+                               s, inp.positions, inp.cu_seqlens)
+    for _ in range(3):
+        out = run_forward(layer, inp, varlen=False)
+        assert layer.status() == B.LLAMA_OK
+        assert_close(to_f64(out), ref["out"], s.dtype, "out")
+    layer.close()
 
 
 def test_explicit_position_ids():
