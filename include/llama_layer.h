@@ -186,13 +186,14 @@ LLAMA_API int llama_layer_status(llama_layer_t* layer, void* stream);
  * with these sizes, for checking individual stages:
  *   [0] q|k|v after RoPE   [tokens, n_heads*d + 2*n_kv_heads*d]
  *   [1] attention output    [tokens, n_heads*d]
- *   [2] h (after o_proj + residual) [tokens, hidden]              fp32
+ *   [2] h (after o_proj + residual) [tokens, hidden]
  *   [3] act = silu(gate)*up [tokens, intermediate]
  * Element types: fp32 layers keep everything in fp32.  bf16 layers (bf16
  * input, weights, output and cache) keep their intermediates in fp16, which
  * holds bf16 values exactly and rounds 8x finer: q|k|v is fp16 for
  * llama_layer_forward and bf16 for llama_layer_decode (it is written to the
- * bf16 cache); the attention output is fp16; act is fp16 holding act / 16.
+ * bf16 cache); the attention output is fp16; h is fp16 holding h / 256 (the
+ * MLP input and the residual of down_proj); act is fp16 holding act / 16.
  * decode == 1 gives the decode layout (tokens <= 256). */
 #define LLAMA_WS_NUM 4
 LLAMA_API int llama_layer_workspace_offsets(const llama_layer_t* layer, int tokens,

@@ -79,7 +79,8 @@ __device__ __forceinline__ void st_f16x4(__half* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 
-// q, k, v of the new tokens: row scale 1/RMS, RoPE at start_pos on q and k,
+// q, k, v of the new tokens (the GEMM's operand is already x / RMS(x)): RoPE
+// at start_pos on q and k,
 // all three -> qkv[b, :], k and v also -> cache row start_pos[b].  Head
 // boundaries fall on 4-row groups and head_dim divides 128, so the RoPE
 // partner rows i +- D/2 sit D/8 lanes away in the same warp.
@@ -91,7 +92,6 @@ __global__ void __launch_bounds__(FT) finalize_qkv_kernel(DecodeArgs a,
   const int lane = threadIdx.x & 31;
   if (b >= a.batch) return;
   const int sp = a.start_pos[b];
-  const float r1 = a.r1[b];
   float4 x = gather_rows(a, plan, t, b);
   if (!start_ok(sp, a)) {
     if (lane == 0) set_status(a.status, ST_BAD_START_POS);
@@ -101,7 +101,6 @@ __global__ void __launch_bounds__(FT) finalize_qkv_kernel(DecodeArgs a,
   const int hq = a.n_heads, hkv = a.n_kv_heads;
   const int n = t * 128 + lane * 4;
   const int head = n / D, i = n - head * D;
-  x.x *= r1; x.y *= r1; x.z *= r1; x.w *= r1;
   const int dl = half / 4;  // partner lane offset
   float4 y;
   y.x = __shfl_xor_sync(0xffffffffu, x.x, dl);
@@ -125,8 +124,8 @@ __global__ void __launch_bounds__(FT) finalize_qkv_kernel(DecodeArgs a,
   }
 }
 
-// h = x + o_proj: fp32 copy (residual of the down projection), fp16 copy of
-// h (operand of gate_up, whose packed weights hold g_post) and the row sums
+// h = x + o_proj: fp16 copy h / 256 (operand of gate_up, whose packed
+// weights hold g_post, and residual of the down projection) and the row sums
 // of h^2.
 __global__ void __launch_bounds__(FT) finalize_o_kernel(DecodeArgs a,
                                                         TcStreamK plan) {
@@ -139,7 +138,6 @@ __global__ void __launch_bounds__(FT) finalize_o_kernel(DecodeArgs a,
   const float4 xv = ld_bf16x4(a.x + (size_t)b * H + n);
   const float4 o = gather_rows(a, plan, t, b);
   const float4 h = make_float4(xv.x + o.x, xv.y + o.y, xv.z + o.z, xv.w + o.w);
-  *reinterpret_cast<float4*>(a.h32 + (size_t)b * H + n) = h;
   st_f16x4(a.hg + (size_t)b * H + n,
            make_float4(h.x * kHgScale, h.y * kHgScale, h.z * kHgScale, h.w * kHgScale));
   const float ss = warp_sum(h.x * h.x + h.y * h.y + h.z * h.z + h.w * h.w);
@@ -170,7 +168,7 @@ __global__ void __launch_bounds__(FT) finalize_gu_kernel(DecodeArgs a,
            make_float4(av[0], av[1], av[2], av[3]));
 }
 
-// out = h + down_proj.
+// out = h + down_proj, h from its fp16 copy.
 __global__ void __launch_bounds__(FT) finalize_down_kernel(DecodeArgs a,
                                                            TcStreamK plan) {
   pdl_trigger();
@@ -179,7 +177,11 @@ __global__ void __launch_bounds__(FT) finalize_down_kernel(DecodeArgs a,
   const int lane = threadIdx.x & 31;
   if (b >= a.batch) return;
   const int H = a.hidden, n = t * 128 + lane * 4;
-  const float4 h = __ldcg(reinterpret_cast<const float4*>(a.h32 + (size_t)b * H + n));
+  const uint2 hu = __ldcg(reinterpret_cast<const uint2*>(a.hg + (size_t)b * H + n));
+  const float2 h01 = __half22float2(*reinterpret_cast<const __half2*>(&hu.x));
+  const float2 h23 = __half22float2(*reinterpret_cast<const __half2*>(&hu.y));
+  constexpr float hs = 1.0f / kHgScale;
+  const float4 h = make_float4(hs * h01.x, hs * h01.y, hs * h23.x, hs * h23.y);
   const float4 d = gather_rows(a, plan, t, b);
   constexpr float is = 1.0f / kActScale;
   st_bf16x4(a.out + (size_t)b * H + n,

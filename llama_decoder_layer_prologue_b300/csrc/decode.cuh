@@ -28,8 +28,7 @@ struct DecodeArgs {
   __half* attn;            // [B, Hq * D] fp16
   float* attn_part;        // split-KV records
   int max_chunks, n_rep_rec;
-  float* h32;              // [B, H] h in fp32
-  __half* hg;              // [B, H] fp16(h * kHgScale), gate_up operand
+  __half* hg;              // [B, H] fp16(h * kHgScale): gate_up operand, residual
   __half* act;             // [B, I] fp16(act * kActScale)
   __nv_bfloat16* out;      // [B, H]
   int* status;

@@ -122,22 +122,15 @@ __device__ __forceinline__ void store_16x32(void* p, size_t off, const float* v,
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
-// Residual words per 32-column chunk and chunks held in registers ahead of
-// use (the rest of TC_RESID's fp32 residual is requested into L2 first).
-template <int EPI>
-constexpr int kResidWords = EPI == TC_RESID_SS ? 16 : 32;
-template <int BN, int EPI>
-constexpr int kResidAhead = EPI == TC_RESID_SS ? BN / 64 : 2;
+// Residual words (16-bit pairs) per 32-column chunk; every chunk of the
+// part is loaded before the accumulator wait.
+constexpr int kResidWords = 16;
 
 // Inputs of one tile's epilogue that do not depend on the accumulator,
 // loaded before waiting for it: the residual of the first column chunk, the
 // row's RMS statistics, its RoPE position and cos / sin of the first chunk.
 struct EpiPre {
-  uint32_t w[64];           // residual chunks (bf16 pairs or fp32 bits)
+  uint32_t w[64];           // residual chunks (bf16 / fp16 pairs)
   uint32_t cs[32], sn[32];  // TC_QKV: cos / sin (fp32 bits) of frequencies 0..31
   float f;               // TC_QKV: 1/RMS; TC_SWIGLU: sum of h^2
   int p;                 // TC_QKV: position
@@ -153,27 +146,20 @@ __device__ __forceinline__ void epilogue_prefetch(EpiPre& pre, int row, bool val
                                                   const TcEpiArgs& ep) {
   if (!valid) return;
   if constexpr (EPI == TC_RESID_SS || EPI == TC_RESID) {
-    // TC_RESID_SS: every chunk of the bf16 residual (16 words each);
-    // TC_RESID: the first two fp32 chunks, the rest requested into L2
-    constexpr int RW = kResidWords<EPI>, AHEAD = kResidAhead<BN, EPI>;
+    // every chunk of the part's 16-bit residual (bf16 x for TC_RESID_SS,
+    // the fp16 copy of h for TC_RESID)
+    constexpr int RW = kResidWords;
     const int cb = chunk_begin<BN>(part);
 #pragma unroll
     for (int k = 0; k < BN / 64; ++k) {
       const int col = n0 + (cb + k) * 32;
       if (col >= N) break;
       const size_t off = (size_t)row * ep.ldo + col;
-      if (k < AHEAD) {
-        if constexpr (EPI == TC_RESID_SS)
-          ld_words<RW>(static_cast<const __nv_bfloat16*>(ep.residual) + off,
-                       pre.w + k * RW, ep.vec32);
-        else
-          ld_words<RW>(static_cast<const float*>(ep.residual) + off, pre.w + k * RW, true);
-      } else {
-        prefetch_l2(static_cast<const float*>(ep.residual) + off);
-      }
+      ld_words<RW>(static_cast<const uint16_t*>(ep.residual) + off, pre.w + k * RW,
+                   EPI == TC_RESID_SS ? ep.vec32 != 0 : true);
     }
   } else if constexpr (EPI == TC_QKV) {
-    pre.f = ep.rowscale[row];
+    pre.f = ep.rowscale ? ep.rowscale[row] : 1.f;
     int p = ep.pos[row];
     if (p < 0 || p >= ep.max_pos) {
       set_status(ep.status, ST_BAD_POSITION);
@@ -219,7 +205,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
   if constexpr (EPI == TC_STORE || EPI == TC_RESID || EPI == TC_RESID_SS) {
     // unrolled over the part's chunks so that the residual registers of
     // every chunk stay in place (no copies that would wait on the loads)
-    constexpr int RW = kResidWords<EPI>, AHEAD = kResidAhead<BN, EPI>;
+    constexpr int RW = kResidWords;
     float ss = 0.f;
     const int cb = chunk_begin<BN>(part);
 #pragma unroll
@@ -239,24 +225,20 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
             v[2 * j + 1] += r.y;
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
-          uint32_t hb[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) hb[j] = __float_as_uint(v[j]);
-          st_words<32>(static_cast<float*>(ep.out) + off, hb, true);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= ep.out_scale;
-          store_16x32(ep.out2, off, v, ep.out_f16, true);
+          for (int j = 0; j < 32; ++j) {
+            ss = fmaf(v[j], v[j], ss);
+            v[j] *= ep.out_scale;
+          }
+          store_16x32(ep.out, off, v, ep.out_f16, true);
         } else if constexpr (EPI == TC_RESID) {
-          const float sc = ep.in_scale;
-          const int slot = (k % AHEAD) * RW;
+          const float sc = ep.in_scale, rsc = ep.res_scale;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = fmaf(sc, v[j], __uint_as_float(pre.w[slot + j]));
+          for (int j = 0; j < 16; ++j) {
+            const float2 r = unpack_f16x2(pre.w[k * RW + j]);
+            v[2 * j] = fmaf(sc, v[2 * j], rsc * r.x);
+            v[2 * j + 1] = fmaf(sc, v[2 * j + 1], rsc * r.y);
+          }
           store_16x32(ep.out, off, v, false, ep.vec32);
-          // refill the slot with the chunk AHEAD further on (now in L2)
-          if (k + AHEAD < BN / 64 && col + AHEAD * 32 < N)
-            ld_words<RW>(static_cast<const float*>(ep.residual) + off + AHEAD * 32,
-                         pre.w + slot, true);
         } else {
           store_16x32(ep.out, off, v, false, ep.vec32);
         }
@@ -641,7 +623,6 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
   if (grid <= 0) return cudaSuccess;
   TcEpiArgs e = ep;
   const uintptr_t al = reinterpret_cast<uintptr_t>(e.out) |
-                       reinterpret_cast<uintptr_t>(e.out2) |
                        reinterpret_cast<uintptr_t>(e.residual);
   e.vec32 = (al & 31) == 0 && e.ldo % 16 == 0;
   if (!e.status) {

@@ -10,19 +10,18 @@ namespace llama {
 
 enum TcEpi : int {
   TC_STORE = 0,     // out = acc (bf16)
-  TC_QKV = 1,       // out = r1[m] * acc, RoPE on q / k head columns
-  TC_RESID_SS = 2,  // h = res + acc: out = h (fp32), out2 = 16-bit(h * out_scale),
+  TC_QKV = 1,       // out = r1[m] * acc (r1 = 1 without rowscale), RoPE on q / k
+  TC_RESID_SS = 2,  // h = res (bf16) + acc: out = 16-bit(h * out_scale),
                     // ss_out[m] += sum over the row of h^2
   TC_SWIGLU = 3,    // gate|up interleaved by 128: out = silu(r2 g) * (r2 u)
-  TC_RESID = 4,     // out = res (fp32) + acc
+  TC_RESID = 4,     // out = res_scale * res (fp16) + in_scale * acc (bf16)
   TC_PARTIAL = 5,   // stream-K fp32 partials: part[tile][slot][bn][128]
 };
 
 struct TcEpiArgs {
   void* out = nullptr;  // bf16 [M, ldo] (TC_SWIGLU: [M, N/2]); fp32 partials
   int ldo = 0;
-  void* out2 = nullptr;            // TC_RESID_SS: 16-bit h * out_scale
-  const void* residual = nullptr;  // TC_RESID_SS: bf16; TC_RESID: fp32 [M, ldo]
+  const void* residual = nullptr;  // TC_RESID_SS: bf16; TC_RESID: fp16 [M, ldo]
   const float* rowscale = nullptr; // r1 [M]
   const float* ss_in = nullptr;    // sum of squares of h [M] (TC_SWIGLU)
   float* ss_out = nullptr;         // TC_RESID_SS
@@ -35,10 +34,11 @@ struct TcEpiArgs {
   int* status = nullptr;
   // operand / output types and power-of-two scales of the fp16 path
   int ab_f16 = 0;        // A and B are fp16 (else bf16)
-  int out_f16 = 0;       // TC_QKV / TC_SWIGLU output (out2 for TC_RESID_SS) is fp16
+  int out_f16 = 0;       // TC_QKV / TC_SWIGLU / TC_RESID_SS output is fp16
   float in_scale = 1.f;  // TC_SWIGLU: gate / up = in_scale * r2 * acc;
-                         // TC_RESID: out = res + in_scale * acc
-  float out_scale = 1.f; // TC_SWIGLU: act stored * out_scale; TC_RESID_SS: out2 * out_scale
+                         // TC_RESID: out = res_scale * res + in_scale * acc
+  float res_scale = 1.f; // TC_RESID
+  float out_scale = 1.f; // TC_SWIGLU: act stored * out_scale; TC_RESID_SS: h * out_scale
   int pdl = 0;           // launch with programmatic dependent launch
   // Split tiles (whole-tile epilogues): when sk_part is set and the tiles do
   // not fill whole rounds of the grid, tc_gemm spreads the first

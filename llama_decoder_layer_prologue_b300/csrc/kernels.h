@@ -28,6 +28,11 @@ struct Dims {
 void simt_row_rms(bool is_bf16, const void* x, int rows, int H, float eps,
                   float* r, float* zero, cudaStream_t s);
 
+// bf16 rows of width H (a multiple of 128): r and zero as simt_row_rms, and
+// xn[row] = fp16(x[row] * r[row]).
+void simt_row_norm_f16(const void* x, int rows, int H, float eps, float* r,
+                       float* zero, void* xn, cudaStream_t s);
+
 // Positions and sequence checks: pos[t] = t - start of t's sequence (when
 // fill_pos), validates cu_seqlens (device) when given, else padded seq_len.
 void launch_positions(const int32_t* cu, int n_seq, int seq_len, int T,

@@ -105,7 +105,7 @@ void rope_inv_freq(const llama_layer_config& c, double* f) {
 }
 
 struct WsLayout {
-  size_t pos, r1, ss2, qkv, attn, h, hg, act, sk, total;
+  size_t pos, r1, ss2, xn, qkv, attn, h, hg, act, sk, total;
 };
 
 WsLayout ws_layout(const llama_layer_config& c, int tokens) {
@@ -117,10 +117,15 @@ WsLayout ws_layout(const llama_layer_config& c, int tokens) {
   w.pos = o; o = align_up(o + T * 4);
   w.r1 = o; o = align_up(o + T * 4);
   w.ss2 = o; o = align_up(o + T * 4);
+  w.xn = o;  // bf16 layers: fp16 x / RMS(x), the QKV operand
+  if (es == 2) o = align_up(o + T * c.hidden * 2);
   w.qkv = o; o = align_up(o + T * nqkv * es);
   w.attn = o; o = align_up(o + T * c.n_heads * c.head_dim * es);
-  w.h = o; o = align_up(o + T * c.hidden * 4);     // fp32
-  w.hg = o; o = align_up(o + T * c.hidden * es);   // MLP input
+  // h: fp32 layers keep it in fp32 (w.h) and scale it by g_post into w.hg;
+  // bf16 layers keep only the fp16 copy h / 256 in w.hg, which is both the
+  // MLP input and the residual of down_proj
+  w.h = o; if (es == 4) o = align_up(o + T * c.hidden * 4);
+  w.hg = o; o = align_up(o + T * c.hidden * es);
   w.act = o; o = align_up(o + T * c.intermediate * es);
   w.sk = o;  // split-tile pieces of the tensor-core GEMMs (bf16 layers)
   if (c.dtype == LLAMA_DTYPE_BF16 && T > 0) o = align_up(o + kMaxSkCtas * kSkSlotBytes);
@@ -215,7 +220,10 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
   mark(L, s, "rmsnorm_stats");
   launch_positions(cu, n_seq, seq_len, T, reinterpret_cast<int32_t*>(ws + w.pos),
                    pos_in == nullptr, L->status, s);
-  simt_row_rms(b16, x, T, dm.H, dm.eps, r1, ss2, s);
+  if (b16)
+    simt_row_norm_f16(x, T, dm.H, dm.eps, r1, ss2, ws + w.xn, s);
+  else
+    simt_row_rms(b16, x, T, dm.H, dm.eps, r1, ss2, s);
   L->launches += 2;
   if (b16) {
     cudaError_t e;
@@ -232,9 +240,11 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     TcEpiArgs ep;
     ep.status = L->status;
     ep.pdl = 1;
-    // a2 + a3: QKV projection, row scale 1/RMS, RoPE on q and k.
-    if (!tc_encode_bf16(&ta, x, T, dm.H, 128)) return LLAMA_ERR_CUDA;
-    ep.out = qkv; ep.ldo = dm.Nqkv; ep.rowscale = r1; ep.pos = pos;
+    // a2 + a3: QKV projection of x / RMS(x) (fp16) with the g_in-folded
+    // fp16 weights, RoPE on q and k.
+    if (!tc_encode_bf16(&ta, ws + w.xn, T, dm.H, 128)) return LLAMA_ERR_CUDA;
+    ep.ab_f16 = 1;
+    ep.out = qkv; ep.ldo = dm.Nqkv; ep.pos = pos;
     ep.cos_t = cos_t; ep.sin_t = sin_t; ep.head_dim = dm.d;
     ep.rope_cols = (dm.Hq + dm.Hkv) * dm.d; ep.max_pos = dm.max_pos;
     ep.out_f16 = 1;  // q | k | v in fp16 for the attention
@@ -259,7 +269,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep = TcEpiArgs();
     ep.status = L->status;
     ep.pdl = 1;
-    ep.out = h; ep.out2 = ws + w.hg; ep.ldo = dm.H; ep.residual = x;
+    ep.out = ws + w.hg; ep.ldo = dm.H; ep.residual = x;
     ep.ss_out = ss2;
     ep.ab_f16 = 1; ep.out_f16 = 1; ep.out_scale = kHgScale;
     mark(L, s, "o_proj_residual");
@@ -285,7 +295,8 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep = TcEpiArgs();
     ep.status = L->status;
     ep.pdl = 1;
-    ep.out = out; ep.ldo = dm.H; ep.residual = h;
+    ep.out = out; ep.ldo = dm.H; ep.residual = ws + w.hg;
+    ep.res_scale = 1.0f / kHgScale;  // h from its fp16 copy
     ep.ab_f16 = 1; ep.in_scale = 1.0f / kActScale;
     mark(L, s, "down_residual");
     split(ep);
@@ -318,7 +329,7 @@ constexpr int kDecodeChunk = 256;  // tokens per decode pass (<= GEMM bn)
 int decode_bn(int B) { return B <= 64 ? 64 : (B <= 128 ? 128 : 256); }
 
 struct DecLayout {
-  size_t r1, ss2, qkv, attn, hg, h32, act, part, attn_part, total;
+  size_t r1, ss2, xn, qkv, attn, hg, act, part, attn_part, total;
   int bn, max_chunks, rec;
   TcStreamK plan[4];  // QKV, O, GU, DOWN
 };
@@ -345,9 +356,9 @@ DecLayout dec_layout(const llama_layer* L, int B, int max_seq) {
   size_t o = 0;
   w.r1 = o; o = align_up(o + T * 4);
   w.ss2 = o; o = align_up(o + T * 4);
+  w.xn = o; o = align_up(o + T * dm.H * 2);  // fp16 x / RMS(x)
   w.qkv = o; o = align_up(o + T * dm.Nqkv * es);
   w.attn = o; o = align_up(o + T * dm.Hq * dm.d * es);
-  w.h32 = o; o = align_up(o + T * dm.H * 4);
   w.hg = o; o = align_up(o + T * dm.H * es);
   w.act = o; o = align_up(o + T * dm.I * es);
   w.part = o; o = align_up(o + part);
@@ -381,7 +392,6 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   a.attn = reinterpret_cast<__half*>(ws + w.attn);
   a.attn_part = reinterpret_cast<float*>(ws + w.attn_part);
   a.max_chunks = w.max_chunks; a.n_rep_rec = w.rec;
-  a.h32 = reinterpret_cast<float*>(ws + w.h32);
   a.hg = reinterpret_cast<__half*>(ws + w.hg);
   a.act = reinterpret_cast<__half*>(ws + w.act);
   a.out = static_cast<__nv_bfloat16*>(out);
@@ -403,7 +413,7 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
     ep.pdl = 1;
     ep.part_slots = w.plan[stage].slots;
     ep.status = L->status;
-    ep.ab_f16 = stage != DEC_QKV;  // fp16 weights and activations after QKV
+    ep.ab_f16 = 1;  // fp16 weights and activations
     mark(L, s, kGemmName[stage]);
     if (tc_gemm(TC_PARTIAL, w.bn, wmap, tb, N_out, B, K, ep, L->sm_count, s) !=
         cudaSuccess)
@@ -416,10 +426,10 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
 
   // a1: 1/RMS of every new token (and zero the sums of h^2).
   mark(L, s, "rmsnorm_stats");
-  simt_row_rms(true, x, B, dm.H, dm.eps, const_cast<float*>(a.r1), a.ss2, s);
+  simt_row_norm_f16(x, B, dm.H, dm.eps, const_cast<float*>(a.r1), a.ss2, ws + w.xn, s);
   ++L->launches;
   // a2 + a3 + cache append.
-  int rc = project(DEC_QKV, L->ta_wqkv, x, dm.Nqkv, dm.H);
+  int rc = project(DEC_QKV, L->ta_wqkv, ws + w.xn, dm.Nqkv, dm.H);
   if (rc) return rc;
   // a6: split-KV attention over rows 0..start_pos[b].
   mark(L, s, "attention");
@@ -546,12 +556,12 @@ int llama_layer_init(const llama_layer_config* cfg,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& dm = L->dm;
 
-  // bf16 layers: W_qkv (times g_in) stays bf16 (its A operand is the bf16
-  // input x); W_o, W_gate_up and W_down become fp16, the type of the
-  // intermediates they multiply.
+  // bf16 layers: every packed weight is fp16, the type of the
+  // intermediates it multiplies (x / RMS(x), attn, h, act); fp16 holds bf16
+  // weights exactly and W_qkv * g_in within 2^-12.
   const bool f16 = L->bf16;
   launch_pack(L->bf16, wts->w_qkv, wts->g_in, L->packed + pl.wqkv, dm.Nqkv,
-              dm.H, 0, false, s);
+              dm.H, 0, f16, s);
   launch_pack(L->bf16, wts->w_o, nullptr, L->packed + pl.wo, dm.H,
               dm.Hq * dm.d, 0, f16, s);
   launch_pack(L->bf16, wts->g_post, nullptr, L->packed + pl.gpost, 1, dm.H, 0,
@@ -636,14 +646,14 @@ int llama_layer_workspace_offsets(const llama_layer_t* L, int tokens, int decode
     DecLayout w = dec_layout(L, tokens, 1);
     offsets[0] = w.qkv;
     offsets[1] = w.attn;
-    offsets[2] = w.h32;
+    offsets[2] = w.hg;
     offsets[3] = w.act;
     return LLAMA_OK;
   }
   WsLayout w = ws_layout(L->cfg, tokens);
   offsets[0] = w.qkv;
   offsets[1] = w.attn;
-  offsets[2] = w.h;
+  offsets[2] = L->bf16 ? w.hg : w.h;
   offsets[3] = w.act;
   return LLAMA_OK;
 }

@@ -51,6 +51,46 @@ __global__ void row_rms_kernel(const T* __restrict__ x, int rows, int H,
   }
 }
 
+// bf16 rows: r[row] = 1/RMS as above, zero[row] = 0, and the normalised row
+// xn = fp16(x * r) (the operand of the QKV projection, whose packed weights
+// hold g_in).  One warp per row; the second pass re-reads the row the warp
+// has just read (L1).
+__global__ void row_norm_f16_kernel(const __nv_bfloat16* __restrict__ x, int rows,
+                                    int H, float eps, float* __restrict__ r,
+                                    float* __restrict__ zero,
+                                    __half* __restrict__ xn) {
+  pdl_trigger();
+  pdl_wait();
+  int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const __nv_bfloat16* xr = x + (size_t)row * H + lane * 4;
+  float ss[4] = {0.f, 0.f, 0.f, 0.f};
+  int j = 0;
+  for (; j + 512 <= H; j += 512) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ss[u] += sumsq4(xr + j + u * 128);
+  }
+  for (; j < H; j += 128) ss[0] += sumsq4(xr + j);
+  const float rs = rsqrtf(warp_sum((ss[0] + ss[1]) + (ss[2] + ss[3])) / (float)H + eps);
+  if (lane == 0) {
+    r[row] = rs;
+    if (zero) zero[row] = 0.f;
+  }
+  __half* out = xn + (size_t)row * H + lane * 4;
+  for (j = 0; j < H; j += 128) {
+    const uint2 u = *reinterpret_cast<const uint2*>(xr + j);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    __half2 lo = __floats2half2_rn(a.x * rs, a.y * rs);
+    __half2 hi = __floats2half2_rn(b.x * rs, b.y * rs);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&lo);
+    o.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + j) = o;
+  }
+}
+
 // ----------------------------------------------------------------- positions
 // One block per sequence.  Checks the prefix sums; writes pos[t] = t - start.
 __global__ void positions_kernel(const int32_t* __restrict__ cu, int n_seq,
@@ -320,6 +360,66 @@ void simt_row_rms(bool is_bf16, const void* x, int rows, int H, float eps,
   if (rows <= 0) return;
   DISPATCH(is_bf16, launch_pdl(row_rms_kernel<T>, dim3((rows + 7) / 8), dim3(256), 0,
                                s, (const T*)x, rows, H, eps, r, zero));
+}
+
+// The same for rows of exactly 128 * STEPS elements, held in registers: every
+// load of a lane is in flight at once and the row is read once.
+template <int STEPS>
+__global__ void row_norm_f16_reg_kernel(const __nv_bfloat16* __restrict__ x,
+                                        int rows, float eps, float* __restrict__ r,
+                                        float* __restrict__ zero,
+                                        __half* __restrict__ xn) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int H = 128 * STEPS;
+  int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const __nv_bfloat16* xr = x + (size_t)row * H + lane * 4;
+  uint2 u[STEPS];
+#pragma unroll
+  for (int j = 0; j < STEPS; ++j) u[j] = __ldg(reinterpret_cast<const uint2*>(xr + 128 * j));
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < STEPS; ++j) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[j].x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[j].y));
+    ss = fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(b.x, b.x, fmaf(b.y, b.y, ss))));
+  }
+  const float rs = rsqrtf(warp_sum(ss) / (float)H + eps);
+  if (lane == 0) {
+    r[row] = rs;
+    if (zero) zero[row] = 0.f;
+  }
+  __half* out = xn + (size_t)row * H + lane * 4;
+#pragma unroll
+  for (int j = 0; j < STEPS; ++j) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[j].x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[j].y));
+    __half2 lo = __floats2half2_rn(a.x * rs, a.y * rs);
+    __half2 hi = __floats2half2_rn(b.x * rs, b.y * rs);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&lo);
+    o.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + 128 * j) = o;
+  }
+}
+
+void simt_row_norm_f16(const void* x, int rows, int H, float eps, float* r,
+                       float* zero, void* xn, cudaStream_t s) {
+  if (rows <= 0) return;
+  const dim3 grid((rows + 7) / 8), block(256);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  auto* o = static_cast<__half*>(xn);
+  switch (H) {
+    case 1024: launch_pdl(row_norm_f16_reg_kernel<8>, grid, block, 0, s, xb, rows, eps, r, zero, o); return;
+    case 2048: launch_pdl(row_norm_f16_reg_kernel<16>, grid, block, 0, s, xb, rows, eps, r, zero, o); return;
+    case 3072: launch_pdl(row_norm_f16_reg_kernel<24>, grid, block, 0, s, xb, rows, eps, r, zero, o); return;
+    case 4096: launch_pdl(row_norm_f16_reg_kernel<32>, grid, block, 0, s, xb, rows, eps, r, zero, o); return;
+    case 5120: launch_pdl(row_norm_f16_reg_kernel<40>, grid, block, 0, s, xb, rows, eps, r, zero, o); return;
+    default:
+      launch_pdl(row_norm_f16_kernel, grid, block, 0, s, xb, rows, H, eps, r, zero, o);
+  }
 }
 
 void launch_positions(const int32_t* cu, int n_seq, int seq_len, int T,

@@ -147,20 +147,21 @@ class LlamaLayer:
 
     def stages(self, tokens: int, decode: bool = False) -> dict:
         """The intermediates of the last call with `tokens` rows (element
-        types as llama_layer_workspace_offsets documents; act is returned
-        already multiplied back by 16 for bf16 layers)."""
+        types as llama_layer_workspace_offsets documents; for bf16 layers h
+        and act are returned already multiplied back by 256 and 16)."""
         off = B.llama_layer_workspace_offsets(self.handle, tokens, int(decode))
         s = self.shape
         bf = self.dtype == torch.bfloat16
         f16 = torch.float16 if bf else torch.float32
         types = {"qkv": (s.n_qkv, torch.bfloat16 if (bf and decode) else f16),
-                 "attn": (s.q_size, f16), "h": (s.hidden, torch.float32),
+                 "attn": (s.q_size, f16), "h": (s.hidden, f16 if bf else torch.float32),
                  "act": (s.intermediate, f16)}
         views = {}
         for (name, (width, dt)), o in zip(types.items(), off):
             n = tokens * width * torch.tensor([], dtype=dt).element_size()
             views[name] = self.workspace[o:o + n].view(dt).view(tokens, width)
         if bf:
+            views["h"] = views["h"].float() * 256.0
             views["act"] = views["act"].float() * 16.0
         return views
 
