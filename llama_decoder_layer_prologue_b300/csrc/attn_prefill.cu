@@ -18,12 +18,14 @@
 //               divides by l and stores fp16.
 //   warp 8      TMA producer: the two Q tiles once per item, then K(j), V(j)
 //               into a ring of single-tile slots.
-//   warp 9      one thread issues tcgen05.mma in the order
-//               S_A(j+1), PV_A(j), S_B(j+1), PV_B(j): S = Q K^T into the
-//               tile's TMEM S buffer, O += P V into its TMEM O buffer (V read
-//               as an MN-major operand straight from its TMA tile).  While one
-//               warpgroup computes its softmax the tensor core works on the
-//               other's products (P buffers: see AttnLayout).
+//   warps 9, 10 one thread of warp 9 + t issues the tcgen05.mma of query
+//               tile t in the order S_t(0), then S_t(j+1), PV_t(j): S = Q K^T
+//               into the tile's TMEM S buffer, O += P V into its TMEM O
+//               buffer (V read as an MN-major operand straight from its TMA
+//               tile, P from TMEM or shared memory: see AttnLayout).  The two
+//               tiles' products reach the tensor core independently, so while
+//               one warpgroup computes its softmax the tensor core works on
+//               the other's products.
 // Rescaling of O is lazy: a row's reference max only moves (and O is
 // rescaled in TMEM) when the new max exceeds it by more than 8 in the log2
 // domain, so P stays <= 2^8.  Items run longest causal range first.  Every
@@ -44,7 +46,7 @@ constexpr float kRescaleLog2 = 8.0f;
 // 12 warps = 3 warpgroups: the register file is shared out per warpgroup,
 // so the block launches at 168 registers a thread (384 x 168 = 64512) and
 // then moves registers with setmaxnreg: the two softmax warpgroups go up to
-// kSoftmaxRegs, the producer / MMA warpgroup (warps 8..11, 10 and 11 idle)
+// kSoftmaxRegs, the producer / MMA warpgroup (warps 8..11, 11 idle)
 // down to kControlRegs; 2 x 128 x 200 + 128 x 104 = 64512.
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
@@ -52,16 +54,17 @@ constexpr int kSoftmaxRegs = 200, kControlRegs = 104;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168,
               "register split exceeds the launch allocation");
 
-// Shared memory, 224 KB either way: two query tiles, the P tiles and 8
-// (head_dim 64) or 4 (head_dim 128) single-tile K / V slots.  For head_dim 64
-// each query tile has its own P tile (SEP_P): a warpgroup then only waits for
-// its own previous P V.  For head_dim 128 the two query tiles share one P
-// tile, written in turn (tile A of step j after P V_B of step j - 1, tile B
-// after P V_A of step j), which keeps room for 4 slots of 32 KB.
+// head_dim 64: each query tile has its own P tile in tensor memory (P_TMEM,
+// 64 columns of fp16 pairs after S and O), which the P V product reads as
+// its A operand; shared memory holds the two query tiles and 8 K / V slots,
+// and a warpgroup only waits for its own previous P V.  head_dim 128: S and
+// O fill the 512 columns, so the two query tiles share one P tile in shared
+// memory, written in turn (tile A of step j after P V_B of step j - 1, tile B
+// after P V_A of step j), next to 4 slots of 32 KB.
 template <int D>
 struct AttnLayout {
   static constexpr int AN = 128;                    // keys per K / V tile
-  static constexpr bool SEP_P = D == 64;
+  static constexpr bool P_TMEM = D == 64;
   static constexpr int ATOMS = D / 64;  // 128-byte swizzle atoms per row
   static constexpr uint32_t Q_BYTES = AM * D * 2;   // one query tile
   static constexpr uint32_t KV_BYTES = AN * D * 2;  // one K or V tile (a slot)
@@ -69,12 +72,14 @@ struct AttnLayout {
   static constexpr int SLOTS = D == 64 ? 8 : 4;
   static constexpr uint32_t Q_OFF = 0;              // Q_A, Q_B
   static constexpr uint32_t P_OFF = Q_OFF + 2 * Q_BYTES;
-  static constexpr uint32_t KV_OFF = P_OFF + (SEP_P ? 2 : 1) * P_BYTES;
+  static constexpr uint32_t KV_OFF = P_OFF + (P_TMEM ? 0 : P_BYTES);
   static constexpr uint32_t BAR_OFF = KV_OFF + SLOTS * KV_BYTES;
   static constexpr uint32_t TOTAL = BAR_OFF + 512 + 1024;
-  // S_A [0, AN), S_B [AN, 2 AN), O_A [2 AN, 2 AN + D), O_B [2 AN + D, 2 AN + 2 D)
+  // S_A [0, AN), S_B [AN, 2 AN), O_A [2 AN, 2 AN + D), O_B [2 AN + D, 2 AN + 2 D),
+  // then (P_TMEM) P_A, P_B: AN / 2 columns each
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(2 * AN + 2 * D <= (int)TMEM_COLS, "tensor memory budget");
+  static constexpr uint32_t P_COL = 2 * AN + 2 * D;
+  static_assert(P_COL + (P_TMEM ? AN : 0) <= TMEM_COLS, "tensor memory budget");
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
 
@@ -163,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_free = pv_done + 2;             // [2]
   uint64_t* q_full = o_free + 2;
   uint64_t* q_empty = q_full + 1;
-  uint64_t* drain = q_empty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* drain = q_empty + 1;             // [2] per MMA warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::SLOTS; ++s) {
       mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&kv_empty[s], 2);  // a commit from each MMA warp
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
@@ -182,8 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_free[t], 128);
     }
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    mbar_init(drain, 1);
+    mbar_init(q_empty, 2);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -249,10 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop (its values stay warp-uniform); one
-    // elected lane issues each MMA / commit.
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp kMmaWarp + t issues the products of query tile t in order,
+    // S_t(0), then S_t(j+1), PV_t(j) for each j; the two warps share the
+    // tensor core, so neither tile's products wait for the other tile's
+    // softmax.  K / V slots and the Q tiles are released by a commit from
+    // each warp (barrier count 2).  One elected lane issues.
+    const int t = warp - kMmaWarp;
     constexpr uint32_t idesc_s = idesc_f16(AM, AN);
     constexpr uint32_t idesc_pv = idesc_f16(AM, D) | (1u << 16);  // B MN-major
     // descriptor bases; a K step adds its byte offset >> 4 to the address
@@ -264,6 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait_sleep(b, parity, a.status, abort_flag));
     };
+    const uint64_t qd = q_desc + t * Q16;
+    const uint32_t s_tmem = tmem_base + t * AN;
+    const uint32_t o_tmem = tmem_base + 2 * AN + t * D;
     uint32_t g = 0, n = 0, k = 0;  // tiles, K / V loads consumed, items
     bool ok = true, issued_any = false;
     for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
@@ -276,80 +289,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++k;
       const int nt = it.n_tiles;
       // K(j) is K / V load number n + 2 j, V(j) number n + 2 j + 1.
-      // Issue order: S_A(0) S_B(0), then per j: S_A(j+1) PV_A(j) S_B(j+1) PV_B(j).
-      for (int step = -1; step < 2 * nt && ok; ++step) {
-        // step -1: S_A(0), S_B(0); step 2j: S_A(j+1), PV_A(j);
-        // step 2j+1: S_B(j+1), PV_B(j)
-        const int j = step < 0 ? -1 : step >> 1;
-        const int tt = step < 0 ? 0 : step & 1;
-        for (int t = 0; t < 2; ++t) {
-          if (step >= 0 && t != tt) continue;
-          const int js = j + 1;  // tile of the S product
-          if (js >= nt) break;
-          const uint32_t kn = n + 2 * js;
-          if (t == 0 && !wait_all(&kv_full[kn % L::SLOTS], (kn / L::SLOTS) & 1)) {
-            ok = false;
-            break;
-          }
-          const uint32_t gs = g + js;
-          if (!wait_all(&s_free[t], (gs & 1) ^ 1)) {
+      for (int step = -1; step < nt && ok; ++step) {
+        const int js = step + 1;  // tile of the S product
+        if (js < nt) {
+          const uint32_t kn = n + 2 * js, gs = g + js;
+          if (!wait_all(&kv_full[kn % L::SLOTS], (kn / L::SLOTS) & 1) ||
+              !wait_all(&s_free[t], (gs & 1) ^ 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t qd = q_desc + t * Q16;
           const uint64_t kd = k_desc + (kn % L::SLOTS) * SLOT16;
-          const uint32_t d_tmem = tmem_base + t * AN;
           if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t qo = ((kk / 4) * (AM * 128) + (kk % 4) * 32) >> 4;
               const uint32_t ko = ((kk / 4) * (AN * 128) + (kk % 4) * 32) >> 4;
-              tc_mma_bf16_nc(d_tmem, qd + qo, kd + ko, idesc_s, kk > 0 ? 1u : 0u);
+              tc_mma_bf16_nc(s_tmem, qd + qo, kd + ko, idesc_s, kk > 0 ? 1u : 0u);
             }
             tc_commit(&s_full[t]);
-            if (t == 1) {
-              tc_commit(&kv_empty[kn % L::SLOTS]);  // K(js) no longer needed
-              if (js == nt - 1) tc_commit(q_empty);
-            }
+            tc_commit(&kv_empty[kn % L::SLOTS]);  // this tile is done with K(js)
+            if (js == nt - 1) tc_commit(q_empty);  // ... and with its Q tile
           }
           __syncwarp();
           issued_any = true;
         }
-        if (!ok || step < 0) continue;
-        // PV_tt(j)
+        if (step < 0) continue;
+        // PV_t(j)
+        const int j = step;
         const uint32_t vn = n + 2 * j + 1, gp = g + j;
         const bool first = j == 0;
-        if ((tt == 0 && !wait_all(&kv_full[vn % L::SLOTS], (vn / L::SLOTS) & 1)) ||
-            !wait_all(&p_full[tt], gp & 1) ||
-            (first && k > 1 && !wait_all(&o_free[tt], (k - 2) & 1))) {
+        if (!wait_all(&kv_full[vn % L::SLOTS], (vn / L::SLOTS) & 1) ||
+            !wait_all(&p_full[t], gp & 1) ||
+            (first && k > 1 && !wait_all(&o_free[t], (k - 2) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint64_t vd = v_desc + (vn % L::SLOTS) * SLOT16;
-        const uint64_t pd = p_desc + (L::SEP_P ? tt * (L::P_BYTES >> 4) : 0);
-        const uint32_t o_tmem = tmem_base + 2 * AN + tt * D;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < AN / 16; ++kk) {
-            const uint32_t po = ((kk / 4) * (AM * 128) + (kk % 4) * 32) >> 4;
-            tc_mma_bf16_nc(o_tmem, pd + po, vd + kk * (2048 >> 4), idesc_pv,
-                           (!first || kk > 0) ? 1u : 0u);
+            if constexpr (L::P_TMEM) {  // A = P_t in tensor memory, 8 columns per K step
+              tc_mma_ts(o_tmem, tmem_base + L::P_COL + t * (AN / 2) + kk * 8,
+                        vd + kk * (2048 >> 4), idesc_pv, (!first || kk > 0) ? 1u : 0u);
+            } else {
+              const uint32_t po = ((kk / 4) * (AM * 128) + (kk % 4) * 32) >> 4;
+              tc_mma_bf16_nc(o_tmem, p_desc + po, vd + kk * (2048 >> 4), idesc_pv,
+                             (!first || kk > 0) ? 1u : 0u);
+            }
           }
-          tc_commit(&pv_done[tt]);
-          if (tt == 1) tc_commit(&kv_empty[vn % L::SLOTS]);  // V(j) no longer needed
+          tc_commit(&pv_done[t]);
+          tc_commit(&kv_empty[vn % L::SLOTS]);  // this tile is done with V(j)
         }
         __syncwarp();
+        issued_any = true;
       }
       g += nt;
       n += 2 * nt;
     }
-    if (!ok && issued_any) {  // wait for the MMAs in flight
+    if (!ok && issued_any) {  // wait for this warp's MMAs in flight
       volatile int own = 0;
-      if (elect_one()) tc_commit(drain);
+      if (elect_one()) tc_commit(&drain[t]);
       __syncwarp();
-      mbar_wait_sleep(drain, 0, a.status, &own);
+      mbar_wait_sleep(&drain[t], 0, a.status, &own);
     }
     }
   } else {
@@ -359,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;  // row of the tile == TMEM lane
     const uint32_t lane_base = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = t * AN, o_col = 2 * AN + t * D;
-    uint8_t* prow = smem + L::P_OFF + (L::SEP_P ? t * L::P_BYTES : 0) + r * 128;
+    uint8_t* prow = smem + L::P_OFF + r * 128;  // shared P tile (head_dim 128)
     const float scale = 1.4426950408889634f * rsqrtf((float)D);  // log2(e)/sqrt(d)
     uint32_t g = 0;
     bool ok = true;
@@ -429,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           add2(ps[c & 7], ps[(c & 7) + 1], s[c], s[c + 1]);
         }
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-        if constexpr (L::SEP_P) {
+        if constexpr (L::P_TMEM) {
           // This tile's P buffer and O are free once its previous P V is
           // done (for the first tile of an item the epilogue already waited).
           if (j > 0) {
@@ -463,18 +466,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(ta, o);
           }
         }
-        // P as fp16 into the 128-byte swizzled A tile
+        if constexpr (L::P_TMEM) {
+          // P as fp16 pairs into this row's TMEM lane (the P V A operand)
+          const uint32_t p_tmem = lane_base + L::P_COL + t * (AN / 2);
 #pragma unroll
-        for (int c16 = 0; c16 < AN / 8; ++c16) {
-          uint4 u;
-          u.x = pack_f16x2(s[c16 * 8 + 0], s[c16 * 8 + 1]);
-          u.y = pack_f16x2(s[c16 * 8 + 2], s[c16 * 8 + 3]);
-          u.z = pack_f16x2(s[c16 * 8 + 4], s[c16 * 8 + 5]);
-          u.w = pack_f16x2(s[c16 * 8 + 6], s[c16 * 8 + 7]);
-          const int atom = c16 / 8, cc = c16 % 8;
-          *reinterpret_cast<uint4*>(prow + atom * (AM * 128) + ((cc ^ (r & 7)) << 4)) = u;
+          for (int h = 0; h < AN / 32; ++h) {
+            uint32_t w[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              w[q] = pack_f16x2(s[h * 32 + 2 * q], s[h * 32 + 2 * q + 1]);
+            tmem_st16_words(p_tmem + h * 16, w);
+          }
+          tmem_wait_st();
+        } else {
+          // P as fp16 into the 128-byte swizzled A tile
+#pragma unroll
+          for (int c16 = 0; c16 < AN / 8; ++c16) {
+            uint4 u;
+            u.x = pack_f16x2(s[c16 * 8 + 0], s[c16 * 8 + 1]);
+            u.y = pack_f16x2(s[c16 * 8 + 2], s[c16 * 8 + 3]);
+            u.z = pack_f16x2(s[c16 * 8 + 4], s[c16 * 8 + 5]);
+            u.w = pack_f16x2(s[c16 * 8 + 6], s[c16 * 8 + 7]);
+            const int atom = c16 / 8, cc = c16 % 8;
+            *reinterpret_cast<uint4*>(prow + atom * (AM * 128) + ((cc ^ (r & 7)) << 4)) = u;
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
       }

@@ -369,6 +369,18 @@ __device__ __forceinline__ void tc_mma_bf16_nc(uint32_t d_tmem, uint64_t adesc,
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
+// The same with the A operand in tensor memory (M = 128 rows in lanes
+// 0..127, K along the columns, two 16-bit elements per 32-bit column, the
+// even one in the low half): a K step of 16 advances a_tmem by 8 columns.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem,
+                                          uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
 // True in exactly one lane of the (fully active) warp.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
@@ -437,6 +449,22 @@ __device__ __forceinline__ void tmem_pin(float& x) { asm volatile("" : "+f"(x));
 
 // Each thread of the warp writes 32 consecutive fp32 columns of its TMEM
 // lane, then waits for the stores to land.
+// Stores 16 consecutive 32-bit columns of this thread's lane (16 words)
+// without waiting: call tmem_wait_st() before the stored columns are read.
+__device__ __forceinline__ void tmem_st16_words(uint32_t taddr, const uint32_t* w) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
+      "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+      "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]),
+      "r"(w[14]), "r"(w[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
