@@ -54,13 +54,12 @@ constexpr int kSoftmaxRegs = 200, kControlRegs = 104;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168,
               "register split exceeds the launch allocation");
 
-// head_dim 64: each query tile has its own P tile in tensor memory (P_TMEM,
-// 64 columns of fp16 pairs after S and O), which the P V product reads as
-// its A operand; shared memory holds the two query tiles and 8 K / V slots,
-// and a warpgroup only waits for its own previous P V.  head_dim 128: S and
-// O fill the 512 columns, so the two query tiles share one P tile in shared
-// memory, written in turn (tile A of step j after P V_B of step j - 1, tile B
-// after P V_A of step j), next to 4 slots of 32 KB.
+// Each query tile has its own P tile, so a warpgroup only waits for its own
+// previous P V.  head_dim 64: P lives in tensor memory (P_TMEM, 64 columns of
+// fp16 pairs after S and O) and the P V product reads it as its A operand;
+// shared memory holds the two query tiles and 8 K / V slots.  head_dim 128:
+// S and O fill the 512 columns, so the two P tiles are 128-byte swizzled
+// shared-memory tiles, next to the query tiles and 3 K / V slots of 32 KB.
 template <int D>
 struct AttnLayout {
   static constexpr int AN = 128;                    // keys per K / V tile
@@ -69,10 +68,10 @@ struct AttnLayout {
   static constexpr uint32_t Q_BYTES = AM * D * 2;   // one query tile
   static constexpr uint32_t KV_BYTES = AN * D * 2;  // one K or V tile (a slot)
   static constexpr uint32_t P_BYTES = AM * AN * 2;  // one P tile
-  static constexpr int SLOTS = D == 64 ? 8 : 4;
+  static constexpr int SLOTS = D == 64 ? 8 : 3;
   static constexpr uint32_t Q_OFF = 0;              // Q_A, Q_B
   static constexpr uint32_t P_OFF = Q_OFF + 2 * Q_BYTES;
-  static constexpr uint32_t KV_OFF = P_OFF + (P_TMEM ? 0 : P_BYTES);
+  static constexpr uint32_t KV_OFF = P_OFF + (P_TMEM ? 0 : 2 * P_BYTES);
   static constexpr uint32_t BAR_OFF = KV_OFF + SLOTS * KV_BYTES;
   static constexpr uint32_t TOTAL = BAR_OFF + 512 + 1024;
   // S_A [0, AN), S_B [AN, 2 AN), O_A [2 AN, 2 AN + D), O_B [2 AN + D, 2 AN + 2 D),
@@ -335,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         vd + kk * (2048 >> 4), idesc_pv, (!first || kk > 0) ? 1u : 0u);
             } else {
               const uint32_t po = ((kk / 4) * (AM * 128) + (kk % 4) * 32) >> 4;
-              tc_mma_bf16_nc(o_tmem, p_desc + po, vd + kk * (2048 >> 4), idesc_pv,
+              tc_mma_bf16_nc(o_tmem, p_desc + t * (L::P_BYTES >> 4) + po,
+                             vd + kk * (2048 >> 4), idesc_pv,
                              (!first || kk > 0) ? 1u : 0u);
             }
           }
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;  // row of the tile == TMEM lane
     const uint32_t lane_base = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = t * AN, o_col = 2 * AN + t * D;
-    uint8_t* prow = smem + L::P_OFF + r * 128;  // shared P tile (head_dim 128)
+    uint8_t* prow = smem + L::P_OFF + t * L::P_BYTES + r * 128;  // head_dim 128
     const float scale = 1.4426950408889634f * rsqrtf((float)D);  // log2(e)/sqrt(d)
     uint32_t g = 0;
     bool ok = true;
@@ -432,28 +432,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           add2(ps[c & 7], ps[(c & 7) + 1], s[c], s[c + 1]);
         }
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-        if constexpr (L::P_TMEM) {
-          // This tile's P buffer and O are free once its previous P V is
-          // done (for the first tile of an item the epilogue already waited).
-          if (j > 0) {
-            if (!warp_wait(&pv_done[t], (g - 1) & 1)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+        // This tile's P buffer and O are free once its previous P V is done
+        // (for the first tile of an item the epilogue already waited).
+        if (j > 0) {
+          if (!warp_wait(&pv_done[t], (g - 1) & 1)) {
+            ok = false;
+            break;
           }
-        } else {
-          // The shared P buffer is free once the P V before ours is done:
-          // tile A of step g follows P V_B of step g - 1, tile B follows P
-          // V_A of step g.  Either also means our own previous P V is done,
-          // so O can be rescaled.
-          if (t == 1 || g > 0) {
-            if (!warp_wait(&pv_done[t ^ 1], t == 1 ? (g & 1) : ((g - 1) & 1))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
+          tc_fence_after();
         }
         if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
