@@ -531,9 +531,11 @@ def run_ours(args, rank, local_rank, world):
         e2e = {"value": world * n_e2e * tokens / (e2e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
                "steps": n_e2e, "ms_per_step": e2e_ms / n_e2e,
-               "api": "LlamaLayer.%s_from_host (pinned host buffers, "
-                      "cudaMemcpyAsync on the layer's stream)"
-                      % ("decode" if decode else "forward")}
+               "api": ("LlamaLayer.decode_from_host (pinned host buffers, "
+                       "cudaMemcpyAsync on the layer's stream)" if decode else
+                       "LlamaLayer.forward_from_host -> llama_layer_forward_host "
+                       "(pinned host buffers; groups of whole sequences, copies "
+                       "in and out on two streams overlapping the layer)")}
 
     if rank != 0:
         if dist is not None:

@@ -130,9 +130,11 @@ LLAMA_API int llama_layer_packed_bytes(const llama_layer_config* cfg, size_t* by
  * untouched until llama_layer_destroy), builds the RoPE cos/sin table in
  * double precision on the host and uploads it as fp32, and returns a host
  * handle in *out.  Synchronises `stream` before returning.  Repacking folds
- * g_in into the columns of W_qkv (x_n W^T = r * x (g . W)^T with r the row's
- * 1/RMS), keeps a copy of g_post (the MLP input is h * g_post, scaled by r in
- * the epilogue) and interleaves the gate and up rows in blocks of 128. */
+ * g_in into the columns of W_qkv (x_n W^T = (r x) (g . W)^T with r the row's
+ * 1/RMS), for bf16 layers folds g_post into the columns of W_gate_up the same
+ * way (the fp32 layer keeps a copy of g_post and scales h by it), stores bf16
+ * layers' weights as fp16 and interleaves the gate and up rows in blocks of
+ * 128. */
 LLAMA_API int llama_layer_init(const llama_layer_config* cfg,
                      const llama_layer_weights* weights, void* packed,
                      size_t packed_bytes, void* stream, llama_layer_t** out);
@@ -161,6 +163,28 @@ LLAMA_API int llama_layer_forward(llama_layer_t* layer, const void* x, void* out
                         const int32_t* position_ids, const int32_t* cu_seqlens,
                         int n_seq, int seq_len, int total_tokens,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* The prefill forward with its input and output in host memory, the copies
+ * overlapped with the layer: the batch is split into `chunks` groups of whole
+ * sequences (0: groups of at least 4096 tokens; at most LLAMA_HOST_MAX_CHUNKS
+ * and n_seq; a packed batch, cu_seqlens != NULL, is one group), and while the
+ * layer runs on group i on `stream`, group i + 1 is copied in and group i - 1
+ * copied out on two streams the layer owns.  Positions restart at 0 in every
+ * sequence.
+ *   x_host, out_host [total_tokens, hidden] host memory (page-locked for the
+ *                    copies to be asynchronous and overlap)
+ *   x_dev, out_dev   [total_tokens, hidden] device staging buffers (distinct)
+ *   cu_seqlens       NULL or device int32 prefix sums, as llama_layer_forward
+ * `workspace` as llama_layer_forward for total_tokens (the groups use it in
+ * turn).  Returns once everything is enqueued; work enqueued on `stream`
+ * afterwards runs after the last copy out, so synchronising `stream` makes
+ * out_host valid.  The host buffers must stay allocated until then. */
+#define LLAMA_HOST_MAX_CHUNKS 8
+LLAMA_API int llama_layer_forward_host(llama_layer_t* layer, const void* x_host,
+                                       void* out_host, void* x_dev, void* out_dev,
+                                       const int32_t* cu_seqlens, int n_seq, int seq_len,
+                                       int total_tokens, int chunks, void* workspace,
+                                       size_t workspace_bytes, void* stream);
 
 /* One decode step ("llama3 结构详解" 3.2; model.py walkthrough 3): one new
  * token per sequence.

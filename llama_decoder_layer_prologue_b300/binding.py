@@ -40,6 +40,7 @@ EXPORTS = (
     "llama_layer_destroy", "llama_layer_strerror", "llama_gemm_bf16",
     "llama_layer_set_timing", "llama_layer_stage_times",
     "llama_layer_launch_count", "llama_gemm_bf16_streamk_static",
+    "llama_layer_forward_host",
 )
 
 
@@ -109,6 +110,8 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(_I)]),
         "llama_layer_launch_count": (_I, [_P]),
         "llama_gemm_bf16_streamk_static": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+        "llama_layer_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                          _P, _SZ, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -165,6 +168,17 @@ def llama_layer_forward(layer: int, x: int, out: int, position_ids: int | None,
            lib().llama_layer_forward(layer, x, out, position_ids, cu_seqlens,
                                      n_seq, seq_len, total_tokens, workspace,
                                      workspace_bytes, stream))
+
+
+def llama_layer_forward_host(layer: int, x_host: int, out_host: int, x_dev: int,
+                             out_dev: int, cu_seqlens: int | None, n_seq: int,
+                             seq_len: int, total_tokens: int, chunks: int,
+                             workspace: int, workspace_bytes: int,
+                             stream: int) -> None:
+    _check("llama_layer_forward_host",
+           lib().llama_layer_forward_host(layer, x_host, out_host, x_dev, out_dev,
+                                          cu_seqlens, n_seq, seq_len, total_tokens,
+                                          chunks, workspace, workspace_bytes, stream))
 
 
 def llama_layer_decode(layer: int, x: int, out: int, cache_k: int,

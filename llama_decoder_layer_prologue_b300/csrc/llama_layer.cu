@@ -7,6 +7,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 
 #include "../../include/llama_layer.h"
@@ -156,6 +157,11 @@ struct llama_layer {
   int launches;  // kernels launched by the last forward / decode call
   uint32_t* sk_flag;  // split-tile flags (packed buffer, zeroed at init)
   uint32_t sk_epoch;  // value of the last split-tile launch's flags
+  // llama_layer_forward_host: copy streams and events, created on first use
+  cudaStream_t h2d, d2h;
+  cudaEvent_t ev_start, ev_done, ev_in[LLAMA_HOST_MAX_CHUNKS],
+      ev_comp[LLAMA_HOST_MAX_CHUNKS];
+  bool host_ready;
 };
 
 namespace {
@@ -552,6 +558,7 @@ int llama_layer_init(const llama_layer_config* cfg,
   L->status = reinterpret_cast<int*>(L->packed + pl.status);
   L->sk_flag = reinterpret_cast<uint32_t*>(L->packed + pl.skflag);
   L->sk_epoch = 0;
+  L->host_ready = false;
   L->sm_count = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& dm = L->dm;
@@ -681,6 +688,99 @@ int llama_layer_forward(llama_layer_t* L, const void* x, void* out,
                       static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+int host_setup(llama_layer* L) {
+  if (L->host_ready) return LLAMA_OK;
+  const unsigned ef = cudaEventDisableTiming;
+  bool ok = cudaStreamCreateWithFlags(&L->h2d, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&L->d2h, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&L->ev_start, ef) == cudaSuccess &&
+            cudaEventCreateWithFlags(&L->ev_done, ef) == cudaSuccess;
+  for (int c = 0; ok && c < LLAMA_HOST_MAX_CHUNKS; ++c)
+    ok = cudaEventCreateWithFlags(&L->ev_in[c], ef) == cudaSuccess &&
+         cudaEventCreateWithFlags(&L->ev_comp[c], ef) == cudaSuccess;
+  if (!ok) return LLAMA_ERR_CUDA;  // (the few objects made stay until exit)
+  L->host_ready = true;
+  return LLAMA_OK;
+}
+
+}  // namespace
+
+int llama_layer_forward_host(llama_layer_t* L, const void* x_host, void* out_host,
+                             void* x_dev, void* out_dev, const int32_t* cu_seqlens,
+                             int n_seq, int seq_len, int total_tokens, int chunks,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (!L || !x_host || !out_host || chunks < 0) return LLAMA_ERR_INVALID_ARG;
+  if (total_tokens == 0) return LLAMA_OK;
+  // the device-side checks are llama_layer_forward's, on the whole batch
+  if (!x_dev || !out_dev || total_tokens < 0 || !aligned(x_dev, 16) ||
+      !aligned(out_dev, 16) || x_dev == out_dev)
+    return LLAMA_ERR_INVALID_ARG;
+  if (n_seq <= 0 || seq_len <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!cu_seqlens && (long)n_seq * seq_len != total_tokens) return LLAMA_ERR_INVALID_ARG;
+  if (cu_seqlens && (!aligned(cu_seqlens, 4) || (long)n_seq > total_tokens))
+    return LLAMA_ERR_INVALID_ARG;
+  if (seq_len > L->cfg.max_position) return LLAMA_ERR_INVALID_ARG;
+  if ((size_t)seq_len * sizeof(float) > 200 * 1024) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
+  if (workspace_bytes < ws_layout(L->cfg, total_tokens).total)
+    return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+  int rc = host_setup(L);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // groups of whole sequences: chunks = 0 picks >= 4096 tokens a group;
+  // packed (varlen) batches run as one group
+  int nc = chunks;
+  if (nc == 0) nc = total_tokens / 4096;
+  nc = std::max(1, std::min({nc, n_seq, LLAMA_HOST_MAX_CHUNKS}));
+  if (cu_seqlens) nc = 1;
+  const size_t row = (size_t)L->cfg.hidden * (L->bf16 ? 2 : 4);
+  auto first_seq = [&](int c) { return (int)((long)c * n_seq / nc); };
+  auto first_row = [&](int c) {
+    return cu_seqlens ? (c == 0 ? 0 : total_tokens) : first_seq(c) * seq_len;
+  };
+  // copies in: the staging buffer is free once earlier work on `stream` is
+  if (cudaEventRecord(L->ev_start, s) != cudaSuccess ||
+      cudaStreamWaitEvent(L->h2d, L->ev_start, 0) != cudaSuccess)
+    return LLAMA_ERR_CUDA;
+  for (int c = 0; c < nc; ++c) {
+    const size_t r0 = first_row(c), r1 = first_row(c + 1);
+    if (cudaMemcpyAsync(static_cast<char*>(x_dev) + r0 * row,
+                        static_cast<const char*>(x_host) + r0 * row, (r1 - r0) * row,
+                        cudaMemcpyHostToDevice, L->h2d) != cudaSuccess ||
+        cudaEventRecord(L->ev_in[c], L->h2d) != cudaSuccess)
+      return LLAMA_ERR_CUDA;
+  }
+  // the layer on each group as soon as its rows are in, each group's rows
+  // copied out as soon as it is done
+  int launches = 0;
+  for (int c = 0; c < nc; ++c) {
+    const int r0 = first_row(c), r1 = first_row(c + 1);
+    const int q = cu_seqlens ? n_seq : first_seq(c + 1) - first_seq(c);
+    if (cudaStreamWaitEvent(s, L->ev_in[c], 0) != cudaSuccess) return LLAMA_ERR_CUDA;
+    rc = forward_impl(L, static_cast<char*>(x_dev) + (size_t)r0 * row,
+                      static_cast<char*>(out_dev) + (size_t)r0 * row, nullptr,
+                      cu_seqlens, q, seq_len, r1 - r0,
+                      static_cast<char*>(workspace), s);
+    if (rc) return rc;
+    launches += L->launches;
+    if (cudaEventRecord(L->ev_comp[c], s) != cudaSuccess ||
+        cudaStreamWaitEvent(L->d2h, L->ev_comp[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<char*>(out_host) + (size_t)r0 * row,
+                        static_cast<const char*>(out_dev) + (size_t)r0 * row,
+                        (size_t)(r1 - r0) * row, cudaMemcpyDeviceToHost,
+                        L->d2h) != cudaSuccess)
+      return LLAMA_ERR_CUDA;
+  }
+  L->launches = launches;
+  // `stream` continues after the last copy out
+  if (cudaEventRecord(L->ev_done, L->d2h) != cudaSuccess ||
+      cudaStreamWaitEvent(s, L->ev_done, 0) != cudaSuccess)
+    return LLAMA_ERR_CUDA;
+  return LLAMA_OK;
+}
+
 int llama_layer_decode(llama_layer_t* L, const void* x, void* out,
                        void* cache_k, void* cache_v, const int32_t* start_pos,
                        int batch, int max_seq, void* workspace,
@@ -764,6 +864,16 @@ int llama_layer_launch_count(const llama_layer_t* L) {
 
 void llama_layer_destroy(llama_layer_t* L) {
   if (L) free_timing(L);
+  if (L && L->host_ready) {
+    cudaStreamDestroy(L->h2d);
+    cudaStreamDestroy(L->d2h);
+    cudaEventDestroy(L->ev_start);
+    cudaEventDestroy(L->ev_done);
+    for (int c = 0; c < LLAMA_HOST_MAX_CHUNKS; ++c) {
+      cudaEventDestroy(L->ev_in[c]);
+      cudaEventDestroy(L->ev_comp[c]);
+    }
+  }
   delete L;
 }
 

@@ -113,13 +113,28 @@ class LlamaLayer:
                              stream_ptr())
         return out
 
-    def forward_from_host(self, x_host, out_host, x_dev, out_dev, **kw):
-        """One forward whose input and output live in (pinned) host memory:
-        copy x in, run the layer, copy out back, all on the current stream.
-        ``x_dev`` / ``out_dev`` are device buffers of the same shape."""
-        x_dev.copy_(x_host, non_blocking=True)
-        self.forward(x_dev, out=out_dev, **kw)
-        out_host.copy_(out_dev, non_blocking=True)
+    def forward_from_host(self, x_host, out_host, x_dev, out_dev,
+                          cu_seqlens=None, n_seq=None, seq_len=None, chunks=0):
+        """One forward whose input and output live in (pinned) host memory,
+        through llama_layer_forward_host: groups of whole sequences are copied
+        in, run and copied out with the copies overlapping the layer (chunks =
+        0 picks groups of >= 4096 tokens).  ``x_dev`` / ``out_dev`` are device
+        staging buffers of the same shape; out_host is valid once the current
+        stream is synchronised."""
+        T = x_host.shape[0]
+        if cu_seqlens is None:
+            seq_len = seq_len or T
+            n_seq = n_seq or (T // seq_len)
+        else:
+            n_seq = cu_seqlens.numel() - 1
+            assert seq_len is not None, "varlen needs max_seqlen"
+        self.ensure_workspace(T)
+        B.llama_layer_forward_host(
+            self.handle, x_host.data_ptr(), out_host.data_ptr(), x_dev.data_ptr(),
+            out_dev.data_ptr(),
+            cu_seqlens.data_ptr() if cu_seqlens is not None else None,
+            n_seq, seq_len, T, chunks, self.workspace.data_ptr(),
+            self.workspace.numel(), stream_ptr())
         return out_host
 
     def decode_from_host(self, x_host, out_host, x_dev, out_dev, cache_k,

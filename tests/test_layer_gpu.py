@@ -101,6 +101,57 @@ def test_split_tiles_repeated_calls():
     layer.close()
 
 
+@pytest.mark.parametrize("chunks", [0, 3, 6])
+def test_forward_host_groups_match_the_oracle(chunks):
+    # input and output in pinned host memory; groups of whole sequences are
+    # copied in, run and copied out on separate streams (0: one group here)
+    s = shape(512, 8, 2, 64, 1024, **L3)
+    w = synth.custom_workload("host", s, "padded", batch=6, seq=700)
+    inp = synth.make_inputs(w)
+    layer = build_layer(inp)
+    T = inp.tokens
+    x_dev = to_device(inp.x)
+    dev_out = run_forward(layer, inp, varlen=False).clone()
+    x_h = x_dev.cpu().pin_memory()
+    out_h = torch.full_like(x_h, float("nan")).pin_memory()
+    stage_x = torch.empty_like(x_dev)
+    stage_out = torch.empty_like(x_dev)
+    layer.forward_from_host(x_h, out_h, stage_x, stage_out, n_seq=6, seq_len=700,
+                            chunks=chunks)
+    torch.cuda.current_stream().synchronize()
+    assert layer.status() == B.LLAMA_OK
+    assert layer.launch_count() > 0
+    ref = oracle.decoder_layer(synth.to_f64(inp.x), weights_f64(inp.weights),
+                               s, inp.positions, inp.cu_seqlens)
+    assert_close(to_f64(out_h), ref["out"], s.dtype, "host out")
+    # the same layer on the device-resident input, up to the order of the
+    # row-sum atomics (a bf16 ulp at most)
+    d = (out_h.float() - dev_out.cpu().float()).abs()
+    assert float(d.max()) <= 2.0 ** -7 * float(dev_out.float().abs().max())
+    layer.close()
+
+
+def test_forward_host_packed_batch():
+    s = shape(256, 4, 2, 64, 256, **L3)
+    w = synth.custom_workload("hostv", s, "varlen", total_tokens=900, min_len=1,
+                              max_len=300)
+    inp = synth.make_inputs(w)
+    layer = build_layer(inp)
+    x_h = to_device(inp.x, pin=True)
+    out_h = torch.full_like(x_h, float("nan")).pin_memory()
+    stage_x = torch.empty(x_h.shape, dtype=x_h.dtype, device="cuda")
+    stage_out = torch.empty_like(stage_x)
+    cu = to_device(inp.cu_seqlens)
+    S = int(np.diff(inp.cu_seqlens).max())
+    layer.forward_from_host(x_h, out_h, stage_x, stage_out, cu_seqlens=cu, seq_len=S)
+    torch.cuda.current_stream().synchronize()
+    assert layer.status() == B.LLAMA_OK
+    ref = oracle.decoder_layer(synth.to_f64(inp.x), weights_f64(inp.weights),
+                               s, inp.positions, inp.cu_seqlens)
+    assert_close(to_f64(out_h), ref["out"], s.dtype, "host out (packed)")
+    layer.close()
+
+
 def test_explicit_position_ids():
     s = shape(256, 4, 2, 64, 256, **L3)
     w = synth.custom_workload("pos", s, "padded", batch=2, seq=64)
