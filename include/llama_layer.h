@@ -166,7 +166,7 @@ LLAMA_API int llama_layer_forward(llama_layer_t* layer, const void* x, void* out
 
 /* The prefill forward with its input and output in host memory, the copies
  * overlapped with the layer: the batch is split into `chunks` groups of whole
- * sequences (0: groups of at least 4096 tokens; at most LLAMA_HOST_MAX_CHUNKS
+ * sequences (0: groups of at least 2048 tokens; at most LLAMA_HOST_MAX_CHUNKS
  * and n_seq; a packed batch, cu_seqlens != NULL, is one group), and while the
  * layer runs on group i on `stream`, group i + 1 is copied in and group i - 1
  * copied out on two streams the layer owns.  Positions restart at 0 in every

@@ -729,10 +729,11 @@ int llama_layer_forward_host(llama_layer_t* L, const void* x_host, void* out_hos
   int rc = host_setup(L);
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // groups of whole sequences: chunks = 0 picks >= 4096 tokens a group;
-  // packed (varlen) batches run as one group
+  // groups of whole sequences: chunks = 0 picks >= 2048 tokens a group (a
+  // group's copies are exposed only at the ends of the pipeline, and 2048-row
+  // GEMMs still fill the GPU); packed (varlen) batches run as one group
   int nc = chunks;
-  if (nc == 0) nc = total_tokens / 4096;
+  if (nc == 0) nc = total_tokens / 2048;
   nc = std::max(1, std::min({nc, n_seq, LLAMA_HOST_MAX_CHUNKS}));
   if (cu_seqlens) nc = 1;
   const size_t row = (size_t)L->cfg.hidden * (L->bf16 ? 2 : 4);

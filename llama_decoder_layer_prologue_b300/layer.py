@@ -118,7 +118,7 @@ class LlamaLayer:
         """One forward whose input and output live in (pinned) host memory,
         through llama_layer_forward_host: groups of whole sequences are copied
         in, run and copied out with the copies overlapping the layer (chunks =
-        0 picks groups of >= 4096 tokens).  ``x_dev`` / ``out_dev`` are device
+        0 picks groups of >= 2048 tokens).  ``x_dev`` / ``out_dev`` are device
         staging buffers of the same shape; out_host is valid once the current
         stream is synchronised."""
         T = x_host.shape[0]

@@ -104,7 +104,7 @@ def test_split_tiles_repeated_calls():
 @pytest.mark.parametrize("chunks", [0, 3, 6])
 def test_forward_host_groups_match_the_oracle(chunks):
     # input and output in pinned host memory; groups of whole sequences are
-    # copied in, run and copied out on separate streams (0: one group here)
+    # copied in, run and copied out on separate streams (0: two groups here)
     s = shape(512, 8, 2, 64, 1024, **L3)
     w = synth.custom_workload("host", s, "padded", batch=6, seq=700)
     inp = synth.make_inputs(w)
