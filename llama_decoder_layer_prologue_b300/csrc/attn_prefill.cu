@@ -47,10 +47,11 @@ constexpr float kRescaleLog2 = 8.0f;
 // so the block launches at 168 registers a thread (384 x 168 = 64512) and
 // then moves registers with setmaxnreg: the two softmax warpgroups go up to
 // kSoftmaxRegs, the producer / MMA warpgroup (warps 8..11, 11 idle)
-// down to kControlRegs; 2 x 128 x 200 + 128 x 104 = 64512.
+// down to kControlRegs; 2 x 128 x 216 + 128 x 72 = 64512 (the split with the
+// fewest spills: the softmax row holds 128 scores).
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr int kSoftmaxRegs = 200, kControlRegs = 104;
+constexpr int kSoftmaxRegs = 216, kControlRegs = 72;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168,
               "register split exceeds the launch allocation");
 
