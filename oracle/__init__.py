@@ -25,5 +25,6 @@ from .layer import (  # noqa: F401
     decoder_layer,
     decoder_layer_rows,
     decoder_layer_decode,
+    decoder_layer_cached,
     layer_inv_freq,
 )

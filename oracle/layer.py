@@ -279,3 +279,51 @@ def decoder_layer_decode(x: np.ndarray, w, cfg, cache_rows,
     hn = rms_norm(h, w.g_post, cfg.rms_eps)
     act, mlp = swiglu_mlp(hn, w.w_gate_up, w.w_down)
     return dict(q=q, k_new=k, v_new=v, attn=attn, h=h, act=act, out=h + mlp)
+
+
+def decoder_layer_cached(x: np.ndarray, w, cfg, cache_rows, start_pos: np.ndarray,
+                         S: int) -> dict:
+    """S new tokens per sequence against a KV cache: the general form of the
+    Meta Attention.forward with start_pos and seqlen > 1 ([the7] 3.2: the new
+    keys / values go to cache rows start_pos .. start_pos + S - 1 and the
+    queries attend to rows 0 .. start_pos + S - 1; [csdn] "5. Transformer":
+    the mask is zeros over the start_pos cached columns followed by the
+    causal triangle over the new tokens).
+
+    x [B * S, hidden], rows b * S .. b * S + S - 1 the new tokens of sequence
+    b at positions start_pos[b] .. start_pos[b] + S - 1; ``cache_rows(b, n)``
+    as for decoder_layer_decode.  Returns out [B * S, H], the new cache rows
+    k_new / v_new [B * S, Hkv, d] and the intermediates.
+    """
+    BS = x.shape[0]
+    B = BS // S
+    d = cfg.head_dim
+    n_rep = cfg.n_heads // cfg.n_kv_heads
+    positions = (np.repeat(np.asarray(start_pos, dtype=np.int64), S) +
+                 np.tile(np.arange(S), B))
+    xn = rms_norm(x, w.g_in, cfg.rms_eps)
+    qkv = xn @ w.w_qkv.T
+    q, k, v = _split_qkv(qkv, cfg)
+    cos, sin = rope_cos_sin(positions, layer_inv_freq(cfg))
+    q, k = apply_rope(q, cos, sin), apply_rope(k, cos, sin)
+    attn = np.zeros((BS, cfg.n_heads, d))
+    for b in range(B):
+        sp = int(start_pos[b])
+        old_k, old_v = cache_rows(b, sp)
+        new = slice(b * S, (b + 1) * S)
+        keys = repeat_kv(np.concatenate([old_k, k[new]], axis=0), n_rep)
+        values = repeat_kv(np.concatenate([old_v, v[new]], axis=0), n_rep)
+        # mask row i: the sp cached columns, then new columns 0 .. i
+        mask = np.concatenate([np.zeros((S, sp)),
+                               np.triu(np.full((S, S), -np.inf), k=1)], axis=1)
+        for hh in range(cfg.n_heads):
+            sc = q[new, hh] @ keys[:, hh].T / math.sqrt(d) + mask
+            sc = sc - sc.max(axis=1, keepdims=True)
+            p = np.exp(sc)
+            p = p / p.sum(axis=1, keepdims=True)
+            attn[new, hh] = p @ values[:, hh]
+    attn = attn.reshape(BS, -1)
+    h = x + attn @ w.w_o.T
+    hn = rms_norm(h, w.g_post, cfg.rms_eps)
+    act, mlp = swiglu_mlp(hn, w.w_gate_up, w.w_down)
+    return dict(q=q, k_new=k, v_new=v, attn=attn, h=h, act=act, out=h + mlp)

@@ -170,6 +170,74 @@ def test_decode_equals_last_row_of_prefill():
                                    rtol=1e-12, atol=1e-13)
 
 
+def test_cached_chunk_equals_the_rest_of_a_prefill():
+    """A sequence split into a cached prefix (rotated k / v from the prefill
+    of the whole sequence) and a chunk of S new tokens: the chunk must
+    reproduce the prefill's rows and new cache rows after the prefix."""
+    cfg = SMALL_L3
+    w = weights(cfg)
+    S = 5
+    prefix = [9, 0, 3, 14]
+    seqs = [RNG.standard_normal((p + S, cfg.hidden)) for p in prefix]
+    pre = [oracle.decoder_layer(s, w, cfg, np.arange(len(s)),
+                                np.array([0, len(s)])) for s in seqs]
+    cache = lambda b, n: (pre[b]["k"][:n], pre[b]["v"][:n])
+    x_new = np.concatenate([s[-S:] for s in seqs])
+    got = oracle.decoder_layer_cached(x_new, w, cfg, cache, np.array(prefix), S)
+    for b, p in enumerate(prefix):
+        rows = slice(b * S, (b + 1) * S)
+        np.testing.assert_allclose(got["out"][rows], pre[b]["out"][p:],
+                                   rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(got["k_new"][rows], pre[b]["k"][p:],
+                                   rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(got["v_new"][rows], pre[b]["v"][p:],
+                                   rtol=1e-12, atol=1e-13)
+
+
+def test_cached_chunk_of_one_token_is_decode():
+    cfg = SMALL_L3
+    w = weights(cfg)
+    sp = np.array([3, 0, 11])
+    cache_k = [RNG.standard_normal((n, cfg.n_kv_heads, cfg.head_dim)) for n in sp]
+    cache_v = [RNG.standard_normal((n, cfg.n_kv_heads, cfg.head_dim)) for n in sp]
+    cache = lambda b, n: (cache_k[b][:n], cache_v[b][:n])
+    x = RNG.standard_normal((len(sp), cfg.hidden))
+    a = oracle.decoder_layer_cached(x, w, cfg, cache, sp, 1)
+    b = oracle.decoder_layer_decode(x, w, cfg, cache, sp)
+    for key in ("out", "attn", "k_new", "v_new"):
+        np.testing.assert_allclose(a[key], b[key], rtol=1e-13, atol=1e-14)
+
+
+def test_cached_chunk_with_empty_cache_is_prefill():
+    cfg = SMALL
+    w = weights(cfg)
+    B, S = 3, 6
+    x = RNG.standard_normal((B * S, cfg.hidden))
+    empty = lambda b, n: (np.zeros((0, cfg.n_kv_heads, cfg.head_dim)),) * 2
+    a = oracle.decoder_layer_cached(x, w, cfg, empty, np.zeros(B, np.int64), S)
+    pos = np.tile(np.arange(S), B)
+    ref = oracle.decoder_layer(x, w, cfg, pos, np.arange(0, B * S + 1, S))
+    np.testing.assert_allclose(a["out"], ref["out"], rtol=1e-12, atol=1e-12)
+
+
+def test_cached_chunk_is_causal_within_the_chunk():
+    # changing the last new token leaves every earlier token's output exactly
+    # as it was (row i sees the prefix and new rows 0 .. i only)
+    cfg = SMALL_L3
+    w = weights(cfg)
+    S, sp = 4, np.array([6])
+    ck = RNG.standard_normal((6, cfg.n_kv_heads, cfg.head_dim))
+    cv = RNG.standard_normal((6, cfg.n_kv_heads, cfg.head_dim))
+    cache = lambda b, n: (ck[:n], cv[:n])
+    x = RNG.standard_normal((S, cfg.hidden))
+    y = x.copy()
+    y[-1] += 1.0
+    a = oracle.decoder_layer_cached(x, w, cfg, cache, sp, S)["out"]
+    b = oracle.decoder_layer_cached(y, w, cfg, cache, sp, S)["out"]
+    np.testing.assert_array_equal(a[:-1], b[:-1])
+    assert not np.allclose(a[-1], b[-1])
+
+
 # ----------------------------------------------------------------- shapes
 def test_1b_shapes_match_page_printout():
     rows = {}
