@@ -55,6 +55,9 @@ DESCRIPTIONS = {
               "causal within each sequence",
     "decode": "KV-cache decode 8B-shaped layer bf16: batch 64 x 1 new token, "
               "start_pos U{512..8191} (seeded), cache [64, 8192, 8, 128] bf16",
+    "chunked": "chunked prefill with a KV cache, 8B-shaped layer bf16: 16 "
+               "sequences x 4 new tokens, start_pos U{512..8188} (seeded), cache "
+               "[16, 8192, 8, 128] bf16 (llama_layer_forward_cached)",
 }
 
 # Kernel sources behind each stage: a recorded DRAM traffic figure is only
@@ -87,7 +90,7 @@ def parse_args():
 
 
 DEFAULT_STEPS = {"tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
-                 "decode": 3000}
+                 "decode": 3000, "chunked": 1500}
 
 
 def dist_env():
@@ -316,16 +319,23 @@ class OracleRunner:
         np, inp, synth = self.np, self.inp, self.synth
         s = inp.workload.shape
         if inp.workload.kind == "decode":
-            b = max(1, min(n, inp.tokens))
-            x = synth.to_f64(inp.x[:b])
+            S = inp.workload.seq_tokens
+            nseq = inp.workload.batch
+            b = max(1, min(-(-n // S), nseq))  # whole sequences
+            x = synth.to_f64(inp.x[:b * S])
             sp = inp.start_pos[:b]
 
             def rows(i, k):
                 return (synth.to_f64(inp.cache_k[i, :k]), synth.to_f64(inp.cache_v[i, :k]))
 
+            if S == 1:
+                def run():
+                    self.oracle.decoder_layer_decode(x, self.w, s, rows, sp)
+                return run, b, f"first {b} of {nseq} decode sequences"
+
             def run():
-                self.oracle.decoder_layer_decode(x, self.w, s, rows, sp)
-            return run, b, f"first {b} of {inp.tokens} decode sequences"
+                self.oracle.decoder_layer_cached(x, self.w, s, rows, sp, S)
+            return run, b * S, f"first {b} of {nseq} sequences x {S} new tokens"
         cu = inp.cu_seqlens.astype(np.int64)
         n = max(1, min(n, inp.tokens))
         whole = int(np.searchsorted(cu, n, side="right") - 1)
@@ -402,12 +412,16 @@ def run_ours(args, rank, local_rank, world):
     x = to_device(inp.x)
     out = torch.empty_like(x)
     decode = w.kind == "decode"
+    S_new = w.seq_tokens
     if decode:
         ck, cv = to_device(inp.cache_k), to_device(inp.cache_v)
         sp = to_device(inp.start_pos)
 
         def step(o=out):
-            layer.decode(x, ck, cv, sp, out=o)
+            if S_new == 1:
+                layer.decode(x, ck, cv, sp, out=o)
+            else:
+                layer.forward_cached(x, ck, cv, sp, S_new, out=o)
     else:
         varlen = w.kind == "varlen"
         cu = to_device(inp.cu_seqlens) if varlen else None
@@ -512,7 +526,9 @@ def run_ours(args, rank, local_rank, world):
             ev2[i][0].record(stream)
             for h_, d_ in zip(extra_h, extra_d):
                 d_.copy_(h_, non_blocking=True)
-            if decode:
+            if decode and S_new > 1:
+                layer.forward_cached_from_host(x_h, out_h, x, out, ck, cv, sp, S_new)
+            elif decode:
                 layer.decode_from_host(x_h, out_h, x, out, ck, cv, sp)
             elif w.kind == "varlen":
                 layer.forward_from_host(x_h, out_h, x, out, cu_seqlens=cu, seq_len=seq)
@@ -531,8 +547,9 @@ def run_ours(args, rank, local_rank, world):
         e2e = {"value": world * n_e2e * tokens / (e2e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
                "steps": n_e2e, "ms_per_step": e2e_ms / n_e2e,
-               "api": ("LlamaLayer.decode_from_host (pinned host buffers, "
-                       "cudaMemcpyAsync on the layer's stream)" if decode else
+               "api": ("LlamaLayer.%s_from_host (pinned host buffers, "
+                       "cudaMemcpyAsync on the layer's stream)"
+                       % ("decode" if S_new == 1 else "forward_cached") if decode else
                        "LlamaLayer.forward_from_host -> llama_layer_forward_host "
                        "(pinned host buffers; groups of whole sequences, copies "
                        "in and out on two streams overlapping the layer)")}

@@ -202,6 +202,31 @@ LLAMA_API int llama_layer_decode(llama_layer_t* layer, const void* x, void* out,
                        int batch, int max_seq, void* workspace,
                        size_t workspace_bytes, void* stream);
 
+/* Chunked prefill with a KV cache ("llama3 结构详解" 3.2, the Meta
+ * Attention.forward with start_pos and seqlen > 1; Llama-3 model.py
+ * walkthrough "5. Transformer": the mask is zeros over the cached columns
+ * followed by the causal triangle): seq_tokens new tokens per sequence.
+ *   x          [batch * seq_tokens, hidden] device; rows b * seq_tokens ..
+ *              (b + 1) * seq_tokens - 1 are sequence b's new tokens
+ *   out        [batch * seq_tokens, hidden] device (must not alias x)
+ *   cache_k/v  as llama_layer_decode; the new tokens' rotated keys and values
+ *              are written at rows start_pos[b] .. start_pos[b] + seq_tokens - 1
+ *   start_pos  [batch] device int32: the position of sequence b's first new
+ *              token; every new token's position must be < max_seq and
+ *              < max_position (checked on the device, status word)
+ * New token i of sequence b attends to cache rows 0 .. start_pos[b] + i.
+ * seq_tokens = 1 is llama_layer_decode.  The attention of each new token
+ * reads its prefix on its own (the decode kernels), which suits short chunks
+ * (a few tokens per sequence, e.g. checking drafted tokens).  bf16 layers;
+ * an fp32 layer takes seq_tokens = 1 only (LLAMA_ERR_UNSUPPORTED_SHAPE).
+ * `workspace` must hold llama_layer_workspace_bytes(layer, 0,
+ * >= batch * seq_tokens, >= max_seq). */
+LLAMA_API int llama_layer_forward_cached(llama_layer_t* layer, const void* x, void* out,
+                                         void* cache_k, void* cache_v,
+                                         const int32_t* start_pos, int batch,
+                                         int seq_tokens, int max_seq, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, reads and clears the device status word.  Returns
  * LLAMA_OK, LLAMA_ERR_DEVICE_TIMEOUT or LLAMA_ERR_DEVICE_BAD_INPUT. */
 LLAMA_API int llama_layer_status(llama_layer_t* layer, void* stream);

@@ -40,7 +40,7 @@ EXPORTS = (
     "llama_layer_destroy", "llama_layer_strerror", "llama_gemm_bf16",
     "llama_layer_set_timing", "llama_layer_stage_times",
     "llama_layer_launch_count", "llama_gemm_bf16_streamk_static",
-    "llama_layer_forward_host",
+    "llama_layer_forward_host", "llama_layer_forward_cached",
 )
 
 
@@ -112,6 +112,8 @@ def lib() -> ctypes.CDLL:
         "llama_gemm_bf16_streamk_static": (_I, [_P, _P, _P, _I, _I, _I, _P]),
         "llama_layer_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                           _P, _SZ, _P]),
+        "llama_layer_forward_cached": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P,
+                                            _SZ, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -179,6 +181,16 @@ def llama_layer_forward_host(layer: int, x_host: int, out_host: int, x_dev: int,
            lib().llama_layer_forward_host(layer, x_host, out_host, x_dev, out_dev,
                                           cu_seqlens, n_seq, seq_len, total_tokens,
                                           chunks, workspace, workspace_bytes, stream))
+
+
+def llama_layer_forward_cached(layer: int, x: int, out: int, cache_k: int,
+                               cache_v: int, start_pos: int, batch: int,
+                               seq_tokens: int, max_seq: int, workspace: int,
+                               workspace_bytes: int, stream: int) -> None:
+    _check("llama_layer_forward_cached",
+           lib().llama_layer_forward_cached(layer, x, out, cache_k, cache_v, start_pos,
+                                            batch, seq_tokens, max_seq, workspace,
+                                            workspace_bytes, stream))
 
 
 def llama_layer_decode(layer: int, x: int, out: int, cache_k: int,

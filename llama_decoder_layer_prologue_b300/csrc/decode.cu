@@ -30,6 +30,15 @@ __device__ __forceinline__ bool start_ok(int sp, const DecodeArgs& a) {
   return sp >= 0 && sp < a.max_seq && sp < a.max_pos;
 }
 
+// Sequence and position of token row b of this pass.
+__device__ __forceinline__ void row_seq_pos(const DecodeArgs& a, int b, int& seq,
+                                            int& sp) {
+  const int r = a.row0 + b;
+  seq = r / a.seq_tokens;
+  const int p0 = a.start_pos[seq];
+  sp = p0 < 0 ? -1 : p0 + (r - seq * a.seq_tokens);  // negative stays invalid
+}
+
 // Sum over tile t's slots of rows 4 lane .. 4 lane + 3 of token b.
 __device__ __forceinline__ float4 gather_rows(const DecodeArgs& a,
                                               const TcStreamK& plan, int t,
@@ -81,7 +90,8 @@ __device__ __forceinline__ void st_f16x4(__half* p, float4 v) {
 
 // q, k, v of the new tokens (the GEMM's operand is already x / RMS(x)): RoPE
 // at start_pos on q and k,
-// all three -> qkv[b, :], k and v also -> cache row start_pos[b].  Head
+// all three -> qkv[b, :], k and v also -> cache row sp of the token's
+// sequence (row_seq_pos).  Head
 // boundaries fall on 4-row groups and head_dim divides 128, so the RoPE
 // partner rows i +- D/2 sit D/8 lanes away in the same warp.
 __global__ void __launch_bounds__(FT) finalize_qkv_kernel(DecodeArgs a,
@@ -91,7 +101,8 @@ __global__ void __launch_bounds__(FT) finalize_qkv_kernel(DecodeArgs a,
   const int t = blockIdx.x, b = blockIdx.y * FB + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= a.batch) return;
-  const int sp = a.start_pos[b];
+  int seq, sp;
+  row_seq_pos(a, b, seq, sp);
   float4 x = gather_rows(a, plan, t, b);
   if (!start_ok(sp, a)) {
     if (lane == 0) set_status(a.status, ST_BAD_START_POS);
@@ -120,7 +131,7 @@ __global__ void __launch_bounds__(FT) finalize_qkv_kernel(DecodeArgs a,
   if (head >= hq) {
     const int g = head < hq + hkv ? head - hq : head - hq - hkv;
     __nv_bfloat16* cache = head < hq + hkv ? a.cache_k : a.cache_v;
-    st_bf16x4(cache + (((size_t)b * a.max_seq + sp) * hkv + g) * D + i, x);
+    st_bf16x4(cache + (((size_t)seq * a.max_seq + sp) * hkv + g) * D + i, x);
   }
 }
 
@@ -190,8 +201,9 @@ __global__ void __launch_bounds__(FT) finalize_down_kernel(DecodeArgs a,
 }
 
 // ------------------------------------------------------------ attention
-// Split-KV: CTA (split c, kv head g, sequence b) takes cache rows
-// [KS c, min(KS c + KS, start_pos + 1)) and the n_rep query heads of g (the
+// Split-KV: CTA (split c, kv head g, token row b) takes rows
+// [KS c, min(KS c + KS, sp + 1)) of the cache of the row's sequence (sp its
+// position, row_seq_pos) and the n_rep query heads of g (the
 // rows of one 16-row MMA tile).  The rows stream through a 3-stage cp.async
 // ring of 64-key tiles; each of the 4 warps scores 16 keys of a tile with
 // mma.sync (S = Q K^T), keeps its own online softmax (log2 domain) and P V
@@ -211,7 +223,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
   bf16* sK = sQ + 16 * P;            // [NST][KT][P]
   bf16* sV = sK + NST * KT * P;      // [NST][KT][P]
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int sp = a.start_pos[b];
+  int seq, sp;
+  row_seq_pos(a, b, seq, sp);
   if (!start_ok(sp, a)) return;
   const int n_keys = sp + 1, k0 = c * KS;
   if (k0 >= n_keys) return;
@@ -228,8 +241,8 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
     cp_async16(smem_u32(sQ + row * P + ch * 8), src, row < n_rep ? 16 : 0);
   }
   const size_t row_stride = (size_t)a.n_kv_heads * D;
-  const bf16* kbase = a.cache_k + (size_t)b * a.max_seq * row_stride + g * D;
-  const bf16* vbase = a.cache_v + (size_t)b * a.max_seq * row_stride + g * D;
+  const bf16* kbase = a.cache_k + (size_t)seq * a.max_seq * row_stride + g * D;
+  const bf16* vbase = a.cache_v + (size_t)seq * a.max_seq * row_stride + g * D;
   auto load_tile = [&](int j, int st) {
     bf16* dk = sK + st * KT * P;
     bf16* dv = sV + st * KT * P;
@@ -396,7 +409,8 @@ __global__ void __launch_bounds__(CT) attn_combine_kernel(DecodeArgs a) {
   const int g = h / n_rep, row = h % n_rep;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __half* o = a.attn + (size_t)b * a.n_heads * D + h * D;
-  const int sp = a.start_pos[b];
+  int seq, sp;
+  row_seq_pos(a, b, seq, sp);
   if (!start_ok(sp, a)) {
     for (int i = threadIdx.x; i < D; i += CT) o[i] = __float2half_rn(0.f);
     return;

@@ -13,7 +13,11 @@ namespace llama {
 enum DecStage : int { DEC_QKV = 0, DEC_O = 1, DEC_GU = 2, DEC_DOWN = 3 };
 
 struct DecodeArgs {
-  int batch, bn;  // tokens; column stride of the GEMM partials
+  int batch, bn;  // tokens of this pass; column stride of the GEMM partials
+  // token row b of this pass is row row0 + b of the call: sequence
+  // (row0 + b) / seq_tokens, position start_pos[that sequence] +
+  // (row0 + b) % seq_tokens (seq_tokens = 1: one new token per sequence)
+  int row0, seq_tokens;
   int hidden, n_heads, n_kv_heads, head_dim, inter, nqkv;
   int max_seq, max_pos;
   float eps;
@@ -21,7 +25,7 @@ struct DecodeArgs {
   const __nv_bfloat16* x;  // [B, H] layer input
   const float* r1;         // [B] 1/RMS(x)
   float* ss2;              // [B] sum of h^2 (zeroed before DEC_O)
-  const int32_t* start_pos;
+  const int32_t* start_pos;  // [sequences] of the whole call
   const float *cos_t, *sin_t;
   __nv_bfloat16* qkv;      // [B, nqkv]
   __nv_bfloat16 *cache_k, *cache_v;  // [B, max_seq, Hkv, D]

@@ -374,14 +374,17 @@ DecLayout dec_layout(const llama_layer* L, int B, int max_seq) {
   return w;
 }
 
+// One pass over token rows row0 .. row0 + B - 1 of a call (x / out point at
+// the pass's first row; the cache and start_pos are the whole call's).
 int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
-                 const int32_t* start_pos, int B, int max_seq, char* ws,
-                 cudaStream_t s) {
+                 const int32_t* start_pos, int row0, int seq_tokens, int B,
+                 int max_seq, char* ws, cudaStream_t s) {
   const Dims& dm = L->dm;
   const DecLayout w = dec_layout(L, B, max_seq);
   const char* P = L->packed;
   DecodeArgs a;
   a.batch = B; a.bn = w.bn;
+  a.row0 = row0; a.seq_tokens = seq_tokens;
   a.hidden = dm.H; a.n_heads = dm.Hq; a.n_kv_heads = dm.Hkv;
   a.head_dim = dm.d; a.inter = dm.I; a.nqkv = dm.Nqkv;
   a.max_seq = max_seq; a.max_pos = dm.max_pos; a.eps = dm.eps;
@@ -450,23 +453,23 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   return cuda_err(cudaGetLastError());
 }
 
+// B token rows: seq_tokens consecutive rows per sequence (1 for decode).
 int decode_impl(llama_layer* L, const void* x, void* out, void* ck, void* cv,
                 const int32_t* start_pos, int B, int max_seq, char* ws,
-                cudaStream_t s) {
+                cudaStream_t s, int seq_tokens = 1) {
   const llama_layer_config& c = L->cfg;
   const Dims& dm = L->dm;
   const bool b16 = L->bf16;
   begin_call(L);
   if (b16) {
     const size_t es = 2, row = (size_t)dm.H * es;
-    const size_t cache_seq = (size_t)max_seq * dm.Hkv * dm.d * es;
+    // passes of <= kDecodeChunk rows, in order: a pass's rows see the cache
+    // rows every earlier pass (and their own) appended
     for (int b0 = 0; b0 < B; b0 += kDecodeChunk) {
       const int nb = B - b0 < kDecodeChunk ? B - b0 : kDecodeChunk;
       int rc = decode_chunk(L, static_cast<const char*>(x) + b0 * row,
-                            static_cast<char*>(out) + b0 * row,
-                            static_cast<char*>(ck) + b0 * cache_seq,
-                            static_cast<char*>(cv) + b0 * cache_seq,
-                            start_pos + b0, nb, max_seq, ws, s);
+                            static_cast<char*>(out) + b0 * row, ck, cv, start_pos,
+                            b0, seq_tokens, nb, max_seq, ws, s);
       if (rc) return rc;
     }
     mark(L, s, nullptr);
@@ -801,6 +804,31 @@ int llama_layer_decode(llama_layer_t* L, const void* x, void* out,
   return decode_impl(L, x, out, cache_k, cache_v, start_pos, batch, max_seq,
                      static_cast<char*>(workspace),
                      static_cast<cudaStream_t>(stream));
+}
+
+int llama_layer_forward_cached(llama_layer_t* L, const void* x, void* out,
+                               void* cache_k, void* cache_v, const int32_t* start_pos,
+                               int batch, int seq_tokens, int max_seq, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (!L || !x || !out || batch < 0 || seq_tokens <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || x == out) return LLAMA_ERR_INVALID_ARG;
+  if (batch == 0) return LLAMA_OK;
+  if (!cache_k || !cache_v || !start_pos || max_seq <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned(cache_k, 16) || !aligned(cache_v, 16) || !aligned(start_pos, 4) ||
+      cache_k == cache_v)
+    return LLAMA_ERR_INVALID_ARG;
+  if (seq_tokens > max_seq) return LLAMA_ERR_INVALID_ARG;
+  if (!L->bf16 && seq_tokens > 1) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  const long rows = (long)batch * seq_tokens;
+  if (rows > (1L << 30)) return LLAMA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
+  if (workspace_bytes < decode_ws_bytes(L, (int)rows, max_seq))
+    return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+  if (!L->bf16 && (size_t)max_seq * sizeof(float) > 200 * 1024)
+    return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  return decode_impl(L, x, out, cache_k, cache_v, start_pos, (int)rows, max_seq,
+                     static_cast<char*>(workspace), static_cast<cudaStream_t>(stream),
+                     seq_tokens);
 }
 
 int llama_layer_status(llama_layer_t* L, void* stream) {

@@ -113,6 +113,22 @@ class LlamaLayer:
                              stream_ptr())
         return out
 
+    def forward_cached(self, x, cache_k, cache_v, start_pos, seq_tokens, out=None):
+        """seq_tokens new tokens per sequence against the KV cache (x rows
+        b * seq_tokens .. are sequence b's, at positions start_pos[b] ..)."""
+        rows = x.shape[0]
+        assert rows % seq_tokens == 0, "x holds whole chunks"
+        max_seq = cache_k.shape[1]
+        self.ensure_workspace(0, rows, max_seq)
+        if out is None:
+            out = torch.empty_like(x)
+        B.llama_layer_forward_cached(self.handle, x.data_ptr(), out.data_ptr(),
+                                     cache_k.data_ptr(), cache_v.data_ptr(),
+                                     start_pos.data_ptr(), rows // seq_tokens,
+                                     seq_tokens, max_seq, self.workspace.data_ptr(),
+                                     self.workspace.numel(), stream_ptr())
+        return out
+
     def forward_from_host(self, x_host, out_host, x_dev, out_dev,
                           cu_seqlens=None, n_seq=None, seq_len=None, chunks=0):
         """One forward whose input and output live in (pinned) host memory,
@@ -143,6 +159,14 @@ class LlamaLayer:
         the KV cache stays resident on the device."""
         x_dev.copy_(x_host, non_blocking=True)
         self.decode(x_dev, cache_k, cache_v, start_pos, out=out_dev)
+        out_host.copy_(out_dev, non_blocking=True)
+        return out_host
+
+    def forward_cached_from_host(self, x_host, out_host, x_dev, out_dev, cache_k,
+                                 cache_v, start_pos, seq_tokens):
+        """forward_cached with host input / output (see decode_from_host)."""
+        x_dev.copy_(x_host, non_blocking=True)
+        self.forward_cached(x_dev, cache_k, cache_v, start_pos, seq_tokens, out=out_dev)
         out_host.copy_(out_dev, non_blocking=True)
         return out_host
 

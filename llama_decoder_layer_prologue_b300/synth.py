@@ -84,6 +84,7 @@ class Workload:
     max_len: int = 1024
     max_seq: int = 8192  # decode: cache rows per sequence
     min_start: int = 512
+    seq_tokens: int = 1  # decode: new tokens per sequence (> 1: chunked prefill)
 
     @property
     def seed(self) -> int:
@@ -115,6 +116,8 @@ WORKLOADS = {
     "varlen": Workload("varlen", 3, _SHAPE_8B, "varlen", total_tokens=16384),
     "decode": Workload("decode", 4, _SHAPE_8B, "decode", batch=64,
                        max_seq=8192, min_start=512),
+    "chunked": Workload("chunked", 5, _SHAPE_8B, "decode", batch=16,
+                        max_seq=8192, min_start=512, seq_tokens=4),
 }
 
 
@@ -221,7 +224,7 @@ def make_inputs(w: Workload | str, with_cache: bool = True,
     elif w.kind == "varlen":
         T = w.total_tokens
     else:
-        T = w.batch
+        T = w.batch * w.seq_tokens
     H, I = s.hidden, s.intermediate
     x = _fill_normal(kids[0], T * H, 0.0, 1.0, s.dtype).reshape(T, H)
 
@@ -250,10 +253,12 @@ def make_inputs(w: Workload | str, with_cache: bool = True,
         positions = np.concatenate(
             [np.arange(L, dtype=np.int32) for L in lens])
     else:
-        start_pos = rng.integers(w.min_start, w.max_seq,
+        S = w.seq_tokens  # the chunk ends within the cache
+        start_pos = rng.integers(w.min_start, w.max_seq - S + 1,
                                  size=w.batch).astype(np.int32)
-        cu = np.arange(T + 1, dtype=np.int32)
-        positions = start_pos.copy()
+        cu = np.arange(0, T + 1, S, dtype=np.int32)
+        positions = (np.repeat(start_pos, S) +
+                     np.tile(np.arange(S, dtype=np.int32), w.batch)).astype(np.int32)
         if with_cache:
             cache_k = _make_cache(kids[8], w, start_pos)
             cache_v = _make_cache(kids[9], w, start_pos)

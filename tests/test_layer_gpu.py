@@ -208,6 +208,58 @@ def check_decode(s, batch, max_seq, start_pos, stages=True):
     layer.close()
 
 
+def check_cached(s, batch, S, max_seq, start_pos):
+    # S new tokens per sequence against the cache (chunked prefill)
+    w = synth.custom_workload("chunk", s, "decode", batch=batch, max_seq=max_seq,
+                              min_start=0)
+    inp = synth.make_inputs(w)
+    sp = np.asarray(start_pos, dtype=np.int32)
+    ck_np = synth._make_cache(np.random.SeedSequence(5), w, sp)
+    cv_np = synth._make_cache(np.random.SeedSequence(6), w, sp)
+    rng = np.random.default_rng(17)
+    x_np = synth.bf16_round_bits(rng.standard_normal((batch * S, s.hidden),
+                                                     dtype=np.float32))
+    layer = build_layer(inp)
+    ck = to_device(poison_cache(ck_np, sp))
+    cv = to_device(poison_cache(cv_np, sp))
+    ck0, cv0 = ck.clone(), cv.clone()
+    out = layer.forward_cached(to_device(x_np), ck, cv, to_device(sp), S)
+    torch.cuda.synchronize()
+    assert layer.status() == B.LLAMA_OK
+    rows = lambda b, n: (synth.to_f64(ck_np[b, :n]), synth.to_f64(cv_np[b, :n]))
+    ref = oracle.decoder_layer_cached(synth.to_f64(x_np), weights_f64(inp.weights),
+                                      s, rows, sp, S)
+    assert_close(to_f64(out), ref["out"], s.dtype, f"chunk out (S={S})")
+    for b, p in enumerate(sp):
+        new = slice(b * S, (b + 1) * S)
+        assert_stage_close(to_f64(ck[b, p:p + S]), ref["k_new"][new], s.dtype, "k rows")
+        assert_stage_close(to_f64(cv[b, p:p + S]), ref["v_new"][new], s.dtype, "v rows")
+        assert torch.equal(ck[b, :p], ck0[b, :p])  # the prefix is untouched
+        assert torch.equal(cv[b, :p], cv0[b, :p])
+        assert torch.isnan(ck[b, p + S:].float()).all()  # nothing after the chunk
+        assert torch.isnan(cv[b, p + S:].float()).all()
+    layer.close()
+
+
+@pytest.mark.parametrize("S", [1, 3, 8])
+def test_forward_cached_chunks(S):
+    s = shape(256, 4, 2, 64, 256, **L3)
+    # includes an empty prefix and a chunk ending on the last cache row
+    check_cached(s, batch=5, S=S, max_seq=300, start_pos=[0, 123, 1, 300 - S, 77])
+
+
+def test_forward_cached_pass_boundary_inside_a_sequence():
+    # 40 x 7 = 280 rows: the 256-row passes split sequence 36 after 4 tokens
+    s = shape(256, 4, 2, 64, 256, **L3)
+    sp = [(29 * b) % 180 for b in range(40)]
+    check_cached(s, batch=40, S=7, max_seq=192, start_pos=sp)
+
+
+def test_forward_cached_d128():
+    s = shape(512, 8, 2, 128, 384)
+    check_cached(s, batch=3, S=5, max_seq=600, start_pos=[512, 0, 37])
+
+
 def test_decode_small_bf16_edges():
     s = shape(256, 4, 2, 64, 256, **L3)
     check_decode(s, batch=5, max_seq=300, start_pos=[0, 299, 1, 150, 257])
