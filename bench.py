@@ -67,7 +67,9 @@ STAGE_SOURCES = {
     "qkv_rope": ["gemm_tc.cu", "gemm_tc.cuh", "common.cuh"],
     "o_proj_residual": ["gemm_tc.cu", "gemm_tc.cuh", "common.cuh"],
     "down_residual": ["gemm_tc.cu", "gemm_tc.cuh", "common.cuh"],
-    "attention": ["attn_prefill.cu", "decode.cu", "common.cuh"],
+    "attention": ["attn_prefill.cu", "attn_prefill.cuh", "common.cuh"],
+    # the decode / chunked workloads' attention is the split-KV kernel
+    "attention_decode": ["decode.cu", "decode.cuh", "common.cuh"],
 }
 
 
@@ -113,7 +115,10 @@ def recorded_traffic(workload: str, stage: str):
     path = os.path.join(ROOT, "profiles", "dram_traffic.md")
     if not os.path.exists(path):
         return None
-    want = src_sha(STAGE_SOURCES.get(stage, []))
+    key = stage
+    if stage == "attention" and workload in ("decode", "chunked"):
+        key = "attention_decode"
+    want = src_sha(STAGE_SOURCES.get(key, []))
     with open(path) as fh:
         for line in fh:
             cells = [c.strip() for c in line.strip().strip("|").split("|")]
