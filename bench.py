@@ -95,6 +95,25 @@ DEFAULT_STEPS = {"tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
                  "decode": 3000, "chunked": 1500}
 
 
+def max_over_ranks(dist, x: float) -> float:
+    """The largest x of all ranks (x itself without a process group): the
+    job's time is its slowest replica's."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, tokens_per_step: int, slowest_ms: float) -> float:
+    """Tokens per second of the whole job: every replica processed
+    steps x tokens_per_step tokens in at most slowest_ms (weak scaling)."""
+    return world * steps * tokens_per_step / (slowest_ms / 1e3)
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
             int(os.environ.get("WORLD_SIZE", "1")))
@@ -498,13 +517,10 @@ def run_ours(args, rank, local_rank, world):
     if rc != 0:
         raise RuntimeError(f"layer status after the timed steps: {rc}")
 
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(dist, total_ms)
 
     tokens = inp.tokens
-    value = world * K * tokens / (total_ms / 1e3)
+    value = job_throughput(world, K, tokens, total_ms)
     work = algorithmic_work(inp)
     pk = peaks()
 
@@ -542,14 +558,11 @@ def run_ours(args, rank, local_rank, world):
             ev2[i][1].record(stream)
         torch.cuda.synchronize()
         e2e_ms = float(sum(a.elapsed_time(b) for a, b in ev2))
-        if dist is not None:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(dist, e2e_ms)
         bi = x_h.numel() * x_h.element_size() + sum(
             h_.numel() * h_.element_size() for h_ in extra_h)
         bo = out_h.numel() * out_h.element_size()
-        e2e = {"value": world * n_e2e * tokens / (e2e_ms / 1e3), "unit": UNIT,
+        e2e = {"value": job_throughput(world, n_e2e, tokens, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
                "steps": n_e2e, "ms_per_step": e2e_ms / n_e2e,
                "api": ("LlamaLayer.%s_from_host (pinned host buffers, "
