@@ -227,6 +227,16 @@ LLAMA_API int llama_layer_forward_cached(llama_layer_t* layer, const void* x, vo
                                          int seq_tokens, int max_seq, void* workspace,
                                          size_t workspace_bytes, void* stream);
 
+/* Self-test of the bounded waits the library's pipelined kernels use (no
+ * layer needed): one block waits on an mbarrier that nothing arrives on and
+ * on a device flag that nothing sets, each up to the library's wait limit
+ * (2 s).  Synchronises `stream` and writes observed[0] / observed[1] = 1 if
+ * the mbarrier / flag wait completed, 0 if it gave up, and observed[2] = the
+ * status word the waits wrote (bit 1: a wait ran out).  A working build gives
+ * {0, 0, 1} and leaves the context usable.  Returns LLAMA_OK, or
+ * LLAMA_ERR_CUDA if the launch or the copy fails. */
+LLAMA_API int llama_selftest_bounded_waits(int observed[3], void* stream);
+
 /* Synchronises `stream`, reads and clears the device status word.  Returns
  * LLAMA_OK, LLAMA_ERR_DEVICE_TIMEOUT or LLAMA_ERR_DEVICE_BAD_INPUT. */
 LLAMA_API int llama_layer_status(llama_layer_t* layer, void* stream);

@@ -41,6 +41,7 @@ EXPORTS = (
     "llama_layer_set_timing", "llama_layer_stage_times",
     "llama_layer_launch_count", "llama_gemm_bf16_streamk_static",
     "llama_layer_forward_host", "llama_layer_forward_cached",
+    "llama_selftest_bounded_waits",
 )
 
 
@@ -114,6 +115,7 @@ def lib() -> ctypes.CDLL:
                                           _P, _SZ, _P]),
         "llama_layer_forward_cached": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P,
                                             _SZ, _P]),
+        "llama_selftest_bounded_waits": (_I, [ctypes.POINTER(_I), _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -191,6 +193,13 @@ def llama_layer_forward_cached(layer: int, x: int, out: int, cache_k: int,
            lib().llama_layer_forward_cached(layer, x, out, cache_k, cache_v, start_pos,
                                             batch, seq_tokens, max_seq, workspace,
                                             workspace_bytes, stream))
+
+
+def llama_selftest_bounded_waits(stream: int) -> tuple[int, int, int]:
+    """(mbarrier wait completed, flag wait completed, status word)."""
+    obs = (_I * 3)()
+    _check("llama_selftest_bounded_waits", lib().llama_selftest_bounded_waits(obs, stream))
+    return tuple(obs)
 
 
 def llama_layer_decode(layer: int, x: int, out: int, cache_k: int,
