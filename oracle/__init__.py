@@ -15,6 +15,8 @@ from .layer import (  # noqa: F401
     rms_norm,
     rope_inv_freq,
     llama3_scale_inv_freq,
+    linear_scale_inv_freq,
+    dynamic_ntk_base,
     rope_cos_sin,
     rotate_half,
     apply_rope,

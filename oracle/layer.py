@@ -77,13 +77,43 @@ def llama3_scale_inv_freq(inv_freq: np.ndarray, factor: float,
     return out
 
 
+def linear_scale_inv_freq(inv_freq: np.ndarray, factor: float) -> np.ndarray:
+    """Linear position scaling ([verl] 1, LlamaLinearScalingRotaryEmbedding:
+    t = t / scaling_factor): the angle (t / factor) * f_i is t * (f_i / factor),
+    so every inverse frequency is divided by the factor."""
+    return inv_freq / factor
+
+
+def dynamic_ntk_base(base: float, head_dim: int, factor: float, table_len: int,
+                     original_max_pos: int) -> float:
+    """Dynamic NTK scaling ([verl] 1, LlamaDynamicNTKScalingRotaryEmbedding:
+    the base is adjusted to the length).  The pages name the method only; the
+    reading taken is the published NTK-aware rule for a table of table_len
+    positions: beyond the original context the base becomes
+    base * (factor * table_len / original_max_pos - (factor - 1)) ** (d / (d - 2)),
+    which leaves the highest frequency (i = 0) as it is and divides the
+    lowest (i = d/2 - 1) by exactly the bracketed scale; within the original
+    context the base is unchanged."""
+    if table_len <= original_max_pos:
+        return base
+    scale = factor * table_len / original_max_pos - (factor - 1.0)
+    return base * scale ** (head_dim / (head_dim - 2.0))
+
+
 def layer_inv_freq(cfg) -> np.ndarray:
-    """The inverse frequencies a layer config asks for."""
-    f = rope_inv_freq(cfg.head_dim, cfg.rope_base)
+    """The inverse frequencies a layer config asks for (rope_scaling 0: none,
+    1: Llama3, 2: linear, 3: dynamic NTK for a table of max_position rows)."""
+    base = cfg.rope_base
+    if cfg.rope_scaling == 3:
+        base = dynamic_ntk_base(base, cfg.head_dim, cfg.rope_factor,
+                                cfg.max_position, cfg.rope_original_max_pos)
+    f = rope_inv_freq(cfg.head_dim, base)
     if cfg.rope_scaling == 1:
         f = llama3_scale_inv_freq(f, cfg.rope_factor, cfg.rope_low_freq_factor,
                                   cfg.rope_high_freq_factor,
                                   cfg.rope_original_max_pos)
+    elif cfg.rope_scaling == 2:
+        f = linear_scale_inv_freq(f, cfg.rope_factor)
     return f
 
 

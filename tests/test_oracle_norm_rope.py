@@ -187,3 +187,54 @@ def test_rope_matches_complex_form():
     zr = z * freqs_cis
     np.testing.assert_allclose(y[..., : d // 2], zr.real, atol=1e-12)
     np.testing.assert_allclose(y[..., d // 2:], zr.imag, atol=1e-12)
+
+
+# ------------------------------------------- linear and dynamic NTK scaling
+def _cfg(scaling, factor=4.0, max_position=4096, original=1024, d=64, base=10000.0):
+    import types
+    return types.SimpleNamespace(head_dim=d, rope_base=base, rope_scaling=scaling,
+                                 rope_factor=factor, rope_low_freq_factor=1.0,
+                                 rope_high_freq_factor=4.0,
+                                 rope_original_max_pos=original,
+                                 max_position=max_position)
+
+
+def test_linear_scaling_divides_the_positions():
+    # the page's statement t = t / factor: the scaled table at position p is
+    # the unscaled table at p / factor (non-integer positions included)
+    f = 4.0
+    p = np.array([0, 1, 3, 7, 100, 4095], dtype=np.float64)
+    cos_s, sin_s = oracle.rope_cos_sin(p, oracle.layer_inv_freq(_cfg(2, factor=f)))
+    cos_u, sin_u = oracle.rope_cos_sin(p / f, oracle.rope_inv_freq(64, 10000.0))
+    np.testing.assert_allclose(cos_s, cos_u, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sin_s, sin_u, rtol=0, atol=1e-12)
+
+
+def test_dynamic_ntk_leaves_the_original_context_alone():
+    plain = oracle.rope_inv_freq(64, 10000.0)
+    for L in (512, 1024):  # at or within the original 1024 positions
+        np.testing.assert_array_equal(
+            oracle.layer_inv_freq(_cfg(3, max_position=L)), plain)
+
+
+def test_dynamic_ntk_divides_the_lowest_frequency_by_the_scale():
+    # beyond the original context: the highest frequency stays 1 and the
+    # lowest is divided by exactly scale = factor * L / orig - (factor - 1),
+    # the property the d / (d - 2) exponent is chosen for
+    for d, f, L, orig in ((64, 4.0, 4096, 1024), (128, 8.0, 12000, 8192)):
+        plain = oracle.rope_inv_freq(d, 500000.0)
+        got = oracle.layer_inv_freq(_cfg(3, factor=f, max_position=L, original=orig,
+                                         d=d, base=500000.0))
+        scale = f * L / orig - (f - 1.0)
+        assert got[0] == 1.0
+        np.testing.assert_allclose(got[-1], plain[-1] / scale, rtol=1e-12)
+        assert np.all(got <= plain) and np.all(np.diff(got) < 0)
+
+
+def test_dynamic_ntk_is_continuous_at_the_original_length():
+    # scale = 1 at L = orig, so the table does not jump there
+    just = oracle.layer_inv_freq(_cfg(3, max_position=1025))
+    plain = oracle.rope_inv_freq(64, 10000.0)
+    assert just[0] == plain[0] == 1.0
+    assert np.all(just[1:] < plain[1:])  # one row past: already (slightly) scaled
+    np.testing.assert_allclose(just, plain, rtol=1e-2)
