@@ -78,6 +78,8 @@ extern "C" {
 
 #define LLAMA_ROPE_NONE 0
 #define LLAMA_ROPE_LLAMA3 1
+#define LLAMA_ROPE_LINEAR 2
+#define LLAMA_ROPE_DYNAMIC_NTK 3
 
 /* Layer shape and RoPE settings.
  * Supported: head_dim in {64, 128}; n_heads % n_kv_heads == 0 and
@@ -89,7 +91,15 @@ extern "C" {
  * w_i = 2*pi / f_i, frequencies with w_i < original_max_pos / high_freq_factor
  * are kept, those with w_i > original_max_pos / low_freq_factor are divided by
  * rope_factor, and in between f_i becomes (1 - s) f_i / rope_factor + s f_i
- * with s = (original_max_pos / w_i - low) / (high - low). */
+ * with s = (original_max_pos / w_i - low) / (high - low).  Linear scaling
+ * ("parallel_attention.py" section 1, t = t / scaling_factor): every f_i is
+ * divided by rope_factor (> 0).  Dynamic NTK scaling (same section, the base
+ * adjusted to the length; the published NTK-aware rule for a table of
+ * max_position rows): when max_position > original_max_pos the base becomes
+ * rope_base * (rope_factor * max_position / original_max_pos -
+ * (rope_factor - 1))^(d / (d - 2)), else it is unchanged (rope_factor >= 1,
+ * original_max_pos > 0).  The low / high frequency factors are read by the
+ * Llama3 scaling only. */
 typedef struct {
   int hidden;
   int n_heads;
@@ -98,7 +108,7 @@ typedef struct {
   int intermediate;
   float rms_eps;
   double rope_base;
-  int rope_scaling; /* LLAMA_ROPE_NONE or LLAMA_ROPE_LLAMA3 */
+  int rope_scaling; /* LLAMA_ROPE_NONE, _LLAMA3, _LINEAR or _DYNAMIC_NTK */
   double rope_factor;
   double rope_low_freq_factor;
   double rope_high_freq_factor;
@@ -124,6 +134,12 @@ typedef struct llama_layer llama_layer_t;
 /* Bytes of device memory llama_layer_init needs for the packed weights, the
  * RoPE table and the status word.  Host only. */
 LLAMA_API int llama_layer_packed_bytes(const llama_layer_config* cfg, size_t* bytes);
+
+/* The RoPE inverse frequencies f_i, i = 0 .. head_dim/2 - 1, the layer
+ * builds its cos / sin table from (in double precision, with the scaling of
+ * cfg->rope_scaling): writes head_dim / 2 values to inv_freq (host memory).
+ * Validates cfg like llama_layer_packed_bytes.  Host only. */
+LLAMA_API int llama_rope_inv_freq(const llama_layer_config* cfg, double* inv_freq);
 
 /* Validates cfg, repacks the weights into `packed` (caller-owned device
  * memory of at least llama_layer_packed_bytes; it must stay allocated and

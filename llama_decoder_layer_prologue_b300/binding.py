@@ -28,6 +28,8 @@ LLAMA_DTYPE_F32 = 0
 LLAMA_DTYPE_BF16 = 1
 LLAMA_ROPE_NONE = 0
 LLAMA_ROPE_LLAMA3 = 1
+LLAMA_ROPE_LINEAR = 2
+LLAMA_ROPE_DYNAMIC_NTK = 3
 LLAMA_WS_NUM = 4
 LLAMA_MAX_STAGES = 16
 LLAMA_MAX_TIMED_CALLS = 4096
@@ -41,7 +43,7 @@ EXPORTS = (
     "llama_layer_set_timing", "llama_layer_stage_times",
     "llama_layer_launch_count", "llama_gemm_bf16_streamk_static",
     "llama_layer_forward_host", "llama_layer_forward_cached",
-    "llama_selftest_bounded_waits",
+    "llama_selftest_bounded_waits", "llama_rope_inv_freq",
 )
 
 
@@ -116,6 +118,8 @@ def lib() -> ctypes.CDLL:
         "llama_layer_forward_cached": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P,
                                             _SZ, _P]),
         "llama_selftest_bounded_waits": (_I, [ctypes.POINTER(_I), _P]),
+        "llama_rope_inv_freq": (_I, [ctypes.POINTER(llama_layer_config),
+                                     ctypes.POINTER(ctypes.c_double)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -193,6 +197,13 @@ def llama_layer_forward_cached(layer: int, x: int, out: int, cache_k: int,
            lib().llama_layer_forward_cached(layer, x, out, cache_k, cache_v, start_pos,
                                             batch, seq_tokens, max_seq, workspace,
                                             workspace_bytes, stream))
+
+
+def llama_rope_inv_freq(cfg: "llama_layer_config", head_dim: int) -> list[float]:
+    """The layer's RoPE inverse frequencies (host only, no device needed)."""
+    out = (ctypes.c_double * (head_dim // 2))()
+    _check("llama_rope_inv_freq", lib().llama_rope_inv_freq(ctypes.byref(cfg), out))
+    return list(out)
 
 
 def llama_selftest_bounded_waits(stream: int) -> tuple[int, int, int]:

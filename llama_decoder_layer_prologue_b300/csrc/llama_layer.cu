@@ -75,6 +75,11 @@ int check_config(const llama_layer_config* c) {
         !(c->rope_high_freq_factor > c->rope_low_freq_factor) ||
         c->rope_original_max_pos <= 0)
       return LLAMA_ERR_INVALID_ARG;
+  } else if (c->rope_scaling == LLAMA_ROPE_LINEAR) {
+    if (!(c->rope_factor > 0.0)) return LLAMA_ERR_INVALID_ARG;
+  } else if (c->rope_scaling == LLAMA_ROPE_DYNAMIC_NTK) {
+    if (!(c->rope_factor >= 1.0) || c->rope_original_max_pos <= 0)
+      return LLAMA_ERR_INVALID_ARG;
   } else if (c->rope_scaling != LLAMA_ROPE_NONE) {
     return LLAMA_ERR_UNSUPPORTED_SHAPE;
   }
@@ -82,12 +87,20 @@ int check_config(const llama_layer_config* c) {
 }
 
 // RoPE inverse frequencies in double precision ("parallel_attention.py"
-// section 1: inv_freq_i = 1 / base^(2i/d); Llama3 piecewise scaling as stated
-// in llama_layer.h).
+// section 1: inv_freq_i = 1 / base^(2i/d); the Llama3, linear and dynamic NTK
+// scalings as stated in llama_layer.h).
 void rope_inv_freq(const llama_layer_config& c, double* f) {
   const int half = c.head_dim / 2;
+  double base = c.rope_base;
+  if (c.rope_scaling == LLAMA_ROPE_DYNAMIC_NTK &&
+      c.max_position > c.rope_original_max_pos) {
+    const double scale = c.rope_factor * c.max_position / c.rope_original_max_pos -
+                         (c.rope_factor - 1.0);
+    base *= pow(scale, (double)c.head_dim / (c.head_dim - 2.0));
+  }
   for (int i = 0; i < half; ++i) {
-    double v = pow(c.rope_base, -2.0 * i / c.head_dim);
+    double v = pow(base, -2.0 * i / c.head_dim);
+    if (c.rope_scaling == LLAMA_ROPE_LINEAR) v /= c.rope_factor;
     if (c.rope_scaling == LLAMA_ROPE_LLAMA3) {
       const double wl = 2.0 * M_PI / v;
       const double orig = c.rope_original_max_pos;
@@ -517,6 +530,14 @@ size_t decode_ws_bytes(const llama_layer* L, int batch, int max_seq) {
 }  // namespace
 
 extern "C" {
+
+int llama_rope_inv_freq(const llama_layer_config* cfg, double* inv_freq) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!inv_freq) return LLAMA_ERR_INVALID_ARG;
+  rope_inv_freq(*cfg, inv_freq);
+  return LLAMA_OK;
+}
 
 int llama_layer_packed_bytes(const llama_layer_config* cfg, size_t* bytes) {
   int rc = check_config(cfg);

@@ -92,6 +92,37 @@ def test_llama3_factors_are_checked():
     assert e.value.code == B.LLAMA_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("scaling,factor,max_position,d", [
+    (B.LLAMA_ROPE_NONE, 1.0, 4096, 64), (B.LLAMA_ROPE_LLAMA3, 8.0, 8192, 128),
+    (B.LLAMA_ROPE_LINEAR, 4.0, 4096, 64), (B.LLAMA_ROPE_LINEAR, 2.5, 4096, 128),
+    (B.LLAMA_ROPE_DYNAMIC_NTK, 4.0, 16384, 64),  # beyond the original 8192
+    (B.LLAMA_ROPE_DYNAMIC_NTK, 2.0, 12000, 128),
+    (B.LLAMA_ROPE_DYNAMIC_NTK, 4.0, 8192, 64),  # within it: unscaled
+])
+def test_library_rope_table_matches_the_oracle(scaling, factor, max_position, d):
+    # the cos / sin table the layer uploads comes from these frequencies,
+    # computed on the host in double precision
+    import oracle
+    s = synth.LayerShape(hidden=256, n_heads=4, n_kv_heads=2, head_dim=d,
+                         intermediate=256, rms_eps=1e-5, rope_base=500000.0,
+                         rope_scaling=scaling, rope_factor=factor,
+                         rope_low_freq_factor=1.0, rope_high_freq_factor=4.0,
+                         rope_original_max_pos=8192, max_position=max_position)
+    got = B.llama_rope_inv_freq(make_config(s), d)
+    import numpy as np
+    np.testing.assert_allclose(got, oracle.layer_inv_freq(s), rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("scaling,factor", [(B.LLAMA_ROPE_LINEAR, 0.0),
+                                            (B.LLAMA_ROPE_DYNAMIC_NTK, 0.5)])
+def test_rope_scaling_factors_are_checked(scaling, factor):
+    cfg = cfg_of("1b")
+    cfg.rope_scaling, cfg.rope_factor = scaling, factor
+    with pytest.raises(B.LlamaError) as e:
+        B.llama_layer_packed_bytes(cfg)
+    assert e.value.code == B.LLAMA_ERR_INVALID_ARG
+
+
 def test_init_rejects_null_weights_before_touching_a_device():
     cfg = cfg_of("tiny")
     w = B.llama_layer_weights()

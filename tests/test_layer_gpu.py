@@ -70,6 +70,12 @@ def test_tiny_fp32_workload():
     # head_dim 128 packed sequences, many shorter than a query tile
     ("varlen_d128_short", shape(512, 4, 2, 128, 256, **L3), "varlen",
      dict(total_tokens=400, min_len=1, max_len=40)),
+    # linear and dynamic NTK RoPE scaling (table-only variants)
+    ("linear_rope", shape(256, 4, 2, 64, 256, rope_scaling=2, rope_factor=4.0),
+     "padded", dict(batch=2, seq=100)),
+    ("dynamic_ntk_rope", shape(256, 4, 2, 64, 256, rope_scaling=3, rope_factor=2.0,
+                               rope_original_max_pos=1024, max_position=4096),
+     "varlen", dict(total_tokens=600, min_len=1, max_len=400)),
     # GEMMs with 64 K-blocks whose tiles leave the last round of 148 SMs
     # partly idle run the split-tile phase (tiles cut between two CTAs):
     # here QKV (384 tiles), o_proj (256) and gate_up (304) ...
@@ -78,7 +84,7 @@ def test_tiny_fp32_workload():
     # ... and down_proj (200 tiles, ragged last row tile, packed sequences)
     ("split_tiles_down_varlen", shape(512, 8, 2, 64, 4096, **L3), "varlen",
      dict(total_tokens=12700, min_len=1, max_len=1000)),
-])
+], ids=lambda case: case[0])
 def test_small_bf16_forward(case):
     name, s, kind, kw = case
     w = synth.custom_workload(name, s, kind, **kw)
