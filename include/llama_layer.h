@@ -308,10 +308,19 @@ LLAMA_API void llama_layer_destroy(llama_layer_t* layer);
 /* Static string for a return code. */
 LLAMA_API const char* llama_layer_strerror(int code);
 
+/* out = bf16(x / RMS(x) * g) per row, RMS(x) = sqrt(mean(x^2) + eps): the
+ * model's final RMSNorm before the output projection ("模型层" 9.5; Llama-3
+ * model.py walkthrough "5. Transformer", self.norm then self.output).  x, out
+ * [rows, hidden] bf16 and g [hidden] bf16, device, 16-byte aligned, out must
+ * not alias x; hidden % 128 == 0; fp32 arithmetic, one rounding. */
+LLAMA_API int llama_rmsnorm_bf16(const void* x, const void* g, void* out, int rows,
+                                 int hidden, float eps, void* stream);
+
 /* D[M, N] = A[M, K] . B[N, K]^T in bf16 with fp32 accumulation, on the same
  * tcgen05 / TMA GEMM the layer's projections use (the contraction of every
- * nn.Linear on the pages).  A, B, D device, row-major, 16-byte aligned;
- * K % 8 == 0, N % 32 == 0. */
+ * nn.Linear on the pages, and the model's output projection to the vocabulary
+ * logits).  A, B, D device, row-major, 16-byte aligned; K % 8 == 0,
+ * N % 32 == 0. */
 LLAMA_API int llama_gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K,
                     void* stream);
 

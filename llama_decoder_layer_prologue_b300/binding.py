@@ -43,7 +43,7 @@ EXPORTS = (
     "llama_layer_set_timing", "llama_layer_stage_times",
     "llama_layer_launch_count", "llama_gemm_bf16_streamk_static",
     "llama_layer_forward_host", "llama_layer_forward_cached",
-    "llama_selftest_bounded_waits", "llama_rope_inv_freq",
+    "llama_selftest_bounded_waits", "llama_rope_inv_freq", "llama_rmsnorm_bf16",
 )
 
 
@@ -120,6 +120,7 @@ def lib() -> ctypes.CDLL:
         "llama_selftest_bounded_waits": (_I, [ctypes.POINTER(_I), _P]),
         "llama_rope_inv_freq": (_I, [ctypes.POINTER(llama_layer_config),
                                      ctypes.POINTER(ctypes.c_double)]),
+        "llama_rmsnorm_bf16": (_I, [_P, _P, _P, _I, _I, ctypes.c_float, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -204,6 +205,12 @@ def llama_rope_inv_freq(cfg: "llama_layer_config", head_dim: int) -> list[float]
     out = (ctypes.c_double * (head_dim // 2))()
     _check("llama_rope_inv_freq", lib().llama_rope_inv_freq(ctypes.byref(cfg), out))
     return list(out)
+
+
+def llama_rmsnorm_bf16(x: int, g: int, out: int, rows: int, hidden: int, eps: float,
+                       stream: int) -> None:
+    _check("llama_rmsnorm_bf16", lib().llama_rmsnorm_bf16(x, g, out, rows, hidden, eps,
+                                                          stream))
 
 
 def llama_selftest_bounded_waits(stream: int) -> tuple[int, int, int]:

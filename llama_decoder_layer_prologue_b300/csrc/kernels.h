@@ -28,6 +28,10 @@ struct Dims {
 void simt_row_rms(bool is_bf16, const void* x, int rows, int H, float eps,
                   float* r, float* zero, cudaStream_t s);
 
+// bf16 rows of width H (a multiple of 128): out = bf16(x / RMS(x) * g).
+void simt_rmsnorm_bf16(const void* x, const void* g, int rows, int H, float eps,
+                       void* out, cudaStream_t s);
+
 // bf16 rows of width H (a multiple of 128): r and zero as simt_row_rms, and
 // xn[row] = fp16(x[row] * r[row]).
 void simt_row_norm_f16(const void* x, int rows, int H, float eps, float* r,

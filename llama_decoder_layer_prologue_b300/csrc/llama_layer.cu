@@ -941,6 +941,18 @@ const char* llama_layer_strerror(int code) {
   return "unknown error";
 }
 
+int llama_rmsnorm_bf16(const void* x, const void* g, void* out, int rows,
+                       int hidden, float eps, void* stream) {
+  if (!x || !g || !out || rows < 0 || hidden <= 0 || !(eps > 0.f))
+    return LLAMA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(g, 16) || !aligned(out, 16) || x == out)
+    return LLAMA_ERR_INVALID_ARG;
+  if (hidden % 128 != 0) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return LLAMA_OK;
+  simt_rmsnorm_bf16(x, g, rows, hidden, eps, out, static_cast<cudaStream_t>(stream));
+  return cuda_err(cudaGetLastError());
+}
+
 int llama_gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K,
                     void* stream) {
   if (!A || !B || !D || M < 0 || N < 0 || K <= 0) return LLAMA_ERR_INVALID_ARG;

@@ -91,6 +91,44 @@ __global__ void row_norm_f16_kernel(const __nv_bfloat16* __restrict__ x, int row
   }
 }
 
+// bf16 rows: out = bf16(x / RMS(x) * g), the model's final RMSNorm ("模型层"
+// 9.5 / the model.py walkthrough 5: the norm before the output projection).
+// One warp per row; fp32 statistics and product, one rounding.
+__global__ void rmsnorm_bf16_kernel(const __nv_bfloat16* __restrict__ x,
+                                    const __nv_bfloat16* __restrict__ g, int rows,
+                                    int H, float eps, __nv_bfloat16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const __nv_bfloat16* xr = x + (size_t)row * H + lane * 4;
+  float ss[4] = {0.f, 0.f, 0.f, 0.f};
+  int j = 0;
+  for (; j + 512 <= H; j += 512) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ss[u] += sumsq4(xr + j + u * 128);
+  }
+  for (; j < H; j += 128) ss[0] += sumsq4(xr + j);
+  const float rs = rsqrtf(warp_sum((ss[0] + ss[1]) + (ss[2] + ss[3])) / (float)H + eps);
+  __nv_bfloat16* o = out + (size_t)row * H + lane * 4;
+  const __nv_bfloat16* gl = g + lane * 4;
+  for (j = 0; j < H; j += 128) {
+    const uint2 u = *reinterpret_cast<const uint2*>(xr + j);
+    const uint2 w = *reinterpret_cast<const uint2*>(gl + j);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+    const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * rs * ga.x, a.y * rs * ga.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(b.x * rs * gb.x, b.y * rs * gb.y);
+    uint2 r;
+    r.x = *reinterpret_cast<uint32_t*>(&lo);
+    r.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(o + j) = r;
+  }
+}
+
 // ----------------------------------------------------------------- positions
 // One block per sequence.  Checks the prefix sums; writes pos[t] = t - start.
 __global__ void positions_kernel(const int32_t* __restrict__ cu, int n_seq,
@@ -420,6 +458,14 @@ void simt_row_norm_f16(const void* x, int rows, int H, float eps, float* r,
     default:
       launch_pdl(row_norm_f16_kernel, grid, block, 0, s, xb, rows, H, eps, r, zero, o);
   }
+}
+
+void simt_rmsnorm_bf16(const void* x, const void* g, int rows, int H, float eps,
+                       void* out, cudaStream_t s) {
+  if (rows <= 0) return;
+  launch_pdl(rmsnorm_bf16_kernel, dim3((rows + 7) / 8), dim3(256), 0, s,
+             static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(g),
+             rows, H, eps, static_cast<__nv_bfloat16*>(out));
 }
 
 void launch_positions(const int32_t* cu, int n_seq, int seq_len, int T,

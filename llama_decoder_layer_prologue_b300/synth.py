@@ -25,7 +25,13 @@ Recipe (every workload):
     token's row only at an index <= 8191, so the upper bound 8192 given for
     this workload is read as the cache length.  Rows [0, start_pos) hold
     N(0, 1) values taken to be already-rotated keys / values; the other rows
-    are zero here (tests poison them with NaN).
+    are zero here (tests poison them with NaN).  Chunked (seq_tokens > 1):
+    start_pos ~ U{512..8192 - seq_tokens}, so every chunk ends in the cache.
+  * Model (stacked layers): x and the first layer's weights are the
+    workload's own draws; layer l > 0 draws its weights as the same workload
+    with index + 1000 l; the final RMSNorm weight ~ 1 + N(0, 0.1) and the
+    output projection [vocab, hidden] ~ N(0, 0.02) draw from the children of
+    ``SeedSequence(7000 + workload index)``.
 """
 
 from __future__ import annotations
@@ -283,3 +289,35 @@ def custom_workload(name: str, shape: LayerShape, kind: str, index: int = 50,
                     **kw) -> Workload:
     """A workload with the same recipe and other sizes (edge-case tests)."""
     return Workload(name, index, shape, kind, **kw)
+
+
+@dataclasses.dataclass
+class ModelInputs:
+    """Inputs of a stack of decoder layers, the final RMSNorm and the output
+    projection (the model-level workload)."""
+    first: LayerInputs          # x, positions, cu_seqlens and layer 0's weights
+    layers: list                # LayerWeights of every layer (layers[0] is first's)
+    g_final: np.ndarray         # [hidden]
+    w_lm: np.ndarray            # [vocab, hidden]
+
+    @property
+    def tokens(self) -> int:
+        return self.first.tokens
+
+
+def make_model_inputs(w: Workload | str, n_layers: int, vocab: int) -> ModelInputs:
+    """Draw the inputs of an n_layers stack with a vocab-wide output
+    projection on workload ``w``'s tokens (see the module docstring)."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    first = make_inputs(w)
+    layers = [first.weights]
+    for l in range(1, n_layers):
+        wl = dataclasses.replace(w, index=w.index + 1000 * l)
+        layers.append(make_inputs(wl, with_cache=False).weights)
+    s = w.shape
+    kids = np.random.SeedSequence(7000 + w.index).spawn(2)
+    g_final = _fill_normal(kids[0], s.hidden, 1.0, 0.1, s.dtype)
+    w_lm = _fill_normal(kids[1], vocab * s.hidden, 0.0, 0.02, s.dtype).reshape(
+        vocab, s.hidden)
+    return ModelInputs(first, layers, g_final, w_lm)

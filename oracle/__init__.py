@@ -28,5 +28,6 @@ from .layer import (  # noqa: F401
     decoder_layer_rows,
     decoder_layer_decode,
     decoder_layer_cached,
+    model_forward,
     layer_inv_freq,
 )

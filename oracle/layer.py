@@ -357,3 +357,18 @@ def decoder_layer_cached(x: np.ndarray, w, cfg, cache_rows, start_pos: np.ndarra
     hn = rms_norm(h, w.g_post, cfg.rms_eps)
     act, mlp = swiglu_mlp(hn, w.w_gate_up, w.w_down)
     return dict(q=q, k_new=k, v_new=v, attn=attn, h=h, act=act, out=h + mlp)
+
+
+def model_forward(x: np.ndarray, layers, cfg, positions: np.ndarray,
+                  cu_seqlens: np.ndarray, g_final: np.ndarray, w_lm: np.ndarray) -> dict:
+    """A stack of decoder layers, the final RMSNorm and the output projection
+    ([nanotron] 9.5, the layers applied in turn; [csdn] "5. Transformer":
+    h = layer(h) for every layer, then the norm, then the output projection
+    to the vocabulary logits).  ``layers`` holds one weight set per layer (as
+    decoder_layer takes); w_lm [vocab, hidden].  Returns the last hidden
+    state, its normalised form and the logits [T, vocab]."""
+    h = x
+    for w in layers:
+        h = decoder_layer(h, w, cfg, positions, cu_seqlens)["out"]
+    hn = rms_norm(h, g_final, cfg.rms_eps)
+    return dict(hidden=h, normed=hn, logits=hn @ w_lm.T)

@@ -238,6 +238,32 @@ def test_cached_chunk_is_causal_within_the_chunk():
     assert not np.allclose(a[-1], b[-1])
 
 
+def test_model_stack_hands_each_layer_the_previous_output():
+    """A layer with zero o_proj and down_proj weights returns its input
+    exactly (both residual branches add zero), so inserting one before or
+    after a real layer must leave the logits unchanged bit for bit."""
+    import types
+    cfg = SMALL_L3
+    w = weights(cfg)
+    ident = types.SimpleNamespace(**vars(w))
+    ident.w_o = np.zeros_like(w.w_o)
+    ident.w_down = np.zeros_like(w.w_down)
+    lens = [6, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    pos = np.concatenate([np.arange(L) for L in lens])
+    x = RNG.standard_normal((cu[-1], cfg.hidden))
+    g = 1.0 + 0.1 * RNG.standard_normal(cfg.hidden)
+    w_lm = 0.02 * RNG.standard_normal((64, cfg.hidden))
+    one = oracle.model_forward(x, [w], cfg, pos, cu, g, w_lm)
+    for stack in ([ident, w], [w, ident], [ident, w, ident]):
+        got = oracle.model_forward(x, stack, cfg, pos, cu, g, w_lm)
+        np.testing.assert_array_equal(got["logits"], one["logits"])
+    np.testing.assert_array_equal(
+        one["hidden"], oracle.decoder_layer(x, w, cfg, pos, cu)["out"])
+    two = oracle.model_forward(x, [w, w], cfg, pos, cu, g, w_lm)
+    assert not np.allclose(two["logits"], one["logits"])
+
+
 # ----------------------------------------------------------------- shapes
 def test_1b_shapes_match_page_printout():
     rows = {}
