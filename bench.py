@@ -55,6 +55,9 @@ DESCRIPTIONS = {
               "causal within each sequence",
     "decode": "KV-cache decode 8B-shaped layer bf16: batch 64 x 1 new token, "
               "start_pos U{512..8191} (seeded), cache [64, 8192, 8, 128] bf16",
+    "model1b": "Llama-3.2-1B-shaped model forward bf16: 16 decoder layers (the "
+               "1b layer shape, seeded weights per layer), final RMSNorm and the "
+               "output projection to 128256 logits, batch 4 x seq 2048",
     "chunked": "chunked prefill with a KV cache, 8B-shaped layer bf16: 16 "
                "sequences x 4 new tokens, start_pos U{512..8188} (seeded), cache "
                "[16, 8192, 8, 128] bf16 (llama_layer_forward_cached)",
@@ -92,7 +95,8 @@ def parse_args():
 
 
 DEFAULT_STEPS = {"tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
-                 "decode": 3000, "chunked": 1500}
+                 "decode": 3000, "chunked": 1500, "model1b": 40}
+MODEL = {"model1b": ("1b", 16, 128256)}  # layer workload, layers, vocabulary
 
 
 def max_over_ranks(dist, x: float) -> float:
@@ -313,6 +317,19 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- oracle
+def clock_sampler() -> "ClockSampler":
+    """A sampler of the current CUDA device, found in NVML by its PCI bus id
+    (NVML numbers the GPUs without regard to CUDA_VISIBLE_DEVICES)."""
+    import torch
+
+    p = torch.cuda.get_device_properties(torch.cuda.current_device())
+    bus = None
+    if hasattr(p, "pci_bus_id"):
+        bus = "%08X:%02X:%02X.0" % (getattr(p, "pci_domain_id", 0), p.pci_bus_id,
+                                    getattr(p, "pci_device_id", 0))
+    return ClockSampler(torch.cuda.current_device(), bus)
+
+
 def _f64_weights(inp):
     import types
 
@@ -412,6 +429,200 @@ def cpu_baseline(inp, budget_s: float) -> dict:
             "sample": f"{what} of the workload, fp64 numpy oracle, one pass"}
 
 
+# ----------------------------------------------------------------- model
+def model_flops(shape, tokens_per_seq, n_layers: int, vocab: int) -> float:
+    """Algorithmic FLOPs of one model step: every layer's linears and causal
+    attention (visible pairs only) plus the output projection."""
+    import numpy as np
+
+    s = shape
+    lens = np.asarray(tokens_per_seq, dtype=np.float64)
+    T = float(lens.sum())
+    linear = 2.0 * T * (s.hidden * s.n_qkv + s.q_size * s.hidden +
+                        2 * s.hidden * s.intermediate + s.intermediate * s.hidden)
+    attn = float(np.sum(2.0 * s.head_dim * s.n_heads * lens * (lens + 1)))
+    return n_layers * (linear + attn) + 2.0 * T * s.hidden * vocab
+
+
+def model_oracle_sample(m_in, n_tokens: int):
+    """The oracle on the first n tokens of sequence 0 (a causal prefix is an
+    exact sub-problem): (callable, tokens, description)."""
+    import numpy as np
+
+    import oracle
+    from llama_decoder_layer_prologue_b300 import synth
+
+    inp = m_in.first
+    n = max(1, min(n_tokens, int(inp.cu_seqlens[1])))
+    x = synth.to_f64(inp.x[:n])
+    ws = [_f64_layer(l) for l in m_in.layers]
+    g, wl = synth.to_f64(m_in.g_final), synth.to_f64(m_in.w_lm)
+    pos = inp.positions[:n]
+    cut = np.array([0, n], dtype=np.int64)
+
+    def run():
+        oracle.model_forward(x, ws, inp.workload.shape, pos, cut, g, wl)
+    return run, n, f"first {n} tokens of sequence 0 through all {len(ws)} layers"
+
+
+def _f64_layer(lw):
+    import types
+
+    from llama_decoder_layer_prologue_b300 import synth
+    return types.SimpleNamespace(**{k: synth.to_f64(getattr(lw, k)) for k in
+                                    ("w_qkv", "w_o", "w_gate_up", "w_down", "g_in",
+                                     "g_post")})
+
+
+def run_model(args, rank, local_rank, world):
+    """The model step: every layer, the final norm and the output projection
+    (LlamaModel.forward), timed like the layer workloads."""
+    import numpy as np
+    import torch
+
+    from llama_decoder_layer_prologue_b300 import synth
+    from llama_decoder_layer_prologue_b300.layer import to_device
+    from llama_decoder_layer_prologue_b300.model import LlamaModel
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    base, n_layers, vocab = MODEL[args.workload]
+    m_in = synth.make_model_inputs(base, n_layers, vocab)
+    inp = m_in.first
+    s = inp.workload.shape
+    model = LlamaModel.from_numpy(s, m_in)
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
+    W = args.warmup
+    x = to_device(inp.x)
+    n_seq = len(inp.cu_seqlens) - 1
+    seq = int(inp.cu_seqlens[1])
+    logits = torch.empty(inp.tokens, vocab, dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        model.forward(x, n_seq=n_seq, seq_len=seq, logits=logits)
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for i in range(W):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sampler = clock_sampler() if rank == 0 else None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    if sampler:
+        sampler.__enter__()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.__exit__()
+    region_s = time.perf_counter() - t0
+    if dist is not None:
+        dist.barrier()
+    rc = model.status()
+    if rc != 0:
+        raise RuntimeError(f"model status after the timed steps: {rc}")
+    total_ms = max_over_ranks(dist, float(sum(a.elapsed_time(b) for a, b in ev)))
+    tokens = inp.tokens
+    value = job_throughput(world, K, tokens, total_ms)
+    ms_step = total_ms / K
+    pk = peaks()
+    flops = model_flops(s, np.diff(inp.cu_seqlens), n_layers, vocab)
+
+    # host input -> model -> the last position's logits of every sequence
+    # (what a generator reads back) to the host, copies inside the events
+    e2e = None
+    n_e2e = args.e2e_steps if args.e2e_steps is not None else min(K, 20)
+    if n_e2e > 0:
+        x_h = to_device(inp.x, pin=True)
+        last = torch.as_tensor(inp.cu_seqlens[1:] - 1, dtype=torch.long, device="cuda")
+        out_h = torch.empty(n_seq, vocab, dtype=torch.bfloat16).pin_memory()
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_e2e)]
+        # one untimed pass first: the copies and the index gather run here
+        # for the first time (module loading, pinned-copy setup)
+        x.copy_(x_h, non_blocking=True)
+        model.forward(x, n_seq=n_seq, seq_len=seq, logits=logits)
+        out_h.copy_(logits.index_select(0, last), non_blocking=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(n_e2e):
+            flush.fill_(i & 0xFF)
+            ev2[i][0].record(stream)
+            x.copy_(x_h, non_blocking=True)
+            model.forward(x, n_seq=n_seq, seq_len=seq, logits=logits)
+            out_h.copy_(logits.index_select(0, last), non_blocking=True)
+            ev2[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(dist, float(sum(a.elapsed_time(b) for a, b in ev2)))
+        e2e = {"value": job_throughput(world, n_e2e, tokens, e2e_ms), "unit": UNIT,
+               "h2d_bytes_per_step": int(x_h.numel() * x_h.element_size()),
+               "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()),
+               "steps": n_e2e, "ms_per_step": e2e_ms / n_e2e,
+               "api": "LlamaModel.forward (pinned host input, the last position's "
+                      "logits of every sequence copied back)"}
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    achieved = flops / (ms_step / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": f"whole model step ({n_layers} layers, "
+                "norm, output projection; all launches)",
+                "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops"],
+                "peak_source": f"{pk['source']} bf16 burst",
+                "frac_of_sustained": achieved / pk["bf16_tflops_sustained"],
+                "algorithmic_per_launch": flops, "launch_ms": ms_step,
+                "share_of_step": 1.0, "traffic": None}
+    cpu = None
+    if args.cpu_baseline_seconds > 0:
+        run, n, what = model_oracle_sample(m_in, 4)
+        t = time.perf_counter()
+        run()
+        per_tok = (time.perf_counter() - t) / n
+        n = max(1, int(args.cpu_baseline_seconds / max(per_tok, 1e-6)))
+        run, n, what = model_oracle_sample(m_in, n)
+        t = time.perf_counter()
+        run()
+        dt = time.perf_counter() - t
+        cpu = {"value": n / dt, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+               "seconds": round(dt, 3), "sample": f"{what}, fp64 numpy oracle, one pass"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded x ~ N(0,1), weights ~ N(0,0.02) (each layer its "
+                "own draw), RMSNorm weights ~ 1+N(0,0.1), no trained weights",
+        "config": {"workload": DESCRIPTIONS[args.workload], "name": args.workload,
+                   "tokens_per_step": tokens, "parallelism": f"replicas x{world}",
+                   "l2": "flushed between timed steps (256 MiB write, outside the "
+                         "step's events)", "region_s": round(region_s, 3)},
+        "roofline": roofline, "layer_roofline": None, "stages": None,
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(K * model.launch_count()),
+        "launches_per_step": model.launch_count(),
+        "clocks": sampler.summary() if sampler else None,
+    }
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
 # ----------------------------------------------------------------- our arm
 def run_ours(args, rank, local_rank, world):
     import numpy as np
@@ -471,14 +682,7 @@ def run_ours(args, rank, local_rank, world):
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
-    sampler = None
-    if rank == 0:
-        p = torch.cuda.get_device_properties(torch.cuda.current_device())
-        bus = None
-        if hasattr(p, "pci_bus_id"):
-            bus = "%08X:%02X:%02X.0" % (getattr(p, "pci_domain_id", 0), p.pci_bus_id,
-                                        getattr(p, "pci_device_id", 0))
-        sampler = ClockSampler(torch.cuda.current_device(), bus)
+    sampler = clock_sampler() if rank == 0 else None
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -539,12 +743,8 @@ def run_ours(args, rank, local_rank, world):
             extra_d.append(cu)
         ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n_e2e)]
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-        for i in range(n_e2e):
-            flush.fill_(i & 0xFF)
-            ev2[i][0].record(stream)
+
+        def host_step():
             for h_, d_ in zip(extra_h, extra_d):
                 d_.copy_(h_, non_blocking=True)
             if decode and S_new > 1:
@@ -555,6 +755,15 @@ def run_ours(args, rank, local_rank, world):
                 layer.forward_from_host(x_h, out_h, x, out, cu_seqlens=cu, seq_len=seq)
             else:
                 layer.forward_from_host(x_h, out_h, x, out, n_seq=n_seq, seq_len=seq)
+
+        host_step()  # untimed: first use of the copy streams and pinned copies
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(n_e2e):
+            flush.fill_(i & 0xFF)
+            ev2[i][0].record(stream)
+            host_step()
             ev2[i][1].record(stream)
         torch.cuda.synchronize()
         e2e_ms = float(sum(a.elapsed_time(b) for a, b in ev2))
@@ -677,13 +886,23 @@ def run_reference(args, rank, world):
         return None
     from llama_decoder_layer_prologue_b300 import synth
 
-    inp = synth.make_inputs(args.workload)
     K = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
     W = args.warmup
-    r = OracleRunner(inp)
     per_step = min(4.0, 150.0 / max(1, K + W))  # whole run within minutes
-    n = r.calibrate(per_step)
-    run, tokens, what = r.units(n)
+    if args.workload in MODEL:
+        base, n_layers, vocab = MODEL[args.workload]
+        m_in = synth.make_model_inputs(base, n_layers, vocab)
+        inp = m_in.first
+        run0, n0, _ = model_oracle_sample(m_in, 2)
+        t = time.perf_counter()
+        run0()
+        per_tok = (time.perf_counter() - t) / n0
+        run, tokens, what = model_oracle_sample(m_in, max(1, int(per_step / per_tok)))
+    else:
+        inp = synth.make_inputs(args.workload)
+        r = OracleRunner(inp)
+        n = r.calibrate(per_step)
+        run, tokens, what = r.units(n)
     for _ in range(min(W, 1)):
         run()
     times = []
@@ -719,6 +938,8 @@ def main():
         raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.workload in MODEL:
+        line = run_model(args, rank, local_rank, world)
     else:
         line = run_ours(args, rank, local_rank, world)
     if line is not None:
