@@ -7,6 +7,9 @@ library: it takes numpy float64 arrays (the workload's stored bf16 / fp32
 values converted exactly) and computes the layer straight from the formulas on
 the pages it cites, with no intermediate rounding.
 
+The layer's backward pass (``oracle.backward``) is pinned to torch.autograd
+of a separately written float64 forward and to finite differences.
+
 Every function is pinned by ``tests/test_oracle_*.py`` to closed forms,
 invariants, library routines or brute force (none is "parity unpinned").
 """
