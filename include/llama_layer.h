@@ -46,6 +46,13 @@
  *   - Every wait inside a kernel is bounded; a wait that runs out sets the
  *     status word and the kernel returns (llama_layer_status reports
  *     LLAMA_ERR_DEVICE_TIMEOUT).
+ *   - One layer handle serves one stream at a time: its status word, its
+ *     split-tile flags and the copy streams of llama_layer_forward_host are
+ *     per handle, and a workspace holds one call's intermediates.  Calls on
+ *     one stream may share a workspace (and several layers may, as the
+ *     layers of a model do); concurrent calls need their own handles and
+ *     workspaces.  The handle itself is not locked: call it from one host
+ *     thread at a time.
  */
 #ifndef LLAMA_LAYER_H
 #define LLAMA_LAYER_H
