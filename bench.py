@@ -83,7 +83,14 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=None,
                     help="timed steps (default: about 2 s of work)")
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="1b", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(DESCRIPTIONS),
+                    help="the workload of the headline line (default: the packed "
+                         "varlen 8B-shaped layer, the largest single-GPU workload)")
+    ap.add_argument("--also", default="auto",
+                    help="comma-separated workloads measured after the headline and "
+                         "reported under 'workloads' in the same line ('auto': "
+                         "1b,8b,decode with the default headline, else none; "
+                         "'none': no others)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0,
                     help="CPU work of the oracle baseline (0: leave it out)")
@@ -93,6 +100,9 @@ def parse_args():
                     help="print the per-stage table to stderr")
     return ap.parse_args()
 
+
+HEADLINE = "varlen"
+ALSO_AUTO = ("1b", "8b", "decode")
 
 DEFAULT_STEPS = {"tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
                  "decode": 3000, "chunked": 1500, "model1b": 40}
@@ -132,25 +142,23 @@ def src_sha(files) -> str:
     return h.hexdigest()[:16]
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
 def recorded_traffic(workload: str, stage: str):
-    """DRAM bytes per launch recorded from an ncu capture, if the kernel
-    sources are unchanged since (profiles/dram_traffic.md)."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
-    if not os.path.exists(path):
+    """DRAM bytes per launch recorded from an ncu capture
+    (profiles/dram_traffic.json), if the kernel sources are unchanged since."""
+    if not os.path.exists(TRAFFIC_FILE):
         return None
     key = stage
     if stage == "attention" and workload in ("decode", "chunked"):
         key = "attention_decode"
     want = src_sha(STAGE_SOURCES.get(key, []))
-    with open(path) as fh:
-        for line in fh:
-            cells = [c.strip() for c in line.strip().strip("|").split("|")]
-            if len(cells) >= 4 and cells[0] == workload and cells[1] == stage:
-                try:
-                    value = float(cells[2])
-                except ValueError:
-                    continue
-                return value if cells[3] == want else None
+    with open(TRAFFIC_FILE) as fh:
+        rows = json.load(fh).get("launches", [])
+    for r in rows:
+        if r.get("workload") == workload and r.get("stage") == stage:
+            return float(r["dram_bytes"]) if r.get("sources_sha") == want else None
     return None
 
 
@@ -474,7 +482,7 @@ def _f64_layer(lw):
                                      "g_post")})
 
 
-def run_model(args, rank, local_rank, world):
+def run_model(args, rank, local_rank, world, dist=None):
     """The model step: every layer, the final norm and the output projection
     (LlamaModel.forward), timed like the layer workloads."""
     import numpy as np
@@ -486,10 +494,6 @@ def run_model(args, rank, local_rank, world):
 
     assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
     torch.cuda.set_device(local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     base, n_layers, vocab = MODEL[args.workload]
     m_in = synth.make_model_inputs(base, n_layers, vocab)
     inp = m_in.first
@@ -575,8 +579,6 @@ def run_model(args, rank, local_rank, world):
                "api": "LlamaModel.forward (pinned host input, the last position's "
                       "logits of every sequence copied back)"}
     if rank != 0:
-        if dist is not None:
-            dist.destroy_process_group()
         return None
 
     achieved = flops / (ms_step / 1e3) / 1e12
@@ -618,13 +620,12 @@ def run_model(args, rank, local_rank, world):
         "launches_per_step": model.launch_count(),
         "clocks": sampler.summary() if sampler else None,
     }
-    if dist is not None:
-        dist.destroy_process_group()
     return line
 
 
 # ----------------------------------------------------------------- our arm
-def run_ours(args, rank, local_rank, world):
+def run_ours(args, rank, local_rank, world, dist=None, name=None, cpu_seconds=None):
+    """One workload on our library: the JSON line (rank 0) or None."""
     import numpy as np
     import torch
 
@@ -633,16 +634,15 @@ def run_ours(args, rank, local_rank, world):
 
     assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
     torch.cuda.set_device(local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    name = name or args.workload
+    if cpu_seconds is None:
+        cpu_seconds = args.cpu_baseline_seconds
 
-    inp = synth.make_inputs(args.workload)
+    inp = synth.make_inputs(name)
     w = inp.workload
     s = w.shape
     layer = LlamaLayer.from_numpy(s, inp.weights)
-    K = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[name]
     W = args.warmup
     x = to_device(inp.x)
     out = torch.empty_like(x)
@@ -782,8 +782,6 @@ def run_ours(args, rank, local_rank, world):
                        "in and out on two streams overlapping the layer)")}
 
     if rank != 0:
-        if dist is not None:
-            dist.destroy_process_group()
         return None
 
     stage_ms = {k: statistics.mean(v) for k, v in stages.items()}
@@ -812,7 +810,7 @@ def run_ours(args, rank, local_rank, world):
                         "peak_source": f"{pk['source']} HBM copy",
                         "algorithmic_per_launch": work["bytes"][dom],
                         "launch_ms": dom_ms, "share_of_step": share}
-        roofline["traffic"] = recorded_traffic(args.workload, dom)
+        roofline["traffic"] = recorded_traffic(name, dom)
         roofline["stage_timing"] = (
             f"library CUDA stage events on {n_stage} steps run right after the timed "
             "region (events between kernels disable the launch overlap, so stage "
@@ -843,8 +841,8 @@ def run_ours(args, rank, local_rank, world):
         stage_roof[name] = e
 
     cpu = None
-    if args.cpu_baseline_seconds > 0:
-        cpu = cpu_baseline(inp, args.cpu_baseline_seconds)
+    if cpu_seconds > 0:
+        cpu = cpu_baseline(inp, cpu_seconds)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -853,7 +851,7 @@ def run_ours(args, rank, local_rank, world):
         "dtype": "bf16" if s.dtype == "bf16" else "f32",
         "data": "synthetic: seeded x ~ N(0,1), weights ~ N(0,0.02), RMSNorm "
                 "weights ~ 1+N(0,0.1), no trained weights",
-        "config": {"workload": DESCRIPTIONS[args.workload], "name": args.workload,
+        "config": {"workload": DESCRIPTIONS[name], "name": name,
                    "tokens_per_step": tokens, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (256 MiB write, outside "
                          "the step's events)",
@@ -874,8 +872,6 @@ def run_ours(args, rank, local_rank, world):
                   + (f"{e['gbs']:8.1f} GB/s " if "gbs" in e else "")
                   + (f"frac {e['frac']:.3f}" if "frac" in e else ""),
                   file=sys.stderr)
-    if dist is not None:
-        dist.destroy_process_group()
     return line
 
 
@@ -931,17 +927,72 @@ def run_reference(args, rank, world):
     }
 
 
+def summary_of(line: dict) -> dict:
+    """The figures of one workload's line kept under 'workloads'."""
+    keep = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "roofline",
+            "layer_roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks")
+    out = {k: line.get(k) for k in keep}
+    out["workload"] = line["config"]["workload"]
+    out["tokens_per_step"] = line["config"]["tokens_per_step"]
+    return out
+
+
+def also_list(args) -> list:
+    """The workloads measured after the headline one (see --also)."""
+    if args.also == "auto":
+        return list(ALSO_AUTO) if args.workload == HEADLINE else []
+    if args.also in ("", "none"):
+        return []
+    names = [n.strip() for n in args.also.split(",") if n.strip()]
+    for n in names:
+        if n not in DESCRIPTIONS or n in MODEL:
+            raise SystemExit(f"--also: unknown layer workload {n!r}")
+    return [n for n in names if n != args.workload]
+
+
+def check_world(gpus: int, world: int) -> None:
+    """One process per GPU: N > 1 needs torchrun (WORLD_SIZE = N); a plain
+    `--gpus N` run would time one replica and report it as N GPUs."""
+    if gpus != world:
+        raise SystemExit(
+            f"--gpus {gpus} but WORLD_SIZE={world}: launch N > 1 with "
+            f"`python -m torch.distributed.run --nproc-per-node {gpus} bench.py "
+            f"--gpus {gpus}`")
+
+
 def main():
     args = parse_args()
     rank, local_rank, world = dist_env()
-    if args.gpus != world and world > 1:
-        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    check_world(args.gpus, world)
     if args.impl == "reference":
         line = run_reference(args, rank, world)
-    elif args.workload in MODEL:
-        line = run_model(args, rank, local_rank, world)
-    else:
-        line = run_ours(args, rank, local_rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    import torch
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        if args.workload in MODEL:
+            line = run_model(args, rank, local_rank, world, dist)
+        else:
+            line = run_ours(args, rank, local_rank, world, dist)
+            others = {}
+            for name in also_list(args):
+                torch.cuda.empty_cache()
+                sub = run_ours(args, rank, local_rank, world, dist, name=name,
+                               cpu_seconds=min(args.cpu_baseline_seconds, 4.0))
+                if sub is not None:
+                    others[name] = summary_of(sub)
+            if line is not None and others:
+                line["workloads"] = others
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
     if line is not None:
         print(json.dumps(line), flush=True)
 

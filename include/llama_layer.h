@@ -327,9 +327,18 @@ LLAMA_API int llama_rmsnorm_bf16(const void* x, const void* g, void* out, int ro
  * tcgen05 / TMA GEMM the layer's projections use (the contraction of every
  * nn.Linear on the pages, and the model's output projection to the vocabulary
  * logits).  A, B, D device, row-major, 16-byte aligned; K % 8 == 0,
- * N % 32 == 0. */
+ * N % 32 == 0.  The kernel's bounded waits report into a status word of the
+ * current device that llama_gemm_status reads. */
 LLAMA_API int llama_gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K,
                     void* stream);
+
+/* Synchronises `stream`, then reads and clears the status word of the
+ * standalone GEMMs (llama_gemm_bf16, llama_gemm_bf16_streamk_static) on the
+ * current device: a bounded wait inside one of them that ran out (its output
+ * is then incomplete) gives LLAMA_ERR_DEVICE_TIMEOUT.  The word is shared by
+ * every standalone GEMM on the device since the last read.  Returns LLAMA_OK,
+ * LLAMA_ERR_DEVICE_TIMEOUT or LLAMA_ERR_CUDA. */
+LLAMA_API int llama_gemm_status(void* stream);
 
 /* D[M, N] = A[M, K] . B[N, K]^T in bf16 with fp32 accumulation, without any
  * device memory from the caller beyond A, B and D.  The pages this library
@@ -355,7 +364,9 @@ LLAMA_API int llama_gemm_bf16(const void* A, const void* B, void* D, int M, int 
  * an allocating library routine.  Every call shares the one array, which
  * keeps the last call's partials; a call writes every partial it reads, so
  * nothing has to start at zero.  Calls that overlap on the GPU (other
- * streams, other host threads) race on the array: order them on one stream. */
+ * streams, other host threads) race on the array: order them on one stream.
+ * A bounded wait of the GEMM that runs out is not returned by this call (it
+ * returns once the kernels are enqueued): llama_gemm_status reports it. */
 LLAMA_API int llama_gemm_bf16_streamk_static(const void* A, const void* B, void* D,
                                              int M, int N, int K, void* stream);
 

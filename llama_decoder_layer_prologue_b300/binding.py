@@ -44,6 +44,7 @@ EXPORTS = (
     "llama_layer_launch_count", "llama_gemm_bf16_streamk_static",
     "llama_layer_forward_host", "llama_layer_forward_cached",
     "llama_selftest_bounded_waits", "llama_rope_inv_freq", "llama_rmsnorm_bf16",
+    "llama_gemm_status",
 )
 
 
@@ -121,6 +122,7 @@ def lib() -> ctypes.CDLL:
         "llama_rope_inv_freq": (_I, [ctypes.POINTER(llama_layer_config),
                                      ctypes.POINTER(ctypes.c_double)]),
         "llama_rmsnorm_bf16": (_I, [_P, _P, _P, _I, _I, ctypes.c_float, _P]),
+        "llama_gemm_status": (_I, [_P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -272,6 +274,12 @@ def llama_layer_launch_count(layer: int) -> int:
 def llama_gemm_bf16(A: int, B: int, D: int, M: int, N: int, K: int,
                     stream: int) -> None:
     _check("llama_gemm_bf16", lib().llama_gemm_bf16(A, B, D, M, N, K, stream))
+
+
+def llama_gemm_status(stream: int) -> int:
+    """Synchronises the stream and returns (and clears) the standalone GEMMs'
+    device status: LLAMA_OK or a negative code."""
+    return lib().llama_gemm_status(stream)
 
 
 def llama_gemm_bf16_streamk_static(A: int, B: int, D: int, M: int, N: int,

@@ -544,13 +544,9 @@ cudaError_t launch(const AttnArgs& a, int n_seq, int max_len, int sm_count,
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffff) return cudaErrorInvalidValue;
   auto kern = attn_tc_kernel<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::TOTAL);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (cudaError_t e = ensure_smem_attr(kern, (int)L::TOTAL, attr_done); e != cudaSuccess)
+    return e;
   const int grid = (int)(items < sm_count ? items : sm_count);
   return launch_pdl(kern, dim3(grid), dim3(kThreads), L::TOTAL, s, tq, tkv, a,
                     (int)items, n_hg, n_seq, n_qb);

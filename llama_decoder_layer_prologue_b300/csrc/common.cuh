@@ -9,7 +9,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace llama {
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute belongs to the device, so `done` (owned by the
+// launch site, one bit per device ordinal below 64) records the devices
+// already set; setting it twice from two host threads is harmless.
+template <typename Kern>
+cudaError_t ensure_smem_attr(Kern kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // ------------------------------------------------------------------ PDL
 // Programmatic dependent launch: a kernel launched with launch_pdl may start
@@ -39,6 +57,36 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// A launch whose blocks wait on one another (a flag one CTA sets and another
+// spins on): the cooperative attribute makes the runtime guarantee that every
+// block of the grid is resident at once (the launch fails otherwise), so a
+// wait always ends.  With pdl the kernel may also start under its
+// predecessor; if the runtime refuses the pair, the launch is repeated as a
+// plain cooperative launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                        cudaStream_t s, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess && pdl) {
+    (void)cudaGetLastError();  // a refused launch configuration is not sticky
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  }
+  return e;
 }
 
 // Bits of the device status word.

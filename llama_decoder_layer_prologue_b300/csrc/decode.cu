@@ -495,21 +495,17 @@ cudaError_t decode_attention(const DecodeArgs& a, cudaStream_t s) {
   dim3 grid(a.max_chunks, a.n_kv_heads, a.batch);
   size_t smem = attn_decode_smem(a.head_dim);
   if (a.head_dim == 128) {
-    static bool set = false;
-    if (!set) {
-      cudaFuncSetAttribute(attn_decode_kernel<128>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (cudaError_t e = ensure_smem_attr(attn_decode_kernel<128>, (int)smem, attr_done);
+        e != cudaSuccess)
+      return e;
     cudaError_t e = launch_pdl(attn_decode_kernel<128>, grid, dim3(128), smem, s, a);
     if (e != cudaSuccess) return e;
   } else {
-    static bool set = false;
-    if (!set) {
-      cudaFuncSetAttribute(attn_decode_kernel<64>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (cudaError_t e = ensure_smem_attr(attn_decode_kernel<64>, (int)smem, attr_done);
+        e != cudaSuccess)
+      return e;
     cudaError_t e = launch_pdl(attn_decode_kernel<64>, grid, dim3(128), smem, s, a);
     if (e != cudaSuccess) return e;
   }

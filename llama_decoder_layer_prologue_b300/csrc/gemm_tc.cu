@@ -28,7 +28,9 @@ constexpr int BM = 128, BK = 64, GROUP_M = 16;
 // quadrant, each on half of the tile's columns)
 constexpr int kEpiWarps = 8, kGemmThreads = 64 + 32 * kEpiWarps;
 
-// Status word for GEMMs launched without a layer (llama_gemm_bf16).
+// Status word of the GEMMs launched without a layer (llama_gemm_bf16,
+// llama_gemm_bf16_streamk_static), one per device; read and cleared by
+// tc_take_status.
 __device__ int g_tc_status;
 
 template <int BN, int STAGES>
@@ -613,13 +615,9 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
                    int K, const TcEpiArgs& ep, int grid, cudaStream_t s) {
   using L = Layout<BN, STAGES>;
   auto kern = gemm_tc_kernel<BN, STAGES, EPI>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::TOTAL);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (cudaError_t e = ensure_smem_attr(kern, (int)L::TOTAL, attr_done); e != cudaSuccess)
+    return e;
   if (grid <= 0) return cudaSuccess;
   TcEpiArgs e = ep;
   const uintptr_t al = reinterpret_cast<uintptr_t>(e.out) |
@@ -629,6 +627,10 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
     cudaError_t err = cudaGetSymbolAddress((void**)&e.status, g_tc_status);
     if (err != cudaSuccess) return err;
   }
+  // the split phase's CTAs wait on flags other CTAs set: make them co-resident
+  if (e.sk_tiles > 0)
+    return launch_coop(kern, dim3(grid), dim3(kGemmThreads), L::TOTAL, s, e.pdl != 0, ta,
+                       tb, M, N, K, e);
   if (e.pdl) return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), L::TOTAL, s, ta, tb, M, N, K, e);
   kern<<<grid, kGemmThreads, L::TOTAL, s>>>(ta, tb, M, N, K, e);
   return cudaGetLastError();
@@ -655,6 +657,13 @@ EncodeTiledFn encode_fn() {
 }
 
 }  // namespace
+
+cudaError_t tc_take_status(int* word) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_tc_status, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(int));
+  return e;
+}
 
 bool tc_encode_bf16(CUtensorMap* map, const void* ptr, uint64_t rows,
                     uint64_t cols, uint32_t box_rows) {

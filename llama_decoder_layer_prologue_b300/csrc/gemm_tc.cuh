@@ -48,7 +48,8 @@ struct TcEpiArgs {
   // sk_flag[c + 1] = sk_epoch; c adds them in its epilogue and clears the
   // flag.  sk_part holds grid slots; sk_flag grid + 1 words, zero when no
   // launch is in flight; sk_epoch must be nonzero and differ from the
-  // previous launch that used the same flags.
+  // previous launch that used the same flags.  A GEMM with a split phase is
+  // launched cooperatively, so every CTA that waits has its partner resident.
   float* sk_part = nullptr;
   uint32_t* sk_flag = nullptr;
   uint32_t sk_epoch = 0;
@@ -86,6 +87,11 @@ __host__ __device__ inline int tc_streamk_segments(const TcStreamK& p, int t) {
 cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
                     const CUtensorMap& tb, int M, int N, int K,
                     const TcEpiArgs& ep, int grid_limit, cudaStream_t s);
+
+// Reads and clears the status word that GEMMs launched without a status
+// pointer of their own write (bounded waits that ran out), on the current
+// device.  Synchronous with respect to the device (a plain memcpy).
+cudaError_t tc_take_status(int* word);
 
 // Tiles of the split phase for a whole-tile GEMM of `tiles` tiles of
 // kb_total K-blocks on `grid` CTAs: grid + tiles % grid when the last round

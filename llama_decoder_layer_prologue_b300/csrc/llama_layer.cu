@@ -953,6 +953,16 @@ int llama_rmsnorm_bf16(const void* x, const void* g, void* out, int rows,
   return cuda_err(cudaGetLastError());
 }
 
+int llama_gemm_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (tc_take_status(&word) != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (word & ST_TIMEOUT) return LLAMA_ERR_DEVICE_TIMEOUT;
+  if (word) return LLAMA_ERR_DEVICE_BAD_INPUT;
+  return LLAMA_OK;
+}
+
 int llama_gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K,
                     void* stream) {
   if (!A || !B || !D || M < 0 || N < 0 || K <= 0) return LLAMA_ERR_INVALID_ARG;

@@ -70,11 +70,13 @@ class LlamaModel:
         return sum(l.launch_count() for l in self.layers) + 2
 
     def status(self) -> int:
+        """The first nonzero status of the layers, else that of the output
+        projection (a standalone GEMM)."""
         for l in self.layers:
             rc = l.status()
             if rc != B.LLAMA_OK:
                 return rc
-        return B.LLAMA_OK
+        return B.llama_gemm_status(stream_ptr())
 
     def close(self) -> None:
         for l in self.layers:

@@ -26,7 +26,7 @@ def test_gemm_matches_fp64(M, N, K):
     D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
     B.llama_gemm_bf16(A.data_ptr(), Bm.data_ptr(), D.data_ptr(), M, N, K,
                       torch.cuda.current_stream().cuda_stream)
-    torch.cuda.synchronize()
+    assert B.llama_gemm_status(torch.cuda.current_stream().cuda_stream) == B.LLAMA_OK
     ref = synth.to_f64(a) @ synth.to_f64(b).T
     got = D.float().cpu().numpy().astype(np.float64)
     assert np.all(np.isfinite(got))

@@ -58,3 +58,26 @@ def test_single_process_needs_no_group():
 def test_reference_arm_runs_on_rank_zero_only():
     args = argparse.Namespace(workload="1b", steps=1, warmup=0, gpus=2)
     assert bench.run_reference(args, rank=1, world=2) is None
+
+
+def test_gpus_flag_needs_a_matching_world():
+    """`--gpus N` with N > 1 must come from torchrun (one process per GPU):
+    a single process asked for 2 GPUs refuses instead of timing one replica
+    and reporting it as two."""
+    import pytest
+
+    bench.check_world(1, 1)
+    bench.check_world(2, 2)
+    with pytest.raises(SystemExit, match="WORLD_SIZE=1"):
+        bench.check_world(2, 1)
+    with pytest.raises(SystemExit):
+        bench.check_world(1, 4)
+
+
+def test_headline_also_runs_the_other_layer_workloads():
+    ns = lambda **kw: argparse.Namespace(**{"workload": bench.HEADLINE, "also": "auto",
+                                           **kw})
+    assert bench.also_list(ns()) == list(bench.ALSO_AUTO)
+    assert bench.also_list(ns(workload="1b")) == []
+    assert bench.also_list(ns(also="none")) == []
+    assert bench.also_list(ns(also="8b,varlen")) == ["8b"]

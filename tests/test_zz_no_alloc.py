@@ -57,6 +57,26 @@ def test_two_calls_match_llama_gemm_bf16():
         bound = _bound(exact, K)
         assert np.all(np.abs(g - exact) <= bound), f"call {i}: vs fp64"
         assert np.all(np.abs(g - r) <= 2 * bound), f"call {i}: vs llama_gemm_bf16"
+        assert B.llama_gemm_status(st) == B.LLAMA_OK
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 8, 256), (129, 40, 64), (1024, 200, 512)])
+def test_ragged_shapes_match_fp64(M, N, K):
+    """Ragged M (rows past the last full tile are out of bounds for the TMA
+    loads and skipped by the reduction), N below the 64-column tile, and the
+    256-column tile within the array's limit."""
+    st = torch.cuda.current_stream().cuda_stream
+    a, b = _operands(M, N, K, seed=M + N + K)
+    A, Bm = to_device(a), to_device(b)
+    for call in range(2):
+        got = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        B.llama_gemm_bf16_streamk_static(A.data_ptr(), Bm.data_ptr(), got.data_ptr(),
+                                         M, N, K, st)
+        assert B.llama_gemm_status(st) == B.LLAMA_OK
+        g = got.float().cpu().numpy().astype(np.float64)
+        exact = synth.to_f64(a) @ synth.to_f64(b).T
+        assert np.all(np.isfinite(g)), f"call {call}"
+        assert np.all(np.abs(g - exact) <= _bound(exact, K)), f"call {call}"
 
 
 def test_too_large_for_the_array_is_refused():
