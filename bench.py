@@ -58,6 +58,11 @@ DESCRIPTIONS = {
     "model1b": "Llama-3.2-1B-shaped model forward bf16: 16 decoder layers (the "
                "1b layer shape, seeded weights per layer), final RMSNorm and the "
                "output projection to 128256 logits, batch 4 x seq 2048",
+    "bwd_8b": "backward pass of the Llama-3-8B-shaped layer bf16 (llama_layer_backward: "
+              "forward recomputed, then dx and the weight / norm gradients): batch 2 x "
+              "seq 4096, dL/d(out) ~ N(0,1) seeded",
+    "bwd_1b": "backward pass of the Llama-3.2-1B-shaped layer bf16 (llama_layer_backward): "
+              "batch 4 x seq 2048, dL/d(out) ~ N(0,1) seeded",
     "chunked": "chunked prefill with a KV cache, 8B-shaped layer bf16: 16 "
                "sequences x 4 new tokens, start_pos U{512..8188} (seeded), cache "
                "[16, 8192, 8, 128] bf16 (llama_layer_forward_cached)",
@@ -102,9 +107,10 @@ def parse_args():
 
 
 HEADLINE = "varlen"
+BACKWARD = {"bwd_8b": "8b", "bwd_1b": "1b"}  # backward workload -> its forward workload
 ALSO_AUTO = ("1b", "8b", "decode")
 
-DEFAULT_STEPS = {"tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
+DEFAULT_STEPS = {"bwd_8b": 200, "bwd_1b": 600, "tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
                  "decode": 3000, "chunked": 1500, "model1b": 40}
 MODEL = {"model1b": ("1b", 16, 128256)}  # layer workload, layers, vocabulary
 
@@ -218,6 +224,30 @@ def algorithmic_work(inp) -> dict:
     }
     return dict(kind="decode", bytes={k: float(v) for k, v in stage.items()},
                 total_bytes=total, kv_read=kv_read, weight_bytes=weights, flops={})
+
+
+def algorithmic_work_backward(inp) -> dict:
+    """Per-stage algorithmic FLOPs of one llama_layer_backward call: the
+    forward it recomputes (every stage but down_proj) and the backward
+    proper (each projection twice: dX and dW; the attention's five products
+    of the visible pairs, 2.5 x its forward's two), plus the bytes of the
+    row passes."""
+    w = algorithmic_work(inp)
+    f = w["flops"]
+    s = inp.workload.shape
+    T, H, I, q, nqkv = inp.tokens, s.hidden, s.intermediate, s.q_size, s.n_qkv
+    flops = {k: f[k] for k in ("qkv_rope", "attention", "o_proj_residual", "gate_up_swiglu")}
+    flops.update({
+        "bwd_dw_down": 2.0 * T * H * I, "bwd_swiglu": 2.0 * T * H * I,
+        "bwd_dw_gate_up": 2.0 * T * 2 * I * H, "bwd_dh_mlp": 2.0 * T * 2 * I * H,
+        "bwd_dw_o": 2.0 * T * H * q, "bwd_dattn": 2.0 * T * H * q,
+        "bwd_attention": 2.5 * f["attention"],
+        "bwd_dw_qkv": 2.0 * T * nqkv * H, "bwd_dx_attn": 2.0 * T * nqkv * H})
+    by = {"rmsnorm_stats": float(T * H * 2), "bwd_dout_f16": float(T * H * 4),
+          "bwd_norm2": float(T * H * (2 + 4 + 2 + 4 + 2)),
+          "bwd_norm1": float(T * H * (4 + 4 + 2 + 2))}
+    return dict(kind="prefill", flops=flops, total_flops=sum(flops.values()), bytes=by,
+                weight_bytes=w["weight_bytes"])
 
 
 # ----------------------------------------------------------------- clocks
@@ -353,7 +383,7 @@ class OracleRunner:
     first b sequences of a decode batch.  Prefixes of a causal sequence are
     exact sub-problems (their outputs do not depend on later tokens)."""
 
-    def __init__(self, inp):
+    def __init__(self, inp, backward: bool = False):
         import numpy as np
 
         import oracle
@@ -362,6 +392,8 @@ class OracleRunner:
         self.np, self.oracle, self.synth = np, oracle, synth
         self.inp = inp
         self.w = _f64_weights(inp)
+        self.backward = backward
+        self.dout = synth.to_f64(synth.make_dout(inp)) if backward else None
 
     def units(self, n: int):
         """A sample of n tokens: (callable, tokens, description)."""
@@ -398,6 +430,14 @@ class OracleRunner:
         x = synth.to_f64(inp.x[:n])
         pos = inp.positions[:n]
 
+        if self.backward:
+            from oracle.backward import decoder_layer_backward
+            dout = self.dout[:n]
+
+            def run():
+                decoder_layer_backward(x, self.w, s, pos, cut, dout)
+            return run, n, what + " (backward pass)"
+
         def run():
             self.oracle.decoder_layer(x, self.w, s, pos, cut)
         return run, n, what
@@ -424,8 +464,8 @@ def oracle_threads() -> int:
     return os.cpu_count() or 1
 
 
-def cpu_baseline(inp, budget_s: float) -> dict:
-    r = OracleRunner(inp)
+def cpu_baseline(inp, budget_s: float, backward: bool = False) -> dict:
+    r = OracleRunner(inp, backward)
     n = r.calibrate(min(budget_s, 2.0) / 4)
     n = max(1, int(n * budget_s / (min(budget_s, 2.0) / 4)))
     run, tokens, what = r.units(n)
@@ -624,7 +664,7 @@ def run_model(args, rank, local_rank, world, dist=None):
 
 
 # ----------------------------------------------------------------- our arm
-def run_ours(args, rank, local_rank, world, dist=None, name=None, cpu_seconds=None):
+def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None):
     """One workload on our library: the JSON line (rank 0) or None."""
     import numpy as np
     import torch
@@ -634,15 +674,16 @@ def run_ours(args, rank, local_rank, world, dist=None, name=None, cpu_seconds=No
 
     assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
     torch.cuda.set_device(local_rank)
-    name = name or args.workload
+    wl = wl or args.workload
     if cpu_seconds is None:
         cpu_seconds = args.cpu_baseline_seconds
 
-    inp = synth.make_inputs(name)
+    bwd = wl in BACKWARD
+    inp = synth.make_inputs(BACKWARD.get(wl, wl))
     w = inp.workload
     s = w.shape
     layer = LlamaLayer.from_numpy(s, inp.weights)
-    K = args.steps if args.steps is not None else DEFAULT_STEPS[name]
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[wl]
     W = args.warmup
     x = to_device(inp.x)
     out = torch.empty_like(x)
@@ -668,6 +709,14 @@ def run_ours(args, rank, local_rank, world, dist=None, name=None, cpu_seconds=No
                 layer.forward(x, cu_seqlens=cu, seq_len=seq, out=o)
             else:
                 layer.forward(x, n_seq=n_seq, seq_len=seq, out=o)
+
+        if bwd:  # dL/d(out) in, dx (in `out`) and the weight gradients out
+            dout = to_device(synth.make_dout(inp))
+            grads = layer.backward(x, dout, n_seq=n_seq, seq_len=seq, dx=out)
+            grads.pop("dx")
+
+            def step(o=out):
+                layer.backward(x, dout, n_seq=n_seq, seq_len=seq, dx=o, grads=grads)
 
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
@@ -725,7 +774,7 @@ def run_ours(args, rank, local_rank, world, dist=None, name=None, cpu_seconds=No
 
     tokens = inp.tokens
     value = job_throughput(world, K, tokens, total_ms)
-    work = algorithmic_work(inp)
+    work = algorithmic_work_backward(inp) if bwd else algorithmic_work(inp)
     pk = peaks()
 
     # ---- end to end: host input -> layer -> host output, copies timed
@@ -744,10 +793,18 @@ def run_ours(args, rank, local_rank, world, dist=None, name=None, cpu_seconds=No
         ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n_e2e)]
 
+        if bwd:
+            extra_h.append(to_device(synth.make_dout(inp), pin=True))
+            extra_d.append(dout)
+
         def host_step():
             for h_, d_ in zip(extra_h, extra_d):
                 d_.copy_(h_, non_blocking=True)
-            if decode and S_new > 1:
+            if bwd:
+                x.copy_(x_h, non_blocking=True)
+                step()
+                out_h.copy_(out, non_blocking=True)
+            elif decode and S_new > 1:
                 layer.forward_cached_from_host(x_h, out_h, x, out, ck, cv, sp, S_new)
             elif decode:
                 layer.decode_from_host(x_h, out_h, x, out, ck, cv, sp)
@@ -774,7 +831,10 @@ def run_ours(args, rank, local_rank, world, dist=None, name=None, cpu_seconds=No
         e2e = {"value": job_throughput(world, n_e2e, tokens, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
                "steps": n_e2e, "ms_per_step": e2e_ms / n_e2e,
-               "api": ("LlamaLayer.%s_from_host (pinned host buffers, "
+               "api": ("LlamaLayer.backward (pinned host x and dL/d(out) copied in, "
+                       "dx copied out; the weight gradients stay on the device for the "
+                       "optimizer)") if bwd else
+                      ("LlamaLayer.%s_from_host (pinned host buffers, "
                        "cudaMemcpyAsync on the layer's stream)"
                        % ("decode" if S_new == 1 else "forward_cached") if decode else
                        "LlamaLayer.forward_from_host -> llama_layer_forward_host "
@@ -810,7 +870,7 @@ def run_ours(args, rank, local_rank, world, dist=None, name=None, cpu_seconds=No
                         "peak_source": f"{pk['source']} HBM copy",
                         "algorithmic_per_launch": work["bytes"][dom],
                         "launch_ms": dom_ms, "share_of_step": share}
-        roofline["traffic"] = recorded_traffic(name, dom)
+        roofline["traffic"] = recorded_traffic(wl, dom)
         roofline["stage_timing"] = (
             f"library CUDA stage events on {n_stage} steps run right after the timed "
             "region (events between kernels disable the launch overlap, so stage "
@@ -842,7 +902,7 @@ def run_ours(args, rank, local_rank, world, dist=None, name=None, cpu_seconds=No
 
     cpu = None
     if cpu_seconds > 0:
-        cpu = cpu_baseline(inp, cpu_seconds)
+        cpu = cpu_baseline(inp, cpu_seconds, backward=bwd)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -851,7 +911,7 @@ def run_ours(args, rank, local_rank, world, dist=None, name=None, cpu_seconds=No
         "dtype": "bf16" if s.dtype == "bf16" else "f32",
         "data": "synthetic: seeded x ~ N(0,1), weights ~ N(0,0.02), RMSNorm "
                 "weights ~ 1+N(0,0.1), no trained weights",
-        "config": {"workload": DESCRIPTIONS[name], "name": name,
+        "config": {"workload": DESCRIPTIONS[wl], "name": wl,
                    "tokens_per_step": tokens, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (256 MiB write, outside "
                          "the step's events)",
@@ -895,8 +955,8 @@ def run_reference(args, rank, world):
         per_tok = (time.perf_counter() - t) / n0
         run, tokens, what = model_oracle_sample(m_in, max(1, int(per_step / per_tok)))
     else:
-        inp = synth.make_inputs(args.workload)
-        r = OracleRunner(inp)
+        inp = synth.make_inputs(BACKWARD.get(args.workload, args.workload))
+        r = OracleRunner(inp, args.workload in BACKWARD)
         n = r.calibrate(per_step)
         run, tokens, what = r.units(n)
     for _ in range(min(W, 1)):
@@ -984,7 +1044,7 @@ def main():
             others = {}
             for name in also_list(args):
                 torch.cuda.empty_cache()
-                sub = run_ours(args, rank, local_rank, world, dist, name=name,
+                sub = run_ours(args, rank, local_rank, world, dist, wl=name,
                                cpu_seconds=min(args.cpu_baseline_seconds, 4.0))
                 if sub is not None:
                     others[name] = summary_of(sub)

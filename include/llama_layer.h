@@ -238,17 +238,81 @@ LLAMA_API int llama_layer_decode(llama_layer_t* layer, const void* x, void* out,
  *              token; every new token's position must be < max_seq and
  *              < max_position (checked on the device, status word)
  * New token i of sequence b attends to cache rows 0 .. start_pos[b] + i.
- * seq_tokens = 1 is llama_layer_decode.  The attention of each new token
- * reads its prefix on its own (the decode kernels), which suits short chunks
- * (a few tokens per sequence, e.g. checking drafted tokens).  bf16 layers;
- * an fp32 layer takes seq_tokens = 1 only (LLAMA_ERR_UNSUPPORTED_SHAPE).
- * `workspace` must hold llama_layer_workspace_bytes(layer, 0,
- * >= batch * seq_tokens, >= max_seq). */
+ * seq_tokens = 1 is llama_layer_decode.  Short chunks (seq_tokens <
+ * LLAMA_LONG_CHUNK, e.g. checking drafted tokens) run the decode kernels: the
+ * attention of each new token reads its prefix on its own.  Longer chunks run
+ * the prefill kernels with the tensor-core attention reading the cache: each
+ * prefix is read once per group of query heads, and the keys of cache rows
+ * past start_pos[b] + seq_tokens are read but masked (their values are
+ * replaced by zeros on chip, so whatever those rows hold does not matter).
+ * bf16 layers; an fp32 layer takes seq_tokens = 1 only
+ * (LLAMA_ERR_UNSUPPORTED_SHAPE).  `workspace` must hold
+ * llama_layer_workspace_bytes(layer, 0, >= batch * seq_tokens, >= max_seq)
+ * for short chunks and llama_layer_workspace_bytes(layer, >= batch *
+ * seq_tokens, 0, 0) for long ones. */
+#define LLAMA_LONG_CHUNK 16
 LLAMA_API int llama_layer_forward_cached(llama_layer_t* layer, const void* x, void* out,
                                          void* cache_k, void* cache_v,
                                          const int32_t* start_pos, int batch,
                                          int seq_tokens, int max_seq, void* workspace,
                                          size_t workspace_bytes, void* stream);
+
+/* Gradient buffers of llama_layer_backward: fp32 device memory in the shapes
+ * of the weights they belong to (llama_layer_weights: nn.Linear layout,
+ * rows gate | up for dw_gate_up), 16-byte aligned.  Every buffer is
+ * overwritten (not accumulated into). */
+typedef struct {
+  float *dw_qkv, *dw_o, *dw_gate_up, *dw_down;
+  float *dg_in, *dg_post; /* [hidden] */
+} llama_layer_grads;
+
+/* Workspace bytes of llama_layer_backward for calls of up to `max_tokens`
+ * tokens (the forward's intermediates, recomputed, plus the backward's).
+ * Host only. */
+LLAMA_API int llama_layer_backward_workspace_bytes(const llama_layer_t* layer,
+                                                   int max_tokens, size_t* bytes);
+
+/* Backward pass of the prefill layer: the gradients of a loss L with respect
+ * to the layer's input and weights, given dL/d(out).  The pages train these
+ * layers ("模型层" 9.6 LlamaForTraining puts the decoder under a loss; the
+ * verl "parallel_attention.py" layers are training code) and print only the
+ * forward, so every step is the chain rule applied to it, in reverse order:
+ *   dW_down = dout^T act,  d act = dout W_down,
+ *   d gate = d act * up * silu'(gate),  d up = d act * silu(gate),
+ *   dW_gate_up = [d gate | d up]^T hn,  d hn = [d gate | d up] W_gate_up,
+ *   RMSNorm^T: for y = a r g with r = (mean(a^2) + eps)^(-1/2):
+ *     dg = sum over tokens of dy * a * r,  da = r (dy g) - a r^3 mean((dy g) a),
+ *   dh = dout + RMSNorm^T(d hn),  dW_o = dh^T o,  d o = dh W_o,
+ *   attention: P = softmax(q k^T / sqrt(d) + mask), dP = d o v^T,
+ *     dz = P * (dP - rowsum(d o * o)), dq = dz k / sqrt(d),
+ *     dk = dz^T q / sqrt(d), dv = P^T d o, each kv head's dk and dv summed
+ *     over its n_rep query heads (the transpose of repeat_kv),
+ *   RoPE^T: da = dy cos + [ (dy sin)_2, -(dy sin)_1 ] (halves of the head),
+ *   dW_qkv = [dq | dk | dv]^T xn,  d xn = [dq | dk | dv] W_qkv,
+ *   dx = dh + RMSNorm^T(d xn).
+ * The call recomputes the forward first (nothing of the forward needs to be
+ * kept by the caller) and runs on the tensor cores like the forward; bf16
+ * layers only (an fp32 layer returns LLAMA_ERR_UNSUPPORTED_SHAPE).
+ *   weights      the weights the layer was initialised with (device, bf16,
+ *                unchanged since llama_layer_init): the norm-weight gradients
+ *                read W_qkv, W_gate_up, g_in and g_post as given
+ *   x            [total_tokens, hidden] device bf16, the layer's input
+ *   dout         [total_tokens, hidden] device bf16, dL/d(out)
+ *   dx           [total_tokens, hidden] device bf16 out, dL/dx (must alias
+ *                neither x nor dout)
+ *   grads        the weight gradients (fp32, see llama_layer_grads)
+ *   position_ids, cu_seqlens, n_seq, seq_len, total_tokens: as
+ *                llama_layer_forward
+ * `workspace` must hold llama_layer_backward_workspace_bytes(layer,
+ * >= total_tokens).  Gradients pass through fp16 intermediates (like the
+ * forward's); scale dout so that they stay inside fp16's range, as fp16
+ * training does with its loss scale. */
+LLAMA_API int llama_layer_backward(llama_layer_t* layer, const llama_layer_weights* weights,
+                                   const void* x, const void* dout, void* dx,
+                                   const llama_layer_grads* grads,
+                                   const int32_t* position_ids, const int32_t* cu_seqlens,
+                                   int n_seq, int seq_len, int total_tokens, void* workspace,
+                                   size_t workspace_bytes, void* stream);
 
 /* Self-test of the bounded waits the library's pipelined kernels use (no
  * layer needed): one block waits on an mbarrier that nothing arrives on and
@@ -300,7 +364,8 @@ LLAMA_API int llama_layer_set_timing(llama_layer_t* layer, int ring_calls);
  * *n_stages (may be NULL): 0 when timing is off or the call was not recorded,
  * at most LLAMA_MAX_STAGES (the first ones of a call that has more).  Stages
  * of a prefill: "rmsnorm_stats", "qkv_rope", "attention", "o_proj_residual",
- * "gate_up_swiglu", "down_residual". */
+ * "gate_up_swiglu", "down_residual"; a backward call adds its own stages
+ * (names starting with "bwd_"). */
 LLAMA_API int llama_layer_stage_times(llama_layer_t* layer, int call,
                                       int max_stages, float* ms,
                                       const char** names, int* n_stages);

@@ -44,7 +44,7 @@ EXPORTS = (
     "llama_layer_launch_count", "llama_gemm_bf16_streamk_static",
     "llama_layer_forward_host", "llama_layer_forward_cached",
     "llama_selftest_bounded_waits", "llama_rope_inv_freq", "llama_rmsnorm_bf16",
-    "llama_gemm_status",
+    "llama_gemm_status", "llama_layer_backward_workspace_bytes", "llama_layer_backward",
 )
 
 
@@ -65,6 +65,11 @@ class llama_layer_config(ctypes.Structure):
 class llama_layer_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w_qkv", "w_o", "w_gate_up", "w_down", "g_in", "g_post")]
+
+
+class llama_layer_grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("dw_qkv", "dw_o", "dw_gate_up", "dw_down", "dg_in", "dg_post")]
 
 
 class LlamaError(RuntimeError):
@@ -123,6 +128,10 @@ def lib() -> ctypes.CDLL:
                                      ctypes.POINTER(ctypes.c_double)]),
         "llama_rmsnorm_bf16": (_I, [_P, _P, _P, _I, _I, ctypes.c_float, _P]),
         "llama_gemm_status": (_I, [_P]),
+        "llama_layer_backward_workspace_bytes": (_I, [_P, _I, ctypes.POINTER(_SZ)]),
+        "llama_layer_backward": (_I, [_P, ctypes.POINTER(llama_layer_weights), _P, _P, _P,
+                                      ctypes.POINTER(llama_layer_grads), _P, _P, _I, _I,
+                                      _I, _P, _SZ, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -274,6 +283,24 @@ def llama_layer_launch_count(layer: int) -> int:
 def llama_gemm_bf16(A: int, B: int, D: int, M: int, N: int, K: int,
                     stream: int) -> None:
     _check("llama_gemm_bf16", lib().llama_gemm_bf16(A, B, D, M, N, K, stream))
+
+
+def llama_layer_backward_workspace_bytes(layer: int, max_tokens: int) -> int:
+    n = _SZ()
+    _check("llama_layer_backward_workspace_bytes",
+           lib().llama_layer_backward_workspace_bytes(layer, max_tokens, ctypes.byref(n)))
+    return n.value
+
+
+def llama_layer_backward(layer: int, weights: llama_layer_weights, x: int, dout: int,
+                         dx: int, grads: llama_layer_grads, position_ids, cu_seqlens,
+                         n_seq: int, seq_len: int, total_tokens: int, workspace: int,
+                         workspace_bytes: int, stream: int) -> None:
+    _check("llama_layer_backward",
+           lib().llama_layer_backward(layer, ctypes.byref(weights), x, dout, dx,
+                                      ctypes.byref(grads), position_ids, cu_seqlens,
+                                      n_seq, seq_len, total_tokens, workspace,
+                                      workspace_bytes, stream))
 
 
 def llama_gemm_status(stream: int) -> int:

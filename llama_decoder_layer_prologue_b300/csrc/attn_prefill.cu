@@ -86,10 +86,14 @@ struct AttnLayout {
 struct Item {
   int a0, L, q0, h0, g;  // sequence start and length, first position, heads
   int n_tiles;           // K / V tiles of the causal range (0: nothing to do)
+  int sp;                // position of the sequence's first query (cache: start_pos)
+  int kbase;             // row of the sequence's key 0 in the K / V tensor map
+  int kv_end;            // keys the item's queries can see: rows [0, kv_end)
 };
 
 // Work item i: query block from the top (longest causal range first), then
 // head group, then sequence.  A block is 2 BP positions.
+template <bool CACHED>
 __device__ __forceinline__ Item get_item(const AttnArgs& a, int i, int n_hg,
                                          int n_seq, int n_qb, int BP, int AN) {
   Item it;
@@ -101,19 +105,31 @@ __device__ __forceinline__ Item get_item(const AttnArgs& a, int i, int n_hg,
   it.h0 = hg * a.hpc;
   it.g = it.h0 / n_rep;
   it.q0 = qb * 2 * BP;
-  if (a.cu) {
+  it.sp = 0;
+  if constexpr (CACHED) {
+    const int sp = a.start_pos[s];
+    it.a0 = s * a.seq_len;
+    it.kbase = s * a.max_seq;
+    // flagged by the positions kernel when the chunk does not fit
+    const bool ok = sp >= 0 && sp <= a.max_seq - a.seq_len && sp <= a.max_pos - a.seq_len;
+    it.L = ok ? a.seq_len : 0;
+    it.sp = ok ? sp : 0;
+  } else if (a.cu) {
     const int s0 = a.cu[s], s1 = a.cu[s + 1];
     if (s0 < 0 || s1 < s0 || s1 > a.tokens) {  // flagged by the positions kernel
       it.a0 = 0; it.L = 0;
     } else {
       it.a0 = s0; it.L = s1 - s0;
     }
+    it.kbase = it.a0;
   } else {
     it.a0 = s * a.seq_len;
     it.L = a.seq_len;
+    it.kbase = it.a0;
   }
   const int hi = min(it.q0 + 2 * BP, it.L);
-  it.n_tiles = it.q0 < it.L ? (hi + AN - 1) / AN : 0;
+  it.kv_end = it.sp + hi;
+  it.n_tiles = it.q0 < it.L ? (it.kv_end + AN - 1) / AN : 0;
   return it;
 }
 
@@ -148,10 +164,21 @@ __device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(x));
 }
 
-template <int D>
+// 16-bit pair of the P operand: fp16 with the fp16 q | k | v of the prefill,
+// bf16 with the bf16 cache of a cached chunk (an MMA's A and B share a type).
+template <bool BF>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+  return BF ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+}
+
+// CACHED: keys and values from the KV-cache maps tmK / tmV (rows
+// sequence * max_seq + key, columns kv head * D), bf16 operands; otherwise
+// both from the q|k|v map (tmK == tmV), fp16 operands.
+template <int D, bool CACHED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
-                   const __grid_constant__ CUtensorMap tmKV, AttnArgs a,
+                   const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, AttnArgs a,
                    int n_items, int n_hg, int n_seq, int n_qb) {
   using L = AttnLayout<D>;
   constexpr int AN = L::AN;
@@ -195,7 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmKV);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
   }
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, L::TMEM_COLS);
   tc_fence_before();
@@ -213,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t n = 0, k = 0;  // K / V tiles loaded, items started
       bool ok = true;
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
-        const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP, L::AN);
+        const Item it = get_item<CACHED>(a, i, n_hg, n_seq, n_qb, BP, L::AN);
         if (it.n_tiles == 0) continue;
         if (k > 0 && !mbar_wait_sleep(q_empty, (k - 1) & 1, a.status, abort_flag)) {
           ok = false;
@@ -228,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           &tmQ, q_full, (it.h0 + hh) * D + at * 64,
                           it.a0 + it.q0 + t * BP);
         ++k;
-        const int col[2] = {(a.n_heads + it.g) * D,
-                            (a.n_heads + a.n_kv_heads + it.g) * D};
+        const int col[2] = {CACHED ? it.g * D : (a.n_heads + it.g) * D,
+                            CACHED ? it.g * D : (a.n_heads + a.n_kv_heads + it.g) * D};
         for (int j = 0; ok && j < it.n_tiles; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++n) {  // K(j), then V(j)
             const int sl = n % L::SLOTS;
@@ -241,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* dst = smem + L::KV_OFF + sl * L::KV_BYTES;
             mbar_arrive_expect_tx(&kv_full[sl], L::KV_BYTES);
             for (int at = 0; at < L::ATOMS; ++at)
-              tma_load_2d(dst + at * (AN * 128), &tmKV, &kv_full[sl],
-                          col[kv] + at * 64, it.a0 + j * AN);
+              tma_load_2d(dst + at * (AN * 128), kv ? &tmV : &tmK, &kv_full[sl],
+                          col[kv] + at * 64, it.kbase + j * AN);
           }
         }
       }
@@ -263,8 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // softmax.  K / V slots and the Q tiles are released by a commit from
     // each warp (barrier count 2).  One elected lane issues.
     const int t = warp - kMmaWarp;
-    constexpr uint32_t idesc_s = idesc_f16(AM, AN);
-    constexpr uint32_t idesc_pv = idesc_f16(AM, D) | (1u << 16);  // B MN-major
+    constexpr uint32_t idesc_s = CACHED ? idesc_bf16(AM, AN) : idesc_f16(AM, AN);
+    constexpr uint32_t idesc_pv =
+        (CACHED ? idesc_bf16(AM, D) : idesc_f16(AM, D)) | (1u << 16);  // B MN-major
     // descriptor bases; a K step adds its byte offset >> 4 to the address
     const uint64_t q_desc = sdesc_k128(smem_u32(smem + L::Q_OFF));
     const uint64_t p_desc = sdesc_k128(smem_u32(smem + L::P_OFF));
@@ -280,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t g = 0, n = 0, k = 0;  // tiles, K / V loads consumed, items
     bool ok = true, issued_any = false;
     for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
-      const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP, L::AN);
+      const Item it = get_item<CACHED>(a, i, n_hg, n_seq, n_qb, BP, L::AN);
       if (it.n_tiles == 0) continue;
       if (!wait_all(q_full, k & 1)) {
         ok = false;
@@ -326,6 +355,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        if constexpr (CACHED) {
+          // cache rows past what any query of the item sees hold whatever the
+          // caller left there (NaN included): P is 0 for them, and 0 * NaN
+          // would still poison the sum, so their V rows become zeros
+          const int r0 = it.kv_end - j * AN;
+          if (r0 < AN) {
+            uint8_t* vs = smem + L::KV_OFF + (vn % L::SLOTS) * L::KV_BYTES;
+            const int n16 = (AN - r0) * 8;  // 16-byte pieces per atom
+            for (int e = lane; e < n16 * L::ATOMS; e += 32) {
+              const int at = e / n16, w = e - at * n16;
+              *reinterpret_cast<uint4*>(vs + at * (AN * 128) + (r0 + w / 8) * 128 +
+                                        (w % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+        }
         const uint64_t vd = v_desc + (vn % L::SLOTS) * SLOT16;
         if (elect_one()) {
 #pragma unroll
@@ -373,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __shfl_sync(0xffffffffu, w_ok, 0) != 0;
     };
     for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
-      const Item it = get_item(a, i, n_hg, n_seq, n_qb, BP, L::AN);
+      const Item it = get_item<CACHED>(a, i, n_hg, n_seq, n_qb, BP, L::AN);
       if (it.n_tiles == 0) continue;
       const int q0 = it.q0 + t * BP;  // first position of this tile
       const int pos = q0 + (r % BP);
@@ -397,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // causal mask (keys after the row's position), tile max of the raw
         // scores (8 independent chains)
         const int kb = j * AN;
-        if (kb + AN - 1 > q0) {
-          const int lim = pos - kb;
+        if (kb + AN - 1 > it.sp + q0) {
+          const int lim = it.sp + pos - kb;
 #pragma unroll
           for (int c = 0; c < AN; ++c) s[c] = c > lim ? -INFINITY : s[c];
         }
@@ -461,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t w[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q)
-              w[q] = pack_f16x2(s[h * 32 + 2 * q], s[h * 32 + 2 * q + 1]);
+              w[q] = pack_p<CACHED>(s[h * 32 + 2 * q], s[h * 32 + 2 * q + 1]);
             tmem_st16_words(p_tmem + h * 16, w);
           }
           tmem_wait_st();
@@ -470,10 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c16 = 0; c16 < AN / 8; ++c16) {
             uint4 u;
-            u.x = pack_f16x2(s[c16 * 8 + 0], s[c16 * 8 + 1]);
-            u.y = pack_f16x2(s[c16 * 8 + 2], s[c16 * 8 + 3]);
-            u.z = pack_f16x2(s[c16 * 8 + 4], s[c16 * 8 + 5]);
-            u.w = pack_f16x2(s[c16 * 8 + 6], s[c16 * 8 + 7]);
+            u.x = pack_p<CACHED>(s[c16 * 8 + 0], s[c16 * 8 + 1]);
+            u.y = pack_p<CACHED>(s[c16 * 8 + 2], s[c16 * 8 + 3]);
+            u.z = pack_p<CACHED>(s[c16 * 8 + 4], s[c16 * 8 + 5]);
+            u.w = pack_p<CACHED>(s[c16 * 8 + 6], s[c16 * 8 + 7]);
             const int atom = c16 / 8, cc = c16 % 8;
             *reinterpret_cast<uint4*>(prow + atom * (AM * 128) + ((cc ^ (r & 7)) << 4)) = u;
           }
@@ -491,6 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool valid = pos < it.L;
       const float inv = l > 0.f ? 1.0f / l : 0.f;
+      if (a.lse && valid)  // the row's softmax is 2^(s * scale - lse)
+        a.lse[(size_t)(it.a0 + pos) * a.n_heads + head] = m + __log2f(l);
       __half* out = a.out + (size_t)(it.a0 + (valid ? pos : 0)) * a.n_heads * D + head * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -528,27 +576,34 @@ int heads_per_cta(int n_rep) {
   return h;
 }
 
-template <int D>
+template <int D, bool CACHED>
 cudaError_t launch(const AttnArgs& a, int n_seq, int max_len, int sm_count,
                    cudaStream_t s) {
   using L = AttnLayout<D>;
   constexpr int AN = L::AN;
   const int BP = AM / a.hpc;
-  CUtensorMap tq, tkv;
-  if (!tc_encode_bf16(&tq, a.qkv, a.tokens, a.nqkv, BP) ||
-      !tc_encode_bf16(&tkv, a.qkv, a.tokens, a.nqkv, AN))
-    return cudaErrorInvalidValue;
+  CUtensorMap tq, tk, tv;
+  if (!tc_encode_bf16(&tq, a.qkv, a.tokens, a.nqkv, BP)) return cudaErrorInvalidValue;
+  if constexpr (CACHED) {
+    const uint64_t rows = (uint64_t)n_seq * a.max_seq, cols = (uint64_t)a.n_kv_heads * D;
+    if (!tc_encode_bf16(&tk, a.cache_k, rows, cols, AN) ||
+        !tc_encode_bf16(&tv, a.cache_v, rows, cols, AN))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!tc_encode_bf16(&tk, a.qkv, a.tokens, a.nqkv, AN)) return cudaErrorInvalidValue;
+    tv = tk;
+  }
   const int n_qb = (max_len + 2 * BP - 1) / (2 * BP);
   const int n_hg = a.n_heads / a.hpc;
   const long long items = (long long)n_qb * n_hg * n_seq;
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffff) return cudaErrorInvalidValue;
-  auto kern = attn_tc_kernel<D>;
+  auto kern = attn_tc_kernel<D, CACHED>;
   static std::atomic<uint64_t> attr_done{0};
   if (cudaError_t e = ensure_smem_attr(kern, (int)L::TOTAL, attr_done); e != cudaSuccess)
     return e;
   const int grid = (int)(items < sm_count ? items : sm_count);
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), L::TOTAL, s, tq, tkv, a,
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), L::TOTAL, s, tq, tk, tv, a,
                     (int)items, n_hg, n_seq, n_qb);
 }
 
@@ -560,8 +615,21 @@ cudaError_t attn_prefill(const AttnArgs& args, int n_seq, int max_len,
   const int n_rep = a.n_heads / a.n_kv_heads;
   a.hpc = heads_per_cta(n_rep);
   if (n_seq <= 0 || max_len <= 0 || a.tokens <= 0) return cudaSuccess;
-  if (a.head_dim == 128) return launch<128>(a, n_seq, max_len, sm_count, s);
-  if (a.head_dim == 64) return launch<64>(a, n_seq, max_len, sm_count, s);
+  if (a.head_dim == 128) return launch<128, false>(a, n_seq, max_len, sm_count, s);
+  if (a.head_dim == 64) return launch<64, false>(a, n_seq, max_len, sm_count, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t attn_prefill_cached(const AttnArgs& args, int n_seq, int sm_count,
+                                cudaStream_t s) {
+  AttnArgs a = args;
+  const int n_rep = a.n_heads / a.n_kv_heads;
+  a.hpc = heads_per_cta(n_rep);
+  a.cu = nullptr;
+  if (n_seq <= 0 || a.seq_len <= 0 || a.tokens <= 0) return cudaSuccess;
+  if (!a.cache_k || !a.cache_v || !a.start_pos) return cudaErrorInvalidValue;
+  if (a.head_dim == 128) return launch<128, true>(a, n_seq, a.seq_len, sm_count, s);
+  if (a.head_dim == 64) return launch<64, true>(a, n_seq, a.seq_len, sm_count, s);
   return cudaErrorInvalidValue;
 }
 

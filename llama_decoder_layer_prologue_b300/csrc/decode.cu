@@ -516,3 +516,73 @@ cudaError_t decode_attention(const DecodeArgs& a, cudaStream_t s) {
 }
 
 }  // namespace llama
+
+// ------------------------------------------------------------ long chunks
+namespace llama {
+namespace {
+
+__device__ __forceinline__ bool chunk_fits(int sp, int S, int max_seq, int max_pos) {
+  return sp >= 0 && sp <= max_seq - S && sp <= max_pos - S;
+}
+
+__global__ void chunk_positions_kernel(const int32_t* __restrict__ start_pos, int n_seq,
+                                       int S, int max_seq, int max_pos,
+                                       int32_t* __restrict__ pos, int* status) {
+  pdl_trigger();
+  pdl_wait();
+  const int T = n_seq * S;
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+    const int b = t / S, i = t - b * S;
+    const int sp = start_pos[b];
+    const bool ok = chunk_fits(sp, S, max_seq, max_pos);
+    if (!ok && i == 0) set_status(status, ST_BAD_START_POS);
+    pos[t] = ok ? sp + i : 0;
+  }
+}
+
+// One 16-byte piece of a row of k or v per thread: cache[b, start_pos[b] + i]
+// = qkv[b * S + i, k | v columns].
+__global__ void chunk_append_kernel(const __nv_bfloat16* __restrict__ qkv, int nqkv,
+                                    int q_cols, int kv_cols,
+                                    __nv_bfloat16* __restrict__ ck,
+                                    __nv_bfloat16* __restrict__ cv,
+                                    const int32_t* __restrict__ start_pos, int n_seq, int S,
+                                    int max_seq, int max_pos) {
+  pdl_trigger();
+  pdl_wait();
+  const int per_row = 2 * kv_cols / 8;
+  const long long total = (long long)n_seq * S * per_row;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(e / per_row), w = (int)(e - (long long)t * per_row);
+    const int b = t / S, i = t - b * S;
+    const int sp = start_pos[b];
+    if (!chunk_fits(sp, S, max_seq, max_pos)) continue;
+    const bool is_v = w >= kv_cols / 8;
+    const int c = (is_v ? w - kv_cols / 8 : w) * 8;
+    const uint4 val = *reinterpret_cast<const uint4*>(qkv + (size_t)t * nqkv + q_cols +
+                                                      (is_v ? kv_cols : 0) + c);
+    __nv_bfloat16* dst = (is_v ? cv : ck) + ((size_t)b * max_seq + sp + i) * kv_cols + c;
+    *reinterpret_cast<uint4*>(dst) = val;
+  }
+}
+
+}  // namespace
+
+cudaError_t chunk_positions(const int32_t* start_pos, int n_seq, int S, int max_seq,
+                            int max_pos, int32_t* pos, int* status, cudaStream_t s) {
+  const int T = n_seq * S;
+  const int blocks = (T + 255) / 256 < 1184 ? (T + 255) / 256 : 1184;
+  return launch_pdl(chunk_positions_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, s,
+                    start_pos, n_seq, S, max_seq, max_pos, pos, status);
+}
+
+cudaError_t chunk_append(const __nv_bfloat16* qkv, int nqkv, int q_cols, int kv_cols,
+                         __nv_bfloat16* ck, __nv_bfloat16* cv, const int32_t* start_pos,
+                         int n_seq, int S, int max_seq, int max_pos, int sm_count,
+                         cudaStream_t s) {
+  return launch_pdl(chunk_append_kernel, dim3(sm_count * 4), dim3(256), 0, s, qkv, nqkv,
+                    q_cols, kv_cols, ck, cv, start_pos, n_seq, S, max_seq, max_pos);
+}
+
+}  // namespace llama

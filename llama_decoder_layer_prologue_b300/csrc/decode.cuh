@@ -46,6 +46,18 @@ cudaError_t decode_finalize(int stage, const DecodeArgs& a,
 // then the log-sum-exp combine into a.attn.
 cudaError_t decode_attention(const DecodeArgs& a, cudaStream_t s);
 
+// Long chunks of new tokens (the tensor-core prefill attention over the
+// cache): positions pos[t] = start_pos[t / S] + t % S (0 and the
+// ST_BAD_START_POS bit for a chunk that does not fit the cache or the RoPE
+// table), and the chunk's rotated keys and values (qkv, bf16) written into
+// cache rows start_pos[b] .. start_pos[b] + S - 1.
+cudaError_t chunk_positions(const int32_t* start_pos, int n_seq, int S, int max_seq,
+                            int max_pos, int32_t* pos, int* status, cudaStream_t s);
+cudaError_t chunk_append(const __nv_bfloat16* qkv, int nqkv, int q_cols, int kv_cols,
+                         __nv_bfloat16* ck, __nv_bfloat16* cv, const int32_t* start_pos,
+                         int n_seq, int S, int max_seq, int max_pos, int sm_count,
+                         cudaStream_t s);
+
 size_t attn_decode_smem(int head_dim);
 int attn_decode_chunks(int max_seq);
 

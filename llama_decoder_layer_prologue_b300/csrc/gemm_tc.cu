@@ -147,9 +147,11 @@ __device__ __forceinline__ void epilogue_prefetch(EpiPre& pre, int row, bool val
                                                   int n0, int N, int part,
                                                   const TcEpiArgs& ep) {
   if (!valid) return;
-  if constexpr (EPI == TC_RESID_SS || EPI == TC_RESID) {
+  if constexpr (EPI == TC_RESID_SS || EPI == TC_RESID || EPI == TC_F32_DOT ||
+                EPI == TC_DO) {
     // every chunk of the part's 16-bit residual (bf16 x for TC_RESID_SS,
-    // the fp16 copy of h for TC_RESID)
+    // the fp16 copy of h for TC_RESID, h or x for TC_F32_DOT, the attention
+    // output for TC_DO)
     constexpr int RW = kResidWords;
     const int cb = chunk_begin<BN>(part);
 #pragma unroll
@@ -158,7 +160,7 @@ __device__ __forceinline__ void epilogue_prefetch(EpiPre& pre, int row, bool val
       if (col >= N) break;
       const size_t off = (size_t)row * ep.ldo + col;
       ld_words<RW>(static_cast<const uint16_t*>(ep.residual) + off, pre.w + k * RW,
-                   EPI == TC_RESID_SS ? ep.vec32 != 0 : true);
+                   EPI == TC_RESID ? true : ep.vec32 != 0);
     }
   } else if constexpr (EPI == TC_QKV) {
     pre.f = ep.rowscale ? ep.rowscale[row] : 1.f;
@@ -171,9 +173,33 @@ __device__ __forceinline__ void epilogue_prefetch(EpiPre& pre, int row, bool val
     const int half = ep.head_dim / 2;
     ld_words<32>(ep.cos_t + (size_t)p * half, pre.cs, true);
     ld_words<32>(ep.sin_t + (size_t)p * half, pre.sn, true);
-  } else if constexpr (EPI == TC_SWIGLU) {
+  } else if constexpr (EPI == TC_SWIGLU || EPI == TC_SWIGLU_BWD) {
     pre.f = ep.ss_in[row];
   }
+}
+
+// Column sums over the 32 rows of a warp: v[j] holds lane's value of column
+// j; afterwards v[0] of lane l holds the sum over all lanes of column l
+// (recursive halving: each step trades half of the remaining columns with
+// the lane `off` away, 31 shuffles in all).
+__device__ __forceinline__ void warp_column_sums(float* v, int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+}
+
+// Source row of packed gate|up row n (blocks of 256 packed rows: 128 gate
+// rows, then the 128 matching up rows).
+__device__ __forceinline__ int gate_up_row(int n, int inter) {
+  const int blk = n / 256, w = n % 256;
+  return w < 128 ? blk * 128 + w : inter + blk * 128 + (w - 128);
 }
 
 // Adds the other piece of a split tile (fp32 row `fin`) into this thread's
@@ -203,7 +229,8 @@ __device__ __forceinline__ void add_partial_tmem(uint32_t t_row, const float* fi
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool valid,
                                               int n0, int M, int N, int part,
-                                              const TcEpiArgs& ep, EpiPre& pre) {
+                                              const TcEpiArgs& ep, EpiPre& pre,
+                                              int lane) {
   if constexpr (EPI == TC_STORE || EPI == TC_RESID || EPI == TC_RESID_SS) {
     // unrolled over the part's chunks so that the residual registers of
     // every chunk stay in place (no copies that would wait on the loads)
@@ -312,9 +339,150 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
       int col = n0 / 2 + c * 32;
       if (valid && n0 < N) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          g[j] = silu(r2 * g[j]) * (r2 * u[j]) * ep.out_scale;
+        for (int j = 0; j < 32; ++j) {
+          g[j] *= r2;
+          u[j] *= r2;
+        }
+        if (ep.aux_out) {  // gate and up themselves, for the backward pass
+          const size_t o = (size_t)row * N + n0 + c * 32;
+          store_16x32(ep.aux_out, o, g, true, true);
+          store_16x32(ep.aux_out, o + 128, u, true, true);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) g[j] = silu(g[j]) * u[j] * ep.out_scale;
         store_16x32(ep.out, (size_t)row * ep.ldo + col, g, ep.out_f16, true);
+      }
+    }
+  } else if constexpr (EPI == TC_SWIGLU_BWD) {
+    // this part's 128 columns of d act are one packed gate|up block
+    const float r2 = valid ? rsqrtf(pre.f * ep.inv_h + ep.eps) : 0.f;
+    const int i0 = n0 + part * (BN / 2);
+    const int pb = (i0 / 128) * 256;  // first packed column of the block
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+      float da[32];
+      tmem_ld32(t_row + part * (BN / 2) + c * 32, da);
+      if (!valid || i0 >= N) continue;
+      const size_t o = (size_t)row * 2 * N + pb + c * 32;
+      uint32_t gw[16], uw[16];
+      ld_words<16>(static_cast<const __half*>(ep.aux_in) + o, gw, true);
+      ld_words<16>(static_cast<const __half*>(ep.aux_in) + o + 128, uw, true);
+      float dg_[32], du_[32];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float2 g2 = unpack_f16x2(gw[j]), u2 = unpack_f16x2(uw[j]);
+        const float gg[2] = {g2.x, g2.y}, uu[2] = {u2.x, u2.y};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float sg = 1.0f / (1.0f + __expf(-gg[e]));
+          const float a = da[2 * j + e] * ep.in_scale * r2 * ep.out_scale;
+          du_[2 * j + e] = a * gg[e] * sg;                                // silu(g)
+          dg_[2 * j + e] = a * uu[e] * sg * (1.0f + gg[e] * (1.0f - sg));  // silu'(g)
+        }
+      }
+      store_16x32(ep.out, o, dg_, true, true);
+      store_16x32(ep.out, o + 128, du_, true, true);
+    }
+  } else if constexpr (EPI == TC_F32_DOT) {
+    constexpr int RW = kResidWords;
+    float dot = 0.f;
+    const int cb = chunk_begin<BN>(part);
+#pragma unroll
+    for (int k = 0; k < BN / 64; ++k) {
+      const int c = cb + k;
+      const int col = n0 + c * 32;
+      float v[32];
+      tmem_ld32(t_row + c * 32, v);
+      if (valid && col < N) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 r = ep.res_bf16 ? unpack_bf16x2(pre.w[k * RW + j])
+                                       : unpack_f16x2(pre.w[k * RW + j]);
+          v[2 * j] *= ep.in_scale;
+          v[2 * j + 1] *= ep.in_scale;
+          dot = fmaf(v[2 * j], r.x, dot);
+          dot = fmaf(v[2 * j + 1], r.y, dot);
+        }
+        uint32_t u[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(v[j]);
+        st_words<32>(static_cast<float*>(ep.out) + (size_t)row * ep.ldo + col, u,
+                     ep.vec32 != 0);
+      }
+    }
+    if (valid) atomicAdd(ep.ss_out + row, dot * ep.res_scale);
+  } else if constexpr (EPI == TC_DO) {
+    constexpr int RW = kResidWords;
+    const int cb = chunk_begin<BN>(part);
+    float dot = 0.f;
+#pragma unroll
+    for (int k = 0; k < BN / 64; ++k) {
+      const int c = cb + k;
+      const int col = n0 + c * 32;
+      float v[32];
+      tmem_ld32(t_row + c * 32, v);
+      if (valid && col < N) {
+        uint32_t u[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          u[j] = pack_f16x2(v[2 * j] * ep.in_scale, v[2 * j + 1] * ep.in_scale);
+          const float2 d2 = unpack_f16x2(u[j]), o2 = unpack_f16x2(pre.w[k * RW + j]);
+          dot = fmaf(d2.x, o2.x, fmaf(d2.y, o2.y, dot));
+        }
+        st_words<16>(static_cast<__half*>(ep.out) + (size_t)row * ep.ldo + col, u, true);
+        if ((col + 32) % ep.head_dim == 0) {  // the head's last chunk
+          static_cast<float*>(ep.aux_out)[(size_t)row * (N / ep.head_dim) +
+                                          col / ep.head_dim] = dot;
+          dot = 0.f;
+        }
+      }
+    }
+  } else if constexpr (EPI == TC_DW) {
+    const int src = ep.inter > 0 ? gate_up_row(row, ep.inter) : row;
+    const int cb = chunk_begin<BN>(part);
+#pragma unroll 1
+    for (int k = 0; k < BN / 64; ++k) {
+      const int col = n0 + (cb + k) * 32;
+      float v[32];
+      tmem_ld32(t_row + (cb + k) * 32, v);
+      if (col >= N) continue;  // the same for every lane of the warp
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= ep.in_scale;
+      if (ep.dg) {
+        float p[32];
+        if (valid) {
+          uint32_t w[16];
+          ld_words<16>(static_cast<const __nv_bfloat16*>(ep.w_orig) +
+                           (size_t)src * ep.ldo + col, w, false);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float2 w2 = unpack_bf16x2(w[j]);
+            p[2 * j] = w2.x * v[2 * j];
+            p[2 * j + 1] = w2.y * v[2 * j + 1];
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) p[j] = 0.f;
+        }
+        warp_column_sums(p, lane);
+        atomicAdd(ep.dg + col + lane, p[0]);
+      }
+      if (valid) {
+        if (ep.colscale) {
+          uint32_t gsc[16];
+          ld_words<16>(static_cast<const __nv_bfloat16*>(ep.colscale) + col, gsc, false);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float2 g2 = unpack_bf16x2(gsc[j]);
+            v[2 * j] *= g2.x;
+            v[2 * j + 1] *= g2.y;
+          }
+        }
+        uint32_t u[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(v[j]);
+        st_words<32>(static_cast<float*>(ep.out) + (size_t)src * ep.ldo + col, u,
+                     ep.vec32 != 0);
       }
     }
   }
@@ -384,7 +552,34 @@ struct Sched {
   }
 };
 
-template <int BN, int STAGES, int EPI>
+// Shared-memory image of one operand K-slice (64 K values): K-major, one TMA
+// box of R rows x 128 bytes; MN-major (AMN / BMN), R / 64 boxes of 64 K-rows
+// x 64 MN values (128 bytes), 8 KB apart.  The matching descriptors: K-major
+// steps 32 bytes per K step of 16; MN-major steps 16 rows (2048 bytes) and
+// finds the next 64-wide MN block 8 KB away.
+template <bool MN, int R>
+__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* m,
+                                             uint64_t* bar, int kb, int r0) {
+  if constexpr (MN) {
+#pragma unroll
+    for (int i = 0; i < R / 64; ++i)
+      tma_load_2d(dst + i * 8192, m, bar, r0 + 64 * i, kb * BK);
+  } else {
+    tma_load_2d(dst, m, bar, kb * BK, r0);
+  }
+}
+
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t addr) {
+  return MN ? sdesc_mn128(addr, 8192) : sdesc_k128(addr);
+}
+
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_kstep(int k) {
+  return MN ? (uint64_t)(k * (2048 >> 4)) : (uint64_t)(2 * k);
+}
+
+template <int BN, int STAGES, int EPI, bool AMN = false, bool BMN = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
@@ -444,7 +639,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // requested before waiting for it.
       constexpr bool kWeightsA = EPI == TC_PARTIAL;
       uint32_t pre = 0;
-      {
+      if (kWeightsA || ep.b_const) {
         Sched s2 = sched;
         int pm, pn, pk0, pk1, pt, ps;
         if (s2.next(pm, pn, pk0, pk1, pt, ps)) {
@@ -452,9 +647,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint8_t* sa = smem + pre * L::STAGE;
             mbar_arrive_expect_tx(&full[pre], L::STAGE);
             if (kWeightsA)
-              tma_load_2d(sa, &tmA, &full[pre], kb * BK, pm * BM);
+              load_operand<AMN, BM>(sa, &tmA, &full[pre], kb, pm * BM);
             else
-              tma_load_2d(sa + L::A_BYTES, &tmB, &full[pre], kb * BK, pn * BN);
+              load_operand<BMN, BN>(sa + L::A_BYTES, &tmB, &full[pre], kb, pn * BN);
           }
         }
       }
@@ -468,13 +663,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sa = smem + stage * L::STAGE;
           if (issued < pre) {  // weights already requested, tx already armed
             if (kWeightsA)
-              tma_load_2d(sa + L::A_BYTES, &tmB, &full[stage], kb * BK, nt * BN);
+              load_operand<BMN, BN>(sa + L::A_BYTES, &tmB, &full[stage], kb, nt * BN);
             else
-              tma_load_2d(sa, &tmA, &full[stage], kb * BK, mt * BM);
+              load_operand<AMN, BM>(sa, &tmA, &full[stage], kb, mt * BM);
           } else {
             mbar_arrive_expect_tx(&full[stage], L::STAGE);
-            tma_load_2d(sa, &tmA, &full[stage], kb * BK, mt * BM);
-            tma_load_2d(sa + L::A_BYTES, &tmB, &full[stage], kb * BK, nt * BN);
+            load_operand<AMN, BM>(sa, &tmA, &full[stage], kb, mt * BM);
+            load_operand<BMN, BN>(sa + L::A_BYTES, &tmB, &full[stage], kb, nt * BN);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -496,7 +691,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     pdl_wait();
     if (lane == 0) {
-      const uint32_t idesc = ep.ab_f16 ? idesc_f16(BM, BN) : idesc_bf16(BM, BN);
+      const uint32_t idesc = (ep.ab_f16 ? idesc_f16(BM, BN) : idesc_bf16(BM, BN)) |
+                             (AMN ? 1u << 15 : 0u) | (BMN ? 1u << 16 : 0u);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t local = 0;
@@ -518,11 +714,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * L::STAGE);
-          const uint64_t ad = sdesc_k128(sa), bd = sdesc_k128(sa + L::A_BYTES);
+          const uint64_t ad = operand_desc<AMN>(sa),
+                         bd = operand_desc<BMN>(sa + L::A_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {  // a K step of 16 is 32 bytes
-            tc_mma_bf16_nc(d_tmem, ad + 2 * k, bd + 2 * k, idesc,
-                           (kb > kb0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < BK / 16; ++k) {
+            tc_mma_bf16_nc(d_tmem, ad + operand_kstep<AMN>(k), bd + operand_kstep<BMN>(k),
+                           idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           issued_any = true;
           tc_commit(&empty[stage]);
@@ -591,7 +788,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                abort_flag))
           add_partial_tmem<BN, EPI>(t_row, ep.sk_part + ((size_t)(blockIdx.x + 1) * BM + r) * BN,
                                part);
-        epilogue_tile<BN, EPI>(t_row, row, row < M, nt * BN, M, N, part, ep, pre);
+        epilogue_tile<BN, EPI>(t_row, row, row < M, nt * BN, M, N, part, ep, pre, lane);
         // every thread has read its rows: clear the flag for the next launch
         if (split && atomicAdd(&sk_count[1], 1) == kEpiWarps * 32 - 1)
           ep.sk_flag[blockIdx.x + 1] = 0;
@@ -610,18 +807,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, bool AMN = false, bool BMN = false>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
                    int K, const TcEpiArgs& ep, int grid, cudaStream_t s) {
   using L = Layout<BN, STAGES>;
-  auto kern = gemm_tc_kernel<BN, STAGES, EPI>;
+  auto kern = gemm_tc_kernel<BN, STAGES, EPI, AMN, BMN>;
   static std::atomic<uint64_t> attr_done{0};
   if (cudaError_t e = ensure_smem_attr(kern, (int)L::TOTAL, attr_done); e != cudaSuccess)
     return e;
   if (grid <= 0) return cudaSuccess;
   TcEpiArgs e = ep;
   const uintptr_t al = reinterpret_cast<uintptr_t>(e.out) |
-                       reinterpret_cast<uintptr_t>(e.residual);
+                       reinterpret_cast<uintptr_t>(e.residual) |
+                       reinterpret_cast<uintptr_t>(e.aux_in) |
+                       reinterpret_cast<uintptr_t>(e.aux_out);
   e.vec32 = (al & 31) == 0 && e.ldo % 16 == 0;
   if (!e.status) {
     cudaError_t err = cudaGetSymbolAddress((void**)&e.status, g_tc_status);
@@ -713,7 +912,7 @@ cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
   int grid = tiles < grid_limit ? tiles : grid_limit;
   TcEpiArgs e = ep;
   e.sk_tiles = 0;
-  if (epi != TC_PARTIAL && ep.sk_part && ep.sk_flag && ep.sk_epoch != 0)
+  if (epi <= TC_RESID && ep.sk_part && ep.sk_flag && ep.sk_epoch != 0)
     e.sk_tiles = tc_split_tiles(tiles, grid, (K + BK - 1) / BK);
   switch (epi) {
     case TC_STORE: return launch<256, 4, TC_STORE>(ta, tb, M, N, K, e, grid, s);
@@ -721,6 +920,12 @@ cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
     case TC_RESID_SS: return launch<256, 4, TC_RESID_SS>(ta, tb, M, N, K, e, grid, s);
     case TC_SWIGLU: return launch<256, 4, TC_SWIGLU>(ta, tb, M, N, K, e, grid, s);
     case TC_RESID: return launch<256, 4, TC_RESID>(ta, tb, M, N, K, e, grid, s);
+    case TC_DW: return launch<256, 4, TC_DW, true, true>(ta, tb, M, N, K, e, grid, s);
+    case TC_SWIGLU_BWD:
+      return launch<256, 4, TC_SWIGLU_BWD, false, true>(ta, tb, M, N, K, e, grid, s);
+    case TC_F32_DOT:
+      return launch<256, 4, TC_F32_DOT, false, true>(ta, tb, M, N, K, e, grid, s);
+    case TC_DO: return launch<256, 4, TC_DO, false, true>(ta, tb, M, N, K, e, grid, s);
     case TC_PARTIAL: {
       TcStreamK p = tc_streamk_plan(M, N, K, bn, grid_limit);
       if (p.slots != ep.part_slots) return cudaErrorInvalidValue;

@@ -16,6 +16,21 @@ enum TcEpi : int {
   TC_SWIGLU = 3,    // gate|up interleaved by 128: out = silu(r2 g) * (r2 u)
   TC_RESID = 4,     // out = res_scale * res (fp16) + in_scale * acc (bf16)
   TC_PARTIAL = 5,   // stream-K fp32 partials: part[tile][slot][bn][128]
+  // Backward-pass epilogues.  Their operands are not both K-major: TC_DW
+  // multiplies two activations that share the token dimension (A and B
+  // MN-major: A^T B over tokens), the others multiply an activation by a
+  // weight read along its output dimension (B MN-major: D = A W).
+  TC_DW = 6,        // fp32 out[src row][col] = in_scale * acc * colscale[col];
+                    // dg[col] += sum over rows of w_orig[src row][col] * that
+                    // value before colscale (src row: the gate/up interleave
+                    // undone when inter > 0)
+  TC_SWIGLU_BWD = 7,// acc = d act [T, I]; with gate / up from aux_in (fp16,
+                    // packed gate|up order) and r2 = 1 / RMS(h) from ss_in:
+                    // out (fp16, packed order) = r2 * (d gate | d up) * out_scale
+  TC_F32_DOT = 8,   // fp32 out = in_scale * acc; ss_out[m] += sum over the row
+                    // of out * res_scale * residual (fp16, or bf16 if res_bf16)
+  TC_DO = 9,        // fp16 out = in_scale * acc; aux_out[m * n_heads + head] =
+                    // sum over the head's columns of fp16(out) * residual (fp16)
 };
 
 struct TcEpiArgs {
@@ -40,6 +55,17 @@ struct TcEpiArgs {
   float res_scale = 1.f; // TC_RESID
   float out_scale = 1.f; // TC_SWIGLU: act stored * out_scale; TC_RESID_SS: h * out_scale
   int pdl = 0;           // launch with programmatic dependent launch
+  int b_const = 1;       // B never depends on an earlier kernel (weights): its
+                         // first K-slices may be loaded before the PDL wait
+  // backward-pass epilogues
+  const void* colscale = nullptr;  // TC_DW: bf16 [N] (null: 1)
+  const void* w_orig = nullptr;    // TC_DW: bf16 [rows, ldo] for dg (null: no dg)
+  float* dg = nullptr;             // TC_DW: fp32 [N], accumulated
+  int inter = 0;                   // TC_DW: undo the gate/up interleave of rows
+  const void* aux_in = nullptr;    // TC_SWIGLU_BWD: fp16 gate|up [M, 2 N] (packed)
+  void* aux_out = nullptr;         // TC_SWIGLU: fp16 gate|up [M, N] (packed), or
+                                   // null; TC_DO: fp32 [M, n_heads]
+  int res_bf16 = 0;                // TC_F32_DOT: the residual is bf16
   // Split tiles (whole-tile epilogues): when sk_part is set and the tiles do
   // not fill whole rounds of the grid, tc_gemm spreads the first
   // grid + (tiles % grid) tiles evenly over the CTAs by K-block.  A tile cut
@@ -83,7 +109,11 @@ __host__ __device__ inline int tc_streamk_segments(const TcStreamK& p, int t) {
 // tokens), stream-K over min(grid_limit, K-blocks) CTAs, ep.part_slots must
 // equal tc_streamk_plan(...).slots.  Other epilogues: bn = 256, whole tiles
 // over min(grid_limit, tiles) CTAs, with the split-tile phase when
-// tc_split_tiles() is nonzero and ep.sk_part is set.
+// tc_split_tiles() is nonzero and ep.sk_part is set (K-major epilogues only).
+// Operand maps: a K-major operand of R rows is tc_encode_bf16(map, ptr, R,
+// K, box) over its [R, K] storage (box 128 for A, bn for B); an MN-major
+// operand (TC_DW's A and B, the B of TC_SWIGLU_BWD / TC_F32_DOT / TC_DO) is
+// stored [K, R] and takes tc_encode_bf16(map, ptr, K, R, 64).
 cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
                     const CUtensorMap& tb, int M, int N, int K,
                     const TcEpiArgs& ep, int grid_limit, cudaStream_t s);

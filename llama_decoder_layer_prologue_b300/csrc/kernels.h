@@ -80,6 +80,20 @@ void simt_attention_decode(bool is_bf16, const void* qkv, const void* cache_k,
                            const int32_t* start_pos, int B, int max_seq,
                            const Dims& dm, cudaStream_t s);
 
+// ----------------------------------------------------------------- bwd_rows.cu
+// Row passes of the backward pass (bf16 layers; H a multiple of 8):
+// out = fp16(dout) [rows, H], z1 = z2 = 0 [rows].
+cudaError_t bwd_dout_f16(const void* dout, void* out, int rows, int H, float* z1,
+                         float* z2, int sm_count, cudaStream_t s);
+// dh = dout + u - h r2^2 dot / H with h = hg_scale * hg (fp16), r2 from the
+// row's sum of squares ss: dh32 fp32 and dh16 fp16 [rows, H].
+cudaError_t bwd_norm2(const void* dout, const float* u, const void* hg, float hg_scale,
+                      const float* ss, const float* dot, float eps, float* dh32,
+                      void* dh16, int rows, int H, cudaStream_t s);
+// dx = bf16(dh + r1 u - x r1^3 dot / H) [rows, H].
+cudaError_t bwd_norm1(const float* dh, const float* u, const void* x, const float* r1,
+                      const float* dot, void* dx, int rows, int H, cudaStream_t s);
+
 // ----------------------------------------------------------------- pack.cu
 // out[n, k] = W[src(n), k] * (g ? g[k] : 1), src(n) = n, or the gate/up
 // interleave in blocks of 128 when interleave_inter > 0.  out_f16 (bf16

@@ -12,6 +12,7 @@
 
 #include "../../include/llama_layer.h"
 #include "common.cuh"
+#include "attn_bwd.cuh"
 #include "attn_prefill.cuh"
 #include "decode.cuh"
 #include "gemm_tc.cuh"
@@ -216,9 +217,28 @@ void free_timing(llama_layer* L) {
   L->calls = 0;
 }
 
+// What the backward pass keeps from its forward recomputation beyond the
+// forward's own workspace: the attention's log2 softmax denominators and the
+// gate / up pre-activations.  With saves the forward stops after gate_up.
+struct FwdSaves {
+  float* lse;  // [T, n_heads]
+  void* gu;    // [T, 2 I] fp16, packed gate|up order
+};
+
+// A long chunk of S new tokens per sequence against the KV cache
+// (llama_layer_forward_cached with seq_tokens >= LLAMA_LONG_CHUNK): the
+// prefill path with positions start_pos[b] + i, the chunk's keys and values
+// appended to the cache, and the attention reading the cache.
+struct ChunkArgs {
+  void *cache_k, *cache_v;
+  const int32_t* start_pos;
+  int max_seq;
+};
+
 int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in,
                  const int32_t* cu, int n_seq, int seq_len, int T, char* ws,
-                 cudaStream_t s) {
+                 cudaStream_t s, const FwdSaves* sv = nullptr,
+                 const ChunkArgs* ch = nullptr) {
   const llama_layer_config& c = L->cfg;
   const Dims& dm = L->dm;
   const bool b16 = L->bf16;
@@ -237,8 +257,14 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
 
   begin_call(L);
   mark(L, s, "rmsnorm_stats");
-  launch_positions(cu, n_seq, seq_len, T, reinterpret_cast<int32_t*>(ws + w.pos),
-                   pos_in == nullptr, L->status, s);
+  if (ch) {
+    if (chunk_positions(ch->start_pos, n_seq, seq_len, ch->max_seq, dm.max_pos,
+                        reinterpret_cast<int32_t*>(ws + w.pos), L->status, s) != cudaSuccess)
+      return LLAMA_ERR_CUDA;
+  } else {
+    launch_positions(cu, n_seq, seq_len, T, reinterpret_cast<int32_t*>(ws + w.pos),
+                     pos_in == nullptr, L->status, s);
+  }
   if (b16)
     simt_row_norm_f16(x, T, dm.H, dm.eps, r1, ss2, ws + w.xn, s);
   else
@@ -266,12 +292,23 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.out = qkv; ep.ldo = dm.Nqkv; ep.pos = pos;
     ep.cos_t = cos_t; ep.sin_t = sin_t; ep.head_dim = dm.d;
     ep.rope_cols = (dm.Hq + dm.Hkv) * dm.d; ep.max_pos = dm.max_pos;
-    ep.out_f16 = 1;  // q | k | v in fp16 for the attention
+    // q | k | v in fp16 for the attention; bf16 for a cached chunk, whose
+    // keys and values join the bf16 cache the attention reads them from
+    ep.out_f16 = ch ? 0 : 1;
     mark(L, s, "qkv_rope");
     split(ep);
     e = tc_gemm(TC_QKV, 256, ta, L->tm_wqkv, T, dm.Nqkv, dm.H, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
     ++L->launches;
+    if (ch) {
+      mark(L, s, "cache_append");
+      if (chunk_append(static_cast<const __nv_bfloat16*>(qkv), dm.Nqkv, dm.Hq * dm.d,
+                       dm.Hkv * dm.d, static_cast<__nv_bfloat16*>(ch->cache_k),
+                       static_cast<__nv_bfloat16*>(ch->cache_v), ch->start_pos, n_seq,
+                       seq_len, ch->max_seq, dm.max_pos, L->sm_count, s) != cudaSuccess)
+        return LLAMA_ERR_CUDA;
+      ++L->launches;
+    }
     // a4 / a5: causal GQA attention (padded or varlen).
     AttnArgs aa;
     aa.qkv = static_cast<const __half*>(qkv);
@@ -279,9 +316,19 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     aa.cu = cu; aa.tokens = T; aa.seq_len = seq_len; aa.nqkv = dm.Nqkv;
     aa.n_heads = dm.Hq; aa.n_kv_heads = dm.Hkv; aa.head_dim = dm.d;
     aa.status = L->status;
+    if (sv) aa.lse = sv->lse;
     mark(L, s, "attention");
-    if (attn_prefill(aa, n_seq, seq_len, L->sm_count, s) != cudaSuccess)
+    if (ch) {
+      aa.cache_k = static_cast<const __nv_bfloat16*>(ch->cache_k);
+      aa.cache_v = static_cast<const __nv_bfloat16*>(ch->cache_v);
+      aa.start_pos = ch->start_pos;
+      aa.max_seq = ch->max_seq;
+      aa.max_pos = dm.max_pos;
+      if (attn_prefill_cached(aa, n_seq, L->sm_count, s) != cudaSuccess)
+        return LLAMA_ERR_CUDA;
+    } else if (attn_prefill(aa, n_seq, seq_len, L->sm_count, s) != cudaSuccess) {
       return LLAMA_ERR_CUDA;
+    }
     ++L->launches;
     // a7: o_proj + residual, row sums of h^2 for the second RMSNorm.
     if (!tc_encode_bf16(&ta, attn, T, dm.Hq * dm.d, 128)) return LLAMA_ERR_CUDA;
@@ -304,11 +351,13 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.pdl = 1;
     ep.out = act; ep.ldo = dm.I; ep.ss_in = ss2; ep.inv_h = 1.0f / dm.H; ep.eps = dm.eps;
     ep.ab_f16 = 1; ep.in_scale = 1.0f / kHgScale; ep.out_f16 = 1; ep.out_scale = kActScale;
+    if (sv) ep.aux_out = sv->gu;
     mark(L, s, "gate_up_swiglu");
     split(ep);
     e = tc_gemm(TC_SWIGLU, 256, ta, L->tm_wgu, T, 2 * dm.I, dm.H, ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
     ++L->launches;
+    if (sv) return cuda_err(cudaGetLastError());  // the backward continues from here
     // a9: down_proj + residual.
     if (!tc_encode_bf16(&ta, act, T, dm.I, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
@@ -339,6 +388,193 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
               nullptr, h, s);
     L->launches += 8;
   }
+  mark(L, s, nullptr);
+  return cuda_err(cudaGetLastError());
+}
+
+// Backward workspace: the forward's (recomputed) intermediates, then the
+// saves and the gradients of the intermediates.
+struct BwdLayout {
+  WsLayout fw;
+  size_t lse, dsum, gu, dout16, dgu, du, dot1, dot2, dh32, dh16, dattn, dqkv, total;
+};
+
+BwdLayout bwd_layout(const llama_layer_config& c, int tokens) {
+  BwdLayout b;
+  b.fw = ws_layout(c, tokens);
+  const size_t T = (size_t)(tokens > 0 ? tokens : 0);
+  const size_t H = c.hidden, I = c.intermediate, q = (size_t)c.n_heads * c.head_dim;
+  const size_t nqkv = (size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  size_t o = b.fw.total;
+  b.lse = o; o = align_up(o + T * c.n_heads * 4);
+  b.dsum = o; o = align_up(o + T * c.n_heads * 4);
+  b.gu = o; o = align_up(o + T * 2 * I * 2);
+  b.dout16 = o; o = align_up(o + T * H * 2);
+  b.dgu = o; o = align_up(o + T * 2 * I * 2);
+  b.du = o; o = align_up(o + T * H * 4);
+  b.dot1 = o; o = align_up(o + T * 4);
+  b.dot2 = o; o = align_up(o + T * 4);
+  b.dh32 = o; o = align_up(o + T * H * 4);
+  b.dh16 = o; o = align_up(o + T * H * 2);
+  b.dattn = o; o = align_up(o + T * q * 2);
+  b.dqkv = o; o = align_up(o + T * nqkv * 2);
+  b.total = o;
+  return b;
+}
+
+// Gradients of the prefill layer: the forward recomputed (keeping the
+// attention's softmax denominators and gate / up), then the chain rule in
+// reverse order of the forward's steps ("模型层" 9.6 LlamaForTraining puts
+// this layer under a loss; each step is stated in llama_layer.h).
+int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
+                  const void* dout, void* dx, const llama_layer_grads* gr,
+                  const int32_t* pos_in, const int32_t* cu, int n_seq, int seq_len,
+                  int T, char* ws, cudaStream_t s) {
+  const Dims& dm = L->dm;
+  const BwdLayout b = bwd_layout(L->cfg, T);
+  FwdSaves sv;
+  sv.lse = reinterpret_cast<float*>(ws + b.lse);
+  sv.gu = ws + b.gu;
+  int rc = forward_impl(L, x, nullptr, pos_in, cu, n_seq, seq_len, T, ws, s, &sv);
+  if (rc) return rc;
+  int launches = L->launches;
+  const WsLayout& f = b.fw;
+  const char* P = L->packed;
+  const int32_t* pos = pos_in ? pos_in : reinterpret_cast<const int32_t*>(ws + f.pos);
+  float* dot1 = reinterpret_cast<float*>(ws + b.dot1);
+  float* dot2 = reinterpret_cast<float*>(ws + b.dot2);
+  float* du = reinterpret_cast<float*>(ws + b.du);
+  const int qd = dm.Hq * dm.d;
+  const size_t H = dm.H;
+  auto fail = [](cudaError_t e) { return e != cudaSuccess; };
+  // the norm-weight gradients are sums over many tiles
+  if (fail(cudaMemsetAsync(gr->dg_in, 0, H * sizeof(float), s)) ||
+      fail(cudaMemsetAsync(gr->dg_post, 0, H * sizeof(float), s)))
+    return LLAMA_ERR_CUDA;
+  mark(L, s, "bwd_dout_f16");
+  if (fail(bwd_dout_f16(dout, ws + b.dout16, T, dm.H, dot1, dot2, L->sm_count, s)))
+    return LLAMA_ERR_CUDA;
+  ++launches;
+  // K-major [rows, cols] (box 128 rows) and MN-major [K rows, cols] (box 64)
+  auto kmaj = [](CUtensorMap* m, const void* p, int rows, int cols) {
+    return tc_encode_bf16(m, p, rows, cols, 128);
+  };
+  auto mnmaj = [](CUtensorMap* m, const void* p, int rows, int cols) {
+    return tc_encode_bf16(m, p, rows, cols, 64);
+  };
+  auto gemm = [&](int epi, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
+                  TcEpiArgs ep, const char* name) -> int {
+    ep.status = L->status;
+    ep.pdl = 1;
+    ep.ab_f16 = 1;
+    mark(L, s, name);
+    if (tc_gemm(epi, 256, ta, tb, M, N, K, ep, L->sm_count, s) != cudaSuccess)
+      return LLAMA_ERR_CUDA;
+    ++launches;
+    return LLAMA_OK;
+  };
+  CUtensorMap ta, tb;
+  // dW_down = dout^T act (act stored / 16)
+  if (!mnmaj(&ta, ws + b.dout16, T, dm.H) || !mnmaj(&tb, ws + f.act, T, dm.I))
+    return LLAMA_ERR_CUDA;
+  {
+    TcEpiArgs ep;
+    ep.out = gr->dw_down; ep.ldo = dm.I; ep.in_scale = 1.0f / kActScale; ep.b_const = 0;
+    if ((rc = gemm(TC_DW, ta, tb, dm.H, dm.I, T, ep, "bwd_dw_down"))) return rc;
+  }
+  // d act = dout W_down -> d gate | d up (times 1 / RMS(h)), packed order
+  if (!kmaj(&ta, ws + b.dout16, T, dm.H) || !mnmaj(&tb, P + L->pl.wd, dm.H, dm.I))
+    return LLAMA_ERR_CUDA;
+  {
+    TcEpiArgs ep;
+    ep.out = ws + b.dgu; ep.ldo = 2 * dm.I; ep.aux_in = ws + b.gu;
+    ep.ss_in = reinterpret_cast<const float*>(ws + f.ss2); ep.inv_h = 1.0f / dm.H;
+    ep.eps = dm.eps;
+    if ((rc = gemm(TC_SWIGLU_BWD, ta, tb, T, dm.I, dm.H, ep, "bwd_swiglu"))) return rc;
+  }
+  // dW_gate_up = dgu^T (h / RMS(h)) g_post, dg_post (h stored / 256)
+  if (!mnmaj(&ta, ws + b.dgu, T, 2 * dm.I) || !mnmaj(&tb, ws + f.hg, T, dm.H))
+    return LLAMA_ERR_CUDA;
+  {
+    TcEpiArgs ep;
+    ep.out = gr->dw_gate_up; ep.ldo = dm.H; ep.in_scale = 1.0f / kHgScale; ep.b_const = 0;
+    ep.colscale = w->g_post; ep.w_orig = w->w_gate_up; ep.dg = gr->dg_post; ep.inter = dm.I;
+    if ((rc = gemm(TC_DW, ta, tb, 2 * dm.I, dm.H, T, ep, "bwd_dw_gate_up"))) return rc;
+  }
+  // u2 = dgu W'_gate_up (the gradient of h / RMS(h), times 1 / RMS(h)), sum(u2 h)
+  if (!kmaj(&ta, ws + b.dgu, T, 2 * dm.I) || !mnmaj(&tb, P + L->pl.wgu, 2 * dm.I, dm.H))
+    return LLAMA_ERR_CUDA;
+  {
+    TcEpiArgs ep;
+    ep.out = du; ep.ldo = dm.H; ep.residual = ws + f.hg; ep.res_scale = 1.0f / kHgScale;
+    ep.ss_out = dot2;
+    if ((rc = gemm(TC_F32_DOT, ta, tb, T, dm.H, 2 * dm.I, ep, "bwd_dh_mlp"))) return rc;
+  }
+  mark(L, s, "bwd_norm2");
+  if (fail(bwd_norm2(dout, du, ws + f.hg, 1.0f / kHgScale,
+                     reinterpret_cast<const float*>(ws + f.ss2), dot2, dm.eps,
+                     reinterpret_cast<float*>(ws + b.dh32), ws + b.dh16, T, dm.H, s)))
+    return LLAMA_ERR_CUDA;
+  ++launches;
+  // dW_o = dh^T attn
+  if (!mnmaj(&ta, ws + b.dh16, T, dm.H) || !mnmaj(&tb, ws + f.attn, T, qd))
+    return LLAMA_ERR_CUDA;
+  {
+    TcEpiArgs ep;
+    ep.out = gr->dw_o; ep.ldo = qd; ep.b_const = 0;
+    if ((rc = gemm(TC_DW, ta, tb, dm.H, qd, T, ep, "bwd_dw_o"))) return rc;
+  }
+  // d attn = dh W_o, D = rowsum(d attn * attn) per head
+  if (!kmaj(&ta, ws + b.dh16, T, dm.H) || !mnmaj(&tb, P + L->pl.wo, dm.H, qd))
+    return LLAMA_ERR_CUDA;
+  {
+    TcEpiArgs ep;
+    ep.out = ws + b.dattn; ep.ldo = qd; ep.residual = ws + f.attn;
+    ep.aux_out = ws + b.dsum; ep.head_dim = dm.d;
+    if ((rc = gemm(TC_DO, ta, tb, T, qd, dm.H, ep, "bwd_dattn"))) return rc;
+  }
+  // attention backward -> dq | dk | dv (before RoPE)
+  {
+    AttnBwdArgs ab;
+    ab.qkv = reinterpret_cast<const __half*>(ws + f.qkv);
+    ab.dout = reinterpret_cast<const __half*>(ws + b.dattn);
+    ab.lse = reinterpret_cast<const float*>(ws + b.lse);
+    ab.dsum = reinterpret_cast<const float*>(ws + b.dsum);
+    ab.dqkv = reinterpret_cast<__half*>(ws + b.dqkv);
+    ab.cu = cu; ab.pos = pos;
+    ab.cos_t = reinterpret_cast<const float*>(P + L->pl.cos_t);
+    ab.sin_t = reinterpret_cast<const float*>(P + L->pl.sin_t);
+    ab.tokens = T; ab.seq_len = seq_len; ab.nqkv = dm.Nqkv; ab.n_heads = dm.Hq;
+    ab.n_kv_heads = dm.Hkv; ab.head_dim = dm.d; ab.max_pos = dm.max_pos;
+    ab.status = L->status;
+    mark(L, s, "bwd_attention");
+    if (attn_backward(ab, n_seq, seq_len, L->sm_count, s) != cudaSuccess)
+      return LLAMA_ERR_CUDA;
+    launches += 2;
+  }
+  // dW_qkv = dqkv^T (x / RMS(x)) g_in, dg_in
+  if (!mnmaj(&ta, ws + b.dqkv, T, dm.Nqkv) || !mnmaj(&tb, ws + f.xn, T, dm.H))
+    return LLAMA_ERR_CUDA;
+  {
+    TcEpiArgs ep;
+    ep.out = gr->dw_qkv; ep.ldo = dm.H; ep.b_const = 0;
+    ep.colscale = w->g_in; ep.w_orig = w->w_qkv; ep.dg = gr->dg_in;
+    if ((rc = gemm(TC_DW, ta, tb, dm.Nqkv, dm.H, T, ep, "bwd_dw_qkv"))) return rc;
+  }
+  // u1 = dqkv W'_qkv, sum(u1 x)
+  if (!kmaj(&ta, ws + b.dqkv, T, dm.Nqkv) || !mnmaj(&tb, P + L->pl.wqkv, dm.Nqkv, dm.H))
+    return LLAMA_ERR_CUDA;
+  {
+    TcEpiArgs ep;
+    ep.out = du; ep.ldo = dm.H; ep.residual = x; ep.res_bf16 = 1; ep.ss_out = dot1;
+    if ((rc = gemm(TC_F32_DOT, ta, tb, T, dm.H, dm.Nqkv, ep, "bwd_dx_attn"))) return rc;
+  }
+  mark(L, s, "bwd_norm1");
+  if (fail(bwd_norm1(reinterpret_cast<const float*>(ws + b.dh32), du, x,
+                     reinterpret_cast<const float*>(ws + f.r1), dot1, dx, T, dm.H, s)))
+    return LLAMA_ERR_CUDA;
+  ++launches;
+  L->launches = launches;
   mark(L, s, nullptr);
   return cuda_err(cudaGetLastError());
 }
@@ -712,6 +948,44 @@ int llama_layer_forward(llama_layer_t* L, const void* x, void* out,
                       static_cast<cudaStream_t>(stream));
 }
 
+int llama_layer_backward_workspace_bytes(const llama_layer_t* L, int max_tokens,
+                                         size_t* bytes) {
+  if (!L || !bytes || max_tokens < 0) return LLAMA_ERR_INVALID_ARG;
+  if (!L->bf16) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  *bytes = max_tokens > 0 ? bwd_layout(L->cfg, max_tokens).total : kAlign;
+  return LLAMA_OK;
+}
+
+int llama_layer_backward(llama_layer_t* L, const llama_layer_weights* w, const void* x,
+                         const void* dout, void* dx, const llama_layer_grads* gr,
+                         const int32_t* position_ids, const int32_t* cu_seqlens, int n_seq,
+                         int seq_len, int total_tokens, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (!L || !w || !x || !dout || !dx || !gr || total_tokens < 0) return LLAMA_ERR_INVALID_ARG;
+  if (!L->bf16) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  const void* in[7] = {x, dout, dx, w->w_qkv, w->w_gate_up, w->g_in, w->g_post};
+  for (const void* p : in)
+    if (!p || !aligned(p, 16)) return LLAMA_ERR_INVALID_ARG;
+  const void* out[6] = {gr->dw_qkv, gr->dw_o, gr->dw_gate_up, gr->dw_down, gr->dg_in,
+                        gr->dg_post};
+  for (const void* p : out)
+    if (!p || !aligned(p, 16)) return LLAMA_ERR_INVALID_ARG;
+  if (dx == x || dx == dout) return LLAMA_ERR_INVALID_ARG;
+  if (position_ids && !aligned(position_ids, 4)) return LLAMA_ERR_INVALID_ARG;
+  if (cu_seqlens && !aligned(cu_seqlens, 4)) return LLAMA_ERR_INVALID_ARG;
+  if (total_tokens == 0) return LLAMA_OK;
+  if (n_seq <= 0 || seq_len <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!cu_seqlens && (long)n_seq * seq_len != total_tokens) return LLAMA_ERR_INVALID_ARG;
+  if (cu_seqlens && (long)n_seq > total_tokens) return LLAMA_ERR_INVALID_ARG;
+  if (!position_ids && seq_len > L->cfg.max_position) return LLAMA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
+  if (workspace_bytes < bwd_layout(L->cfg, total_tokens).total)
+    return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+  return backward_impl(L, w, x, dout, dx, gr, position_ids, cu_seqlens, n_seq, seq_len,
+                       total_tokens, static_cast<char*>(workspace),
+                       static_cast<cudaStream_t>(stream));
+}
+
 namespace {
 
 int host_setup(llama_layer* L) {
@@ -843,6 +1117,17 @@ int llama_layer_forward_cached(llama_layer_t* L, const void* x, void* out,
   const long rows = (long)batch * seq_tokens;
   if (rows > (1L << 30)) return LLAMA_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
+  if (seq_tokens >= LLAMA_LONG_CHUNK) {
+    // the prefill path over the cache: each prefix is read once per head
+    // group rather than once per new token
+    if ((long)batch * max_seq > (1L << 31) - 1) return LLAMA_ERR_INVALID_ARG;
+    if (workspace_bytes < ws_layout(L->cfg, (int)rows).total)
+      return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+    ChunkArgs ch{cache_k, cache_v, start_pos, max_seq};
+    return forward_impl(L, x, out, nullptr, nullptr, batch, seq_tokens, (int)rows,
+                        static_cast<char*>(workspace), static_cast<cudaStream_t>(stream),
+                        nullptr, &ch);
+  }
   if (workspace_bytes < decode_ws_bytes(L, (int)rows, max_seq))
     return LLAMA_ERR_WORKSPACE_TOO_SMALL;
   if (!L->bf16 && (size_t)max_seq * sizeof(float) > 200 * 1024)

@@ -65,6 +65,9 @@ class LlamaLayer:
         self.handle = B.llama_layer_init(self.cfg, wts, self.packed.data_ptr(),
                                          nbytes, stream_ptr())
         self.workspace = torch.empty(0, dtype=torch.uint8, device=dev)
+        # the backward pass reads the weights as given (norm-weight gradients)
+        self.weights = ws
+        self._wts = wts
 
     @classmethod
     def from_numpy(cls, shape, weights, device="cuda") -> "LlamaLayer":
@@ -99,6 +102,40 @@ class LlamaLayer:
             n_seq, seq_len, T, self.workspace.data_ptr(),
             self.workspace.numel(), stream_ptr())
         return out
+
+    def backward(self, x, dout, position_ids=None, cu_seqlens=None, n_seq=None,
+                 seq_len=None, dx=None, grads=None):
+        """Gradients of the prefill layer given dL/d(out) (same batch layout
+        as forward): returns dict dx (bf16) and dw_qkv, dw_o, dw_gate_up,
+        dw_down, dg_in, dg_post (fp32, the weights' shapes)."""
+        T = x.shape[0]
+        if cu_seqlens is None:
+            seq_len = seq_len or T
+            n_seq = n_seq or (T // seq_len)
+        else:
+            n_seq = cu_seqlens.numel() - 1
+            assert seq_len is not None, "varlen needs max_seqlen"
+        n = B.llama_layer_backward_workspace_bytes(self.handle, T)
+        if self.workspace.numel() < n:
+            self.workspace = torch.empty(n, dtype=torch.uint8, device=self.device)
+        if dx is None:
+            dx = torch.empty_like(x)
+        if grads is None:
+            names = ("dw_qkv", "dw_o", "dw_gate_up", "dw_down", "dg_in", "dg_post")
+            srcs = (self.weights[0], self.weights[1], self.weights[2], self.weights[3],
+                    self.weights[4], self.weights[5])
+            grads = {k: torch.empty(w.shape, dtype=torch.float32, device=self.device)
+                     for k, w in zip(names, srcs)}
+        g = B.llama_layer_grads(*[grads[k].data_ptr() for k in
+                                  ("dw_qkv", "dw_o", "dw_gate_up", "dw_down", "dg_in",
+                                   "dg_post")])
+        B.llama_layer_backward(
+            self.handle, self._wts, x.data_ptr(), dout.data_ptr(), dx.data_ptr(), g,
+            position_ids.data_ptr() if position_ids is not None else None,
+            cu_seqlens.data_ptr() if cu_seqlens is not None else None,
+            n_seq, seq_len, T, self.workspace.data_ptr(), self.workspace.numel(),
+            stream_ptr())
+        return dict(dx=dx, **grads)
 
     def decode(self, x, cache_k, cache_v, start_pos, out=None):
         Bt = x.shape[0]

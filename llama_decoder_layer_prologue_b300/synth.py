@@ -27,6 +27,8 @@ Recipe (every workload):
     N(0, 1) values taken to be already-rotated keys / values; the other rows
     are zero here (tests poison them with NaN).  Chunked (seq_tokens > 1):
     start_pos ~ U{512..8192 - seq_tokens}, so every chunk ends in the cache.
+  * Backward pass: the incoming gradient dL/d(out) [T, hidden] ~ N(0, 1),
+    drawn from ``SeedSequence(5000 + workload index)`` (``make_dout``).
   * Model (stacked layers): x and the first layer's weights are the
     workload's own draws; layer l > 0 draws its weights as the same workload
     with index + 1000 l; the final RMSNorm weight ~ 1 + N(0, 0.1) and the
@@ -270,6 +272,15 @@ def make_inputs(w: Workload | str, with_cache: bool = True,
             cache_v = _make_cache(kids[9], w, start_pos)
     return LayerInputs(w, x, weights, positions, cu, start_pos, cache_k,
                        cache_v)
+
+
+def make_dout(inp: LayerInputs, scale: float = 1.0) -> np.ndarray:
+    """The incoming gradient of the backward pass, [T, hidden] ~ scale * N(0, 1)
+    in the workload's dtype (see the module docstring)."""
+    w = inp.workload
+    seed = np.random.SeedSequence(5000 + w.index)
+    return _fill_normal(seed, inp.tokens * w.shape.hidden, 0.0, scale,
+                        w.shape.dtype).reshape(inp.tokens, w.shape.hidden)
 
 
 def _make_cache(seed, w: Workload, start_pos):
