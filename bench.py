@@ -58,6 +58,12 @@ DESCRIPTIONS = {
     "model1b": "Llama-3.2-1B-shaped model forward bf16: 16 decoder layers (the "
                "1b layer shape, seeded weights per layer), final RMSNorm and the "
                "output projection to 128256 logits, batch 4 x seq 2048",
+    "chunk64": "chunked prefill with a KV cache, 8B-shaped layer bf16: 16 sequences x 64 "
+               "new tokens, start_pos U{512..8128} (seeded), cache [16, 8192, 8, 128] bf16 "
+               "(llama_layer_forward_cached, tensor-core attention over the cache)",
+    "chunk512": "chunked prefill with a KV cache, 8B-shaped layer bf16: 16 sequences x 512 "
+                "new tokens, start_pos U{512..7680} (seeded), cache [16, 8192, 8, 128] bf16 "
+                "(llama_layer_forward_cached, tensor-core attention over the cache)",
     "bwd_8b": "backward pass of the Llama-3-8B-shaped layer bf16 (llama_layer_backward: "
               "forward recomputed, then dx and the weight / norm gradients): batch 2 x "
               "seq 4096, dL/d(out) ~ N(0,1) seeded",
@@ -110,7 +116,7 @@ HEADLINE = "varlen"
 BACKWARD = {"bwd_8b": "8b", "bwd_1b": "1b"}  # backward workload -> its forward workload
 ALSO_AUTO = ("1b", "8b", "decode")
 
-DEFAULT_STEPS = {"bwd_8b": 200, "bwd_1b": 600, "tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
+DEFAULT_STEPS = {"chunk64": 1000, "chunk512": 300, "bwd_8b": 200, "bwd_1b": 600, "tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
                  "decode": 3000, "chunked": 1500, "model1b": 40}
 MODEL = {"model1b": ("1b", 16, 128256)}  # layer workload, layers, vocabulary
 
@@ -205,6 +211,20 @@ def algorithmic_work(inp) -> dict:
                     bytes={"rmsnorm_stats": float(T * H * es)}, weight_bytes=weights)
     sp = inp.start_pos.astype(np.float64)
     kv_read = float(np.sum(2.0 * sp * Hkv * d * es))
+    S = w.seq_tokens
+    if S >= 16:
+        # long chunks run the prefill kernels: a tensor-core workload (the
+        # prefix of each sequence read once per kv head, the attention over
+        # sp + i + 1 visible keys for new token i)
+        vis = float(np.sum(S * sp + S * (S + 1) / 2.0))
+        flops = {"qkv_rope": 2.0 * T * H * nqkv, "attention": 4.0 * d * Hq * vis,
+                 "o_proj_residual": 2.0 * T * q * H,
+                 "gate_up_swiglu": 2.0 * T * H * 2 * I,
+                 "down_residual": 2.0 * T * I * H}
+        return dict(kind="prefill", flops=flops, total_flops=sum(flops.values()),
+                    bytes={"rmsnorm_stats": float(T * H * es),
+                           "cache_append": float(2 * 2.0 * T * Hkv * d * es)},
+                    weight_bytes=weights, kv_read=kv_read)
     append = 2.0 * T * Hkv * d * es
     act = T * es * (2 * H + nqkv + q + H + 2 * I + I + H)  # x, qkv, o, h, act, out
     total = kv_read + append + weights + act

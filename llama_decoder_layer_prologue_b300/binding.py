@@ -31,6 +31,7 @@ LLAMA_ROPE_LLAMA3 = 1
 LLAMA_ROPE_LINEAR = 2
 LLAMA_ROPE_DYNAMIC_NTK = 3
 LLAMA_WS_NUM = 4
+LLAMA_LONG_CHUNK = 16
 LLAMA_MAX_STAGES = 16
 LLAMA_MAX_TIMED_CALLS = 4096
 

@@ -722,20 +722,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++k;
       const int kp = it.k0 + r;
       const bool kvalid = kp < it.L;
+      // lse and D of query row r of tile q (read one tile ahead, so the
+      // global loads overlap the previous tile's work)
+      auto fetch = [&](int q, float& lv, float& dv) {
+        int h0, q0;
+        k_item_tile(a, it, q, BP, h0, q0);
+        const int qp = q0 + r % BP, qh = h0 + r / BP;
+        const bool qv = qp < it.L;
+        const size_t qrow = (size_t)(it.a0 + (qv ? qp : 0)) * a.n_heads + qh;
+        lv = qv ? a.lse[qrow] : INFINITY;
+        dv = qv ? a.dsum[qrow] : 0.f;
+      };
+      float lse_next, dd_next;
+      fetch(0, lse_next, dd_next);
       for (int q = 0; q < it.nq; ++q, ++gi) {
         int h0, q0;
         k_item_tile(a, it, q, BP, h0, q0);
-        // lse and D of query row r of this tile into shared memory (double
-        // buffered: a thread writes buffer b again only after every thread
-        // has arrived for the tile in between, i.e. is done reading it)
+        // into shared memory (double buffered: a thread writes buffer b
+        // again only after every thread has arrived for the tile in
+        // between, i.e. is done reading it)
         {
           const int b = gi & 1;
-          const int qp = q0 + r % BP, qh = h0 + r / BP;
-          const bool qv = qp < it.L;
-          const size_t qrow = (size_t)(it.a0 + (qv ? qp : 0)) * a.n_heads + qh;
-          lse_s[b * AM + r] = qv ? a.lse[qrow] : INFINITY;
-          dd_s[b * AM + r] = qv ? a.dsum[qrow] : 0.f;
+          lse_s[b * AM + r] = lse_next;
+          dd_s[b * AM + r] = dd_next;
           mbar_arrive(&lse_ready[b]);
+          if (q + 1 < it.nq) fetch(q + 1, lse_next, dd_next);
         }
         if (!warp_wait(&lse_ready[gi & 1], (gi >> 1) & 1) || !warp_wait(s_full, gi & 1)) {
           ok = false;
@@ -744,20 +755,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float* ls = lse_s + (gi & 1) * AM;
         const float* ds = dd_s + (gi & 1) * AM;
-        float p[AM];
-#pragma unroll
-        for (int c = 0; c < AM / 32; ++c)
-          tmem_ld32_nowait(lane_base + L::S_COL + c * 32, p + c * 32);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < AM; ++c) tmem_pin(p[c]);
-        // query column c sits at position q0 + c % BP: key kp is visible to it
-        // when kp <= that position (lse = +inf past the sequence end)
-#pragma unroll
-        for (int c = 0; c < AM; ++c) {
-          const bool vis = kvalid && kp <= q0 + (c % BP);
-          p[c] = vis ? ex2(p[c] * scale - ls[c]) : 0.f;
-        }
         if constexpr (L::P_SEP) {  // P^T / dz^T columns free: previous products done
           if (!warp_wait(p_free, (gi & 1) ^ 1)) {
             ok = false;
@@ -765,22 +762,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
         }
-#pragma unroll
+        // query column c sits at position q0 + c % BP (BP a power of two):
+        // key kp is visible to it when kp <= that position; lse = +inf past
+        // the sequence end.  32 columns at a time: chunk h's P^T / dz^T land
+        // on columns 16 h .. 16 h + 15 of their region, which the in-place
+        // layout has already read (S^T / dP^T chunk h covers 32 h .. 32 h + 31)
+        const int rel = kvalid ? kp - q0 : AM;
+        const int bm = BP - 1;
+#pragma unroll 1
         for (int h = 0; h < AM / 32; ++h) {
+          float sv[32], dp[32];
+          tmem_ld32(lane_base + L::S_COL + h * 32, sv);
+          float p[32];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 l4 = reinterpret_cast<const float4*>(ls + h * 32)[e4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = h * 32 + e4 * 4 + e;
+              p[e4 * 4 + e] = ((c & bm) >= rel) ? ex2(sv[e4 * 4 + e] * scale - lv[e]) : 0.f;
+            }
+          }
           uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = pack_f16x2(p[h * 32 + 2 * e], p[h * 32 + 2 * e + 1]);
+          for (int e = 0; e < 16; ++e) w[e] = pack_f16x2(p[2 * e], p[2 * e + 1]);
           tmem_st16_words(lane_base + L::P_COL + h * 16, w);
-        }
-#pragma unroll
-        for (int h = 0; h < AM / 32; ++h) {
-          float dp[32];
           tmem_ld32(lane_base + L::DP_COL + h * 32, dp);
-          uint32_t w[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 d4 = reinterpret_cast<const float4*>(ds + h * 32)[e4];
+            dp[e4 * 4 + 0] -= d4.x;
+            dp[e4 * 4 + 1] -= d4.y;
+            dp[e4 * 4 + 2] -= d4.z;
+            dp[e4 * 4 + 3] -= d4.w;
+          }
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            w[e] = pack_f16x2(p[h * 32 + 2 * e] * (dp[2 * e] - ds[h * 32 + 2 * e]),
-                              p[h * 32 + 2 * e + 1] * (dp[2 * e + 1] - ds[h * 32 + 2 * e + 1]));
+            w[e] = pack_f16x2(p[2 * e] * dp[2 * e], p[2 * e + 1] * dp[2 * e + 1]);
           tmem_st16_words(lane_base + L::DZ_COL + h * 16, w);
         }
         tmem_wait_st();

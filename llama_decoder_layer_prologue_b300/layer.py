@@ -156,7 +156,9 @@ class LlamaLayer:
         rows = x.shape[0]
         assert rows % seq_tokens == 0, "x holds whole chunks"
         max_seq = cache_k.shape[1]
-        self.ensure_workspace(0, rows, max_seq)
+        # long chunks run the prefill kernels (prefill workspace layout)
+        long = seq_tokens >= B.LLAMA_LONG_CHUNK
+        self.ensure_workspace(rows if long else 0, rows, max_seq)
         if out is None:
             out = torch.empty_like(x)
         B.llama_layer_forward_cached(self.handle, x.data_ptr(), out.data_ptr(),

@@ -126,6 +126,11 @@ WORKLOADS = {
                        max_seq=8192, min_start=512),
     "chunked": Workload("chunked", 5, _SHAPE_8B, "decode", batch=16,
                         max_seq=8192, min_start=512, seq_tokens=4),
+    # long chunks: the tensor-core prefill attention reads the cache
+    "chunk64": Workload("chunk64", 6, _SHAPE_8B, "decode", batch=16,
+                        max_seq=8192, min_start=512, seq_tokens=64),
+    "chunk512": Workload("chunk512", 7, _SHAPE_8B, "decode", batch=16,
+                         max_seq=8192, min_start=512, seq_tokens=512),
 }
 
 

@@ -254,6 +254,24 @@ def test_forward_cached_chunks(S):
     check_cached(s, batch=5, S=S, max_seq=300, start_pos=[0, 123, 1, 300 - S, 77])
 
 
+@pytest.mark.parametrize("S,d,hq,hkv,max_seq,start_pos", [
+    # the shortest long chunk, an empty prefix, a chunk ending on the last row
+    (16, 64, 4, 2, 300, [0, 123, 1, 284, 77]),
+    (64, 64, 8, 2, 700, [0, 600, 257, 636]),
+    # a chunk that is not a multiple of the query tiles
+    (200, 128, 4, 1, 1000, [0, 799, 130]),
+    (512, 128, 8, 2, 1200, [0, 688, 300]),
+    # 8 query heads per kv head: 16 positions per 128-row tile
+    (64, 64, 8, 1, 500, [436, 5, 128]),
+])
+def test_forward_cached_long_chunks(S, d, hq, hkv, max_seq, start_pos):
+    """Chunks of at least LLAMA_LONG_CHUNK new tokens run the tensor-core
+    prefill attention over the cache; rows past each chunk are NaN and must
+    neither be written nor change the result."""
+    s = shape(128 * hq if d == 128 else 64 * hq, hq, hkv, d, 256, **L3)
+    check_cached(s, batch=len(start_pos), S=S, max_seq=max_seq, start_pos=start_pos)
+
+
 def test_forward_cached_pass_boundary_inside_a_sequence():
     # 40 x 7 = 280 rows: the 256-row passes split sequence 36 after 4 tokens
     s = shape(256, 4, 2, 64, 256, **L3)
