@@ -12,11 +12,12 @@
 // stored.  q, k, v, dO, P and dz are fp16 on the tensor cores (fp32
 // accumulation in tensor memory).
 //
-// Two tcgen05 kernels, each persistent (one CTA per SM), 6 warps:
-//   warps 0..3  thread r owns TMEM lane r: softmax recomputation, dz, and
-//               the final read-out of the accumulator with RoPE^T;
-//   warp 4      TMA producer;
-//   warp 5      allocates tensor memory; one elected lane issues tcgen05.mma.
+// Two tcgen05 kernels, each persistent (one CTA per SM), 10 warps:
+//   warps 0..7  two compute warpgroups: thread r of each owns TMEM lane r and
+//               one half of the tile's 128 columns (softmax recomputation,
+//               dz), and half of the accumulator's read-out with RoPE^T;
+//   warp 8      TMA producer;
+//   warp 9      allocates tensor memory; one elected lane issues tcgen05.mma.
 // attn_bwd_dq_kernel: a work item is one query tile (the forward's
 //   GQA-packed 128 rows: hpc heads x 128 / hpc positions); per key tile j of
 //   its causal range S = Q K_j^T and dP = dO V_j^T go to TMEM, the compute
@@ -39,8 +40,20 @@ namespace llama {
 namespace {
 
 constexpr int AM = 128;  // rows of a query tile (and keys of a key tile)
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
+// warps 0..7: two compute warpgroups, each on half of a tile's 128 columns
+// (warps w and w + 4 share TMEM lanes 32 (w % 4) ..); warp 8 TMA producer;
+// warp 9 MMA issuer
+constexpr int kThreads = 320;
+constexpr int kCompute = 256;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+
+// Bounded wait of this file's pipelines: the spinning form (a warp that
+// waits keeps polling), which measured faster here than the form that lets
+// the hardware suspend the warp between polls.
+__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, int* status,
+                                      volatile int* abort_flag) {
+  return mbar_wait(bar, parity, status, abort_flag);
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -220,11 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
-    mbar_init(dz_full, 128);
+    mbar_init(s_free, kCompute);
+    mbar_init(dz_full, kCompute);
     mbar_init(dz_free, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
+    mbar_init(dq_free, kCompute);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -249,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
         const QItem it = q_item(a, i, n_hg, n_seq, n_qb, BP);
         if (it.n_tiles == 0) continue;
-        if (k > 0 && !mbar_wait_sleep(q_empty, (k - 1) & 1, a.status, abort_flag)) {
+        if (k > 0 && !bwait(q_empty, (k - 1) & 1, a.status, abort_flag)) {
           ok = false;
           break;
         }
@@ -262,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kcol = (a.n_heads + it.g) * D, vcol = (a.n_heads + a.n_kv_heads + it.g) * D;
         for (int j = 0; j < it.n_tiles; ++j, ++n) {
           const int sl = n % L::SLOTS;
-          if (!mbar_wait_sleep(&kv_empty[sl], ((n / L::SLOTS) & 1) ^ 1, a.status,
+          if (!bwait(&kv_empty[sl], ((n / L::SLOTS) & 1) ^ 1, a.status,
                                abort_flag)) {
             ok = false;
             break;
@@ -278,9 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t m = n < (uint32_t)L::SLOTS ? n : (uint32_t)L::SLOTS;
         for (uint32_t j = 1; j <= m; ++j) {
           const uint32_t idx = n - j;
-          mbar_wait_sleep(&kv_full[idx % L::SLOTS], (idx / L::SLOTS) & 1, a.status, &own);
+          bwait(&kv_full[idx % L::SLOTS], (idx / L::SLOTS) & 1, a.status, &own);
         }
-        if (k > 0) mbar_wait_sleep(q_full, (k - 1) & 1, a.status, &own);
+        if (k > 0) bwait(q_full, (k - 1) & 1, a.status, &own);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -292,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t kmn_desc = sdesc_mn128(smem_u32(smem + L::KV_OFF), AM * 128);
     constexpr uint32_t PAIR16 = (2 * L::TILE) >> 4, TILE16 = L::TILE >> 4;
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait_sleep(b, parity, a.status, abort_flag));
+      return __all_sync(0xffffffffu, bwait(b, parity, a.status, abort_flag));
     };
     uint32_t g = 0, n = 0, k = 0;
     bool ok = true, issued_any = false;
@@ -359,16 +372,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int own = 0;
       if (elect_one()) tc_commit(drain);
       __syncwarp();
-      mbar_wait_sleep(drain, 0, a.status, &own);
+      bwait(drain, 0, a.status, &own);
     }
   } else {
     // ------------------------------------------------------------ compute
-    const int r = warp * 32 + lane;
-    const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
+    const int wq = warp & 3, wg = warp >> 2;  // lane quadrant, column half
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(wq * 32) << 16);
     const float scale = 1.4426950408889634f * rsqrtf((float)D);  // log2(e)/sqrt(d)
     auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
       int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait_sleep(b, parity, a.status, abort_flag);
+      if (lane == 0) w_ok = bwait(b, parity, a.status, abort_flag);
       return __shfl_sync(0xffffffffu, w_ok, 0) != 0;
     };
     uint32_t g = 0, k = 0;
@@ -388,16 +402,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        float p[AM];
+        // this warpgroup's keys: 64 wg .. 64 wg + 63 of the tile
+        float p[64];
 #pragma unroll
-        for (int c = 0; c < AM / 32; ++c)
-          tmem_ld32_nowait(lane_base + L::S_COL + c * 32, p + c * 32);
+        for (int c = 0; c < 2; ++c)
+          tmem_ld32_nowait(lane_base + L::S_COL + wg * 64 + c * 32, p + c * 32);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < AM; ++c) tmem_pin(p[c]);
-        const int lim = valid ? pos - j * AM : -1;  // keys 0 .. lim of the tile
+        for (int c = 0; c < 64; ++c) tmem_pin(p[c]);
+        const int lim = (valid ? pos - j * AM : -1) - wg * 64;  // keys 0 .. lim visible
 #pragma unroll
-        for (int c = 0; c < AM; ++c) p[c] = c <= lim ? ex2(p[c] * scale - lse) : 0.f;
+        for (int c = 0; c < 64; ++c) p[c] = c <= lim ? ex2(p[c] * scale - lse) : 0.f;
         // the dz columns are free once the previous dQ += dz K is done
         if (!warp_wait(dz_free, (g & 1) ^ 1)) {
           ok = false;
@@ -405,15 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < AM / 32; ++h) {
+        for (int h = 0; h < 2; ++h) {
           float dp[32];
-          tmem_ld32(lane_base + L::DP_COL + h * 32, dp);
+          tmem_ld32(lane_base + L::DP_COL + wg * 64 + h * 32, dp);
           uint32_t w[16];
 #pragma unroll
           for (int q = 0; q < 16; ++q)
             w[q] = pack_f16x2(p[h * 32 + 2 * q] * (dp[2 * q] - dd),
                               p[h * 32 + 2 * q + 1] * (dp[2 * q + 1] - dd));
-          tmem_st16_words(lane_base + L::DZ_COL + h * 16, w);
+          tmem_st16_words(lane_base + L::DZ_COL + wg * 32 + h * 16, w);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -421,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(dz_full);
       }
       if (!ok) break;
-      // ---- dq = dQ / sqrt(d), rotated back, fp16
+      // ---- dq = dQ / sqrt(d), rotated back, fp16 (32-column pairs shared
+      // out between the warpgroups)
       if (!warp_wait(dq_full, (k - 1) & 1)) {
         ok = false;
         break;
@@ -432,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __half* dst = a.dqkv + row * a.nqkv + head * D;
       const float sc = rsqrtf((float)D);
 #pragma unroll 1
-      for (int c = 0; c < half; c += 32) {
+      for (int c = wg * 32; c < half; c += 64) {
         float x1[32], x2[32];
         tmem_ld32_nowait(lane_base + L::DQ_COL + c, x1);
         tmem_ld32_nowait(lane_base + L::DQ_COL + half + c, x2);
@@ -473,6 +489,9 @@ struct DkvLayout {
   static constexpr uint32_t TOTAL = BAR_OFF + 256 + 1024;
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DK_COL = 256, DV_COL = 256 + D;
   static constexpr uint32_t P_COL = P_SEP ? 384 : 0, DZ_COL = P_SEP ? 448 : 128;
+  // P^T / dz^T of column half wg (queries 64 wg ..): their own 32 columns,
+  // or (in place) the first 32 of the 64 S^T / dP^T columns that half read
+  static constexpr uint32_t P_HALF = P_SEP ? 32 : 64;
   static_assert(DV_COL + D <= 512, "tensor memory budget");
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
@@ -546,13 +565,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
     mbar_init(s_full, 1);
-    mbar_init(s_free, L::P_SEP ? 128 : 1);
-    mbar_init(p_full, 128);
+    mbar_init(s_free, L::P_SEP ? kCompute : 1);
+    mbar_init(p_full, kCompute);
     mbar_init(p_free, 1);
     mbar_init(acc_full, 1);
-    mbar_init(acc_free, 128);
-    mbar_init(&lse_ready[0], 128);
-    mbar_init(&lse_ready[1], 128);
+    mbar_init(acc_free, kCompute);
+    mbar_init(&lse_ready[0], kCompute);
+    mbar_init(&lse_ready[1], kCompute);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -577,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
         const KItem it = k_item(a, i, n_seq, BP);
         if (it.nq == 0) continue;
-        if (k > 0 && !mbar_wait_sleep(kv_empty, (k - 1) & 1, a.status, abort_flag)) {
+        if (k > 0 && !bwait(kv_empty, (k - 1) & 1, a.status, abort_flag)) {
           ok = false;
           break;
         }
@@ -591,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           int h0, q0;
           k_item_tile(a, it, q, BP, h0, q0);
           const int sl = n % L::SLOTS;
-          if (!mbar_wait_sleep(&q_empty[sl], ((n / L::SLOTS) & 1) ^ 1, a.status,
+          if (!bwait(&q_empty[sl], ((n / L::SLOTS) & 1) ^ 1, a.status,
                                abort_flag)) {
             ok = false;
             break;
@@ -608,9 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t m = n < (uint32_t)L::SLOTS ? n : (uint32_t)L::SLOTS;
         for (uint32_t j = 1; j <= m; ++j) {
           const uint32_t idx = n - j;
-          mbar_wait_sleep(&q_full[idx % L::SLOTS], (idx / L::SLOTS) & 1, a.status, &own);
+          bwait(&q_full[idx % L::SLOTS], (idx / L::SLOTS) & 1, a.status, &own);
         }
-        if (k > 0) mbar_wait_sleep(kv_full, (k - 1) & 1, a.status, &own);
+        if (k > 0) bwait(kv_full, (k - 1) & 1, a.status, &own);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -622,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t qmn_desc = sdesc_mn128(smem_u32(smem + L::Q_OFF), AM * 128);
     constexpr uint32_t PAIR16 = (2 * L::TILE) >> 4, TILE16 = L::TILE >> 4;
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait_sleep(b, parity, a.status, abort_flag));
+      return __all_sync(0xffffffffu, bwait(b, parity, a.status, abort_flag));
     };
     uint32_t gi = 0, n = 0, k = 0;
     bool ok = true, issued_any = false;
@@ -670,9 +689,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < AM / 16; ++kk) {
             const uint32_t acc = (q > 0 || kk > 0) ? 1u : 0u;
-            tc_mma_ts(tmem_base + L::DV_COL, tmem_base + L::P_COL + kk * 8,
+            const uint32_t col = (kk / 4) * L::P_HALF + (kk % 4) * 8;  // queries 16 kk ..
+            tc_mma_ts(tmem_base + L::DV_COL, tmem_base + L::P_COL + col,
                       qb + TILE16 + kk * (2048 >> 4), idesc_acc, acc);
-            tc_mma_ts(tmem_base + L::DK_COL, tmem_base + L::DZ_COL + kk * 8,
+            tc_mma_ts(tmem_base + L::DK_COL, tmem_base + L::DZ_COL + col,
                       qb + kk * (2048 >> 4), idesc_acc, acc);
           }
           tc_commit(&q_empty[qn % L::SLOTS]);
@@ -702,16 +722,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int own = 0;
       if (elect_one()) tc_commit(drain);
       __syncwarp();
-      mbar_wait_sleep(drain, 0, a.status, &own);
+      bwait(drain, 0, a.status, &own);
     }
   } else {
     // ------------------------------------------------------------ compute
-    const int r = warp * 32 + lane;  // key row of the tile == TMEM lane
-    const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
+    const int wq = warp & 3, wg = warp >> 2;  // lane quadrant, query-column half
+    const int r = wq * 32 + lane;             // key row of the tile == TMEM lane
+    const uint32_t lane_base = tmem_base + ((uint32_t)(wq * 32) << 16);
     const float scale = 1.4426950408889634f * rsqrtf((float)D);
     auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
       int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait_sleep(b, parity, a.status, abort_flag);
+      if (lane == 0) w_ok = bwait(b, parity, a.status, abort_flag);
       return __shfl_sync(0xffffffffu, w_ok, 0) != 0;
     };
     uint32_t gi = 0, k = 0;
@@ -722,19 +743,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++k;
       const int kp = it.k0 + r;
       const bool kvalid = kp < it.L;
-      // lse and D of query row r of tile q (read one tile ahead, so the
-      // global loads overlap the previous tile's work)
-      auto fetch = [&](int q, float& lv, float& dv) {
+      // lse (warpgroup 0) or D (warpgroup 1) of query row r of tile q, read
+      // one tile ahead so the global loads overlap the previous tile's work
+      auto fetch = [&](int q) -> float {
         int h0, q0;
         k_item_tile(a, it, q, BP, h0, q0);
         const int qp = q0 + r % BP, qh = h0 + r / BP;
         const bool qv = qp < it.L;
         const size_t qrow = (size_t)(it.a0 + (qv ? qp : 0)) * a.n_heads + qh;
-        lv = qv ? a.lse[qrow] : INFINITY;
-        dv = qv ? a.dsum[qrow] : 0.f;
+        if (wg == 0) return qv ? a.lse[qrow] : INFINITY;
+        return qv ? a.dsum[qrow] : 0.f;
       };
-      float lse_next, dd_next;
-      fetch(0, lse_next, dd_next);
+      float next = fetch(0);
       for (int q = 0; q < it.nq; ++q, ++gi) {
         int h0, q0;
         k_item_tile(a, it, q, BP, h0, q0);
@@ -743,10 +763,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // between, i.e. is done reading it)
         {
           const int b = gi & 1;
-          lse_s[b * AM + r] = lse_next;
-          dd_s[b * AM + r] = dd_next;
+          (wg == 0 ? lse_s : dd_s)[b * AM + r] = next;
           mbar_arrive(&lse_ready[b]);
-          if (q + 1 < it.nq) fetch(q + 1, lse_next, dd_next);
+          if (q + 1 < it.nq) next = fetch(q + 1);
         }
         if (!warp_wait(&lse_ready[gi & 1], (gi >> 1) & 1) || !warp_wait(s_full, gi & 1)) {
           ok = false;
@@ -764,34 +783,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // query column c sits at position q0 + c % BP (BP a power of two):
         // key kp is visible to it when kp <= that position; lse = +inf past
-        // the sequence end.  32 columns at a time: chunk h's P^T / dz^T land
-        // on columns 16 h .. 16 h + 15 of their region, which the in-place
-        // layout has already read (S^T / dP^T chunk h covers 32 h .. 32 h + 31)
+        // the sequence end.  This warpgroup's 64 columns, 32 at a time: chunk
+        // h's P^T / dz^T land on columns 16 h .. 16 h + 15 of the half's
+        // region, which the in-place layout has already read (S^T / dP^T
+        // chunk h covers 32 h .. 32 h + 31 of the half)
         const int rel = kvalid ? kp - q0 : AM;
         const int bm = BP - 1;
 #pragma unroll 1
-        for (int h = 0; h < AM / 32; ++h) {
+        for (int h = 0; h < 2; ++h) {
+          const int c0 = wg * 64 + h * 32;  // first query column of the chunk
           float sv[32], dp[32];
-          tmem_ld32(lane_base + L::S_COL + h * 32, sv);
+          tmem_ld32(lane_base + L::S_COL + c0, sv);
           float p[32];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 l4 = reinterpret_cast<const float4*>(ls + h * 32)[e4];
+            const float4 l4 = reinterpret_cast<const float4*>(ls + c0)[e4];
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int c = h * 32 + e4 * 4 + e;
+              const int c = c0 + e4 * 4 + e;
               p[e4 * 4 + e] = ((c & bm) >= rel) ? ex2(sv[e4 * 4 + e] * scale - lv[e]) : 0.f;
             }
           }
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) w[e] = pack_f16x2(p[2 * e], p[2 * e + 1]);
-          tmem_st16_words(lane_base + L::P_COL + h * 16, w);
-          tmem_ld32(lane_base + L::DP_COL + h * 32, dp);
+          tmem_st16_words(lane_base + L::P_COL + wg * L::P_HALF + h * 16, w);
+          tmem_ld32(lane_base + L::DP_COL + c0, dp);
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 d4 = reinterpret_cast<const float4*>(ds + h * 32)[e4];
+            const float4 d4 = reinterpret_cast<const float4*>(ds + c0)[e4];
             dp[e4 * 4 + 0] -= d4.x;
             dp[e4 * 4 + 1] -= d4.y;
             dp[e4 * 4 + 2] -= d4.z;
@@ -800,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             w[e] = pack_f16x2(p[2 * e] * dp[2 * e], p[2 * e + 1] * dp[2 * e + 1]);
-          tmem_st16_words(lane_base + L::DZ_COL + h * 16, w);
+          tmem_st16_words(lane_base + L::DZ_COL + wg * L::P_HALF + h * 16, w);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -808,7 +829,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(p_full);
       }
       if (!ok) break;
-      // ---- dk (scaled, rotated back) and dv of the tile's keys
+      // ---- dk (scaled, rotated back) and dv of the tile's keys, 32-column
+      // pieces shared out between the warpgroups
       if (!warp_wait(acc_full, (k - 1) & 1)) {
         ok = false;
         break;
@@ -821,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __half* dv = a.dqkv + row * a.nqkv + (a.n_heads + a.n_kv_heads + it.g) * D;
       const float sc = rsqrtf((float)D);
 #pragma unroll 1
-      for (int c = 0; c < half; c += 32) {
+      for (int c = wg * 32; c < half; c += 64) {
         float x1[32], x2[32];
         tmem_ld32_nowait(lane_base + L::DK_COL + c, x1);
         tmem_ld32_nowait(lane_base + L::DK_COL + half + c, x2);
@@ -834,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kvalid) rope_back_store(a, tp, c, half, sc, x1, x2, dk);
       }
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = wg * 32; c < D; c += 64) {
         float v[32];
         tmem_ld32(lane_base + L::DV_COL + c, v);
         if (kvalid) store_f16x32(dv + c, v, 1.f);

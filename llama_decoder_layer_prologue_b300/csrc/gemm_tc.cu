@@ -23,7 +23,7 @@
 namespace llama {
 namespace {
 
-constexpr int BM = 128, BK = 64, GROUP_M = 16;
+constexpr int BM = 128, BK = 64;
 // warp 0 producer, warp 1 MMA, warps 2..9 epilogue (two per TMEM lane
 // quadrant, each on half of the tile's columns)
 constexpr int kEpiWarps = 8, kGemmThreads = 64 + 32 * kEpiWarps;
@@ -45,12 +45,14 @@ struct Layout {
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles,
+// Tile t of a whole-tile schedule visited in bands of group_m M-tiles (all
+// N-tiles of a band before the next band).
+__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int group_m,
                                             int& m, int& n) {
-  int group = GROUP_M * n_tiles;
+  int group = group_m * n_tiles;
   int g = t / group;
-  int first_m = g * GROUP_M;
-  int gm = min(m_tiles - first_m, GROUP_M);
+  int first_m = g * group_m;
+  int gm = min(m_tiles - first_m, group_m);
   int w = t - g * group;
   m = first_m + w % gm;
   n = w / gm;
@@ -490,7 +492,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
 
 // Work of one CTA as a sequence of segments (tile, K-blocks [kb0, kb1), slot).
 //   tile-stride mode: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...,
-//                     visited in bands of GROUP_M M-tiles.
+//                     visited in bands of group_m M-tiles (tc_group_m).
 //   split phase:      before those, the first sk_tiles tiles (in the same
 //                     order) are shared by K-block: the CTA owns units
 //                     [c W / G, (c + 1) W / G) of W = sk_tiles * kb_total, at
@@ -501,12 +503,13 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
 //                     run inside one tile is a segment whose fp32 partial goes
 //                     to slot (c - first CTA of that tile).
 struct Sched {
-  int m_tiles, n_tiles, kb_total, num_tiles, grid, cta;
+  int m_tiles, n_tiles, kb_total, num_tiles, grid, cta, group_m;
   bool stream_k;
   long long W, g, g_end;
   int next_tile;
 
-  __device__ Sched(int M, int N, int K, int bn, bool sk, int sk_tiles) {
+  __device__ Sched(int M, int N, int K, int bn, bool sk, int sk_tiles, int gm) {
+    group_m = gm;
     m_tiles = (M + BM - 1) / BM;
     n_tiles = (N + bn - 1) / bn;
     kb_total = (K + BK - 1) / BK;
@@ -537,13 +540,13 @@ struct Sched {
         nt = tile - mt * n_tiles;
       } else {
         slot = 0;
-        tile_coords(tile, m_tiles, n_tiles, mt, nt);
+        tile_coords(tile, m_tiles, n_tiles, group_m, mt, nt);
       }
       return true;
     }
     if (next_tile >= num_tiles) return false;
     tile = next_tile;
-    tile_coords(tile, m_tiles, n_tiles, mt, nt);
+    tile_coords(tile, m_tiles, n_tiles, group_m, mt, nt);
     kb0 = 0;
     kb1 = kb_total;
     slot = 0;
@@ -624,7 +627,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  Sched sched(M, N, K, BN, kStreamK, ep.sk_tiles);
+  Sched sched(M, N, K, BN, kStreamK, ep.sk_tiles, ep.group_m);
   int mt, nt, kb0, kb1, tile, slot;
 
   pdl_trigger();
@@ -894,6 +897,22 @@ TcStreamK tc_streamk_plan(int M, int N, int K, int bn, int grid_limit) {
   return p;
 }
 
+int tc_group_m(int M, int N, int K) {
+  // M-tiles per band: the band's A rows (group_m x 128 rows x K) are read
+  // from DRAM once and should stay in L2 while the band's B columns stream
+  // past them; up to 48 MB of A (of the 126 MB L2) per band, in powers of
+  // two between 16 and 64.  Measured on one B300 (gate_up, 100 steps each):
+  // 1B (K = 2048) 64 M-tiles 4.7 % faster than 16; 8B and the varlen pack
+  // (K = 4096) 32 M-tiles 2-2.5 % faster than 16, 64 slower; down_proj
+  // (K = 14336) 16 and 32 alike, 8 about 1 % slower.
+  (void)N;
+  const double a_tile = 128.0 * K * 2;
+  int g = 16;
+  while (g < 64 && 2 * g * a_tile <= 48.0 * (1 << 20)) g *= 2;
+  const int m_tiles = (M + BM - 1) / BM;
+  return g < m_tiles ? g : (m_tiles > 0 ? m_tiles : 1);
+}
+
 int tc_split_tiles(int tiles, int grid, int kb_total) {
   // a split costs a 128 KB store and reload per cut tile and one more
   // epilogue pass: worth it only behind a long main loop
@@ -912,6 +931,7 @@ cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
   int grid = tiles < grid_limit ? tiles : grid_limit;
   TcEpiArgs e = ep;
   e.sk_tiles = 0;
+  e.group_m = tc_group_m(M, N, K);
   if (epi <= TC_RESID && ep.sk_part && ep.sk_flag && ep.sk_epoch != 0)
     e.sk_tiles = tc_split_tiles(tiles, grid, (K + BK - 1) / BK);
   switch (epi) {

@@ -81,6 +81,7 @@ struct TcEpiArgs {
   uint32_t sk_epoch = 0;
   int sk_tiles = 0;      // set by tc_gemm: tiles of the split phase
   int vec32 = 0;         // set by tc_gemm: out / residual rows are 32-byte aligned
+  int group_m = 16;      // set by tc_gemm: M-tiles per band of the tile order
 };
 
 // Encodes a 2-D bf16 tensor map over a row-major [rows, cols] matrix with a
@@ -122,6 +123,10 @@ cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
 // pointer of their own write (bounded waits that ran out), on the current
 // device.  Synchronous with respect to the device (a plain memcpy).
 cudaError_t tc_take_status(int* word);
+
+// M-tiles per band of a whole-tile GEMM's tile order (tiles are visited band
+// by band, all N-tiles of a band in turn).
+int tc_group_m(int M, int N, int K);
 
 // Tiles of the split phase for a whole-tile GEMM of `tiles` tiles of
 // kb_total K-blocks on `grid` CTAs: grid + tiles % grid when the last round

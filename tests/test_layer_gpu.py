@@ -247,7 +247,7 @@ def check_cached(s, batch, S, max_seq, start_pos):
     layer.close()
 
 
-@pytest.mark.parametrize("S", [1, 3, 8])
+@pytest.mark.parametrize("S", [1, 3, 4, 8])
 def test_forward_cached_chunks(S):
     s = shape(256, 4, 2, 64, 256, **L3)
     # includes an empty prefix and a chunk ending on the last cache row
