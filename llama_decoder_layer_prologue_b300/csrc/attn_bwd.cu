@@ -47,12 +47,12 @@ constexpr int kThreads = 320;
 constexpr int kCompute = 256;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 
-// Bounded wait of this file's pipelines: the spinning form (a warp that
-// waits keeps polling), which measured faster here than the form that lets
-// the hardware suspend the warp between polls.
+// Bounded wait of this file's pipelines: the form that lets the hardware
+// suspend a waiting warp (a spinning form measured the same here and takes
+// issue slots from the compute warps).
 __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, int* status,
                                       volatile int* abort_flag) {
-  return mbar_wait(bar, parity, status, abort_flag);
+  return mbar_wait_sleep(bar, parity, status, abort_flag);
 }
 
 __device__ __forceinline__ float ex2(float x) {
