@@ -504,18 +504,24 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
 //                     to slot (c - first CTA of that tile).
 struct Sched {
   int m_tiles, n_tiles, kb_total, num_tiles, grid, cta, group_m;
+  int pair;  // CTA pairs: this CTA's rank (tiles 2 m + pair), else -1
   bool stream_k;
   long long W, g, g_end;
   int next_tile;
 
-  __device__ Sched(int M, int N, int K, int bn, bool sk, int sk_tiles, int gm) {
+  // pr >= 0: the grid runs as CTA pairs (clusters of 2) over pair tiles
+  // (M-tiles 2 m and 2 m + 1 of one N-tile); this CTA takes M-tile 2 m + pr.
+  __device__ Sched(int M, int N, int K, int bn, bool sk, int sk_tiles, int gm,
+                   int pr = -1) {
     group_m = gm;
+    pair = pr;
     m_tiles = (M + BM - 1) / BM;
+    if (pr >= 0) m_tiles = (m_tiles + 1) / 2;
     n_tiles = (N + bn - 1) / bn;
     kb_total = (K + BK - 1) / BK;
     num_tiles = m_tiles * n_tiles;
-    grid = gridDim.x;
-    cta = blockIdx.x;
+    grid = pr >= 0 ? gridDim.x / 2 : gridDim.x;
+    cta = pr >= 0 ? blockIdx.x / 2 : blockIdx.x;
     stream_k = sk;
     const int split = sk ? num_tiles : sk_tiles;
     W = (long long)split * kb_total;
@@ -547,6 +553,7 @@ struct Sched {
     if (next_tile >= num_tiles) return false;
     tile = next_tile;
     tile_coords(tile, m_tiles, n_tiles, group_m, mt, nt);
+    if (pair >= 0) mt = 2 * mt + pair;
     kb0 = 0;
     kb1 = kb_total;
     slot = 0;
@@ -572,6 +579,24 @@ __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* m,
   }
 }
 
+// B K-slice of a CTA pair: this CTA loads its half (rank r: N rows
+// n0 + R/2 r .., or 64-wide MN blocks 2 r, 2 r + 1) and multicasts it into the
+// same place of both CTAs' shared memory; the peer does the other half.  The
+// K-major map has an R/2-row box.
+template <bool MN, int R>
+__device__ __forceinline__ void load_b_pair(uint8_t* dst, const CUtensorMap* m,
+                                            uint64_t* bar, int kb, int n0, int rank) {
+  if constexpr (MN) {
+#pragma unroll
+    for (int i = 0; i < R / 128; ++i) {
+      const int blk = rank * (R / 128) + i;
+      tma_load_2d_mc(dst + blk * 8192, m, bar, n0 + 64 * blk, kb * BK, 0x3);
+    }
+  } else {
+    tma_load_2d_mc(dst + rank * (R / 2) * 128, m, bar, kb * BK, n0 + rank * (R / 2), 0x3);
+  }
+}
+
 template <bool MN>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t addr) {
   return MN ? sdesc_mn128(addr, 8192) : sdesc_k128(addr);
@@ -582,7 +607,11 @@ __device__ __forceinline__ uint64_t operand_kstep(int k) {
   return MN ? (uint64_t)(k * (2048 >> 4)) : (uint64_t)(2 * k);
 }
 
-template <int BN, int STAGES, int EPI, bool AMN = false, bool BMN = false>
+// MC: the grid runs as CTA pairs (clusters of 2) on pair tiles sharing
+// their B tile, each CTA loading half of every B K-slice and multicasting it
+// to both; a stage is free once both CTAs' MMAs are done with it (empty
+// barriers count a multicast commit from each).
+template <int BN, int STAGES, int EPI, bool AMN = false, bool BMN = false, bool MC = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
@@ -606,7 +635,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], MC ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -626,8 +655,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the peer's barriers are initialised before anything is multicast to it
+  uint32_t rank = 0;
+  if constexpr (MC) {
+    rank = cluster_ctarank();
+    cluster_sync();
+  }
 
-  Sched sched(M, N, K, BN, kStreamK, ep.sk_tiles, ep.group_m);
+  Sched sched(M, N, K, BN, kStreamK, ep.sk_tiles, ep.group_m, MC ? (int)rank : -1);
   int mt, nt, kb0, kb1, tile, slot;
 
   pdl_trigger();
@@ -651,6 +686,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_arrive_expect_tx(&full[pre], L::STAGE);
             if (kWeightsA)
               load_operand<AMN, BM>(sa, &tmA, &full[pre], kb, pm * BM);
+            else if constexpr (MC)
+              load_b_pair<BMN, BN>(sa + L::A_BYTES, &tmB, &full[pre], kb, pn * BN, rank);
             else
               load_operand<BMN, BN>(sa + L::A_BYTES, &tmB, &full[pre], kb, pn * BN);
           }
@@ -672,7 +709,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             mbar_arrive_expect_tx(&full[stage], L::STAGE);
             load_operand<AMN, BM>(sa, &tmA, &full[stage], kb, mt * BM);
-            load_operand<BMN, BN>(sa + L::A_BYTES, &tmB, &full[stage], kb, nt * BN);
+            if constexpr (MC)
+              load_b_pair<BMN, BN>(sa + L::A_BYTES, &tmB, &full[stage], kb, nt * BN, rank);
+            else
+              load_operand<BMN, BN>(sa + L::A_BYTES, &tmB, &full[stage], kb, nt * BN);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -688,6 +728,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (uint32_t j = 1; j <= n; ++j) {
           uint32_t idx = issued - j;
           mbar_wait(&full[idx % STAGES], (idx / STAGES) & 1, ep.status, &own);
+        }
+      } else if constexpr (MC) {
+        // the peer's MMA commits to this CTA's empty barriers (its last ones
+        // included) have landed before this CTA may leave
+        uint32_t n = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
+        for (uint32_t j = 1; j <= n; ++j) {
+          uint32_t idx = issued - j;
+          mbar_wait(&empty[idx % STAGES], (idx / STAGES) & 1, ep.status, abort_flag);
         }
       }
     }
@@ -725,7 +773,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                            idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           issued_any = true;
-          tc_commit(&empty[stage]);
+          if constexpr (MC)
+            tc_commit_mc(&empty[stage], 0x3);  // both CTAs read this stage's B
+          else
+            tc_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -808,13 +859,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
+  // neither CTA of a pair leaves while the other may still write to it
+  if constexpr (MC) cluster_sync();
 }
 
-template <int BN, int STAGES, int EPI, bool AMN = false, bool BMN = false>
+template <int BN, int STAGES, int EPI, bool AMN = false, bool BMN = false, bool MC = false>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
                    int K, const TcEpiArgs& ep, int grid, cudaStream_t s) {
   using L = Layout<BN, STAGES>;
-  auto kern = gemm_tc_kernel<BN, STAGES, EPI, AMN, BMN>;
+  auto kern = gemm_tc_kernel<BN, STAGES, EPI, AMN, BMN, MC>;
   static std::atomic<uint64_t> attr_done{0};
   if (cudaError_t e = ensure_smem_attr(kern, (int)L::TOTAL, attr_done); e != cudaSuccess)
     return e;
@@ -828,6 +881,36 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
   if (!e.status) {
     cudaError_t err = cudaGetSymbolAddress((void**)&e.status, g_tc_status);
     if (err != cudaSuccess) return err;
+  }
+  if constexpr (MC) {
+    // pairs: grid = 2 x (pairs that can be resident at once, at most the
+    // pair tiles)
+    static int max_pairs[64] = {};
+    int dev = 0;
+    if (cudaError_t err = cudaGetDevice(&dev); err != cudaSuccess) return err;
+    int pairs = dev < 64 ? max_pairs[dev] : 0;
+    if (pairs <= 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(kGemmThreads);
+      cfg.dynamicSmemBytes = L::TOTAL;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      if (cudaError_t err = cudaOccupancyMaxActiveClusters(&pairs, kern, &cfg);
+          err != cudaSuccess)
+        return err;
+      if (pairs <= 0) return cudaErrorInvalidConfiguration;
+      if (dev < 64) max_pairs[dev] = pairs;
+    }
+    const int pair_tiles = grid;  // tc_gemm passes the pair tiles
+    const int n = pair_tiles < pairs ? pair_tiles : pairs;
+    return launch_cluster2(kern, dim3(2 * n), dim3(kGemmThreads), L::TOTAL, s, e.pdl != 0,
+                           ta, tb, M, N, K, e);
   }
   // the split phase's CTAs wait on flags other CTAs set: make them co-resident
   if (e.sk_tiles > 0)
@@ -932,6 +1015,28 @@ cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
   TcEpiArgs e = ep;
   e.sk_tiles = 0;
   e.group_m = tc_group_m(M, N, K);
+  if (ep.pair && epi != TC_PARTIAL) {
+    // CTA pairs over pair tiles (two M-tiles of one N-tile), bands of
+    // group_m M-tiles = group_m / 2 pair rows
+    e.group_m = e.group_m / 2 > 0 ? e.group_m / 2 : 1;
+    const int pair_tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + bn - 1) / bn);
+    switch (epi) {
+      case TC_QKV: return launch<256, 4, TC_QKV, false, false, true>(ta, tb, M, N, K, e, pair_tiles, s);
+      case TC_RESID_SS:
+        return launch<256, 4, TC_RESID_SS, false, false, true>(ta, tb, M, N, K, e, pair_tiles, s);
+      case TC_SWIGLU:
+        return launch<256, 4, TC_SWIGLU, false, false, true>(ta, tb, M, N, K, e, pair_tiles, s);
+      case TC_RESID:
+        return launch<256, 4, TC_RESID, false, false, true>(ta, tb, M, N, K, e, pair_tiles, s);
+      case TC_DW: return launch<256, 4, TC_DW, true, true, true>(ta, tb, M, N, K, e, pair_tiles, s);
+      case TC_SWIGLU_BWD:
+        return launch<256, 4, TC_SWIGLU_BWD, false, true, true>(ta, tb, M, N, K, e, pair_tiles, s);
+      case TC_F32_DOT:
+        return launch<256, 4, TC_F32_DOT, false, true, true>(ta, tb, M, N, K, e, pair_tiles, s);
+      case TC_DO: return launch<256, 4, TC_DO, false, true, true>(ta, tb, M, N, K, e, pair_tiles, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (epi <= TC_RESID && ep.sk_part && ep.sk_flag && ep.sk_epoch != 0)
     e.sk_tiles = tc_split_tiles(tiles, grid, (K + BK - 1) / BK);
   switch (epi) {
