@@ -84,7 +84,11 @@ STAGE_SOURCES = {
     "attention": ["attn_prefill.cu", "attn_prefill.cuh", "common.cuh"],
     # the decode / chunked workloads' attention is the split-KV kernel
     "attention_decode": ["decode.cu", "decode.cuh", "common.cuh"],
+    "bwd_attention": ["attn_bwd.cu", "attn_bwd.cuh", "common.cuh"],
 }
+for _s in ("bwd_dw_down", "bwd_swiglu", "bwd_dw_gate_up", "bwd_dh_mlp", "bwd_dw_o",
+           "bwd_dattn", "bwd_dw_qkv", "bwd_dx_attn"):
+    STAGE_SOURCES[_s] = STAGE_SOURCES["gate_up_swiglu"]
 
 
 # ----------------------------------------------------------------- helpers
@@ -114,7 +118,7 @@ def parse_args():
 
 HEADLINE = "varlen"
 BACKWARD = {"bwd_8b": "8b", "bwd_1b": "1b"}  # backward workload -> its forward workload
-ALSO_AUTO = ("1b", "8b", "decode")
+ALSO_AUTO = ("1b", "8b", "decode", "bwd_8b", "chunk512")
 
 DEFAULT_STEPS = {"chunk64": 1000, "chunk512": 300, "bwd_8b": 200, "bwd_1b": 600, "tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
                  "decode": 3000, "chunked": 1500, "model1b": 40}

@@ -78,6 +78,7 @@ def test_headline_also_runs_the_other_layer_workloads():
     ns = lambda **kw: argparse.Namespace(**{"workload": bench.HEADLINE, "also": "auto",
                                            **kw})
     assert bench.also_list(ns()) == list(bench.ALSO_AUTO)
+    assert "bwd_8b" in bench.ALSO_AUTO and "decode" in bench.ALSO_AUTO
     assert bench.also_list(ns(workload="1b")) == []
     assert bench.also_list(ns(also="none")) == []
     assert bench.also_list(ns(also="8b,varlen")) == ["8b"]
