@@ -155,6 +155,20 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float b, float c) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(x));
 }
 
+// 2^x of both halves of an fp16 pair (the SFU's packed form: two results per
+// instruction).
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
+  uint32_t y;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+  return y;
+}
+
 // (s0, s1) += (a0, a1)
 __device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
   uint64_t x, y;
@@ -469,16 +483,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
         }
         const float mref = m == -INFINITY ? 0.f : m;
-        // p = 2^(s * scale - m) (paired fp32 FMA), 8 independent partial sums
-        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // p = 2^(s * scale - m): the exponent in fp32 (paired FMA); fp16 P
+        // (the fp16 q|k|v path) takes it as an fp16 pair through the packed
+        // SFU exp2, two results per instruction, and sums the fp16 values
+        // the P V product uses (eight fp16 pair partial sums of 8 pairs,
+        // then fp32); bf16 P (a cached chunk) stays in fp32 throughout
+        uint32_t pw[AN / 2];
+        if constexpr (!CACHED) {
+          uint32_t hs[8];
 #pragma unroll
-        for (int c = 0; c < AN; c += 2) {
-          fma2(s[c], s[c + 1], scale, -mref);
-          s[c] = ex2(s[c]);
-          s[c + 1] = ex2(s[c + 1]);
-          add2(ps[c & 7], ps[(c & 7) + 1], s[c], s[c + 1]);
+          for (int c = 0; c < AN; c += 2) {
+            fma2(s[c], s[c + 1], scale, -mref);
+            pw[c / 2] = ex2_f16x2(pack_f16x2(s[c], s[c + 1]));
+            const int a8 = (c / 2) & 7;
+            hs[a8] = c < 16 ? pw[c / 2] : hadd2_u32(hs[a8], pw[c / 2]);
+          }
+          float lt = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float2 f = unpack_f16x2(hs[e]);
+            lt += f.x + f.y;
+          }
+          l += lt;
+        } else {
+          float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < AN; c += 2) {
+            fma2(s[c], s[c + 1], scale, -mref);
+            s[c] = ex2(s[c]);
+            s[c + 1] = ex2(s[c + 1]);
+            add2(ps[c & 7], ps[(c & 7) + 1], s[c], s[c + 1]);
+            pw[c / 2] = pack_p<CACHED>(s[c], s[c + 1]);
+          }
+          l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         }
-        l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         // This tile's P buffer and O are free once its previous P V is done
         // (for the first tile of an item the epilogue already waited).
         if (j > 0) {
@@ -503,23 +541,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P as fp16 pairs into this row's TMEM lane (the P V A operand)
           const uint32_t p_tmem = lane_base + L::P_COL + t * (AN / 2);
 #pragma unroll
-          for (int h = 0; h < AN / 32; ++h) {
-            uint32_t w[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-              w[q] = pack_p<CACHED>(s[h * 32 + 2 * q], s[h * 32 + 2 * q + 1]);
-            tmem_st16_words(p_tmem + h * 16, w);
-          }
+          for (int h = 0; h < AN / 32; ++h) tmem_st16_words(p_tmem + h * 16, pw + h * 16);
           tmem_wait_st();
         } else {
           // P as fp16 into the 128-byte swizzled A tile
 #pragma unroll
           for (int c16 = 0; c16 < AN / 8; ++c16) {
             uint4 u;
-            u.x = pack_p<CACHED>(s[c16 * 8 + 0], s[c16 * 8 + 1]);
-            u.y = pack_p<CACHED>(s[c16 * 8 + 2], s[c16 * 8 + 3]);
-            u.z = pack_p<CACHED>(s[c16 * 8 + 4], s[c16 * 8 + 5]);
-            u.w = pack_p<CACHED>(s[c16 * 8 + 6], s[c16 * 8 + 7]);
+            u.x = pw[c16 * 4 + 0];
+            u.y = pw[c16 * 4 + 1];
+            u.z = pw[c16 * 4 + 2];
+            u.w = pw[c16 * 4 + 3];
             const int atom = c16 / 8, cc = c16 % 8;
             *reinterpret_cast<uint4*>(prow + atom * (AM * 128) + ((cc ^ (r & 7)) << 4)) = u;
           }
