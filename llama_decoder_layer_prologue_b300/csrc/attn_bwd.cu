@@ -13,21 +13,26 @@
 // accumulation in tensor memory).
 //
 // Two tcgen05 kernels, each persistent (one CTA per SM), 10 warps:
-//   warps 0..7  two compute warpgroups: thread r of each owns TMEM lane r and
-//               one half of the tile's 128 columns (softmax recomputation,
-//               dz), and half of the accumulator's read-out with RoPE^T;
+//   warps 0..7  compute: thread r of warp w owns TMEM lane r (32 (w % 4) + lane)
+//               and 32 of each half tile's 64 columns (warps 0..3 the first,
+//               4..7 the second): softmax recomputation and dz, then half of
+//               the accumulator's read-out with RoPE^T;
 //   warp 8      TMA producer;
 //   warp 9      allocates tensor memory; one elected lane issues tcgen05.mma.
+// A 128 x 128 tile is handled as two halves of 64 columns: the compute warps
+// work through half 0 and then half 1, and the tensor core runs the products
+// of one half while they work on the other.
 // attn_bwd_dq_kernel: a work item is one query tile (the forward's
 //   GQA-packed 128 rows: hpc heads x 128 / hpc positions); per key tile j of
 //   its causal range S = Q K_j^T and dP = dO V_j^T go to TMEM, the compute
-//   warps turn them into dz (fp16, back into TMEM), and dQ += dz K_j reads
-//   dz from TMEM as the A operand and K_j as an MN-major B operand.
+//   warps turn them into dz (fp16, into TMEM), and dQ += dz K_j reads dz from
+//   TMEM as the A operand and K_j as an MN-major B operand.
 // attn_bwd_dkv_kernel: a work item is one key tile (128 keys of one kv
 //   head); per query tile i of every query head of the group that sees it,
 //   S^T = K Q_i^T and dP^T = V dO_i^T go to TMEM, the compute warps form P^T
-//   and dz^T (fp16, back into TMEM), and dV += P^T dO_i, dK += dz^T Q_i
-//   accumulate the whole group in TMEM (no atomics, no repeat_kv).
+//   and dz^T (fp16, over the S^T / dP^T columns they read), and
+//   dV += P^T dO_i, dK += dz^T Q_i accumulate the whole group in TMEM (no
+//   atomics, no repeat_kv).
 // Every wait is bounded (2 s -> status bit, abort, drain, free TMEM).
 #include <cuda_fp16.h>
 #include <math.h>
@@ -40,9 +45,8 @@ namespace llama {
 namespace {
 
 constexpr int AM = 128;  // rows of a query tile (and keys of a key tile)
-// warps 0..7: two compute warpgroups, each on half of a tile's 128 columns
-// (warps w and w + 4 share TMEM lanes 32 (w % 4) ..); warp 8 TMA producer;
-// warp 9 MMA issuer
+// warps 0..7 compute (warps w and w + 4 share TMEM lanes 32 (w % 4) ..);
+// warp 8 TMA producer; warp 9 MMA issuer
 constexpr int kThreads = 320;
 constexpr int kCompute = 256;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
@@ -53,12 +57,6 @@ constexpr int kProducerWarp = 8, kMmaWarp = 9;
 __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, int* status,
                                       volatile int* abort_flag) {
   return mbar_wait_sleep(bar, parity, status, abort_flag);
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 
 int heads_per_tile(int n_rep) {
@@ -162,6 +160,12 @@ __device__ __forceinline__ uint32_t kmajor_step(int kk) {
 }
 
 // =================================================================== dQ
+// Tensor memory of the dQ kernel: S [0, 128), dP [128, 256), dQ [256,
+// 256 + D), dz as fp16 pairs [256 + D, 320 + D).  A key tile is handled as
+// two halves of 64 keys (S / dP columns 64 h ..; dz columns 32 h ..): every
+// compute warp works through half 0 and then half 1, so that the tensor core
+// runs one half's products (dQ += dz K and the next tile's S, dP) while the
+// compute warps work on the other.
 template <int D>
 struct DqLayout {
   static constexpr uint32_t TILE = AM * D * 2;
@@ -169,8 +173,6 @@ struct DqLayout {
   static constexpr uint32_t Q_OFF = 0, DO_OFF = TILE, KV_OFF = 2 * TILE;
   static constexpr uint32_t BAR_OFF = KV_OFF + SLOTS * 2 * TILE;
   static constexpr uint32_t TOTAL = BAR_OFF + 256 + 1024;
-  // TMEM: S [0, 128), dP [128, 256), dQ [256, 256 + D), dz as fp16 pairs
-  // [256 + D, 320 + D)
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256, DZ_COL = 256 + D;
   static_assert(DZ_COL + 64 <= 512, "tensor memory budget");
   static_assert(TOTAL <= 232448, "shared memory budget");
@@ -198,6 +200,26 @@ __device__ __forceinline__ QItem q_item(const AttnBwdArgs& a, int i, int n_hg, i
   return it;
 }
 
+// dz of 32 key columns of one query row: p = 2^(s scale - lse) where
+// visible (MASK: key e visible when e <= lim), dz = p (dP - D) (ndd = -D),
+// packed fp16 pairs into wz.  Two columns at a time: the exponent on the
+// paired fp32 pipe, 2^x of the fp16 pair on the SFU (two results per
+// instruction), p widened back to fp32 for dz.
+template <bool MASK>
+__device__ __forceinline__ void dq_chunk(const float* sv, const float* dp, float scale,
+                                         float lse, float ndd, int lim, uint32_t* wz) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const float2 x = ffma2(sv[e], sv[e + 1], scale, scale, -lse, -lse);
+    uint32_t pw = ex2_f16x2(pack_f16x2(x.x, x.y));
+    if (MASK) pw &= (e <= lim ? 0xffffu : 0u) | (e + 1 <= lim ? 0xffff0000u : 0u);
+    const float2 p = unpack_f16x2(pw);
+    const float2 t = ffma2(dp[e], dp[e + 1], 1.f, 1.f, ndd, ndd);  // dP - D
+    const float2 z = ffma2(p.x, p.y, t.x, t.y, 0.f, 0.f);
+    wz[e / 2] = pack_f16x2(z.x, z.y);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -213,12 +235,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_empty = kv_full + L::SLOTS;   // [SLOTS]
   uint64_t* q_full = kv_empty + L::SLOTS;
   uint64_t* q_empty = q_full + 1;
-  uint64_t* s_full = q_empty + 1;
-  uint64_t* s_free = s_full + 1;   // 128 arrivals: S and dP read
-  uint64_t* dz_full = s_free + 1;  // 128 arrivals: dz written
-  uint64_t* dz_free = dz_full + 1; // commit: dQ += dz K done
-  uint64_t* dq_full = dz_free + 1;
-  uint64_t* dq_free = dq_full + 1; // 128 arrivals: dQ read out
+  uint64_t* s_full = q_empty + 1;  // [2] commit: S, dP of a half computed
+  uint64_t* p_full = s_full + 2;   // [2] 256 arrivals: the half's S, dP read, dz written
+  uint64_t* dz_free = p_full + 2;  // [2] commit: the half's dQ += dz K done
+  uint64_t* dq_full = dz_free + 2;
+  uint64_t* dq_free = dq_full + 1; // 256 arrivals: dQ read out
   uint64_t* drain = dq_free + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -232,10 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, kCompute);
-    mbar_init(dz_full, kCompute);
-    mbar_init(dz_free, 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&p_full[h], kCompute);
+      mbar_init(&dz_free[h], 1);
+    }
     mbar_init(dq_full, 1);
     mbar_init(dq_free, kCompute);
     mbar_init(drain, 1);
@@ -297,13 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kMmaWarp) {
-    constexpr uint32_t idesc_s = idesc_f16(AM, AM);
+    constexpr uint32_t idesc_s = idesc_f16(AM, 64);                // one half's keys
     constexpr uint32_t idesc_dq = idesc_f16(AM, D) | (1u << 16);  // B MN-major
     const uint64_t q_desc = sdesc_k128(smem_u32(smem + L::Q_OFF));
     const uint64_t do_desc = sdesc_k128(smem_u32(smem + L::DO_OFF));
     const uint64_t kv_desc = sdesc_k128(smem_u32(smem + L::KV_OFF));
     const uint64_t kmn_desc = sdesc_mn128(smem_u32(smem + L::KV_OFF), AM * 128);
     constexpr uint32_t PAIR16 = (2 * L::TILE) >> 4, TILE16 = L::TILE >> 4;
+    constexpr uint32_t HALF16 = (64 * 128) >> 4;  // rows 64 .. of a K-major tile
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, bwait(b, parity, a.status, abort_flag));
     };
@@ -318,53 +341,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++k;
       const int nt = it.n_tiles;
-      for (int step = -1; step < nt && ok; ++step) {
-        const int js = step + 1;
-        if (js < nt) {  // S = Q K^T and dP = dO V^T of tile js
-          const uint32_t kn = n + js;
-          if (!wait_all(&kv_full[kn % L::SLOTS], (kn / L::SLOTS) & 1) ||
-              !wait_all(s_free, ((g + js) & 1) ^ 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t kd = kv_desc + (kn % L::SLOTS) * PAIR16;
-          if (elect_one()) {
+      // S = Q K^T and dP = dO V^T of half h of key tile j (its S / dP
+      // columns were read by the compute warps: p_full of the tile before,
+      // waited for ahead of that tile's dQ product)
+      auto issue_s = [&](int j, int h) -> bool {
+        const uint32_t kn = n + j;
+        if (h == 0 && !wait_all(&kv_full[kn % L::SLOTS], (kn / L::SLOTS) & 1)) return false;
+        tc_fence_after();
+        const uint64_t kd = kv_desc + (kn % L::SLOTS) * PAIR16 + h * HALF16;
+        if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t o = kmajor_step(kk);
-              tc_mma_bf16_nc(tmem_base + L::S_COL, q_desc + o, kd + o, idesc_s, kk > 0);
-              tc_mma_bf16_nc(tmem_base + L::DP_COL, do_desc + o, kd + TILE16 + o, idesc_s,
-                             kk > 0);
-            }
-            tc_commit(s_full);
-            if (js == nt - 1) tc_commit(q_empty);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = kmajor_step(kk);
+            tc_mma_bf16_nc(tmem_base + L::S_COL + 64 * h, q_desc + o, kd + o, idesc_s,
+                           kk > 0);
+            tc_mma_bf16_nc(tmem_base + L::DP_COL + 64 * h, do_desc + o, kd + TILE16 + o,
+                           idesc_s, kk > 0);
           }
-          __syncwarp();
-          issued_any = true;
+          tc_commit(&s_full[h]);
+          if (j == nt - 1 && h == 1) tc_commit(q_empty);
         }
-        if (step < 0) continue;
-        const int j = step;  // dQ += dz K_j
+        __syncwarp();
+        issued_any = true;
+        return true;
+      };
+      // dQ += dz K over the 64 keys of half h of tile j
+      auto issue_dq = [&](int j, int h) -> bool {
         const uint32_t jn = n + j;
-        if (!wait_all(dz_full, (g + j) & 1) ||
-            (j == 0 && k > 1 && !wait_all(dq_free, (k - 2) & 1))) {
-          ok = false;
-          break;
-        }
+        if (!wait_all(&p_full[h], (g + j) & 1) ||
+            (j == 0 && h == 0 && k > 1 && !wait_all(dq_free, (k - 2) & 1)))
+          return false;
         tc_fence_after();
         const uint64_t bd = kmn_desc + (jn % L::SLOTS) * PAIR16;
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < AM / 16; ++kk)
-            tc_mma_ts(tmem_base + L::DQ_COL, tmem_base + L::DZ_COL + kk * 8,
-                      bd + kk * (2048 >> 4), idesc_dq, (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&kv_empty[jn % L::SLOTS]);
-          tc_commit(dz_free);
-          if (j == nt - 1) tc_commit(dq_full);
+          for (int kk = 0; kk < 4; ++kk) {
+            // keys 64 h + 16 kk ..: warpgroup kk / 2 wrote them as 8 columns
+            // at 8 (kk % 2) of its 16
+            const uint32_t col = L::DZ_COL + 32 * h + (kk / 2) * 16 + (kk % 2) * 8;
+            tc_mma_ts(tmem_base + L::DQ_COL, tmem_base + col,
+                      bd + (4 * h + kk) * (2048 >> 4), idesc_dq,
+                      (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&dz_free[h]);
+          if (h == 1) tc_commit(&kv_empty[jn % L::SLOTS]);
+          if (j == nt - 1 && h == 1) tc_commit(dq_full);
         }
         __syncwarp();
         issued_any = true;
-      }
+        return true;
+      };
+      ok = issue_s(0, 0) && issue_s(0, 1);
+      for (int j = 0; j < nt && ok; ++j)
+        for (int h = 0; h < 2 && ok; ++h)
+          ok = issue_dq(j, h) && (j + 1 >= nt || issue_s(j + 1, h));
       g += nt;
       n += nt;
     }
@@ -376,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ compute
-    const int wq = warp & 3, wg = warp >> 2;  // lane quadrant, column half
+    const int wq = warp & 3, wg = warp >> 2;  // lane quadrant, 32-key slot of a half
     const int r = wq * 32 + lane;
     const uint32_t lane_base = tmem_base + ((uint32_t)(wq * 32) << 16);
     const float scale = 1.4426950408889634f * rsqrtf((float)D);  // log2(e)/sqrt(d)
@@ -397,43 +427,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lse = valid ? a.lse[row * a.n_heads + head] : 0.f;
       const float dd = valid ? a.dsum[row * a.n_heads + head] : 0.f;
       for (int j = 0; j < it.n_tiles; ++j, ++g) {
-        if (!warp_wait(s_full, g & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // this warpgroup's keys: 64 wg .. 64 wg + 63 of the tile
-        float p[64];
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          tmem_ld32_nowait(lane_base + L::S_COL + wg * 64 + c * 32, p + c * 32);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 64; ++c) tmem_pin(p[c]);
-        const int lim = (valid ? pos - j * AM : -1) - wg * 64;  // keys 0 .. lim visible
-#pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = c <= lim ? ex2(p[c] * scale - lse) : 0.f;
-        // the dz columns are free once the previous dQ += dz K is done
-        if (!warp_wait(dz_free, (g & 1) ^ 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int h = 0; h < 2; ++h) {
-          float dp[32];
-          tmem_ld32(lane_base + L::DP_COL + wg * 64 + h * 32, dp);
-          uint32_t w[16];
+          if (!warp_wait(&s_full[h], g & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int c0 = 64 * h + 32 * wg;  // first key column of this warp's chunk
+          float sv[32], dp[32];
+          tmem_ld32_nowait(lane_base + L::S_COL + c0, sv);
+          tmem_ld32_nowait(lane_base + L::DP_COL + c0, dp);
+          tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            w[q] = pack_f16x2(p[h * 32 + 2 * q] * (dp[2 * q] - dd),
-                              p[h * 32 + 2 * q + 1] * (dp[2 * q + 1] - dd));
-          tmem_st16_words(lane_base + L::DZ_COL + wg * 32 + h * 16, w);
+          for (int e = 0; e < 32; ++e) {
+            tmem_pin(sv[e]);
+            tmem_pin(dp[e]);
+          }
+          // keys 0 .. lim of the chunk are visible (none for a row past the
+          // sequence end); a warp whose rows all see the whole chunk skips
+          // the mask
+          const int lim = (valid ? pos - j * AM : -1) - c0;
+          uint32_t wz[16];
+          if (__all_sync(0xffffffffu, lim >= 31))
+            dq_chunk<false>(sv, dp, scale, lse, -dd, lim, wz);
+          else
+            dq_chunk<true>(sv, dp, scale, lse, -dd, lim, wz);
+          // the half's dz columns are free once its previous dQ += dz K is done
+          if (!warp_wait(&dz_free[h], (g & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tmem_st16_words(lane_base + L::DZ_COL + 32 * h + 16 * wg, wz);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&p_full[h]);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(s_free);
-        mbar_arrive(dz_full);
+        if (!ok) break;
       }
       if (!ok) break;
       // ---- dq = dQ / sqrt(d), rotated back, fp16 (32-column pairs shared
@@ -474,24 +505,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // =================================================================== dK, dV
+// Tensor memory of the dK / dV kernel: S^T [0, 128), dP^T [128, 256), dK
+// [256, 256 + D), dV [256 + D, 256 + 2 D).  A query tile is handled as two
+// halves of 64 queries (columns 64 h .. 64 h + 63 of S^T and dP^T): every
+// compute warp works through half 0 and then half 1, and P^T / dz^T of a
+// half overwrite the first 16 of each 32 S^T / dP^T columns a warpgroup
+// read, so that the tensor core runs one half's products (dV, dK and the
+// next tile's S^T, dP^T) while the compute warps work on the other.
 template <int D>
 struct DkvLayout {
   static constexpr uint32_t TILE = AM * D * 2;
   static constexpr int SLOTS = D == 64 ? 3 : 2;  // (Q, dO) pairs
-  // head_dim 64: P^T and dz^T have their own TMEM columns, so S^T of the next
-  // query tile can be computed while the accumulating products of this one
-  // run; head_dim 128: dK and dV take 256 columns and P^T / dz^T overwrite
-  // the S^T / dP^T columns they come from.
-  static constexpr bool P_SEP = D == 64;
   static constexpr uint32_t K_OFF = 0, V_OFF = TILE, Q_OFF = 2 * TILE;
-  static constexpr uint32_t LSE_OFF = Q_OFF + SLOTS * 2 * TILE;  // [2][128] lse, [2][128] D
+  static constexpr uint32_t LSE_OFF = Q_OFF + SLOTS * 2 * TILE;  // [2][128] -lse, [2][128] -D
   static constexpr uint32_t BAR_OFF = LSE_OFF + 4 * AM * 4;
   static constexpr uint32_t TOTAL = BAR_OFF + 256 + 1024;
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DK_COL = 256, DV_COL = 256 + D;
-  static constexpr uint32_t P_COL = P_SEP ? 384 : 0, DZ_COL = P_SEP ? 448 : 128;
-  // P^T / dz^T of column half wg (queries 64 wg ..): their own 32 columns,
-  // or (in place) the first 32 of the 64 S^T / dP^T columns that half read
-  static constexpr uint32_t P_HALF = P_SEP ? 32 : 64;
   static_assert(DV_COL + D <= 512, "tensor memory budget");
   static_assert(TOTAL <= 232448, "shared memory budget");
 };
@@ -527,6 +556,38 @@ __device__ __forceinline__ void k_item_tile(const AttnBwdArgs& a, const KItem& i
   h0 = it.g * (a.n_heads / a.n_kv_heads) + hgl * a.hpc;
 }
 
+// P^T and dz^T of 32 query columns of one key row: p = 2^(s scale - lse)
+// where visible, dz = p (dP - D); packed fp16 pairs into wp / wz.  nls and
+// nds hold -lse and -D of each column.  MASK: column c (of the tile) is
+// visible when (c & bm) >= rel.  Two columns at a time as in dq_chunk; dz is
+// formed from the same fp16 p that dV's product uses.
+template <bool MASK>
+__device__ __forceinline__ void dkv_chunk(const float* sv, const float* dp, const float* nls,
+                                          const float* nds, float scale, int c0, int bm,
+                                          int rel, uint32_t* wp, uint32_t* wz) {
+#pragma unroll
+  for (int e4 = 0; e4 < 8; ++e4) {
+    const float4 l4 = reinterpret_cast<const float4*>(nls + c0)[e4];
+    const float4 d4 = reinterpret_cast<const float4*>(nds + c0)[e4];
+    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+    for (int e = 0; e < 4; e += 2) {
+      const int j = e4 * 4 + e;
+      const float2 x = ffma2(sv[j], sv[j + 1], scale, scale, lv[e], lv[e + 1]);
+      uint32_t pw = ex2_f16x2(pack_f16x2(x.x, x.y));
+      if (MASK)
+        pw &= ((((c0 + j) & bm) >= rel) ? 0xffffu : 0u) |
+              ((((c0 + j + 1) & bm) >= rel) ? 0xffff0000u : 0u);
+      const float2 p = unpack_f16x2(pw);
+      const float2 t = ffma2(dp[j], dp[j + 1], 1.f, 1.f, dv[e], dv[e + 1]);  // dP - D
+      const float2 z = ffma2(p.x, p.y, t.x, t.y, 0.f, 0.f);
+      wp[j / 2] = pw;
+      wz[j / 2] = pack_f16x2(z.x, z.y);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -537,20 +598,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* lse_s = reinterpret_cast<float*>(smem + L::LSE_OFF);  // [2][128]
-  float* dd_s = lse_s + 2 * AM;                                 // [2][128]
+  float* lse_s = reinterpret_cast<float*>(smem + L::LSE_OFF);  // [2][128] -lse
+  float* dd_s = lse_s + 2 * AM;                                 // [2][128] -D
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* q_full = bar;                   // [SLOTS]
   uint64_t* q_empty = q_full + L::SLOTS;    // [SLOTS]
   uint64_t* kv_full = q_empty + L::SLOTS;
   uint64_t* kv_empty = kv_full + 1;
-  uint64_t* s_full = kv_empty + 1;
-  uint64_t* s_free = s_full + 1;   // P_SEP: 128 arrivals (S^T, dP^T read); else commit
-  uint64_t* p_full = s_free + 1;   // 128 arrivals: P^T and dz^T written
-  uint64_t* p_free = p_full + 1;   // commit: dV, dK products of the tile done
-  uint64_t* acc_full = p_free + 1;
-  uint64_t* acc_free = acc_full + 1;  // 128 arrivals: dK, dV read out
-  uint64_t* lse_ready = acc_free + 1; // [2] 128 arrivals: lse / D of a tile in smem
+  uint64_t* s_full = kv_empty + 1;   // [2] commit: S^T, dP^T of a half computed
+  uint64_t* s_free = s_full + 2;     // [2] commit: the half's dV, dK products done
+  uint64_t* p_full = s_free + 2;     // [2] 256 arrivals: the half's P^T, dz^T written
+  uint64_t* acc_full = p_full + 2;
+  uint64_t* acc_free = acc_full + 1;  // 256 arrivals: dK, dV read out
+  uint64_t* lse_ready = acc_free + 1; // [2] 256 arrivals: lse / D of a tile in smem
   uint64_t* drain = lse_ready + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -564,14 +624,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, L::P_SEP ? kCompute : 1);
-    mbar_init(p_full, kCompute);
-    mbar_init(p_free, 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&s_free[h], 1);
+      mbar_init(&p_full[h], kCompute);
+      mbar_init(&lse_ready[h], kCompute);
+    }
     mbar_init(acc_full, 1);
     mbar_init(acc_free, kCompute);
-    mbar_init(&lse_ready[0], kCompute);
-    mbar_init(&lse_ready[1], kCompute);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -633,13 +693,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kMmaWarp) {
-    constexpr uint32_t idesc_s = idesc_f16(AM, AM);
+    constexpr uint32_t idesc_s = idesc_f16(AM, 64);                 // one half's queries
     constexpr uint32_t idesc_acc = idesc_f16(AM, D) | (1u << 16);  // B MN-major
     const uint64_t k_desc = sdesc_k128(smem_u32(smem + L::K_OFF));
     const uint64_t v_desc = sdesc_k128(smem_u32(smem + L::V_OFF));
     const uint64_t q_desc = sdesc_k128(smem_u32(smem + L::Q_OFF));
     const uint64_t qmn_desc = sdesc_mn128(smem_u32(smem + L::Q_OFF), AM * 128);
     constexpr uint32_t PAIR16 = (2 * L::TILE) >> 4, TILE16 = L::TILE >> 4;
+    constexpr uint32_t HALF16 = (64 * 128) >> 4;  // rows 64 .. of a K-major tile
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, bwait(b, parity, a.status, abort_flag));
     };
@@ -654,67 +715,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++k;
       const int nq = it.nq;
-      // S^T = K Q_q^T, dP^T = V dO_q^T
-      auto issue_s = [&](int q) -> bool {
+      // S^T = K Q^T and dP^T = V dO^T of half h of query tile q (its S^T /
+      // dP^T columns are free once the half's products of the tile before
+      // are done)
+      auto issue_s = [&](int q, int h) -> bool {
         const uint32_t qn = n + q;
-        if (!wait_all(&q_full[qn % L::SLOTS], (qn / L::SLOTS) & 1) ||
-            !wait_all(s_free, ((gi + q) & 1) ^ 1))
+        if ((h == 0 && !wait_all(&q_full[qn % L::SLOTS], (qn / L::SLOTS) & 1)) ||
+            !wait_all(&s_free[h], ((gi + q) & 1) ^ 1))
           return false;
         tc_fence_after();
-        const uint32_t so = (qn % L::SLOTS) * PAIR16;
+        const uint32_t so = (qn % L::SLOTS) * PAIR16 + h * HALF16;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t o = kmajor_step(kk);
-            tc_mma_bf16_nc(tmem_base + L::S_COL, k_desc + o, q_desc + so + o, idesc_s, kk > 0);
-            tc_mma_bf16_nc(tmem_base + L::DP_COL, v_desc + o, q_desc + so + TILE16 + o, idesc_s,
-                           kk > 0);
+            tc_mma_bf16_nc(tmem_base + L::S_COL + 64 * h, k_desc + o, q_desc + so + o,
+                           idesc_s, kk > 0);
+            tc_mma_bf16_nc(tmem_base + L::DP_COL + 64 * h, v_desc + o,
+                           q_desc + so + TILE16 + o, idesc_s, kk > 0);
           }
-          tc_commit(s_full);
-          if (q == nq - 1) tc_commit(kv_empty);  // K and V no longer read
+          tc_commit(&s_full[h]);
+          if (q == nq - 1 && h == 1) tc_commit(kv_empty);  // K and V no longer read
         }
         __syncwarp();
         issued_any = true;
         return true;
       };
-      // dV += P^T dO_q, dK += dz^T Q_q
-      auto issue_acc = [&](int q) -> bool {
+      // dV += P^T dO, dK += dz^T Q over the 64 queries of half h of tile q
+      auto issue_acc = [&](int q, int h) -> bool {
         const uint32_t qn = n + q;
-        if (!wait_all(p_full, (gi + q) & 1) ||
-            (q == 0 && k > 1 && !wait_all(acc_free, (k - 2) & 1)))
+        if (!wait_all(&p_full[h], (gi + q) & 1) ||
+            (q == 0 && h == 0 && k > 1 && !wait_all(acc_free, (k - 2) & 1)))
           return false;
         tc_fence_after();
         const uint64_t qb = qmn_desc + (qn % L::SLOTS) * PAIR16;
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < AM / 16; ++kk) {
-            const uint32_t acc = (q > 0 || kk > 0) ? 1u : 0u;
-            const uint32_t col = (kk / 4) * L::P_HALF + (kk % 4) * 8;  // queries 16 kk ..
-            tc_mma_ts(tmem_base + L::DV_COL, tmem_base + L::P_COL + col,
-                      qb + TILE16 + kk * (2048 >> 4), idesc_acc, acc);
-            tc_mma_ts(tmem_base + L::DK_COL, tmem_base + L::DZ_COL + col,
-                      qb + kk * (2048 >> 4), idesc_acc, acc);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (q > 0 || h > 0 || kk > 0) ? 1u : 0u;
+            // queries 64 h + 16 kk ..: warpgroup kk / 2 wrote them as 8
+            // columns at 8 (kk % 2) of its 32
+            const uint32_t col = 64 * h + (kk / 2) * 32 + (kk % 2) * 8;
+            const uint32_t kb = (4 * h + kk) * (2048 >> 4);
+            tc_mma_ts(tmem_base + L::DV_COL, tmem_base + L::S_COL + col, qb + TILE16 + kb,
+                      idesc_acc, acc);
+            tc_mma_ts(tmem_base + L::DK_COL, tmem_base + L::DP_COL + col, qb + kb, idesc_acc,
+                      acc);
           }
-          tc_commit(&q_empty[qn % L::SLOTS]);
-          if (L::P_SEP)
-            tc_commit(p_free);
-          else
-            tc_commit(s_free);  // S^T / dP^T columns hold P^T / dz^T
-          if (q == nq - 1) tc_commit(acc_full);
+          tc_commit(&s_free[h]);
+          if (h == 1) tc_commit(&q_empty[qn % L::SLOTS]);
+          if (q == nq - 1 && h == 1) tc_commit(acc_full);
         }
         __syncwarp();
         issued_any = true;
         return true;
       };
-      for (int step = -1; step < nq && ok; ++step) {
-        if constexpr (L::P_SEP) {
-          if (step + 1 < nq && !issue_s(step + 1)) ok = false;
-          if (ok && step >= 0 && !issue_acc(step)) ok = false;
-        } else {
-          if (step >= 0 && !issue_acc(step)) ok = false;
-          if (ok && step + 1 < nq && !issue_s(step + 1)) ok = false;
-        }
-      }
+      ok = issue_s(0, 0) && issue_s(0, 1);
+      for (int q = 0; q < nq && ok; ++q)
+        for (int h = 0; h < 2 && ok; ++h)
+          ok = issue_acc(q, h) && (q + 1 >= nq || issue_s(q + 1, h));
       gi += nq;
       n += nq;
     }
@@ -726,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ compute
-    const int wq = warp & 3, wg = warp >> 2;  // lane quadrant, query-column half
+    const int wq = warp & 3, wg = warp >> 2;  // lane quadrant, 32-column slot of a half
     const int r = wq * 32 + lane;             // key row of the tile == TMEM lane
     const uint32_t lane_base = tmem_base + ((uint32_t)(wq * 32) << 16);
     const float scale = 1.4426950408889634f * rsqrtf((float)D);
@@ -743,16 +802,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++k;
       const int kp = it.k0 + r;
       const bool kvalid = kp < it.L;
-      // lse (warpgroup 0) or D (warpgroup 1) of query row r of tile q, read
-      // one tile ahead so the global loads overlap the previous tile's work
+      // -lse (warpgroup 0) or -D (warpgroup 1) of query row r of tile q,
+      // loaded one tile ahead so that the load overlaps the previous tile's
+      // work (-inf, 0 past the sequence end)
       auto fetch = [&](int q) -> float {
         int h0, q0;
         k_item_tile(a, it, q, BP, h0, q0);
         const int qp = q0 + r % BP, qh = h0 + r / BP;
         const bool qv = qp < it.L;
         const size_t qrow = (size_t)(it.a0 + (qv ? qp : 0)) * a.n_heads + qh;
-        if (wg == 0) return qv ? a.lse[qrow] : INFINITY;
-        return qv ? a.dsum[qrow] : 0.f;
+        const float v = ldg_now((wg == 0 ? a.lse : a.dsum) + qrow);
+        if (wg == 0) return qv ? -v : -INFINITY;
+        return qv ? -v : 0.f;
       };
       float next = fetch(0);
       for (int q = 0; q < it.nq; ++q, ++gi) {
@@ -767,66 +828,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&lse_ready[b]);
           if (q + 1 < it.nq) next = fetch(q + 1);
         }
-        if (!warp_wait(&lse_ready[gi & 1], (gi >> 1) & 1) || !warp_wait(s_full, gi & 1)) {
+        if (!warp_wait(&lse_ready[gi & 1], (gi >> 1) & 1)) {
           ok = false;
           break;
         }
-        tc_fence_after();
         const float* ls = lse_s + (gi & 1) * AM;
         const float* ds = dd_s + (gi & 1) * AM;
-        if constexpr (L::P_SEP) {  // P^T / dz^T columns free: previous products done
-          if (!warp_wait(p_free, (gi & 1) ^ 1)) {
+        // query column c sits at position q0 + (c & (BP - 1)) (BP a power of
+        // two): key kp is visible to it when kp <= that position; lse = +inf
+        // past the sequence end.  Below the diagonal (every key of this warp
+        // at or before q0) nothing is masked.
+        const bool full = q0 >= it.k0 + wq * 32 + 31;
+        const int rel = kvalid ? kp - q0 : AM;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          if (!warp_wait(&s_full[h], gi & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-        }
-        // query column c sits at position q0 + c % BP (BP a power of two):
-        // key kp is visible to it when kp <= that position; lse = +inf past
-        // the sequence end.  This warpgroup's 64 columns, 32 at a time: chunk
-        // h's P^T / dz^T land on columns 16 h .. 16 h + 15 of the half's
-        // region, which the in-place layout has already read (S^T / dP^T
-        // chunk h covers 32 h .. 32 h + 31 of the half)
-        const int rel = kvalid ? kp - q0 : AM;
-        const int bm = BP - 1;
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          const int c0 = wg * 64 + h * 32;  // first query column of the chunk
+          const int c0 = 64 * h + 32 * wg;  // first query column of this warp's chunk
           float sv[32], dp[32];
-          tmem_ld32(lane_base + L::S_COL + c0, sv);
-          float p[32];
+          tmem_ld32_nowait(lane_base + L::S_COL + c0, sv);
+          tmem_ld32_nowait(lane_base + L::DP_COL + c0, dp);
+          tmem_wait_ld();
 #pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 l4 = reinterpret_cast<const float4*>(ls + c0)[e4];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = c0 + e4 * 4 + e;
-              p[e4 * 4 + e] = ((c & bm) >= rel) ? ex2(sv[e4 * 4 + e] * scale - lv[e]) : 0.f;
-            }
+          for (int e = 0; e < 32; ++e) {
+            tmem_pin(sv[e]);
+            tmem_pin(dp[e]);
           }
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = pack_f16x2(p[2 * e], p[2 * e + 1]);
-          tmem_st16_words(lane_base + L::P_COL + wg * L::P_HALF + h * 16, w);
-          tmem_ld32(lane_base + L::DP_COL + c0, dp);
-#pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 d4 = reinterpret_cast<const float4*>(ds + c0)[e4];
-            dp[e4 * 4 + 0] -= d4.x;
-            dp[e4 * 4 + 1] -= d4.y;
-            dp[e4 * 4 + 2] -= d4.z;
-            dp[e4 * 4 + 3] -= d4.w;
-          }
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack_f16x2(p[2 * e] * dp[2 * e], p[2 * e + 1] * dp[2 * e + 1]);
-          tmem_st16_words(lane_base + L::DZ_COL + wg * L::P_HALF + h * 16, w);
+          uint32_t wp[16], wz[16];
+          if (full)
+            dkv_chunk<false>(sv, dp, ls, ds, scale, c0, BP - 1, rel, wp, wz);
+          else
+            dkv_chunk<true>(sv, dp, ls, ds, scale, c0, BP - 1, rel, wp, wz);
+          tmem_st16_words(lane_base + L::S_COL + c0, wp);
+          tmem_st16_words(lane_base + L::DP_COL + c0, wz);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&p_full[h]);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        if constexpr (L::P_SEP) mbar_arrive(s_free);
-        mbar_arrive(p_full);
+        if (!ok) break;
       }
       if (!ok) break;
       // ---- dk (scaled, rotated back) and dv of the tile's keys, 32-column

@@ -155,14 +155,6 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float b, float c) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(x));
 }
 
-// 2^x of both halves of an fp16 pair (the SFU's packed form: two results per
-// instruction).
-__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
-  uint32_t y;
-  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
 __device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
   uint32_t y;
   asm("add.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));

@@ -2,8 +2,10 @@
 (parity.BF16_STAGE_MAX_ABS_REL_RMS = 8e-2), reproduced on the CPU.
 
 A numpy emulation of every rounding point of the bf16 layer's kernels (the
-fp16 intermediates and packed weights, fp32 accumulation, the fp16 softmax
-probabilities with an fp32 denominator, the scaled fp16 copies of h and act,
+fp16 intermediates and packed weights, fp32 accumulation, the softmax
+exponent and probabilities in fp16 with their sum in fp32 (the kernel's
+fp16 partial sums of eight values are taken exactly here), the scaled fp16
+copies of h and act,
 the bf16 output) runs on the same seeded inputs as the fp64 oracle.  Its
 stage errors are what a correct implementation of that rounding scheme
 shows: the attention output's largest error is a few percent of its RMS
@@ -69,9 +71,11 @@ def emulate(inp):
         for hh in range(s.n_heads):
             kv = hh // n_rep
             sc = f32(q[a0:a1, hh] @ k[a0:a1, kv].T) * scale + mask
-            p32 = f32(np.exp2(sc - sc.max(axis=1, keepdims=True)))
-            l = p32.sum(axis=1, keepdims=True)
-            attn[a0:a1, hh] = f32(f16(p32) @ v[a0:a1, kv]) / l
+            # the packed exp2: exponent and result in fp16, the row sum
+            # taken from the same fp16 values
+            p16 = f16(np.exp2(f16(sc - sc.max(axis=1, keepdims=True))))
+            l = p16.sum(axis=1, keepdims=True)
+            attn[a0:a1, hh] = f32(p16 @ v[a0:a1, kv]) / l
     attn = f16(attn.reshape(T, -1))
     h = x + f32(attn @ f16(w.w_o).T)
     hg = f16(h / 256.0) * 256.0
