@@ -69,6 +69,10 @@ DESCRIPTIONS = {
               "seq 4096, dL/d(out) ~ N(0,1) seeded",
     "bwd_1b": "backward pass of the Llama-3.2-1B-shaped layer bf16 (llama_layer_backward): "
               "batch 4 x seq 2048, dL/d(out) ~ N(0,1) seeded",
+    "train_8b": "training step of the Llama-3-8B-shaped layer bf16: llama_layer_forward_train "
+                "(the forward, keeping the activations the backward reads) then "
+                "llama_layer_backward_saved (dx and the weight / norm gradients, the forward "
+                "not recomputed): batch 2 x seq 4096, dL/d(out) ~ N(0,1) seeded",
     "chunked": "chunked prefill with a KV cache, 8B-shaped layer bf16: 16 "
                "sequences x 4 new tokens, start_pos U{512..8188} (seeded), cache "
                "[16, 8192, 8, 128] bf16 (llama_layer_forward_cached)",
@@ -118,9 +122,10 @@ def parse_args():
 
 HEADLINE = "varlen"
 BACKWARD = {"bwd_8b": "8b", "bwd_1b": "1b"}  # backward workload -> its forward workload
-ALSO_AUTO = ("1b", "8b", "decode", "bwd_8b", "chunk512")
+TRAIN = {"train_8b": "8b"}  # training-step workload -> its forward workload
+ALSO_AUTO = ("1b", "8b", "decode", "bwd_8b", "train_8b", "chunk512")
 
-DEFAULT_STEPS = {"chunk64": 1000, "chunk512": 300, "bwd_8b": 200, "bwd_1b": 600, "tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
+DEFAULT_STEPS = {"chunk64": 1000, "chunk512": 300, "bwd_8b": 200, "bwd_1b": 600, "train_8b": 200, "tiny": 500, "1b": 2000, "8b": 600, "varlen": 400,
                  "decode": 3000, "chunked": 1500, "model1b": 40}
 MODEL = {"model1b": ("1b", 16, 128256)}  # layer workload, layers, vocabulary
 
@@ -270,6 +275,19 @@ def algorithmic_work_backward(inp) -> dict:
     by = {"rmsnorm_stats": float(T * H * 2), "bwd_dout_f16": float(T * H * 4),
           "bwd_norm2": float(T * H * (2 + 4 + 2 + 4 + 2)),
           "bwd_norm1": float(T * H * (4 + 4 + 2 + 2))}
+    return dict(kind="prefill", flops=flops, total_flops=sum(flops.values()), bytes=by,
+                weight_bytes=w["weight_bytes"])
+
+
+def algorithmic_work_train(inp) -> dict:
+    """Per-stage algorithmic FLOPs of one training step: the whole forward
+    (llama_layer_forward_train) and the backward proper
+    (llama_layer_backward_saved, no recomputation)."""
+    w = algorithmic_work(inp)
+    b = algorithmic_work_backward(inp)
+    flops = dict(w["flops"])
+    flops.update({k: v for k, v in b["flops"].items() if k.startswith("bwd_")})
+    by = dict(b["bytes"])
     return dict(kind="prefill", flops=flops, total_flops=sum(flops.values()), bytes=by,
                 weight_bytes=w["weight_bytes"])
 
@@ -702,8 +720,9 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
     if cpu_seconds is None:
         cpu_seconds = args.cpu_baseline_seconds
 
-    bwd = wl in BACKWARD
-    inp = synth.make_inputs(BACKWARD.get(wl, wl))
+    train = wl in TRAIN
+    bwd = wl in BACKWARD or train
+    inp = synth.make_inputs(BACKWARD.get(wl) or TRAIN.get(wl) or wl)
     w = inp.workload
     s = w.shape
     layer = LlamaLayer.from_numpy(s, inp.weights)
@@ -742,6 +761,13 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
             def step(o=out):
                 layer.backward(x, dout, n_seq=n_seq, seq_len=seq, dx=o, grads=grads)
 
+        if train:  # the layer output too, from the forward that keeps its activations
+            y = torch.empty_like(x)
+
+            def step(o=out):
+                layer.forward_train(x, n_seq=n_seq, seq_len=seq, out=y)
+                layer.backward_saved(x, dout, n_seq=n_seq, seq_len=seq, dx=o, grads=grads)
+
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     for _ in range(W):
@@ -752,6 +778,12 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
     if rc != 0:
         raise RuntimeError(f"layer status after warm-up: {rc}")
     launches_per_step = layer.launch_count()
+    if train:  # two library calls a step
+        layer.forward_train(x, n_seq=n_seq, seq_len=seq, out=y)
+        n_fwd = layer.launch_count()
+        layer.backward_saved(x, dout, n_seq=n_seq, seq_len=seq, dx=out, grads=grads)
+        launches_per_step = n_fwd + layer.launch_count()
+        torch.cuda.synchronize()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
@@ -798,7 +830,8 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
 
     tokens = inp.tokens
     value = job_throughput(world, K, tokens, total_ms)
-    work = algorithmic_work_backward(inp) if bwd else algorithmic_work(inp)
+    work = (algorithmic_work_train(inp) if train else
+            algorithmic_work_backward(inp) if bwd else algorithmic_work(inp))
     pk = peaks()
 
     # ---- end to end: host input -> layer -> host output, copies timed
@@ -855,7 +888,10 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
         e2e = {"value": job_throughput(world, n_e2e, tokens, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
                "steps": n_e2e, "ms_per_step": e2e_ms / n_e2e,
-               "api": ("LlamaLayer.backward (pinned host x and dL/d(out) copied in, "
+               "api": ("LlamaLayer.forward_train + LlamaLayer.backward_saved (pinned "
+                       "host x and dL/d(out) copied in, dx copied out; the layer output "
+                       "and the weight gradients stay on the device)") if train else
+                      ("LlamaLayer.backward (pinned host x and dL/d(out) copied in, "
                        "dx copied out; the weight gradients stay on the device for the "
                        "optimizer)") if bwd else
                       ("LlamaLayer.%s_from_host (pinned host buffers, "
@@ -979,8 +1015,9 @@ def run_reference(args, rank, world):
         per_tok = (time.perf_counter() - t) / n0
         run, tokens, what = model_oracle_sample(m_in, max(1, int(per_step / per_tok)))
     else:
-        inp = synth.make_inputs(BACKWARD.get(args.workload, args.workload))
-        r = OracleRunner(inp, args.workload in BACKWARD)
+        inp = synth.make_inputs(BACKWARD.get(args.workload) or TRAIN.get(args.workload)
+                                or args.workload)
+        r = OracleRunner(inp, args.workload in BACKWARD or args.workload in TRAIN)
         n = r.calibrate(per_step)
         run, tokens, what = r.units(n)
     for _ in range(min(W, 1)):

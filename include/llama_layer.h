@@ -317,6 +317,43 @@ LLAMA_API int llama_layer_backward(llama_layer_t* layer, const llama_layer_weigh
                                    int n_seq, int seq_len, int total_tokens, void* workspace,
                                    size_t workspace_bytes, void* stream);
 
+/* The forward of a training step: `out` exactly as llama_layer_forward
+ * computes it, and the activations the backward reads (x / RMS(x), q | k | v,
+ * the attention output and its softmax denominators, h, gate | up, act and the
+ * RMSNorm statistics) kept in `workspace`, so that llama_layer_backward_saved
+ * can skip the forward's recomputation: a training step (forward for the
+ * loss, then backward) runs the forward once instead of twice.  Arguments as
+ * llama_layer_forward, except that `workspace` must hold
+ * llama_layer_backward_workspace_bytes(layer, >= total_tokens).  bf16 layers
+ * only (LLAMA_ERR_UNSUPPORTED_SHAPE otherwise).  The layer records the call's
+ * workspace, x, position_ids, cu_seqlens, n_seq, seq_len and total_tokens
+ * (host side); any later call through the layer whose workspace overlaps this
+ * one drops the record. */
+LLAMA_API int llama_layer_forward_train(llama_layer_t* layer, const void* x, void* out,
+                                        const int32_t* position_ids,
+                                        const int32_t* cu_seqlens, int n_seq, int seq_len,
+                                        int total_tokens, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+/* llama_layer_backward without the forward's recomputation: the gradients
+ * from the activations the last llama_layer_forward_train call through
+ * `layer` kept in `workspace`.  Arguments, results and rules as
+ * llama_layer_backward; x, position_ids, cu_seqlens, n_seq, seq_len,
+ * total_tokens and workspace must be the ones of that call (the pointers
+ * compared as given), and the workspace not written since, else
+ * LLAMA_ERR_INVALID_ARG (nothing launched).  The backward leaves the kept
+ * activations intact, so it may run again from the same forward.  Enqueue it
+ * on the forward's stream (or order the streams): the kept activations are
+ * read on the device. */
+LLAMA_API int llama_layer_backward_saved(llama_layer_t* layer,
+                                         const llama_layer_weights* weights, const void* x,
+                                         const void* dout, void* dx,
+                                         const llama_layer_grads* grads,
+                                         const int32_t* position_ids,
+                                         const int32_t* cu_seqlens, int n_seq, int seq_len,
+                                         int total_tokens, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
 /* Self-test of the bounded waits the library's pipelined kernels use (no
  * layer needed): one block waits on an mbarrier that nothing arrives on and
  * on a device flag that nothing sets, each up to the library's wait limit

@@ -46,6 +46,7 @@ EXPORTS = (
     "llama_layer_forward_host", "llama_layer_forward_cached",
     "llama_selftest_bounded_waits", "llama_rope_inv_freq", "llama_rmsnorm_bf16",
     "llama_gemm_status", "llama_layer_backward_workspace_bytes", "llama_layer_backward",
+    "llama_layer_forward_train", "llama_layer_backward_saved",
 )
 
 
@@ -133,6 +134,10 @@ def lib() -> ctypes.CDLL:
         "llama_layer_backward": (_I, [_P, ctypes.POINTER(llama_layer_weights), _P, _P, _P,
                                       ctypes.POINTER(llama_layer_grads), _P, _P, _I, _I,
                                       _I, _P, _SZ, _P]),
+        "llama_layer_forward_train": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+        "llama_layer_backward_saved": (_I, [_P, ctypes.POINTER(llama_layer_weights), _P, _P,
+                                            _P, ctypes.POINTER(llama_layer_grads), _P, _P,
+                                            _I, _I, _I, _P, _SZ, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -302,6 +307,26 @@ def llama_layer_backward(layer: int, weights: llama_layer_weights, x: int, dout:
                                       ctypes.byref(grads), position_ids, cu_seqlens,
                                       n_seq, seq_len, total_tokens, workspace,
                                       workspace_bytes, stream))
+
+
+def llama_layer_forward_train(layer: int, x: int, out: int, position_ids, cu_seqlens,
+                              n_seq: int, seq_len: int, total_tokens: int, workspace: int,
+                              workspace_bytes: int, stream: int) -> None:
+    _check("llama_layer_forward_train",
+           lib().llama_layer_forward_train(layer, x, out, position_ids, cu_seqlens, n_seq,
+                                           seq_len, total_tokens, workspace,
+                                           workspace_bytes, stream))
+
+
+def llama_layer_backward_saved(layer: int, weights: llama_layer_weights, x: int, dout: int,
+                               dx: int, grads: llama_layer_grads, position_ids, cu_seqlens,
+                               n_seq: int, seq_len: int, total_tokens: int, workspace: int,
+                               workspace_bytes: int, stream: int) -> None:
+    _check("llama_layer_backward_saved",
+           lib().llama_layer_backward_saved(layer, ctypes.byref(weights), x, dout, dx,
+                                            ctypes.byref(grads), position_ids, cu_seqlens,
+                                            n_seq, seq_len, total_tokens, workspace,
+                                            workspace_bytes, stream))
 
 
 def llama_gemm_status(stream: int) -> int:

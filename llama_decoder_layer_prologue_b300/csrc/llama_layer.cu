@@ -176,11 +176,31 @@ struct llama_layer {
   cudaEvent_t ev_start, ev_done, ev_in[LLAMA_HOST_MAX_CHUNKS],
       ev_comp[LLAMA_HOST_MAX_CHUNKS];
   bool host_ready;
+  // The activations the last llama_layer_forward_train call kept in its
+  // workspace, for llama_layer_backward_saved: that call's arguments.  Any
+  // other call through the layer whose workspace overlaps [ws, ws + bytes)
+  // clears `valid`.
+  struct {
+    const char* ws;
+    size_t bytes;
+    const void* x;
+    const int32_t *pos, *cu;
+    int n_seq, seq_len, tokens;
+    bool valid;
+  } saved;
 };
 
 namespace {
 
 int cuda_err(cudaError_t e) { return e == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA; }
+
+// A call is about to write [ws, ws + bytes): the kept activations are lost
+// if that overlaps them.
+void clobber(llama_layer* L, const void* ws, size_t bytes) {
+  const char* p = static_cast<const char*>(ws);
+  if (L->saved.valid && p < L->saved.ws + L->saved.bytes && L->saved.ws < p + bytes)
+    L->saved.valid = false;
+}
 
 // Starts stage `name` (or ends the call when name is null) on stream s.
 void mark(llama_layer* L, cudaStream_t s, const char* name) {
@@ -373,7 +393,8 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
                 L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
     ++L->launches;
-    if (sv) return cuda_err(cudaGetLastError());  // the backward continues from here
+    // the backward's recomputation (no output) continues from here
+    if (sv && !out) return cuda_err(cudaGetLastError());
     // a9: down_proj + residual.
     if (!tc_encode_bf16(&ta, act, T, dm.I, 128)) return LLAMA_ERR_CUDA;
     ep = TcEpiArgs();
@@ -440,21 +461,34 @@ BwdLayout bwd_layout(const llama_layer_config& c, int tokens) {
   return b;
 }
 
-// Gradients of the prefill layer: the forward recomputed (keeping the
-// attention's softmax denominators and gate / up), then the chain rule in
-// reverse order of the forward's steps ("模型层" 9.6 LlamaForTraining puts
-// this layer under a loss; each step is stated in llama_layer.h).
-int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
-                  const void* dout, void* dx, const llama_layer_grads* gr,
-                  const int32_t* pos_in, const int32_t* cu, int n_seq, int seq_len,
-                  int T, char* ws, cudaStream_t s) {
-  const Dims& dm = L->dm;
-  const BwdLayout b = bwd_layout(L->cfg, T);
+// The forward's activations the backward reads, at their places in the
+// backward workspace (the forward's own intermediates sit in its front part).
+FwdSaves bwd_saves(const BwdLayout& b, char* ws) {
   FwdSaves sv;
   sv.lse = reinterpret_cast<float*>(ws + b.lse);
   sv.gu = ws + b.gu;
-  int rc = forward_impl(L, x, nullptr, pos_in, cu, n_seq, seq_len, T, ws, s, &sv);
-  if (rc) return rc;
+  return sv;
+}
+
+// Gradients of the prefill layer: the forward recomputed (keeping the
+// attention's softmax denominators and gate / up) unless a training forward
+// left them in `ws` (recompute = false), then the chain rule in reverse order
+// of the forward's steps ("模型层" 9.6 LlamaForTraining puts this layer under
+// a loss; each step is stated in llama_layer.h).
+int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
+                  const void* dout, void* dx, const llama_layer_grads* gr,
+                  const int32_t* pos_in, const int32_t* cu, int n_seq, int seq_len,
+                  int T, char* ws, cudaStream_t s, bool recompute) {
+  const Dims& dm = L->dm;
+  const BwdLayout b = bwd_layout(L->cfg, T);
+  int rc = LLAMA_OK;
+  if (recompute) {
+    const FwdSaves sv = bwd_saves(b, ws);
+    rc = forward_impl(L, x, nullptr, pos_in, cu, n_seq, seq_len, T, ws, s, &sv);
+    if (rc) return rc;
+  } else {
+    begin_call(L);
+  }
   int launches = L->launches;
   const WsLayout& f = b.fw;
   const char* P = L->packed;
@@ -992,6 +1026,7 @@ int llama_layer_forward(llama_layer_t* L, const void* x, void* out,
   if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
   if (workspace_bytes < ws_layout(L->cfg, total_tokens).total)
     return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+  clobber(L, workspace, workspace_bytes);
   return forward_impl(L, x, out, position_ids, cu_seqlens, n_seq, seq_len,
                       total_tokens, static_cast<char*>(workspace),
                       static_cast<cudaStream_t>(stream));
@@ -1005,11 +1040,12 @@ int llama_layer_backward_workspace_bytes(const llama_layer_t* L, int max_tokens,
   return LLAMA_OK;
 }
 
-int llama_layer_backward(llama_layer_t* L, const llama_layer_weights* w, const void* x,
-                         const void* dout, void* dx, const llama_layer_grads* gr,
-                         const int32_t* position_ids, const int32_t* cu_seqlens, int n_seq,
-                         int seq_len, int total_tokens, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+// Argument checks shared by llama_layer_backward and llama_layer_backward_saved.
+static int check_backward(const llama_layer_t* L, const llama_layer_weights* w, const void* x,
+                          const void* dout, const void* dx, const llama_layer_grads* gr,
+                          const int32_t* position_ids, const int32_t* cu_seqlens, int n_seq,
+                          int seq_len, int total_tokens, const void* workspace,
+                          size_t workspace_bytes) {
   if (!L || !w || !x || !dout || !dx || !gr || total_tokens < 0) return LLAMA_ERR_INVALID_ARG;
   if (!L->bf16) return LLAMA_ERR_UNSUPPORTED_SHAPE;
   const void* in[7] = {x, dout, dx, w->w_qkv, w->w_gate_up, w->g_in, w->g_post};
@@ -1030,9 +1066,77 @@ int llama_layer_backward(llama_layer_t* L, const llama_layer_weights* w, const v
   if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
   if (workspace_bytes < bwd_layout(L->cfg, total_tokens).total)
     return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+  return LLAMA_OK;
+}
+
+int llama_layer_backward(llama_layer_t* L, const llama_layer_weights* w, const void* x,
+                         const void* dout, void* dx, const llama_layer_grads* gr,
+                         const int32_t* position_ids, const int32_t* cu_seqlens, int n_seq,
+                         int seq_len, int total_tokens, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  int rc = check_backward(L, w, x, dout, dx, gr, position_ids, cu_seqlens, n_seq, seq_len,
+                          total_tokens, workspace, workspace_bytes);
+  if (rc || total_tokens == 0) return rc;
+  clobber(L, workspace, workspace_bytes);
   return backward_impl(L, w, x, dout, dx, gr, position_ids, cu_seqlens, n_seq, seq_len,
                        total_tokens, static_cast<char*>(workspace),
-                       static_cast<cudaStream_t>(stream));
+                       static_cast<cudaStream_t>(stream), true);
+}
+
+int llama_layer_forward_train(llama_layer_t* L, const void* x, void* out,
+                              const int32_t* position_ids, const int32_t* cu_seqlens,
+                              int n_seq, int seq_len, int total_tokens, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!L || !x || !out || total_tokens < 0) return LLAMA_ERR_INVALID_ARG;
+  if (!L->bf16) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(out, 16) || x == out) return LLAMA_ERR_INVALID_ARG;
+  if (position_ids && !aligned(position_ids, 4)) return LLAMA_ERR_INVALID_ARG;
+  if (cu_seqlens && !aligned(cu_seqlens, 4)) return LLAMA_ERR_INVALID_ARG;
+  if (total_tokens == 0) return LLAMA_OK;
+  if (n_seq <= 0 || seq_len <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!cu_seqlens && (long)n_seq * seq_len != total_tokens) return LLAMA_ERR_INVALID_ARG;
+  if (cu_seqlens && (long)n_seq > total_tokens) return LLAMA_ERR_INVALID_ARG;
+  if (!position_ids && seq_len > L->cfg.max_position) return LLAMA_ERR_INVALID_ARG;
+  if ((size_t)seq_len * sizeof(float) > 200 * 1024) return LLAMA_ERR_UNSUPPORTED_SHAPE;
+  if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
+  const BwdLayout b = bwd_layout(L->cfg, total_tokens);
+  if (workspace_bytes < b.total) return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+  clobber(L, workspace, workspace_bytes);
+  char* ws = static_cast<char*>(workspace);
+  const FwdSaves sv = bwd_saves(b, ws);
+  const int rc = forward_impl(L, x, out, position_ids, cu_seqlens, n_seq, seq_len,
+                              total_tokens, ws, static_cast<cudaStream_t>(stream), &sv);
+  if (rc) return rc;
+  L->saved.ws = ws;
+  L->saved.bytes = workspace_bytes;
+  L->saved.x = x;
+  L->saved.pos = position_ids;
+  L->saved.cu = cu_seqlens;
+  L->saved.n_seq = n_seq;
+  L->saved.seq_len = seq_len;
+  L->saved.tokens = total_tokens;
+  L->saved.valid = true;
+  return LLAMA_OK;
+}
+
+int llama_layer_backward_saved(llama_layer_t* L, const llama_layer_weights* w, const void* x,
+                               const void* dout, void* dx, const llama_layer_grads* gr,
+                               const int32_t* position_ids, const int32_t* cu_seqlens,
+                               int n_seq, int seq_len, int total_tokens, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  int rc = check_backward(L, w, x, dout, dx, gr, position_ids, cu_seqlens, n_seq, seq_len,
+                          total_tokens, workspace, workspace_bytes);
+  if (rc || total_tokens == 0) return rc;
+  const auto& sv = L->saved;
+  if (!sv.valid || sv.ws != workspace || sv.x != x || sv.pos != position_ids ||
+      sv.cu != cu_seqlens || sv.n_seq != n_seq || sv.seq_len != seq_len ||
+      sv.tokens != total_tokens)
+    return LLAMA_ERR_INVALID_ARG;
+  // the backward writes only past the forward's activations: they stay
+  // valid for another backward from the same forward
+  return backward_impl(L, w, x, dout, dx, gr, position_ids, cu_seqlens, n_seq, seq_len,
+                       total_tokens, static_cast<char*>(workspace),
+                       static_cast<cudaStream_t>(stream), false);
 }
 
 namespace {
@@ -1073,6 +1177,7 @@ int llama_layer_forward_host(llama_layer_t* L, const void* x_host, void* out_hos
   if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
   if (workspace_bytes < ws_layout(L->cfg, total_tokens).total)
     return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+  clobber(L, workspace, workspace_bytes);
   int rc = host_setup(L);
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1145,6 +1250,7 @@ int llama_layer_decode(llama_layer_t* L, const void* x, void* out,
   if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
   if (workspace_bytes < decode_ws_bytes(L, batch, max_seq))
     return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+  clobber(L, workspace, workspace_bytes);
   return decode_impl(L, x, out, cache_k, cache_v, start_pos, batch, max_seq,
                      static_cast<char*>(workspace),
                      static_cast<cudaStream_t>(stream));
@@ -1166,6 +1272,7 @@ int llama_layer_forward_cached(llama_layer_t* L, const void* x, void* out,
   const long rows = (long)batch * seq_tokens;
   if (rows > (1L << 30)) return LLAMA_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
+  clobber(L, workspace, workspace_bytes);
   if (seq_tokens >= LLAMA_LONG_CHUNK) {
     // the prefill path over the cache: each prefix is read once per head
     // group rather than once per new token

@@ -103,33 +103,79 @@ class LlamaLayer:
             self.workspace.numel(), stream_ptr())
         return out
 
-    def backward(self, x, dout, position_ids=None, cu_seqlens=None, n_seq=None,
-                 seq_len=None, dx=None, grads=None):
-        """Gradients of the prefill layer given dL/d(out) (same batch layout
-        as forward): returns dict dx (bf16) and dw_qkv, dw_o, dw_gate_up,
-        dw_down, dg_in, dg_post (fp32, the weights' shapes)."""
+    @staticmethod
+    def _batch(x, cu_seqlens, n_seq, seq_len):
+        """(n_seq, seq_len) of a padded (cu_seqlens None) or packed batch."""
         T = x.shape[0]
         if cu_seqlens is None:
             seq_len = seq_len or T
-            n_seq = n_seq or (T // seq_len)
-        else:
-            n_seq = cu_seqlens.numel() - 1
-            assert seq_len is not None, "varlen needs max_seqlen"
+            return n_seq or (T // seq_len), seq_len
+        assert seq_len is not None, "varlen needs max_seqlen"
+        return cu_seqlens.numel() - 1, seq_len
+
+    def _ensure_backward_workspace(self, T) -> None:
         n = B.llama_layer_backward_workspace_bytes(self.handle, T)
         if self.workspace.numel() < n:
             self.workspace = torch.empty(n, dtype=torch.uint8, device=self.device)
-        if dx is None:
-            dx = torch.empty_like(x)
+
+    def forward_train(self, x, position_ids=None, cu_seqlens=None, n_seq=None,
+                      seq_len=None, out=None):
+        """The forward of a training step: the output as forward() computes
+        it, and the activations the backward reads kept in this layer's
+        workspace for backward_saved() (same x and batch layout)."""
+        T = x.shape[0]
+        n_seq, seq_len = self._batch(x, cu_seqlens, n_seq, seq_len)
+        self._ensure_backward_workspace(T)
+        if out is None:
+            out = torch.empty_like(x)
+        B.llama_layer_forward_train(
+            self.handle, x.data_ptr(), out.data_ptr(),
+            position_ids.data_ptr() if position_ids is not None else None,
+            cu_seqlens.data_ptr() if cu_seqlens is not None else None,
+            n_seq, seq_len, T, self.workspace.data_ptr(), self.workspace.numel(),
+            stream_ptr())
+        return out
+
+    def _grads(self, grads):
         if grads is None:
             names = ("dw_qkv", "dw_o", "dw_gate_up", "dw_down", "dg_in", "dg_post")
-            srcs = (self.weights[0], self.weights[1], self.weights[2], self.weights[3],
-                    self.weights[4], self.weights[5])
             grads = {k: torch.empty(w.shape, dtype=torch.float32, device=self.device)
-                     for k, w in zip(names, srcs)}
+                     for k, w in zip(names, self.weights)}
         g = B.llama_layer_grads(*[grads[k].data_ptr() for k in
                                   ("dw_qkv", "dw_o", "dw_gate_up", "dw_down", "dg_in",
                                    "dg_post")])
+        return grads, g
+
+    def backward(self, x, dout, position_ids=None, cu_seqlens=None, n_seq=None,
+                 seq_len=None, dx=None, grads=None):
+        """Gradients of the prefill layer given dL/d(out) (same batch layout
+        as forward), the forward recomputed: returns dict dx (bf16) and
+        dw_qkv, dw_o, dw_gate_up, dw_down, dg_in, dg_post (fp32, the weights'
+        shapes)."""
+        T = x.shape[0]
+        n_seq, seq_len = self._batch(x, cu_seqlens, n_seq, seq_len)
+        self._ensure_backward_workspace(T)
+        if dx is None:
+            dx = torch.empty_like(x)
+        grads, g = self._grads(grads)
         B.llama_layer_backward(
+            self.handle, self._wts, x.data_ptr(), dout.data_ptr(), dx.data_ptr(), g,
+            position_ids.data_ptr() if position_ids is not None else None,
+            cu_seqlens.data_ptr() if cu_seqlens is not None else None,
+            n_seq, seq_len, T, self.workspace.data_ptr(), self.workspace.numel(),
+            stream_ptr())
+        return dict(dx=dx, **grads)
+
+    def backward_saved(self, x, dout, position_ids=None, cu_seqlens=None, n_seq=None,
+                       seq_len=None, dx=None, grads=None):
+        """backward() from the activations the last forward_train() kept (the
+        same x, batch layout and workspace; the library refuses otherwise)."""
+        T = x.shape[0]
+        n_seq, seq_len = self._batch(x, cu_seqlens, n_seq, seq_len)
+        if dx is None:
+            dx = torch.empty_like(x)
+        grads, g = self._grads(grads)
+        B.llama_layer_backward_saved(
             self.handle, self._wts, x.data_ptr(), dout.data_ptr(), dx.data_ptr(), g,
             position_ids.data_ptr() if position_ids is not None else None,
             cu_seqlens.data_ptr() if cu_seqlens is not None else None,

@@ -142,6 +142,12 @@ def test_null_handles_are_rejected():
     assert L.llama_layer_forward_cached(None, None, None, None, None, None, 1, 1, 1,
                                         None, 0, None) == B.LLAMA_ERR_INVALID_ARG
     assert L.llama_layer_status(None, None) == B.LLAMA_ERR_INVALID_ARG
+    assert L.llama_layer_forward_train(None, None, None, None, None, 1, 1, 1, None, 0,
+                                       None) == B.LLAMA_ERR_INVALID_ARG
+    w, g = B.llama_layer_weights(), B.llama_layer_grads()
+    for f in (L.llama_layer_backward, L.llama_layer_backward_saved):
+        assert f(None, ctypes.byref(w), None, None, None, ctypes.byref(g), None, None, 1, 1,
+                 1, None, 0, None) == B.LLAMA_ERR_INVALID_ARG
     n = ctypes.c_size_t()
     assert L.llama_layer_workspace_bytes(None, 1, 0, 0, ctypes.byref(n)) == \
         B.LLAMA_ERR_INVALID_ARG
