@@ -910,8 +910,9 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
     roofline = None
     if dom:
         dom_ms = stage_ms[dom]
-        launches = "2 launches: split-KV + combine" if (
-            dom == "attention" and w.kind == "decode" and S_new < 4) else "1 launch"
+        launches = ("2 launches: split-KV + combine" if (
+            dom == "attention" and w.kind == "decode" and S_new < 4) else
+            "2 launches: dQ + dK/dV" if dom == "bwd_attention" else "1 launch")
         share = dom_ms / (sum(stage_ms.values()) or 1.0)
         if dom in work["flops"]:
             achieved = work["flops"][dom] / (dom_ms / 1e3) / 1e12
