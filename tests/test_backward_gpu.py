@@ -98,6 +98,12 @@ def check(inp, varlen, label, repeat=1):
      dict(total_tokens=400, min_len=1, max_len=40)),
     ("long_d64", shape(256, 4, 2, 64, 256, **L3), "padded", dict(batch=1, seq=700)),
     ("long_d128", shape(256, 2, 1, 128, 256, **L3), "padded", dict(batch=1, seq=600)),
+    # more work items than the 148 persistent CTAs in both attention kernels
+    # (288 each): a CTA carries its accumulators, rings and double buffers
+    # from one item to the next
+    ("many_items_d128", shape(512, 8, 8, 128, 256, **L3), "padded", dict(batch=12, seq=300)),
+    ("many_items_varlen_d64", shape(512, 16, 8, 64, 256), "varlen",
+     dict(total_tokens=3200, min_len=100, max_len=400)),
 ], ids=lambda c: c[0])
 def test_backward_matches_oracle(case):
     name, s, kind, kw = case

@@ -74,9 +74,11 @@ def test_train_step_equals_forward_and_backward(case):
 
 
 def test_saved_backward_matches_oracle_8b_shaped():
+    """The 8B-shaped layer on 16 x 256 tokens: M 4096 GEMM grids and more
+    attention work items than CTAs (256 for dK/dV, 1024 for dQ)."""
     s = synth.WORKLOADS["8b"].shape
     inp = synth.make_inputs(synth.custom_workload("train_8b_short", s, "padded", index=311,
-                                                  batch=2, seq=256))
+                                                  batch=16, seq=256))
     layer = build_layer(inp)
     x = to_device(inp.x)
     dout = to_device(synth.make_dout(inp))
