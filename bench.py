@@ -130,6 +130,16 @@ DEFAULT_STEPS = {"chunk64": 1000, "chunk512": 300, "bwd_8b": 200, "bwd_1b": 600,
 MODEL = {"model1b": ("1b", 16, 128256)}  # layer workload, layers, vocabulary
 
 
+def split_kv_attention(shape, seq_tokens: int) -> bool:
+    """Whether the library's chunked prefill of seq_tokens new tokens per
+    sequence uses the split-KV attention (groups of up to 16 / n_rep tokens
+    share a tile; at most two groups a sequence) rather than the tensor-core
+    attention over the cache (llama_layer.h, llama_layer_forward_cached)."""
+    n_rep = shape.n_heads // shape.n_kv_heads
+    tg = min(16 // n_rep, seq_tokens)
+    return seq_tokens < 16 and -(-seq_tokens // tg) <= 2
+
+
 def max_over_ranks(dist, x: float) -> float:
     """The largest x of all ranks (x itself without a process group): the
     job's time is its slowest replica's."""
@@ -911,7 +921,7 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
     if dom:
         dom_ms = stage_ms[dom]
         launches = ("2 launches: split-KV + combine" if (
-            dom == "attention" and w.kind == "decode" and S_new < 4) else
+            dom == "attention" and w.kind == "decode" and split_kv_attention(s, S_new)) else
             "2 launches: dQ + dK/dV" if dom == "bwd_attention" else "1 launch")
         share = dom_ms / (sum(stage_ms.values()) or 1.0)
         if dom in work["flops"]:

@@ -240,14 +240,15 @@ LLAMA_API int llama_layer_decode(llama_layer_t* layer, const void* x, void* out,
  * New token i of sequence b attends to cache rows 0 .. start_pos[b] + i.
  * seq_tokens = 1 is llama_layer_decode.  Short chunks (seq_tokens <
  * LLAMA_LONG_CHUNK, e.g. checking drafted tokens) run the decode
- * projections (weights streamed once for all rows); from 4 new tokens per
- * sequence on, their attention is the tensor-core attention reading the
- * cache, below that the decode kernels' split-KV attention.  Longer chunks
- * run the prefill kernels with the tensor-core attention.  The tensor-core
- * attention reads each prefix once per group of query heads; the keys of
- * cache rows past start_pos[b] + seq_tokens may be read but are masked (their
- * values are replaced by zeros on chip, so whatever those rows hold does not
- * matter).
+ * projections (weights streamed once for all rows).  Their attention is the
+ * split-KV attention, which reads each prefix once per group of up to
+ * 16 / (n_heads / n_kv_heads) new tokens, while a sequence has at most two
+ * such groups (up to 8 new tokens with 4 query heads per kv head), else the
+ * tensor-core attention reading each prefix once per group of query heads.
+ * Longer chunks run the prefill kernels with the tensor-core attention.  The
+ * keys of cache rows past start_pos[b] + seq_tokens may be read but are
+ * masked (the tensor-core attention replaces their values by zeros on chip,
+ * so whatever those rows hold does not matter).
  * bf16 layers; an fp32 layer takes seq_tokens = 1 only
  * (LLAMA_ERR_UNSUPPORTED_SHAPE).  `workspace` must hold
  * llama_layer_workspace_bytes(layer, 0, >= batch * seq_tokens, >= max_seq)

@@ -201,13 +201,16 @@ __global__ void __launch_bounds__(FT) finalize_down_kernel(DecodeArgs a,
 }
 
 // ------------------------------------------------------------ attention
-// Split-KV: CTA (split c, kv head g, token row b) takes rows
-// [KS c, min(KS c + KS, sp + 1)) of the cache of the row's sequence (sp its
-// position, row_seq_pos) and the n_rep query heads of g (the
-// rows of one 16-row MMA tile).  The rows stream through a 3-stage cp.async
-// ring of 64-key tiles; each of the 4 warps scores 16 keys of a tile with
-// mma.sync (S = Q K^T), keeps its own online softmax (log2 domain) and P V
-// accumulator, and the warps merge at the end into one (O, m, l) record.
+// Split-KV: CTA (split c, kv head g, group z) takes a.tg consecutive new
+// tokens of one sequence (positions sp0 .. sp0 + ntok - 1, row_seq_pos) and
+// the n_rep query heads of g for each: row R = t n_rep + r of one 16-row MMA
+// tile is token t, head r.  It reads cache rows [KS c, min(KS c + KS,
+// last position + 1)) of the sequence once for all of them; row R sees the
+// keys up to its own token's position (the chunk's later keys are masked).
+// The rows stream through a 3-stage cp.async ring of 64-key tiles; each of
+// the 4 warps scores 16 keys of a tile with mma.sync (S = Q K^T), keeps its
+// own online softmax (log2 domain) and P V accumulator, and the warps merge
+// at the end into one (O, m, l) record per token.
 constexpr int KS = 512;  // keys per split
 constexpr int KT = 64;   // keys per tile
 constexpr int NST = 3;   // ring stages
@@ -222,23 +225,40 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
   bf16* sQ = reinterpret_cast<bf16*>(smem);
   bf16* sK = sQ + 16 * P;            // [NST][KT][P]
   bf16* sV = sK + NST * KT * P;      // [NST][KT][P]
-  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  int seq, sp;
-  row_seq_pos(a, b, seq, sp);
-  if (!start_ok(sp, a)) return;
-  const int n_keys = sp + 1, k0 = c * KS;
+  const int c = blockIdx.x, g = blockIdx.y, z = blockIdx.z;
+  // the group's tokens: rows b0 .. b0 + ntok - 1 of the pass
+  const int sq = z / a.gps, t0 = (z - sq * a.gps) * a.tg;
+  const int b0 = sq * a.seq_tokens + t0;
+  int seq, sp0;
+  row_seq_pos(a, b0, seq, sp0);
+  if (!start_ok(sp0, a)) return;
+  // tokens whose positions fit the cache and the RoPE table (the rest are
+  // left to the combine kernel, which writes zeros for them)
+  int ntok = min(a.tg, a.seq_tokens - t0);
+  while (ntok > 1 && !start_ok(sp0 + ntok - 1, a)) --ntok;
+  const int n_keys = sp0 + ntok, k0 = c * KS;
   if (k0 >= n_keys) return;
   const int k1 = min(k0 + KS, n_keys);
   const int n_tiles = (k1 - k0 + KT - 1) / KT;
   const int n_rep = a.n_heads / a.n_kv_heads;
+  const int rows = ntok * n_rep;  // <= 16
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
 
-  // ---- Q rows (zero beyond n_rep), part of the first cp.async group
+  // ---- Q rows (zero beyond rows), part of the first cp.async group
   for (int idx = tid; idx < 16 * CH; idx += 128) {
     const int row = idx / CH, ch = idx % CH;
-    const bf16* src = a.qkv + (size_t)b * a.nqkv +
-                      (g * n_rep + (row < n_rep ? row : 0)) * D + ch * 8;
-    cp_async16(smem_u32(sQ + row * P + ch * 8), src, row < n_rep ? 16 : 0);
+    const int rr = row < rows ? row : 0;
+    const bf16* src = a.qkv + (size_t)(b0 + rr / n_rep) * a.nqkv +
+                      (g * n_rep + rr % n_rep) * D + ch * 8;
+    cp_async16(smem_u32(sQ + row * P + ch * 8), src, row < rows ? 16 : 0);
+  }
+  // the last key each of this thread's two accumulator rows sees (-1: an
+  // empty row)
+  int lim[2];
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int R = lane / 4 + 8 * hr;
+    lim[hr] = R < rows ? sp0 + R / n_rep : -1;
   }
   const size_t row_stride = (size_t)a.n_kv_heads * D;
   const bf16* kbase = a.cache_k + (size_t)seq * a.max_seq * row_stride + g * D;
@@ -291,7 +311,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
       for (int e = 0; e < 4; ++e) {
         const int key = k0 + j * KT + warp * 16 + nt * 8 + 2 * (lane % 4) + (e & 1);
         float v = sacc[nt][e] * scale;
-        if (key >= k1) v = -INFINITY;
+        if (key >= k1 || key > lim[e >> 1]) v = -INFINITY;
         sacc[nt][e] = v;
         tmax[e >> 1] = fmaxf(tmax[e >> 1], v);
       }
@@ -344,7 +364,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
     lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 1);
     lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 2);
   }
-  // ---- merge the 4 warps (rows < n_rep only) through shared memory
+  // ---- merge the 4 warps (the group's rows only) through shared memory
   __syncthreads();
   float* sO = reinterpret_cast<float*>(sK);  // [4 warps][16 rows][D]
   float* sM = sO + 4 * 16 * D;               // [4][16]
@@ -366,26 +386,27 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
   }
   __syncthreads();
   const int rec = a.n_rep_rec;  // floats per record: n_rep * (D + 2)
-  float* outp = a.attn_part +
-                (((size_t)b * a.n_kv_heads + g) * a.max_chunks + c) * rec;
-  for (int idx = tid; idx < n_rep * D; idx += 128) {
-    const int row = idx / D, col = idx % D;
+  for (int idx = tid; idx < rows * D; idx += 128) {
+    const int R = idx / D, col = idx % D;  // tile row R: token R / n_rep, head row
+    const int row = R % n_rep;
+    float* outp = a.attn_part +
+                  (((size_t)(b0 + R / n_rep) * a.n_kv_heads + g) * a.max_chunks + c) * rec;
     float m = -INFINITY;
-    for (int w = 0; w < 4; ++w) m = fmaxf(m, sM[w * 16 + row]);
+    for (int w = 0; w < 4; ++w) m = fmaxf(m, sM[w * 16 + R]);
     const float mr = m == -INFINITY ? 0.f : m;
     float o = 0.f;
     for (int w = 0; w < 4; ++w) {
-      const float mw = sM[w * 16 + row];
+      const float mw = sM[w * 16 + R];
       const float mwr = mw == -INFINITY ? 0.f : mw;
-      o += exp2f(mwr - mr) * sO[(w * 16 + row) * D + col];
+      o += exp2f(mwr - mr) * sO[(w * 16 + R) * D + col];
     }
     outp[row * D + col] = o;
     if (col == 0) {
       float l = 0.f;
       for (int w = 0; w < 4; ++w) {
-        const float mw = sM[w * 16 + row];
+        const float mw = sM[w * 16 + R];
         const float mwr = mw == -INFINITY ? 0.f : mw;
-        l += exp2f(mwr - mr) * sL[w * 16 + row];
+        l += exp2f(mwr - mr) * sL[w * 16 + R];
       }
       outp[n_rep * D + row] = mr;
       outp[n_rep * D + n_rep + row] = l;
@@ -492,7 +513,9 @@ cudaError_t decode_finalize(int stage, const DecodeArgs& a,
 }
 
 cudaError_t decode_attention(const DecodeArgs& a, cudaStream_t s) {
-  dim3 grid(a.max_chunks, a.n_kv_heads, a.batch);
+  // a pass of several tokens per sequence holds whole sequences
+  if (a.tg < 1 || a.gps < 1 || a.batch % a.seq_tokens != 0) return cudaErrorInvalidValue;
+  dim3 grid(a.max_chunks, a.n_kv_heads, (a.batch / a.seq_tokens) * a.gps);
   size_t smem = attn_decode_smem(a.head_dim);
   if (a.head_dim == 128) {
     static std::atomic<uint64_t> attr_done{0};

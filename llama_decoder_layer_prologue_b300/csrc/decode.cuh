@@ -32,6 +32,10 @@ struct DecodeArgs {
   __half* attn;            // [B, Hq * D] fp16
   float* attn_part;        // split-KV records
   int max_chunks, n_rep_rec;
+  // split-KV attention groups: tg consecutive new tokens of one sequence
+  // share a CTA's 16-row MMA tile (tg * n_rep <= 16), gps groups per
+  // sequence; a pass of seq_tokens > 1 holds whole sequences
+  int tg, gps;
   __half* hg;              // [B, H] fp16(h * kHgScale): gate_up operand, residual
   __half* act;             // [B, I] fp16(act * kActScale)
   __nv_bfloat16* out;      // [B, H]
@@ -42,8 +46,9 @@ struct DecodeArgs {
 cudaError_t decode_finalize(int stage, const DecodeArgs& a,
                             const TcStreamK& plan, cudaStream_t s);
 
-// Split-KV attention of every new token over cache rows 0..start_pos[b],
-// then the log-sum-exp combine into a.attn.
+// Split-KV attention of every new token over cache rows 0 .. its position
+// (groups of a.tg tokens of a sequence read each key once), then the
+// log-sum-exp combine into a.attn.
 cudaError_t decode_attention(const DecodeArgs& a, cudaStream_t s);
 
 // Long chunks of new tokens (the tensor-core prefill attention over the

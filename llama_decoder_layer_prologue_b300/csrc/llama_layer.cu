@@ -633,7 +633,12 @@ int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
 }
 
 constexpr int kDecodeChunk = 256;  // tokens per decode pass (<= GEMM bn)
-constexpr int kCachedAttnMin = 4;  // new tokens per sequence for the tensor-core attention
+// Short chunks: the split-KV attention reads each sequence's prefix once per
+// group of up to 16 / n_rep new tokens; with more groups than this the
+// tensor-core attention over the cache (one read, 128-row tiles mostly
+// empty) is faster (8B-shaped layer, 16 sequences, prefixes 512..8191: 4 new
+// tokens 74 against 160 us, 8: 124 against 161, 12: 177 against 162).
+constexpr int kMaxPrefixReads = 2;
 
 int decode_bn(int B) { return B <= 64 ? 64 : (B <= 128 ? 128 : 256); }
 
@@ -704,6 +709,11 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   a.attn = reinterpret_cast<__half*>(ws + w.attn);
   a.attn_part = reinterpret_cast<float*>(ws + w.attn_part);
   a.max_chunks = w.max_chunks; a.n_rep_rec = w.rec;
+  {
+    const int n_rep = dm.Hq / dm.Hkv;  // <= 16 (check_config)
+    a.tg = 16 / n_rep < seq_tokens ? 16 / n_rep : seq_tokens;
+    a.gps = (seq_tokens + a.tg - 1) / a.tg;
+  }
   a.hg = reinterpret_cast<__half*>(ws + w.hg);
   a.act = reinterpret_cast<__half*>(ws + w.act);
   a.out = static_cast<__nv_bfloat16*>(out);
@@ -743,14 +753,13 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   // a2 + a3 + cache append.
   int rc = project(DEC_QKV, L->ta_wqkv, ws + w.xn, dm.Nqkv, dm.H);
   if (rc) return rc;
-  // a6: attention over cache rows 0 .. position.  Up to kCachedAttnMin - 1
-  // new tokens per sequence: the split-KV decode attention (each prefix
-  // spread over many CTAs, read once per new token).  More (a pass of whole
-  // sequences): the tensor-core prefill attention over the cache, which reads
-  // each prefix once per group of query heads (measured on 16 x 4 new tokens
-  // of the 8B-shaped layer: 166 us against 189 us).
+  // a6: attention over cache rows 0 .. position.  Up to kMaxPrefixReads
+  // groups of new tokens per sequence: the split-KV decode attention (each
+  // prefix spread over many CTAs, read once per group).  More: the
+  // tensor-core prefill attention over the cache, which reads each prefix
+  // once per group of query heads.  A pass holds whole sequences.
   mark(L, s, "attention");
-  if (seq_tokens >= kCachedAttnMin && row0 % seq_tokens == 0 && B % seq_tokens == 0) {
+  if (a.gps > kMaxPrefixReads && row0 % seq_tokens == 0 && B % seq_tokens == 0) {
     const size_t seq0 = (size_t)(row0 / seq_tokens);
     const size_t cache_seq = (size_t)max_seq * dm.Hkv * dm.d;
     AttnArgs aa;
@@ -793,9 +802,8 @@ int decode_impl(llama_layer* L, const void* x, void* out, void* ck, void* cv,
     const size_t es = 2, row = (size_t)dm.H * es;
     // passes of <= kDecodeChunk rows, in order: a pass's rows see the cache
     // rows every earlier pass (and their own) appended; chunks of several
-    // tokens pass whole sequences (the tensor-core attention takes whole
-    // chunks)
-    const int pass = seq_tokens >= kCachedAttnMin && seq_tokens <= kDecodeChunk
+    // tokens pass whole sequences (both attentions take whole chunks)
+    const int pass = seq_tokens >= 2 && seq_tokens <= kDecodeChunk
                          ? kDecodeChunk / seq_tokens * seq_tokens : kDecodeChunk;
     for (int b0 = 0; b0 < B; b0 += pass) {
       const int nb = B - b0 < pass ? B - b0 : pass;

@@ -247,9 +247,19 @@ def check_cached(s, batch, S, max_seq, start_pos):
     layer.close()
 
 
-@pytest.mark.parametrize("S", [1, 3, 4, 8])
-def test_forward_cached_chunks(S):
-    s = shape(256, 4, 2, 64, 256, **L3)
+@pytest.mark.parametrize("S,hq,hkv", [
+    # 2 query heads per kv head: up to 8 new tokens share one split-KV tile
+    (1, 4, 2), (3, 4, 2), (4, 4, 2), (8, 4, 2),
+    # one head per kv head: 15 tokens in one 16-row tile
+    (15, 4, 4),
+    # 8 query heads per kv head: groups of 2 tokens; 4 tokens are two groups
+    # (split-KV), 5 are three (the tensor-core attention over the cache)
+    (4, 8, 1), (5, 8, 1),
+    # 4 query heads per kv head, 12 tokens: three groups of 4 (tensor core)
+    (12, 8, 2),
+])
+def test_forward_cached_chunks(S, hq, hkv):
+    s = shape(64 * hq, hq, hkv, 64, 256, **L3)
     # includes an empty prefix and a chunk ending on the last cache row
     check_cached(s, batch=5, S=S, max_seq=300, start_pos=[0, 123, 1, 300 - S, 77])
 
@@ -272,8 +282,9 @@ def test_forward_cached_long_chunks(S, d, hq, hkv, max_seq, start_pos):
     check_cached(s, batch=len(start_pos), S=S, max_seq=max_seq, start_pos=start_pos)
 
 
-def test_forward_cached_pass_boundary_inside_a_sequence():
-    # 40 x 7 = 280 rows: the 256-row passes split sequence 36 after 4 tokens
+def test_forward_cached_two_passes():
+    # 40 x 7 = 280 rows: passes of whole sequences (36 x 7 = 252 rows, then
+    # 28); the second pass's attention sees what the first appended
     s = shape(256, 4, 2, 64, 256, **L3)
     sp = [(29 * b) % 180 for b in range(40)]
     check_cached(s, batch=40, S=7, max_seq=192, start_pos=sp)

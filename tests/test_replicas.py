@@ -11,6 +11,7 @@ import torch.distributed as dist
 import torch.multiprocessing as mp
 
 import bench
+from llama_decoder_layer_prologue_b300 import synth
 
 
 def _free_port() -> int:
@@ -82,3 +83,15 @@ def test_headline_also_runs_the_other_layer_workloads():
     assert bench.also_list(ns(workload="1b")) == []
     assert bench.also_list(ns(also="none")) == []
     assert bench.also_list(ns(also="8b,varlen")) == ["8b"]
+
+
+def test_split_kv_route_follows_the_library():
+    """The bench's label of the chunked attention follows the library's
+    route: split-KV while a sequence's new tokens form at most two groups of
+    16 / n_rep, else the tensor-core attention over the cache."""
+    s8 = synth.WORKLOADS["8b"].shape  # 4 query heads per kv head: groups of 4
+    assert [bench.split_kv_attention(s8, S) for S in (1, 4, 8, 9, 12, 15)] == \
+        [True, True, True, False, False, False]
+    mha = synth.custom_workload("m", synth.WORKLOADS["tiny"].shape, "decode").shape
+    assert mha.n_heads // mha.n_kv_heads == 2  # groups of 8
+    assert bench.split_kv_attention(mha, 15) and not bench.split_kv_attention(mha, 17)

@@ -1,7 +1,8 @@
-"""The five workloads at their full sizes, in the launch configuration the
-bench times.  Prefill workloads compare every row of every stage (q|k|v,
+"""The workloads at their full sizes, in the launch configuration the bench
+times.  Prefill workloads compare every row of every stage (q|k|v,
 attention, h, act, output) with the oracle run on the whole batch; decode
-compares every sequence and the cache rows written."""
+and the 16 x 4 chunked prefill compare every new token and the cache rows
+written."""
 
 import numpy as np
 import pytest
@@ -66,4 +67,29 @@ def test_decode_workload():
     sp = torch.as_tensor(inp.start_pos, device="cuda").long()
     assert_stage_close(to_f64(ck[b_idx, sp]), ref["k_new"], s.dtype, "k rows")
     assert_stage_close(to_f64(cv[b_idx, sp]), ref["v_new"], s.dtype, "v rows")
+    layer.close()
+
+
+def test_chunked_workload():
+    """16 sequences x 4 new tokens against 8192-row caches (prefixes
+    512..8188): the split-KV attention with the four tokens of a sequence in
+    one tile, reading each prefix once."""
+    inp = synth.make_inputs("chunked")
+    s = inp.workload.shape
+    S = inp.workload.seq_tokens
+    layer = build_layer(inp)
+    ck = to_device(poison_cache(inp.cache_k, inp.start_pos))
+    cv = to_device(poison_cache(inp.cache_v, inp.start_pos))
+    out = layer.forward_cached(to_device(inp.x), ck, cv, to_device(inp.start_pos), S)
+    torch.cuda.synchronize()
+    assert layer.status() == B.LLAMA_OK
+    rows = lambda b, n: (synth.to_f64(inp.cache_k[b, :n]),
+                         synth.to_f64(inp.cache_v[b, :n]))
+    ref = oracle.decoder_layer_cached(synth.to_f64(inp.x), weights_f64(inp.weights), s,
+                                      rows, inp.start_pos, S)
+    assert_close(to_f64(out), ref["out"], s.dtype, "chunked out")
+    for b, p in enumerate(inp.start_pos):
+        new = slice(b * S, (b + 1) * S)
+        assert_stage_close(to_f64(ck[b, p:p + S]), ref["k_new"][new], s.dtype, "k rows")
+        assert_stage_close(to_f64(cv[b, p:p + S]), ref["v_new"][new], s.dtype, "v rows")
     layer.close()
