@@ -215,16 +215,43 @@ constexpr int KS = 512;  // keys per split
 constexpr int KT = 64;   // keys per tile
 constexpr int NST = 3;   // ring stages
 
+// Shared memory of the split-KV kernel: NST stages of K and V tiles (D / 64
+// swizzle atoms of KT rows x 128 bytes each, as TMA writes them with the
+// 128-byte swizzle), then the 16 padded Q rows and the stages' mbarriers.
 template <int D>
-__global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
+struct DecSmem {
+  static constexpr uint32_t TILE = KT * D * 2;  // one K or V tile
+  static constexpr uint32_t P = D + 8;          // padded Q row (bf16 elements)
+  static constexpr uint32_t K_OFF = 0, V_OFF = NST * TILE, Q_OFF = 2 * NST * TILE;
+  static constexpr uint32_t BAR_OFF = Q_OFF + 16 * P * 2;
+  static constexpr uint32_t TOTAL = BAR_OFF + 64 + 1024;  // + alignment slack
+  // the warps' merge reuses the K stages: [4][16][D] fp32 O, [4][16] m, l
+  static_assert(4 * 16 * D * 4 + 2 * 4 * 16 * 4 <= NST * TILE, "merge space");
+};
+
+// Byte offset of 16-byte chunk c (of the row's D / 8) of row r in a tile.
+template <int D>
+__device__ __forceinline__ uint32_t dec_tile_off(int r, int c) {
+  return (uint32_t)((c / 8) * (KT * 128) + r * 128 + (((c % 8) ^ (r & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) attn_decode_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                          const __grid_constant__ CUtensorMap tmV,
+                                                          DecodeArgs a) {
   pdl_trigger();
   pdl_wait();
-  constexpr int P = D + 8;  // padded row (bf16 elements): conflict-free ldmatrix
+  using L = DecSmem<D>;
+  constexpr int P = L::P;
   constexpr int CH = D / 8;  // 16-byte chunks per row
-  extern __shared__ __align__(16) uint8_t smem[];
-  bf16* sQ = reinterpret_cast<bf16*>(smem);
-  bf16* sK = sQ + 16 * P;            // [NST][KT][P]
-  bf16* sV = sK + NST * KT * P;      // [NST][KT][P]
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem + L::K_OFF;  // [NST][TILE]
+  uint8_t* sV = smem + L::V_OFF;  // [NST][TILE]
+  bf16* sQ = reinterpret_cast<bf16*>(smem + L::Q_OFF);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);  // [NST]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + NST);
   const int c = blockIdx.x, g = blockIdx.y, z = blockIdx.z;
   // the group's tokens: rows b0 .. b0 + ntok - 1 of the pass
   const int sq = z / a.gps, t0 = (z - sq * a.gps) * a.tg;
@@ -244,13 +271,39 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
   const int rows = ntok * n_rep;  // <= 16
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
 
-  // ---- Q rows (zero beyond rows), part of the first cp.async group
+  if (tid == 0) {
+    for (int st = 0; st < NST; ++st) mbar_init(&full[st], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  // ---- Q rows (zero beyond rows)
   for (int idx = tid; idx < 16 * CH; idx += 128) {
     const int row = idx / CH, ch = idx % CH;
     const int rr = row < rows ? row : 0;
     const bf16* src = a.qkv + (size_t)(b0 + rr / n_rep) * a.nqkv +
                       (g * n_rep + rr % n_rep) * D + ch * 8;
     cp_async16(smem_u32(sQ + row * P + ch * 8), src, row < rows ? 16 : 0);
+  }
+  cp_async_commit();
+  __syncthreads();  // the barriers are initialised
+  // K / V tile j: cache rows seq * max_seq + k0 + KT j .. of kv head g, one
+  // TMA box per 64 columns (rows past the tensor come back as zeros)
+  const int crow = seq * a.max_seq + k0;
+  auto issue = [&](int j) {
+    const int st = j % NST;
+    mbar_arrive_expect_tx(&full[st], 2 * L::TILE);
+#pragma unroll
+    for (int at = 0; at < D / 64; ++at) {
+      tma_load_2d(sK + st * L::TILE + at * (KT * 128), &tmK, &full[st], g * D + at * 64,
+                  crow + j * KT);
+      tma_load_2d(sV + st * L::TILE + at * (KT * 128), &tmV, &full[st], g * D + at * 64,
+                  crow + j * KT);
+    }
+  };
+  if (tid == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    for (int j = 0; j < NST - 1 && j < n_tiles; ++j) issue(j);
   }
   // the last key each of this thread's two accumulator rows sees (-1: an
   // empty row)
@@ -260,38 +313,32 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
     const int R = lane / 4 + 8 * hr;
     lim[hr] = R < rows ? sp0 + R / n_rep : -1;
   }
-  const size_t row_stride = (size_t)a.n_kv_heads * D;
-  const bf16* kbase = a.cache_k + (size_t)seq * a.max_seq * row_stride + g * D;
-  const bf16* vbase = a.cache_v + (size_t)seq * a.max_seq * row_stride + g * D;
-  auto load_tile = [&](int j, int st) {
-    bf16* dk = sK + st * KT * P;
-    bf16* dv = sV + st * KT * P;
-    for (int idx = tid; idx < KT * CH; idx += 128) {
-      const int row = idx / CH, ch = idx % CH;
-      const int key = k0 + j * KT + row;
-      const bool ok = key < k1;
-      const size_t off = (ok ? (size_t)key * row_stride : 0) + ch * 8;
-      cp_async16(smem_u32(dk + row * P + ch * 8), kbase + off, ok ? 16 : 0);
-      cp_async16(smem_u32(dv + row * P + ch * 8), vbase + off, ok ? 16 : 0);
-    }
-  };
-#pragma unroll
-  for (int st = 0; st < NST - 1; ++st) {
-    if (st < n_tiles) load_tile(st, st);
-    cp_async_commit();
-  }
+  cp_async_wait<0>();
 
   const float scale = 1.4426950408889634f * rsqrtf((float)D);  // log2(e)/sqrt(d)
   float oacc[D / 8][4] = {};
   float mrow[2] = {-INFINITY, -INFINITY};
   float lrow[2] = {0.f, 0.f};
-  for (int j = 0; j < n_tiles; ++j) {
-    if (j + NST - 1 < n_tiles) load_tile(j + NST - 1, (j + NST - 1) % NST);
-    cp_async_commit();
-    cp_async_wait<NST - 1>();
-    __syncthreads();
-    const bf16* tk = sK + (j % NST) * KT * P;
-    const bf16* tv = sV + (j % NST) * KT * P;
+  bool ok = true;
+  int j = 0;
+  for (; j < n_tiles; ++j) {
+    // stage (j - 1) % NST was released by the barrier that ended iteration j - 1
+    if (tid == 0 && j + NST - 1 < n_tiles) issue(j + NST - 1);
+    ok = __syncthreads_and(mbar_wait(&full[j % NST], (j / NST) & 1, a.status, abort_flag));
+    if (!ok) break;
+    const uint32_t tk = smem_u32(sK + (j % NST) * L::TILE);
+    const uint32_t tv = smem_u32(sV + (j % NST) * L::TILE);
+    if (k0 + (j + 1) * KT > k1) {
+      // the split's last tile: V rows past its last key hold whatever the
+      // cache holds there (P is 0 for them, but 0 * NaN would not be)
+      uint8_t* vz = sV + (j % NST) * L::TILE;
+      const int r0 = k1 - (k0 + j * KT);
+      for (int idx = tid; idx < (KT - r0) * CH; idx += 128) {
+        const int r = r0 + idx / CH, ch = idx % CH;
+        *reinterpret_cast<uint4*>(vz + dec_tile_off<D>(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncthreads();
+    }
     // S = Q K^T for this warp's 16 keys (2 n-tiles of 8)
     float sacc[2][4] = {};
 #pragma unroll
@@ -299,7 +346,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
       uint32_t af[4], bfr[4];
       ldsm_x4(af, smem_u32(sQ + (lane % 16) * P + kk * 16 + (lane / 16) * 8));
       const int krow = warp * 16 + (lane / 16) * 8 + (lane % 8);
-      ldsm_x4(bfr, smem_u32(tk + krow * P + kk * 16 + ((lane / 8) % 2) * 8));
+      ldsm_x4(bfr, tk + dec_tile_off<D>(krow, kk * 2 + (lane / 8) % 2));
       mma_16816(sacc[0], af, bfr[0], bfr[1]);
       mma_16816(sacc[1], af, bfr[2], bfr[3]);
     }
@@ -352,13 +399,23 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
     for (int dt = 0; dt < D / 8; dt += 2) {
       uint32_t vf[4];
       const int vrow = warp * 16 + (lane % 8) + ((lane / 8) % 2) * 8;
-      ldsm_x4_t(vf, smem_u32(tv + vrow * P + dt * 8 + (lane / 16) * 8));
+      ldsm_x4_t(vf, tv + dec_tile_off<D>(vrow, dt + lane / 16));
       mma_16816(oacc[dt], pf, vf[0], vf[1]);
       mma_16816(oacc[dt + 1], pf, vf[2], vf[3]);
     }
     __syncthreads();  // stage j % NST is refilled by iteration j + 1
   }
-  cp_async_wait<0>();
+  if (!ok) {
+    // a load that never landed (status already set): let the other copies
+    // issued into this block's shared memory land (bounded), then leave
+    if (tid == 0) {
+      volatile int own = 0;
+      for (int jj = j + 1; jj < n_tiles && jj < j + NST; ++jj)
+        mbar_wait(&full[jj % NST], (jj / NST) & 1, a.status, &own);
+    }
+    __syncthreads();
+    return;
+  }
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
     lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 1);
@@ -366,7 +423,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(DecodeArgs a) {
   }
   // ---- merge the 4 warps (the group's rows only) through shared memory
   __syncthreads();
-  float* sO = reinterpret_cast<float*>(sK);  // [4 warps][16 rows][D]
+  float* sO = reinterpret_cast<float*>(sK);  // [4 warps][16 rows][D] over the K stages
   float* sM = sO + 4 * 16 * D;               // [4][16]
   float* sL = sM + 4 * 16;                   // [4][16]
   const int r0 = lane / 4;
@@ -485,10 +542,7 @@ __global__ void __launch_bounds__(CT) attn_combine_kernel(DecodeArgs a) {
 }  // namespace
 
 size_t attn_decode_smem(int head_dim) {
-  const size_t P = head_dim + 8;
-  size_t load = (16 + 2 * NST * KT) * P * sizeof(bf16);
-  size_t merge = 16 * P * 2 + (size_t)4 * 16 * head_dim * 4 + 2 * 4 * 16 * 4;
-  return load > merge ? load : merge;
+  return head_dim == 128 ? DecSmem<128>::TOTAL : DecSmem<64>::TOTAL;
 }
 
 int attn_decode_chunks(int max_seq) { return (max_seq + KS - 1) / KS; }
@@ -516,20 +570,29 @@ cudaError_t decode_attention(const DecodeArgs& a, cudaStream_t s) {
   // a pass of several tokens per sequence holds whole sequences
   if (a.tg < 1 || a.gps < 1 || a.batch % a.seq_tokens != 0) return cudaErrorInvalidValue;
   dim3 grid(a.max_chunks, a.n_kv_heads, (a.batch / a.seq_tokens) * a.gps);
-  size_t smem = attn_decode_smem(a.head_dim);
+  // the caches as [sequences x max_seq rows, kv heads x D] bf16, up to the
+  // pass's last sequence; tiles of 64 rows x 64 columns
+  const uint64_t n_seq = (uint64_t)(a.row0 + a.batch - 1) / a.seq_tokens + 1;
+  CUtensorMap tk, tv;
+  if (!tc_encode_bf16(&tk, a.cache_k, n_seq * a.max_seq, (uint64_t)a.n_kv_heads * a.head_dim,
+                      KT) ||
+      !tc_encode_bf16(&tv, a.cache_v, n_seq * a.max_seq, (uint64_t)a.n_kv_heads * a.head_dim,
+                      KT))
+    return cudaErrorInvalidValue;
+  const size_t smem = attn_decode_smem(a.head_dim);
   if (a.head_dim == 128) {
     static std::atomic<uint64_t> attr_done{0};
     if (cudaError_t e = ensure_smem_attr(attn_decode_kernel<128>, (int)smem, attr_done);
         e != cudaSuccess)
       return e;
-    cudaError_t e = launch_pdl(attn_decode_kernel<128>, grid, dim3(128), smem, s, a);
+    cudaError_t e = launch_pdl(attn_decode_kernel<128>, grid, dim3(128), smem, s, tk, tv, a);
     if (e != cudaSuccess) return e;
   } else {
     static std::atomic<uint64_t> attr_done{0};
     if (cudaError_t e = ensure_smem_attr(attn_decode_kernel<64>, (int)smem, attr_done);
         e != cudaSuccess)
       return e;
-    cudaError_t e = launch_pdl(attn_decode_kernel<64>, grid, dim3(128), smem, s, a);
+    cudaError_t e = launch_pdl(attn_decode_kernel<64>, grid, dim3(128), smem, s, tk, tv, a);
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = cudaGetLastError();
