@@ -282,9 +282,12 @@ def algorithmic_work_backward(inp) -> dict:
         "bwd_dw_o": 2.0 * T * H * q, "bwd_dattn": 2.0 * T * H * q,
         "bwd_attention": 2.5 * f["attention"],
         "bwd_dw_qkv": 2.0 * T * nqkv * H, "bwd_dx_attn": 2.0 * T * nqkv * H})
+    # the norm-weight gradients' per-32-row-group column sums, added up
+    groups = 8 * (-(-nqkv // 256) + -(-(2 * I) // 256))
     by = {"rmsnorm_stats": float(T * H * 2), "bwd_dout_f16": float(T * H * 4),
           "bwd_norm2": float(T * H * (2 + 4 + 2 + 4 + 2)),
-          "bwd_norm1": float(T * H * (4 + 4 + 2 + 2))}
+          "bwd_norm1": float(T * H * (4 + 4 + 2 + 2)),
+          "bwd_dg": float(groups * H * 4 + 2 * H * 4)}
     return dict(kind="prefill", flops=flops, total_flops=sum(flops.values()), bytes=by,
                 weight_bytes=w["weight_bytes"])
 

@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(FT) finalize_o_kernel(DecodeArgs a,
   st_f16x4(a.hg + (size_t)b * H + n,
            make_float4(h.x * kHgScale, h.y * kHgScale, h.z * kHgScale, h.w * kHgScale));
   const float ss = warp_sum(h.x * h.x + h.y * h.y + h.z * h.z + h.w * h.w);
-  if (lane == 0) atomicAdd(a.ss2 + b, ss);
+  if (lane == 0) a.ss2[(size_t)b * a.ss_np + t] = ss;  // this tile's slot
 }
 
 // act = silu(r2 gate) * (r2 up); packed tiles 2k / 2k+1 are the gate / up
@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(FT) finalize_gu_kernel(DecodeArgs a,
   const int k = blockIdx.x, b = blockIdx.y * FB + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= a.batch) return;
-  const float ss = a.ss2[b];
+  float ss = 0.f;  // the o_proj tiles' slots, in tile order
+  for (int i = 0; i < a.ss_np; ++i) ss += a.ss2[(size_t)b * a.ss_np + i];
   const float4 gs = gather_rows(a, plan, 2 * k, b);
   const float4 us = gather_rows(a, plan, 2 * k + 1, b);
   const float r2 = rsqrtf(ss * (1.0f / a.hidden) + a.eps) / kHgScale;

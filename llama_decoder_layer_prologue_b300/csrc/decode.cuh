@@ -24,7 +24,8 @@ struct DecodeArgs {
   const float* part;  // stream-K partials of the current projection
   const __nv_bfloat16* x;  // [B, H] layer input
   const float* r1;         // [B] 1/RMS(x)
-  float* ss2;              // [B] sum of h^2 (zeroed before DEC_O)
+  float* ss2;              // [B, ss_np] sum of h^2 over each o_proj tile's rows
+  int ss_np;               // o_proj output tiles (H / 128)
   const int32_t* start_pos;  // [sequences] of the whole call
   const float *cos_t, *sin_t;
   __nv_bfloat16* qkv;      // [B, nqkv]

@@ -176,7 +176,11 @@ __device__ __forceinline__ void epilogue_prefetch(EpiPre& pre, int row, bool val
     ld_words<32>(ep.cos_t + (size_t)p * half, pre.cs, true);
     ld_words<32>(ep.sin_t + (size_t)p * half, pre.sn, true);
   } else if constexpr (EPI == TC_SWIGLU || EPI == TC_SWIGLU_BWD) {
-    pre.f = ep.ss_in[row];
+    // the row's sum of squares from its slots, added in slot order
+    const float* sp = ep.ss_in + (size_t)row * ep.ss_np;
+    float sum = 0.f;
+    for (int i = 0; i < ep.ss_np; ++i) sum += sp[i];
+    pre.f = sum;
   }
 }
 
@@ -276,7 +280,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
       }
     }
     if constexpr (EPI == TC_RESID_SS) {
-      if (valid) atomicAdd(ep.ss_out + row, ss);
+      if (valid) ep.ss_out[(size_t)row * ep.ss_np + (n0 / BN) * 2 + part] = ss;
     }
   } else if constexpr (EPI == TC_QKV) {
     const int d = ep.head_dim, half = d / 2;
@@ -412,7 +416,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
                      ep.vec32 != 0);
       }
     }
-    if (valid) atomicAdd(ep.ss_out + row, dot * ep.res_scale);
+    if (valid) ep.ss_out[(size_t)row * ep.ss_np + (n0 / BN) * 2 + part] = dot * ep.res_scale;
   } else if constexpr (EPI == TC_DO) {
     constexpr int RW = kResidWords;
     const int cb = chunk_begin<BN>(part);
@@ -467,7 +471,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, bool vali
           for (int j = 0; j < 32; ++j) p[j] = 0.f;
         }
         warp_column_sums(p, lane);
-        atomicAdd(ep.dg + col + lane, p[0]);
+        ep.dg[(size_t)(row / 32) * N + col + lane] = p[0];  // this warp's 32 rows
       }
       if (valid) {
         if (ep.colscale) {

@@ -12,7 +12,8 @@ enum TcEpi : int {
   TC_STORE = 0,     // out = acc (bf16)
   TC_QKV = 1,       // out = r1[m] * acc (r1 = 1 without rowscale), RoPE on q / k
   TC_RESID_SS = 2,  // h = res (bf16) + acc: out = 16-bit(h * out_scale),
-                    // ss_out[m] += sum over the row of h^2
+                    // ss_out[m * ss_np + s] = sum of h^2 over the row's
+                    // columns of slot s (below)
   TC_SWIGLU = 3,    // gate|up interleaved by 128: out = silu(r2 g) * (r2 u)
   TC_RESID = 4,     // out = res_scale * res (fp16) + in_scale * acc (bf16)
   TC_PARTIAL = 5,   // stream-K fp32 partials: part[tile][slot][bn][128]
@@ -21,14 +22,17 @@ enum TcEpi : int {
   // MN-major: A^T B over tokens), the others multiply an activation by a
   // weight read along its output dimension (B MN-major: D = A W).
   TC_DW = 6,        // fp32 out[src row][col] = in_scale * acc * colscale[col];
-                    // dg[col] += sum over rows of w_orig[src row][col] * that
-                    // value before colscale (src row: the gate/up interleave
-                    // undone when inter > 0)
+                    // dg[(m / 32) * N + col] = sum over the 32 rows m of a
+                    // warp of w_orig[src row][col] * that value before
+                    // colscale (src row: the gate/up interleave undone when
+                    // inter > 0); the caller adds the row groups up
   TC_SWIGLU_BWD = 7,// acc = d act [T, I]; with gate / up from aux_in (fp16,
-                    // packed gate|up order) and r2 = 1 / RMS(h) from ss_in:
+                    // packed gate|up order) and r2 = 1 / RMS(h) from ss_in
+                    // (slots added as TC_SWIGLU does):
                     // out (fp16, packed order) = r2 * (d gate | d up) * out_scale
-  TC_F32_DOT = 8,   // fp32 out = in_scale * acc; ss_out[m] += sum over the row
-                    // of out * res_scale * residual (fp16, or bf16 if res_bf16)
+  TC_F32_DOT = 8,   // fp32 out = in_scale * acc; ss_out[m * ss_np + s] = sum
+                    // over the row's columns of slot s of out * res_scale *
+                    // residual (fp16, or bf16 if res_bf16)
   TC_DO = 9,        // fp16 out = in_scale * acc; aux_out[m * n_heads + head] =
                     // sum over the head's columns of fp16(out) * residual (fp16)
 };
@@ -38,8 +42,13 @@ struct TcEpiArgs {
   int ldo = 0;
   const void* residual = nullptr;  // TC_RESID_SS: bf16; TC_RESID: fp16 [M, ldo]
   const float* rowscale = nullptr; // r1 [M]
-  const float* ss_in = nullptr;    // sum of squares of h [M] (TC_SWIGLU)
-  float* ss_out = nullptr;         // TC_RESID_SS
+  // Row sums as fixed-order partials (so that a call's result does not
+  // depend on the order in which tiles finish): slot 2 n + half holds the
+  // sum over column half `half` of 256-column tile n; ss_np slots per row.
+  const float* ss_in = nullptr;    // TC_SWIGLU / TC_SWIGLU_BWD: sums of h^2
+  float* ss_out = nullptr;         // TC_RESID_SS, TC_F32_DOT
+  int ss_np = 0;                   // slots per row: 2 * ceil(N / 256) of the
+                                   // GEMM that wrote them
   float inv_h = 0.f, eps = 0.f;
   const int32_t* pos = nullptr;    // TC_QKV: position of every row
   const float* cos_t = nullptr;    // [max_pos, d/2]
@@ -60,7 +69,8 @@ struct TcEpiArgs {
   // backward-pass epilogues
   const void* colscale = nullptr;  // TC_DW: bf16 [N] (null: 1)
   const void* w_orig = nullptr;    // TC_DW: bf16 [rows, ldo] for dg (null: no dg)
-  float* dg = nullptr;             // TC_DW: fp32 [N], accumulated
+  float* dg = nullptr;             // TC_DW: fp32 [4 x (M-tiles run), N] row-group
+                                   // sums (CTA pairs: M-tiles rounded up to even)
   int inter = 0;                   // TC_DW: undo the gate/up interleave of rows
   const void* aux_in = nullptr;    // TC_SWIGLU_BWD: fp16 gate|up [M, 2 N] (packed)
   void* aux_out = nullptr;         // TC_SWIGLU: fp16 gate|up [M, N] (packed), or

@@ -82,17 +82,21 @@ void simt_attention_decode(bool is_bf16, const void* qkv, const void* cache_k,
 
 // ----------------------------------------------------------------- bwd_rows.cu
 // Row passes of the backward pass (bf16 layers; H a multiple of 8):
-// out = fp16(dout) [rows, H], z1 = z2 = 0 [rows].
-cudaError_t bwd_dout_f16(const void* dout, void* out, int rows, int H, float* z1,
-                         float* z2, int sm_count, cudaStream_t s);
+// out = fp16(dout) [rows, H].
+cudaError_t bwd_dout_f16(const void* dout, void* out, int rows, int H, int sm_count,
+                         cudaStream_t s);
 // dh = dout + u - h r2^2 dot / H with h = hg_scale * hg (fp16), r2 from the
-// row's sum of squares ss: dh32 fp32 and dh16 fp16 [rows, H].
+// row's sum of squares: dh32 fp32 and dh16 fp16 [rows, H].  ss and dot hold
+// np fixed-order slots per row, added in slot order.
 cudaError_t bwd_norm2(const void* dout, const float* u, const void* hg, float hg_scale,
-                      const float* ss, const float* dot, float eps, float* dh32,
+                      const float* ss, const float* dot, int np, float eps, float* dh32,
                       void* dh16, int rows, int H, cudaStream_t s);
-// dx = bf16(dh + r1 u - x r1^3 dot / H) [rows, H].
+// dx = bf16(dh + r1 u - x r1^3 dot / H) [rows, H] (dot: np slots per row).
 cudaError_t bwd_norm1(const float* dh, const float* u, const void* x, const float* r1,
-                      const float* dot, void* dx, int rows, int H, cudaStream_t s);
+                      const float* dot, int np, void* dx, int rows, int H, cudaStream_t s);
+// out_k[c] = sum over g < ng_k of part_k[g * N + c], in order, for k = 0, 1.
+cudaError_t bwd_col_sums(const float* part0, int ng0, float* out0, const float* part1,
+                         int ng1, float* out1, int N, cudaStream_t s);
 
 // ----------------------------------------------------------------- pack.cu
 // out[n, k] = W[src(n), k] * (g ? g[k] : 1), src(n) = n, or the gate/up

@@ -123,6 +123,11 @@ struct WsLayout {
   size_t pos, r1, ss2, xn, qkv, attn, h, hg, act, sk, total;
 };
 
+// Fixed-order row sums of a GEMM with `N` output columns in 256-column
+// tiles: two slots (column halves) per tile, so that the sum of a row does
+// not depend on the order in which tiles finish (TcEpiArgs::ss_np).
+int row_sum_slots(int N) { return 2 * ((N + 255) / 256); }
+
 WsLayout ws_layout(const llama_layer_config& c, int tokens) {
   size_t es = c.dtype == LLAMA_DTYPE_BF16 ? 2 : 4;
   size_t T = (size_t)(tokens > 0 ? tokens : 0);
@@ -131,7 +136,8 @@ WsLayout ws_layout(const llama_layer_config& c, int tokens) {
   size_t o = 0;
   w.pos = o; o = align_up(o + T * 4);
   w.r1 = o; o = align_up(o + T * 4);
-  w.ss2 = o; o = align_up(o + T * 4);
+  // bf16 layers: the slots of sum(h^2) per row; fp32 layers: one float
+  w.ss2 = o; o = align_up(o + T * 4 * (es == 2 ? row_sum_slots(c.hidden) : 1));
   w.xn = o;  // bf16 layers: fp16 x / RMS(x), the QKV operand
   if (es == 2) o = align_up(o + T * c.hidden * 2);
   w.qkv = o; o = align_up(o + T * nqkv * es);
@@ -286,7 +292,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
                      pos_in == nullptr, L->status, s);
   }
   if (b16)
-    simt_row_norm_f16(x, T, dm.H, dm.eps, r1, ss2, ws + w.xn, s);
+    simt_row_norm_f16(x, T, dm.H, dm.eps, r1, nullptr, ws + w.xn, s);
   else
     simt_row_rms(b16, x, T, dm.H, dm.eps, r1, ss2, s);
   L->launches += 2;
@@ -368,7 +374,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.status = L->status;
     ep.pdl = 1;
     ep.out = ws + w.hg; ep.ldo = dm.H; ep.residual = x;
-    ep.ss_out = ss2;
+    ep.ss_out = ss2; ep.ss_np = row_sum_slots(dm.H);
     ep.ab_f16 = 1; ep.out_f16 = 1; ep.out_scale = kHgScale;
     mark(L, s, "o_proj_residual");
     split(ep);
@@ -383,7 +389,8 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep = TcEpiArgs();
     ep.status = L->status;
     ep.pdl = 1;
-    ep.out = act; ep.ldo = dm.I; ep.ss_in = ss2; ep.inv_h = 1.0f / dm.H; ep.eps = dm.eps;
+    ep.out = act; ep.ldo = dm.I; ep.ss_in = ss2; ep.ss_np = row_sum_slots(dm.H);
+    ep.inv_h = 1.0f / dm.H; ep.eps = dm.eps;
     ep.ab_f16 = 1; ep.in_scale = 1.0f / kHgScale; ep.out_f16 = 1; ep.out_scale = kActScale;
     if (sv) ep.aux_out = sv->gu;
     mark(L, s, "gate_up_swiglu");
@@ -435,7 +442,9 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
 // saves and the gradients of the intermediates.
 struct BwdLayout {
   WsLayout fw;
-  size_t lse, dsum, gu, dout16, dgu, du, dot1, dot2, dh32, dh16, dattn, dqkv, total;
+  size_t lse, dsum, gu, dout16, dgu, du, dot1, dot2, dh32, dh16, dattn, dqkv, dg_in, dg_post,
+      total;
+  int np, ng_in, ng_post;  // row-sum slots per row; 32-row groups of W_qkv, W_gate_up
 };
 
 BwdLayout bwd_layout(const llama_layer_config& c, int tokens) {
@@ -451,12 +460,21 @@ BwdLayout bwd_layout(const llama_layer_config& c, int tokens) {
   b.dout16 = o; o = align_up(o + T * H * 2);
   b.dgu = o; o = align_up(o + T * 2 * I * 2);
   b.du = o; o = align_up(o + T * H * 4);
-  b.dot1 = o; o = align_up(o + T * 4);
-  b.dot2 = o; o = align_up(o + T * 4);
+  b.np = row_sum_slots(c.hidden);
+  b.dot1 = o; o = align_up(o + T * 4 * b.np);
+  b.dot2 = o; o = align_up(o + T * 4 * b.np);
   b.dh32 = o; o = align_up(o + T * H * 4);
   b.dh16 = o; o = align_up(o + T * H * 2);
   b.dattn = o; o = align_up(o + T * q * 2);
   b.dqkv = o; o = align_up(o + T * nqkv * 2);
+  // the norm-weight gradients' column sums per 32-row group of the dW GEMMs,
+  // added up in group order at the end: 4 groups per 128-row tile, for every
+  // tile the CTA pairs run (an odd tile count gets a partner past the rows,
+  // whose groups hold zeros)
+  b.ng_in = (int)((nqkv + 255) / 256 * 8);
+  b.ng_post = (int)((2 * I + 255) / 256 * 8);
+  b.dg_in = o; o = align_up(o + (size_t)b.ng_in * H * 4);
+  b.dg_post = o; o = align_up(o + (size_t)b.ng_post * H * 4);
   b.total = o;
   return b;
 }
@@ -499,12 +517,8 @@ int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
   const int qd = dm.Hq * dm.d;
   const size_t H = dm.H;
   auto fail = [](cudaError_t e) { return e != cudaSuccess; };
-  // the norm-weight gradients are sums over many tiles
-  if (fail(cudaMemsetAsync(gr->dg_in, 0, H * sizeof(float), s)) ||
-      fail(cudaMemsetAsync(gr->dg_post, 0, H * sizeof(float), s)))
-    return LLAMA_ERR_CUDA;
   mark(L, s, "bwd_dout_f16");
-  if (fail(bwd_dout_f16(dout, ws + b.dout16, T, dm.H, dot1, dot2, L->sm_count, s)))
+  if (fail(bwd_dout_f16(dout, ws + b.dout16, T, dm.H, L->sm_count, s)))
     return LLAMA_ERR_CUDA;
   ++launches;
   // K-major [rows, cols] (box 128 rows) and MN-major [K rows, cols] (box 64)
@@ -541,7 +555,8 @@ int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
   {
     TcEpiArgs ep;
     ep.out = ws + b.dgu; ep.ldo = 2 * dm.I; ep.aux_in = ws + b.gu;
-    ep.ss_in = reinterpret_cast<const float*>(ws + f.ss2); ep.inv_h = 1.0f / dm.H;
+    ep.ss_in = reinterpret_cast<const float*>(ws + f.ss2); ep.ss_np = b.np;
+    ep.inv_h = 1.0f / dm.H;
     ep.eps = dm.eps;
     if ((rc = gemm(TC_SWIGLU_BWD, ta, tb, T, dm.I, dm.H, ep, "bwd_swiglu"))) return rc;
   }
@@ -551,7 +566,8 @@ int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
   {
     TcEpiArgs ep;
     ep.out = gr->dw_gate_up; ep.ldo = dm.H; ep.in_scale = 1.0f / kHgScale; ep.b_const = 0;
-    ep.colscale = w->g_post; ep.w_orig = w->w_gate_up; ep.dg = gr->dg_post; ep.inter = dm.I;
+    ep.colscale = w->g_post; ep.w_orig = w->w_gate_up; ep.inter = dm.I;
+    ep.dg = reinterpret_cast<float*>(ws + b.dg_post);
     if ((rc = gemm(TC_DW, ta, tb, 2 * dm.I, dm.H, T, ep, "bwd_dw_gate_up"))) return rc;
   }
   // u2 = dgu W'_gate_up (the gradient of h / RMS(h), times 1 / RMS(h)), sum(u2 h)
@@ -560,12 +576,12 @@ int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
   {
     TcEpiArgs ep;
     ep.out = du; ep.ldo = dm.H; ep.residual = ws + f.hg; ep.res_scale = 1.0f / kHgScale;
-    ep.ss_out = dot2;
+    ep.ss_out = dot2; ep.ss_np = b.np;
     if ((rc = gemm(TC_F32_DOT, ta, tb, T, dm.H, 2 * dm.I, ep, "bwd_dh_mlp"))) return rc;
   }
   mark(L, s, "bwd_norm2");
   if (fail(bwd_norm2(dout, du, ws + f.hg, 1.0f / kHgScale,
-                     reinterpret_cast<const float*>(ws + f.ss2), dot2, dm.eps,
+                     reinterpret_cast<const float*>(ws + f.ss2), dot2, b.np, dm.eps,
                      reinterpret_cast<float*>(ws + b.dh32), ws + b.dh16, T, dm.H, s)))
     return LLAMA_ERR_CUDA;
   ++launches;
@@ -611,7 +627,8 @@ int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
   {
     TcEpiArgs ep;
     ep.out = gr->dw_qkv; ep.ldo = dm.H; ep.b_const = 0;
-    ep.colscale = w->g_in; ep.w_orig = w->w_qkv; ep.dg = gr->dg_in;
+    ep.colscale = w->g_in; ep.w_orig = w->w_qkv;
+    ep.dg = reinterpret_cast<float*>(ws + b.dg_in);
     if ((rc = gemm(TC_DW, ta, tb, dm.Nqkv, dm.H, T, ep, "bwd_dw_qkv"))) return rc;
   }
   // u1 = dqkv W'_qkv, sum(u1 x)
@@ -619,12 +636,20 @@ int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
     return LLAMA_ERR_CUDA;
   {
     TcEpiArgs ep;
-    ep.out = du; ep.ldo = dm.H; ep.residual = x; ep.res_bf16 = 1; ep.ss_out = dot1;
+    ep.out = du; ep.ldo = dm.H; ep.residual = x; ep.res_bf16 = 1;
+    ep.ss_out = dot1; ep.ss_np = b.np;
     if ((rc = gemm(TC_F32_DOT, ta, tb, T, dm.H, dm.Nqkv, ep, "bwd_dx_attn"))) return rc;
   }
   mark(L, s, "bwd_norm1");
   if (fail(bwd_norm1(reinterpret_cast<const float*>(ws + b.dh32), du, x,
-                     reinterpret_cast<const float*>(ws + f.r1), dot1, dx, T, dm.H, s)))
+                     reinterpret_cast<const float*>(ws + f.r1), dot1, b.np, dx, T, dm.H, s)))
+    return LLAMA_ERR_CUDA;
+  ++launches;
+  // dg_in, dg_post: the dW GEMMs' row-group sums added up in order
+  mark(L, s, "bwd_dg");
+  if (fail(bwd_col_sums(reinterpret_cast<const float*>(ws + b.dg_in), b.ng_in, gr->dg_in,
+                        reinterpret_cast<const float*>(ws + b.dg_post), b.ng_post,
+                        gr->dg_post, dm.H, s)))
     return LLAMA_ERR_CUDA;
   ++launches;
   L->launches = launches;
@@ -669,7 +694,7 @@ DecLayout dec_layout(const llama_layer* L, int B, int max_seq) {
   w.rec = n_rep * (dm.d + 2);
   size_t o = 0;
   w.r1 = o; o = align_up(o + T * 4);
-  w.ss2 = o; o = align_up(o + T * 4);
+  w.ss2 = o; o = align_up(o + T * 4 * (size_t)((dm.H + 127) / 128));  // per o_proj tile
   w.xn = o; o = align_up(o + T * dm.H * 2);  // fp16 x / RMS(x)
   w.qkv = o; o = align_up(o + T * dm.Nqkv * es);
   w.attn = o; o = align_up(o + T * dm.Hq * dm.d * es);
@@ -700,6 +725,7 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.r1 = reinterpret_cast<const float*>(ws + w.r1);
   a.ss2 = reinterpret_cast<float*>(ws + w.ss2);
+  a.ss_np = (dm.H + 127) / 128;
   a.start_pos = start_pos;
   a.cos_t = reinterpret_cast<const float*>(P + L->pl.cos_t);
   a.sin_t = reinterpret_cast<const float*>(P + L->pl.sin_t);
@@ -746,9 +772,9 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
                ? LLAMA_OK : LLAMA_ERR_CUDA;
   };
 
-  // a1: 1/RMS of every new token (and zero the sums of h^2).
+  // a1: 1/RMS of every new token.
   mark(L, s, "rmsnorm_stats");
-  simt_row_norm_f16(x, B, dm.H, dm.eps, const_cast<float*>(a.r1), a.ss2, ws + w.xn, s);
+  simt_row_norm_f16(x, B, dm.H, dm.eps, const_cast<float*>(a.r1), nullptr, ws + w.xn, s);
   ++L->launches;
   // a2 + a3 + cache append.
   int rc = project(DEC_QKV, L->ta_wqkv, ws + w.xn, dm.Nqkv, dm.H);

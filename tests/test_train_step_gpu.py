@@ -4,14 +4,12 @@ backward that reads them instead of recomputing the forward).  The forward
 computes what llama_layer_forward computes and the backward what
 llama_layer_backward computes, through the same kernels on the same values,
 so both are compared bit for bit with those calls (themselves compared with
-the fp64 oracle in test_layer_gpu.py and test_backward_gpu.py).  The
-exception is the norm-weight gradients: each is a sum of per-tile partials
-added with atomics, whose order varies from call to call, so those two are
-compared to fp32 rounding.  The row sums of squares of h (the second
-RMSNorm) and of u a (the RMSNorm^T steps) are atomic sums too, of two
-partials per 256-column tile: the bit-for-bit cases have hidden 256, one
-tile, two partials, whose sum does not depend on the order.  One case at the
-8B shape is compared with the oracle's chain rule directly.  A saved backward whose
+the fp64 oracle in test_layer_gpu.py and test_backward_gpu.py): every sum
+that tiles contribute to (the row sums of squares of h, the RMSNorm^T row
+dots, the norm-weight gradients) is added in a fixed order, so a call's
+result does not depend on the order in which tiles finish
+(test_reproducible_gpu.py).  One case at the 8B shape is compared with the
+oracle's chain rule directly.  A saved backward whose
 arguments do not match the training forward, or whose workspace another call
 has written since, is refused before anything is launched."""
 
@@ -39,9 +37,9 @@ def batch_args(inp, varlen):
 
 CASES = [
     ("padded_llama3", shape(256, 4, 2, 64, 384, **L3), "padded", dict(batch=2, seq=130)),
-    ("varlen_d128", shape(256, 2, 1, 128, 256, **L3), "varlen",
+    ("varlen_d128", shape(512, 4, 2, 128, 256, **L3), "varlen",
      dict(total_tokens=500, min_len=1, max_len=200)),
-    ("gqa8", shape(256, 8, 1, 64, 256, **L3), "padded", dict(batch=2, seq=90)),
+    ("gqa8", shape(768, 8, 1, 64, 256, **L3), "padded", dict(batch=2, seq=90)),
 ]
 
 
@@ -65,11 +63,7 @@ def test_train_step_equals_forward_and_backward(case):
     assert torch.equal(out, out_ref), name
     for k in GRADS:
         for g in (g1, g2):
-            if k in ("dg_in", "dg_post"):
-                tol = 1e-5 * float(g_ref[k].abs().max())
-                assert float((g[k] - g_ref[k]).abs().max()) <= tol, (name, k)
-            else:
-                assert torch.equal(g[k], g_ref[k]), (name, k)
+            assert torch.equal(g[k], g_ref[k]), (name, k)
     layer.close()
 
 
