@@ -257,9 +257,14 @@ def check_cached(s, batch, S, max_seq, start_pos):
     (4, 8, 1), (5, 8, 1),
     # 4 query heads per kv head, 12 tokens: three groups of 4 (tensor core)
     (12, 8, 2),
+    # 3 query heads per kv head: groups of 5 tokens (15 of the 16 rows)
+    (5, 3, 1), (7, 3, 1),
+    # 16 query heads per kv head: one token a group; 2 tokens split-KV, 3 the
+    # tensor core
+    (2, 16, 1), (3, 16, 1),
 ])
 def test_forward_cached_chunks(S, hq, hkv):
-    s = shape(64 * hq, hq, hkv, 64, 256, **L3)
+    s = shape(max(256, 64 * hq), hq, hkv, 64, 256, **L3)
     # includes an empty prefix and a chunk ending on the last cache row
     check_cached(s, batch=5, S=S, max_seq=300, start_pos=[0, 123, 1, 300 - S, 77])
 
