@@ -724,6 +724,7 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
     import numpy as np
     import torch
 
+    from llama_decoder_layer_prologue_b300 import binding as B
     from llama_decoder_layer_prologue_b300 import synth
     from llama_decoder_layer_prologue_b300.layer import LlamaLayer, to_device
 
@@ -857,6 +858,11 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
         if decode:
             extra_h.append(to_device(inp.start_pos, pin=True))
             extra_d.append(sp)
+        cu_h = None
+        if w.kind == "varlen" and not decode and not bwd:
+            # the host-buffer forward reads the host cu_seqlens to cut the
+            # batch into groups and copies each group's rebased prefix sums
+            cu_h = torch.from_numpy(inp.cu_seqlens.copy())
         elif w.kind == "varlen":
             extra_h.append(to_device(inp.cu_seqlens, pin=True))
             extra_d.append(cu)
@@ -879,7 +885,7 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
             elif decode:
                 layer.decode_from_host(x_h, out_h, x, out, ck, cv, sp)
             elif w.kind == "varlen":
-                layer.forward_from_host(x_h, out_h, x, out, cu_seqlens=cu, seq_len=seq)
+                layer.forward_from_host(x_h, out_h, x, out, cu_seqlens=cu_h, seq_len=seq)
             else:
                 layer.forward_from_host(x_h, out_h, x, out, n_seq=n_seq, seq_len=seq)
 
@@ -897,6 +903,11 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
         e2e_ms = max_over_ranks(dist, e2e_ms)
         bi = x_h.numel() * x_h.element_size() + sum(
             h_.numel() * h_.element_size() for h_ in extra_h)
+        if cu_h is not None:  # the groups' rebased copies: n_seq + groups entries
+            groups = (5 if inp.tokens >= 16384 else
+                      min(max(1, inp.tokens // 2048), cu_h.numel() - 1,
+                          B.LLAMA_HOST_MAX_CHUNKS))
+            bi += 4 * (cu_h.numel() + groups)
         bo = out_h.numel() * out_h.element_size()
         e2e = {"value": job_throughput(world, n_e2e, tokens, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),

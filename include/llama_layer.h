@@ -188,16 +188,27 @@ LLAMA_API int llama_layer_forward(llama_layer_t* layer, const void* x, void* out
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* The prefill forward with its input and output in host memory, the copies
- * overlapped with the layer: the batch is split into `chunks` groups of whole
- * sequences (0: groups of at least 2048 tokens; at most LLAMA_HOST_MAX_CHUNKS
- * and n_seq; a packed batch, cu_seqlens != NULL, is one group), and while the
- * layer runs on group i on `stream`, group i + 1 is copied in and group i - 1
- * copied out on two streams the layer owns.  Positions restart at 0 in every
- * sequence.
+ * overlapped with the layer: the batch is split into groups of whole
+ * sequences, and while the layer runs on group i on `stream`, group i + 1 is
+ * copied in and group i - 1 copied out on two streams the layer owns.
+ * chunks > 0 asks for min(chunks, n_seq, LLAMA_HOST_MAX_CHUNKS) groups of
+ * about equal token counts; chunks = 0 picks them: five groups of 1/16,
+ * 3/16, 1/2, 3/16 and 1/16 of the tokens for a batch of at least 16384
+ * tokens (small first and last groups, whose copies alone are exposed),
+ * else groups of at least 2048 tokens.  Each cut falls at the first sequence
+ * that starts at or after its token count, so a group may hold no rows (it
+ * is skipped).  Positions restart at 0 in every sequence.
  *   x_host, out_host [total_tokens, hidden] host memory (page-locked for the
  *                    copies to be asynchronous and overlap)
  *   x_dev, out_dev   [total_tokens, hidden] device staging buffers (distinct)
- *   cu_seqlens       NULL or device int32 prefix sums, as llama_layer_forward
+ *   cu_seqlens       NULL (n_seq sequences of seq_len tokens) or HOST int32
+ *                    prefix sums [n_seq + 1] under llama_layer_forward's rules
+ *                    (cu[0] = 0, non-decreasing, cu[n_seq] = total_tokens, no
+ *                    length above seq_len), checked on the host
+ *                    (LLAMA_ERR_INVALID_ARG) and read before the call returns;
+ *                    each group's copy, rebased to start at 0, is staged
+ *                    through page-locked memory the layer owns into the
+ *                    workspace
  * `workspace` as llama_layer_forward for total_tokens (the groups use it in
  * turn).  Returns once everything is enqueued; work enqueued on `stream`
  * afterwards runs after the last copy out, so synchronising `stream` makes

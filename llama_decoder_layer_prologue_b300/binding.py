@@ -24,6 +24,8 @@ LLAMA_ERR_DEVICE_TIMEOUT = -5
 LLAMA_ERR_DEVICE_BAD_INPUT = -6
 LLAMA_ERR_UNSUPPORTED_DEVICE = -7
 
+LLAMA_HOST_MAX_CHUNKS = 8  # groups of llama_layer_forward_host
+
 LLAMA_DTYPE_F32 = 0
 LLAMA_DTYPE_BF16 = 1
 LLAMA_ROPE_NONE = 0

@@ -120,7 +120,7 @@ void rope_inv_freq(const llama_layer_config& c, double* f) {
 }
 
 struct WsLayout {
-  size_t pos, r1, ss2, xn, qkv, attn, h, hg, act, sk, total;
+  size_t pos, r1, ss2, xn, qkv, attn, h, hg, act, sk, cu, total;
 };
 
 // Fixed-order row sums of a GEMM with `N` output columns in 256-column
@@ -150,6 +150,11 @@ WsLayout ws_layout(const llama_layer_config& c, int tokens) {
   w.act = o; o = align_up(o + T * c.intermediate * es);
   w.sk = o;  // split-tile pieces of the tensor-core GEMMs (bf16 layers)
   if (c.dtype == LLAMA_DTYPE_BF16 && T > 0) o = align_up(o + kMaxSkCtas * kSkSlotBytes);
+  // llama_layer_forward_host on a packed batch: the groups' rebased
+  // cu_seqlens (n_seq + groups <= T + LLAMA_HOST_MAX_CHUNKS entries).  Last,
+  // so that a group's forward on fewer rows, whose regions all lie below its
+  // own w.cu, never reaches it.
+  w.cu = o; o = align_up(o + (T + LLAMA_HOST_MAX_CHUNKS + 1) * 4);
   w.total = o;
   return w;
 }
@@ -182,6 +187,13 @@ struct llama_layer {
   cudaEvent_t ev_start, ev_done, ev_in[LLAMA_HOST_MAX_CHUNKS],
       ev_comp[LLAMA_HOST_MAX_CHUNKS];
   bool host_ready;
+  // packed batches: the groups' cu_seqlens arrays, each rebased to start at
+  // 0, in page-locked memory (cu_cap entries) until ev_cu says that the
+  // copy which reads them has run
+  int32_t* cu_host;
+  size_t cu_cap;
+  cudaEvent_t ev_cu;
+  bool cu_pending;
   // The activations the last llama_layer_forward_train call kept in its
   // workspace, for llama_layer_backward_saved: that call's arguments.  Any
   // other call through the layer whose workspace overlaps [ws, ws + bytes)
@@ -936,6 +948,9 @@ int llama_layer_init(const llama_layer_config* cfg,
   L->sk_flag = reinterpret_cast<uint32_t*>(L->packed + pl.skflag);
   L->sk_epoch = 0;
   L->host_ready = false;
+  L->cu_host = nullptr;
+  L->cu_cap = 0;
+  L->cu_pending = false;
   L->sm_count = sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& dm = L->dm;
@@ -1181,7 +1196,8 @@ int host_setup(llama_layer* L) {
   bool ok = cudaStreamCreateWithFlags(&L->h2d, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&L->d2h, cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&L->ev_start, ef) == cudaSuccess &&
-            cudaEventCreateWithFlags(&L->ev_done, ef) == cudaSuccess;
+            cudaEventCreateWithFlags(&L->ev_done, ef) == cudaSuccess &&
+            cudaEventCreateWithFlags(&L->ev_cu, ef) == cudaSuccess;
   for (int c = 0; ok && c < LLAMA_HOST_MAX_CHUNKS; ++c)
     ok = cudaEventCreateWithFlags(&L->ev_in[c], ef) == cudaSuccess &&
          cudaEventCreateWithFlags(&L->ev_comp[c], ef) == cudaSuccess;
@@ -1204,60 +1220,115 @@ int llama_layer_forward_host(llama_layer_t* L, const void* x_host, void* out_hos
     return LLAMA_ERR_INVALID_ARG;
   if (n_seq <= 0 || seq_len <= 0) return LLAMA_ERR_INVALID_ARG;
   if (!cu_seqlens && (long)n_seq * seq_len != total_tokens) return LLAMA_ERR_INVALID_ARG;
-  if (cu_seqlens && (!aligned(cu_seqlens, 4) || (long)n_seq > total_tokens))
-    return LLAMA_ERR_INVALID_ARG;
+  if (cu_seqlens) {
+    // the host copy is checked here, each group's rebased copy again on the
+    // device by the forward
+    if ((long)n_seq > total_tokens || cu_seqlens[0] != 0 ||
+        cu_seqlens[n_seq] != total_tokens)
+      return LLAMA_ERR_INVALID_ARG;
+    for (int i = 0; i < n_seq; ++i)
+      if (cu_seqlens[i + 1] < cu_seqlens[i] || cu_seqlens[i + 1] - cu_seqlens[i] > seq_len)
+        return LLAMA_ERR_INVALID_ARG;
+  }
   if (seq_len > L->cfg.max_position) return LLAMA_ERR_INVALID_ARG;
   if ((size_t)seq_len * sizeof(float) > 200 * 1024) return LLAMA_ERR_UNSUPPORTED_SHAPE;
   if (!workspace || !aligned(workspace, kAlign)) return LLAMA_ERR_INVALID_ARG;
-  if (workspace_bytes < ws_layout(L->cfg, total_tokens).total)
-    return LLAMA_ERR_WORKSPACE_TOO_SMALL;
+  const WsLayout wl = ws_layout(L->cfg, total_tokens);
+  if (workspace_bytes < wl.total) return LLAMA_ERR_WORKSPACE_TOO_SMALL;
   clobber(L, workspace, workspace_bytes);
   int rc = host_setup(L);
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // groups of whole sequences: chunks = 0 picks >= 2048 tokens a group (a
-  // group's copies are exposed only at the ends of the pipeline, and 2048-row
-  // GEMMs still fill the GPU); packed (varlen) batches run as one group
+  // groups of whole sequences.  `cut[c]` is the token count before which
+  // group c starts (cut at the first sequence that starts at or after it).
+  // chunks = 0: a batch of >= 16384 tokens in five groups of 1/16, 3/16,
+  // 1/2, 3/16 and 1/16 of its tokens (the first group's copy in and the last
+  // group's copy out are the only exposed copies, so they are kept small;
+  // each next group's copy in, ~2.4x faster per token than the layer on the
+  // 8B shape, hides behind the group before, and the large middle group
+  // keeps the GEMMs at full size); a smaller one in groups of >= 2048 tokens
   int nc = chunks;
-  if (nc == 0) nc = total_tokens / 2048;
-  nc = std::max(1, std::min({nc, n_seq, LLAMA_HOST_MAX_CHUNKS}));
-  if (cu_seqlens) nc = 1;
-  const size_t row = (size_t)L->cfg.hidden * (L->bf16 ? 2 : 4);
-  auto first_seq = [&](int c) { return (int)((long)c * n_seq / nc); };
-  auto first_row = [&](int c) {
-    return cu_seqlens ? (c == 0 ? 0 : total_tokens) : first_seq(c) * seq_len;
+  long cut[LLAMA_HOST_MAX_CHUNKS + 1];
+  const long T = total_tokens;
+  if (chunks == 0 && T >= 16384) {
+    nc = 5;
+    const long sixteenths[6] = {0, 1, 4, 12, 15, 16};
+    for (int c = 0; c <= nc; ++c) cut[c] = sixteenths[c] * T / 16;
+  } else {
+    if (nc == 0) nc = total_tokens / 2048;
+    nc = std::max(1, std::min({nc, n_seq, LLAMA_HOST_MAX_CHUNKS}));
+    for (int c = 0; c <= nc; ++c) cut[c] = (long)c * T / nc;
+  }
+  int seq0[LLAMA_HOST_MAX_CHUNKS + 1];
+  seq0[0] = 0;
+  seq0[nc] = n_seq;
+  for (int c = 1; c < nc; ++c) {
+    seq0[c] = cu_seqlens ? (int)(std::lower_bound(cu_seqlens, cu_seqlens + n_seq, cut[c]) -
+                                 cu_seqlens)
+                         : (int)std::min<long>(n_seq, (cut[c] + seq_len - 1) / seq_len);
+    seq0[c] = std::max(seq0[c], seq0[c - 1]);
+  }
+  auto row0 = [&](int c) {
+    return cu_seqlens ? (size_t)cu_seqlens[seq0[c]] : (size_t)seq0[c] * seq_len;
   };
-  // copies in: the staging buffer is free once earlier work on `stream` is
+  const size_t row = (size_t)L->cfg.hidden * (L->bf16 ? 2 : 4);
+  // copies in: the staging buffers are free once earlier work on `stream` is
   if (cudaEventRecord(L->ev_start, s) != cudaSuccess ||
       cudaStreamWaitEvent(L->h2d, L->ev_start, 0) != cudaSuccess)
     return LLAMA_ERR_CUDA;
-  for (int c = 0; c < nc; ++c) {
-    const size_t r0 = first_row(c), r1 = first_row(c + 1);
-    if (cudaMemcpyAsync(static_cast<char*>(x_dev) + r0 * row,
-                        static_cast<const char*>(x_host) + r0 * row, (r1 - r0) * row,
-                        cudaMemcpyHostToDevice, L->h2d) != cudaSuccess ||
-        cudaEventRecord(L->ev_in[c], L->h2d) != cudaSuccess)
+  int32_t* cu_dev = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wl.cu);
+  if (cu_seqlens) {
+    // group c's cu_seqlens, rebased to its first row, at entry seq0[c] + c;
+    // the page-locked buffer is rewritten only after the previous call's
+    // copy of it has run
+    const size_t need = (size_t)n_seq + nc;
+    if (L->cu_pending && cudaEventSynchronize(L->ev_cu) != cudaSuccess) return LLAMA_ERR_CUDA;
+    L->cu_pending = false;
+    if (L->cu_cap < need) {
+      if (L->cu_host) cudaFreeHost(L->cu_host);
+      L->cu_host = nullptr;
+      L->cu_cap = 0;
+      const size_t cap = std::max(need, (size_t)1024);
+      if (cudaMallocHost(reinterpret_cast<void**>(&L->cu_host), cap * 4) != cudaSuccess)
+        return LLAMA_ERR_CUDA;
+      L->cu_cap = cap;
+    }
+    for (int c = 0; c < nc; ++c)
+      for (int i = seq0[c]; i <= seq0[c + 1]; ++i)
+        L->cu_host[i + c] = cu_seqlens[i] - cu_seqlens[seq0[c]];
+    if (cudaMemcpyAsync(cu_dev, L->cu_host, need * 4, cudaMemcpyHostToDevice, L->h2d) !=
+            cudaSuccess ||
+        cudaEventRecord(L->ev_cu, L->h2d) != cudaSuccess)
       return LLAMA_ERR_CUDA;
+    L->cu_pending = true;
+  }
+  for (int c = 0; c < nc; ++c) {
+    const size_t r0 = row0(c), r1 = row0(c + 1);
+    if (r1 > r0 &&
+        cudaMemcpyAsync(static_cast<char*>(x_dev) + r0 * row,
+                        static_cast<const char*>(x_host) + r0 * row, (r1 - r0) * row,
+                        cudaMemcpyHostToDevice, L->h2d) != cudaSuccess)
+      return LLAMA_ERR_CUDA;
+    if (cudaEventRecord(L->ev_in[c], L->h2d) != cudaSuccess) return LLAMA_ERR_CUDA;
   }
   // the layer on each group as soon as its rows are in, each group's rows
-  // copied out as soon as it is done
+  // copied out as soon as it is done (groups without rows are skipped)
   int launches = 0;
   for (int c = 0; c < nc; ++c) {
-    const int r0 = first_row(c), r1 = first_row(c + 1);
-    const int q = cu_seqlens ? n_seq : first_seq(c + 1) - first_seq(c);
+    const size_t r0 = row0(c), r1 = row0(c + 1);
+    if (r1 == r0) continue;
     if (cudaStreamWaitEvent(s, L->ev_in[c], 0) != cudaSuccess) return LLAMA_ERR_CUDA;
-    rc = forward_impl(L, static_cast<char*>(x_dev) + (size_t)r0 * row,
-                      static_cast<char*>(out_dev) + (size_t)r0 * row, nullptr,
-                      cu_seqlens, q, seq_len, r1 - r0,
-                      static_cast<char*>(workspace), s);
+    rc = forward_impl(L, static_cast<char*>(x_dev) + r0 * row,
+                      static_cast<char*>(out_dev) + r0 * row, nullptr,
+                      cu_seqlens ? cu_dev + seq0[c] + c : nullptr, seq0[c + 1] - seq0[c],
+                      seq_len, (int)(r1 - r0), static_cast<char*>(workspace), s);
     if (rc) return rc;
     launches += L->launches;
     if (cudaEventRecord(L->ev_comp[c], s) != cudaSuccess ||
         cudaStreamWaitEvent(L->d2h, L->ev_comp[c], 0) != cudaSuccess ||
-        cudaMemcpyAsync(static_cast<char*>(out_host) + (size_t)r0 * row,
-                        static_cast<const char*>(out_dev) + (size_t)r0 * row,
-                        (size_t)(r1 - r0) * row, cudaMemcpyDeviceToHost,
-                        L->d2h) != cudaSuccess)
+        cudaMemcpyAsync(static_cast<char*>(out_host) + r0 * row,
+                        static_cast<const char*>(out_dev) + r0 * row, (r1 - r0) * row,
+                        cudaMemcpyDeviceToHost, L->d2h) != cudaSuccess)
       return LLAMA_ERR_CUDA;
   }
   L->launches = launches;
@@ -1392,6 +1463,9 @@ void llama_layer_destroy(llama_layer_t* L) {
   if (L && L->host_ready) {
     cudaStreamDestroy(L->h2d);
     cudaStreamDestroy(L->d2h);
+    if (L->cu_pending) cudaEventSynchronize(L->ev_cu);
+    if (L->cu_host) cudaFreeHost(L->cu_host);
+    cudaEventDestroy(L->ev_cu);
     cudaEventDestroy(L->ev_start);
     cudaEventDestroy(L->ev_done);
     for (int c = 0; c < LLAMA_HOST_MAX_CHUNKS; ++c) {

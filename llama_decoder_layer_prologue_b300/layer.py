@@ -219,14 +219,19 @@ class LlamaLayer:
         """One forward whose input and output live in (pinned) host memory,
         through llama_layer_forward_host: groups of whole sequences are copied
         in, run and copied out with the copies overlapping the layer (chunks =
-        0 picks groups of >= 2048 tokens).  ``x_dev`` / ``out_dev`` are device
+        0 lets the library pick the groups).  ``x_dev`` / ``out_dev`` are device
         staging buffers of the same shape; out_host is valid once the current
-        stream is synchronised."""
+        stream is synchronised.  ``cu_seqlens`` of a packed batch is a host
+        int32 tensor: the library cuts the batch into groups with it."""
         T = x_host.shape[0]
         if cu_seqlens is None:
             seq_len = seq_len or T
             n_seq = n_seq or (T // seq_len)
         else:
+            if (cu_seqlens.device.type != "cpu" or cu_seqlens.dtype != torch.int32
+                    or not cu_seqlens.is_contiguous()):
+                raise ValueError("cu_seqlens of forward_from_host: a contiguous "
+                                 "host int32 tensor")
             n_seq = cu_seqlens.numel() - 1
             assert seq_len is not None, "varlen needs max_seqlen"
         self.ensure_workspace(T)

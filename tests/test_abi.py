@@ -28,6 +28,19 @@ def test_header_declarations_match_binding():
     assert declared_functions() == sorted(B.EXPORTS)
 
 
+def test_header_constants_match_binding():
+    # every integer #define of the header that the binding names has the
+    # header's value
+    defs = dict(re.findall(r"^#define\s+(LLAMA_[A-Z0-9_]+)\s+\(?(-?\d+)\)?",
+                           open(HEADER).read(), flags=re.M))
+    named = {k: v for k, v in vars(B).items() if k.startswith("LLAMA_") and
+             isinstance(v, int)}
+    assert "LLAMA_HOST_MAX_CHUNKS" in named
+    for k, v in named.items():
+        assert k in defs, k
+        assert int(defs[k]) == v, k
+
+
 def test_library_exports_every_declared_symbol():
     L = B.lib()
     for name in declared_functions():

@@ -130,31 +130,123 @@ def test_forward_host_groups_match_the_oracle(chunks):
     ref = oracle.decoder_layer(synth.to_f64(inp.x), weights_f64(inp.weights),
                                s, inp.positions, inp.cu_seqlens)
     assert_close(to_f64(out_h), ref["out"], s.dtype, "host out")
-    # the same layer on the device-resident input, up to the order of the
-    # row-sum atomics (a bf16 ulp at most)
+    # the same layer on the device-resident input, up to the GEMMs' split of
+    # K, which depends on a group's tile count (a bf16 ulp at most)
     d = (out_h.float() - dev_out.cpu().float()).abs()
     assert float(d.max()) <= 2.0 ** -7 * float(dev_out.float().abs().max())
     layer.close()
 
 
-def test_forward_host_packed_batch():
+# (chunks, sequence lengths summing to 900 or None for drawn ones): one group,
+# three, eight; empty sequences and a last group of one empty sequence (cut
+# at 225 / 450 / 675 tokens: rows 0-305, 305-556, 556-900, none); a long first
+# sequence that leaves the second of three groups without rows
+PACKED_HOST_CASES = [
+    (0, None),
+    (1, None),
+    (3, None),
+    (8, None),
+    (4, [0, 5, 0, 300, 1, 0, 250, 344, 0]),
+    (8, [700, 100, 100]),
+]
+
+
+@pytest.mark.parametrize("chunks,lens", PACKED_HOST_CASES)
+def test_forward_host_packed_batch(chunks, lens):
+    # a packed batch through host buffers: the host cu_seqlens cuts it into
+    # groups of whole sequences, each run on its rebased copy
     s = shape(256, 4, 2, 64, 256, **L3)
     w = synth.custom_workload("hostv", s, "varlen", total_tokens=900, min_len=1,
                               max_len=300)
+    inp = synth.make_inputs(w)
+    if lens is not None:
+        assert sum(lens) == inp.tokens
+        inp.cu_seqlens = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        inp.positions = np.concatenate(
+            [np.arange(n, dtype=np.int32) for n in lens]).astype(np.int32)
+    layer = build_layer(inp)
+    x_h = to_device(inp.x, pin=True)
+    out_h = torch.full_like(x_h, float("nan")).pin_memory()
+    stage_x = torch.empty(x_h.shape, dtype=x_h.dtype, device="cuda")
+    stage_out = torch.empty_like(stage_x)
+    cu_h = torch.from_numpy(inp.cu_seqlens.copy())
+    S = int(np.diff(inp.cu_seqlens).max())
+    layer.forward_from_host(x_h, out_h, stage_x, stage_out, cu_seqlens=cu_h, seq_len=S,
+                            chunks=chunks)
+    torch.cuda.current_stream().synchronize()
+    assert layer.status() == B.LLAMA_OK
+    assert layer.launch_count() > 0
+    ref = oracle.decoder_layer(synth.to_f64(inp.x), weights_f64(inp.weights),
+                               s, inp.positions, inp.cu_seqlens)
+    assert_close(to_f64(out_h), ref["out"], s.dtype, "host out (packed)")
+    # twice more on the same handle without a synchronise between the calls
+    # (the second waits for the first's copy of the rebased arrays)
+    out_h2 = torch.full_like(x_h, float("nan")).pin_memory()
+    for o in (out_h, out_h2):
+        layer.forward_from_host(x_h, o, stage_x, stage_out, cu_seqlens=cu_h,
+                                seq_len=S, chunks=chunks)
+    torch.cuda.current_stream().synchronize()
+    assert layer.status() == B.LLAMA_OK
+    assert torch.equal(out_h2, out_h)
+    layer.close()
+
+
+@pytest.mark.parametrize("kind", ["varlen", "padded"])
+def test_forward_host_five_groups(kind):
+    # >= 16384 tokens with chunks = 0: groups cut at 1/16, 1/4, 3/4 and 15/16
+    # of the tokens
+    s = shape(256, 4, 2, 64, 256, **L3)
+    if kind == "varlen":
+        w = synth.custom_workload("host5v", s, "varlen", total_tokens=16384, min_len=1,
+                                  max_len=700)
+    else:
+        w = synth.custom_workload("host5p", s, "padded", batch=32, seq=512)
     inp = synth.make_inputs(w)
     layer = build_layer(inp)
     x_h = to_device(inp.x, pin=True)
     out_h = torch.full_like(x_h, float("nan")).pin_memory()
     stage_x = torch.empty(x_h.shape, dtype=x_h.dtype, device="cuda")
     stage_out = torch.empty_like(stage_x)
-    cu = to_device(inp.cu_seqlens)
     S = int(np.diff(inp.cu_seqlens).max())
-    layer.forward_from_host(x_h, out_h, stage_x, stage_out, cu_seqlens=cu, seq_len=S)
+    if kind == "varlen":
+        layer.forward_from_host(x_h, out_h, stage_x, stage_out,
+                                cu_seqlens=torch.from_numpy(inp.cu_seqlens.copy()),
+                                seq_len=S)
+    else:
+        layer.forward_from_host(x_h, out_h, stage_x, stage_out, n_seq=32, seq_len=S)
     torch.cuda.current_stream().synchronize()
     assert layer.status() == B.LLAMA_OK
     ref = oracle.decoder_layer(synth.to_f64(inp.x), weights_f64(inp.weights),
                                s, inp.positions, inp.cu_seqlens)
-    assert_close(to_f64(out_h), ref["out"], s.dtype, "host out (packed)")
+    assert_close(to_f64(out_h), ref["out"], s.dtype, "host out (five groups)")
+    # the whole batch on the device in one call: equal up to the GEMMs'
+    # split of K, which depends on a group's tile count (a bf16 ulp at most)
+    dev = run_forward(layer, inp, varlen=kind == "varlen").cpu().float()
+    d = (out_h.float() - dev).abs()
+    assert float(d.max()) <= 2.0 ** -7 * float(dev.abs().max())
+    layer.close()
+
+
+def test_forward_host_rejects_bad_host_cu_seqlens():
+    s = shape(256, 4, 2, 64, 256, **L3)
+    w = synth.custom_workload("hostbad", s, "varlen", total_tokens=64, min_len=1,
+                              max_len=32)
+    inp = synth.make_inputs(w)
+    layer = build_layer(inp)
+    x_h = to_device(inp.x, pin=True)
+    out_h = torch.empty_like(x_h).pin_memory()
+    stage_x = torch.empty(x_h.shape, dtype=x_h.dtype, device="cuda")
+    stage_out = torch.empty_like(stage_x)
+    for bad in ([1, 30, 64], [0, 40, 30, 64], [0, 30, 63], [0, 10, 64]):
+        cu_h = torch.tensor(bad, dtype=torch.int32)
+        with pytest.raises(B.LlamaError) as e:
+            layer.forward_from_host(x_h, out_h, stage_x, stage_out, cu_seqlens=cu_h,
+                                    seq_len=32, chunks=2)
+        assert e.value.code == B.LLAMA_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        layer.forward_from_host(x_h, out_h, stage_x, stage_out,
+                                cu_seqlens=to_device(inp.cu_seqlens), seq_len=32)
+    assert layer.status() == B.LLAMA_OK
     layer.close()
 
 
