@@ -538,6 +538,76 @@ __device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t cta_mask) {
       : "memory");
 }
 
+// ---------------------------------------------- CTA pairs (cta_group::2)
+// One tcgen05.mma over the two SMs of a CTA pair (cluster ranks 0 and 1): an
+// M = 256 tile whose rows 0..127 come from rank 0's shared memory and land in
+// rank 0's tensor memory, rows 128..255 likewise in rank 1, the B tile split
+// along N between the two (each CTA holds N / 2 rows of it at the same
+// shared-memory offset).  Rank 0 issues; every tcgen05 instruction of such a
+// kernel uses cta_group::2.
+
+// The shared::cluster address of the variable at p's offset in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_rank(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+// Warp-wide, in both CTAs of the pair: the same `ncols` columns of both
+// CTAs' tensor memory; the address written to *dst_smem in each.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile(
+      "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+          smem_u32(dst_smem)),
+      "r"(ncols)
+      : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+               "r"(ncols)
+               : "memory");
+}
+
+// tc_mma_bf16_nc over the pair (M = 256 in the instruction descriptor).
+__device__ __forceinline__ void tc_mma_pair_nc(uint32_t d_tmem, uint64_t adesc,
+                                               uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// Arrive on the mbarrier at bar's offset in each CTA of cta_mask once every
+// pair MMA issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::"
+      "cluster.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// 2-D tiled load into this CTA's shared memory, completing its bytes on the
+// mbarrier at shared::cluster address `bar` (in either CTA of the pair).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* m,
+                                                 uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Arrive (release, cluster scope) on the mbarrier at shared::cluster address
+// `bar`.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+
 // Each thread of the warp reads 32 consecutive fp32 columns of its TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];

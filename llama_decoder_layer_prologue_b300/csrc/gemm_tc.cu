@@ -33,10 +33,11 @@ constexpr int kEpiWarps = 8, kGemmThreads = 64 + 32 * kEpiWarps;
 // tc_take_status.
 __device__ int g_tc_status;
 
-template <int BN, int STAGES>
+// HALF_B: each CTA of a cta_group::2 pair holds BN / 2 rows of the B slice.
+template <int BN, int STAGES, bool HALF_B = false>
 struct Layout {
   static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t B_BYTES = (HALF_B ? BN / 2 : BN) * BK * 2;
   static constexpr uint32_t STAGE = A_BYTES + B_BYTES;
   static constexpr uint32_t BAR_OFF = STAGES * STAGE;
   static constexpr uint32_t TOTAL = BAR_OFF + 256 + 1024;
@@ -601,6 +602,21 @@ __device__ __forceinline__ void load_b_pair(uint8_t* dst, const CUtensorMap* m,
   }
 }
 
+// load_operand for a cta_group::2 pair: R rows (K-major) or R / 64 MN blocks
+// of this CTA's own operand share, into its own shared memory, completing on
+// the mbarrier at shared::cluster address `bar` (rank 0's).
+template <bool MN, int R>
+__device__ __forceinline__ void load_operand_pair(uint8_t* dst, const CUtensorMap* m,
+                                                  uint32_t bar, int kb, int r0) {
+  if constexpr (MN) {
+#pragma unroll
+    for (int i = 0; i < R / 64; ++i)
+      tma_load_2d_pair(dst + i * 8192, m, bar, r0 + 64 * i, kb * BK);
+  } else {
+    tma_load_2d_pair(dst, m, bar, kb * BK, r0);
+  }
+}
+
 template <bool MN>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t addr) {
   return MN ? sdesc_mn128(addr, 8192) : sdesc_k128(addr);
@@ -615,12 +631,22 @@ __device__ __forceinline__ uint64_t operand_kstep(int k) {
 // their B tile, each CTA loading half of every B K-slice and multicasting it
 // to both; a stage is free once both CTAs' MMAs are done with it (empty
 // barriers count a multicast commit from each).
-template <int BN, int STAGES, int EPI, bool AMN = false, bool BMN = false, bool MC = false>
+// CG2 (with MC): the pair runs one M = 256 tcgen05.mma
+// (cta_group::2) per K step instead of two M = 128 ones.  Each CTA loads its
+// own A rows and its half of the B slice (no multicast), both completing on
+// rank 0's full barrier; rank 0's thread issues every MMA and commits each
+// stage to both CTAs' empty barriers and each tile to both CTAs' acc_full;
+// both CTAs' epilogues release an accumulator on rank 0's acc_empty.  Per
+// K step each SM's tensor core reads 16 KB of operands from its shared
+// memory instead of 24 KB, and a stage holds 32 KB instead of 48.
+template <int BN, int STAGES, int EPI, bool AMN = false, bool BMN = false, bool MC = false,
+          bool CG2 = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
                    TcEpiArgs ep) {
-  using L = Layout<BN, STAGES>;
+  static_assert(!CG2 || (MC && EPI != TC_PARTIAL), "cta_group::2 runs as CTA pairs");
+  using L = Layout<BN, STAGES, CG2>;
   constexpr bool kStreamK = EPI == TC_PARTIAL;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -639,11 +665,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], MC ? 2 : 1);
+      mbar_init(&empty[s], MC && !CG2 ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], kEpiWarps);
+      mbar_init(&acc_empty[a], CG2 ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -654,7 +680,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, L::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (CG2)
+      tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
+    else
+      tmem_alloc(tmem_slot, L::TMEM_COLS);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -680,6 +711,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // depend on the previous kernel: their first STAGES K-slices are
       // requested before waiting for it.
       constexpr bool kWeightsA = EPI == TC_PARTIAL;
+      // cta_group::2: every copy of the pair completes on rank 0's full
+      // barrier, which rank 0 arms for both CTAs' bytes
+      const bool arm = !CG2 || rank == 0;
+      constexpr uint32_t kArmBytes = CG2 ? 2 * L::STAGE : L::STAGE;
       uint32_t pre = 0;
       if (kWeightsA || ep.b_const) {
         Sched s2 = sched;
@@ -687,9 +722,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (s2.next(pm, pn, pk0, pk1, pt, ps)) {
           for (int kb = pk0; kb < pk1 && pre < (uint32_t)STAGES; ++kb, ++pre) {
             uint8_t* sa = smem + pre * L::STAGE;
-            mbar_arrive_expect_tx(&full[pre], L::STAGE);
+            if (arm) mbar_arrive_expect_tx(&full[pre], kArmBytes);
             if (kWeightsA)
               load_operand<AMN, BM>(sa, &tmA, &full[pre], kb, pm * BM);
+            else if constexpr (CG2)
+              load_operand_pair<BMN, BN / 2>(sa + L::A_BYTES, &tmB, mapa_rank(&full[pre], 0),
+                                             kb, pn * BN + (int)rank * (BN / 2));
             else if constexpr (MC)
               load_b_pair<BMN, BN>(sa + L::A_BYTES, &tmB, &full[pre], kb, pn * BN, rank);
             else
@@ -705,7 +743,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           uint8_t* sa = smem + stage * L::STAGE;
-          if (issued < pre) {  // weights already requested, tx already armed
+          if constexpr (CG2) {
+            const uint32_t fb = mapa_rank(&full[stage], 0);
+            if (issued >= pre && arm) mbar_arrive_expect_tx(&full[stage], kArmBytes);
+            load_operand_pair<AMN, BM>(sa, &tmA, fb, kb, mt * BM);
+            if (issued >= pre)
+              load_operand_pair<BMN, BN / 2>(sa + L::A_BYTES, &tmB, fb, kb,
+                                             nt * BN + (int)rank * (BN / 2));
+          } else if (issued < pre) {  // weights already requested, tx already armed
             if (kWeightsA)
               load_operand<BMN, BN>(sa + L::A_BYTES, &tmB, &full[stage], kb, nt * BN);
             else
@@ -725,7 +770,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      if (!ok) {  // let the copies already issued land before leaving
+      if (!ok && CG2 && rank != 0) {
+        // this CTA's copies complete on rank 0's barriers, which rank 0's
+        // producer drains before the pair's closing cluster barrier
+      } else if (!ok) {  // let the copies already issued land before leaving
         volatile int own = 0;
         if (issued < pre) issued = pre;  // prefetched stages are in flight too
         uint32_t n = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
@@ -745,8 +793,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     pdl_wait();
-    if (lane == 0) {
-      const uint32_t idesc = (ep.ab_f16 ? idesc_f16(BM, BN) : idesc_bf16(BM, BN)) |
+    if (lane == 0 && (!CG2 || rank == 0)) {
+      constexpr int kMmaM = CG2 ? 2 * BM : BM;
+      const uint32_t idesc = (ep.ab_f16 ? idesc_f16(kMmaM, BN) : idesc_bf16(kMmaM, BN)) |
                              (AMN ? 1u << 15 : 0u) | (BMN ? 1u << 16 : 0u);
       int stage = 0;
       uint32_t phase = 0;
@@ -773,11 +822,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                          bd = operand_desc<BMN>(sa + L::A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            tc_mma_bf16_nc(d_tmem, ad + operand_kstep<AMN>(k), bd + operand_kstep<BMN>(k),
-                           idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            if constexpr (CG2)
+              tc_mma_pair_nc(d_tmem, ad + operand_kstep<AMN>(k), bd + operand_kstep<BMN>(k),
+                             idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            else
+              tc_mma_bf16_nc(d_tmem, ad + operand_kstep<AMN>(k), bd + operand_kstep<BMN>(k),
+                             idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           issued_any = true;
-          if constexpr (MC)
+          if constexpr (CG2)
+            tc_commit_pair(&empty[stage], 0x3);  // the stage is free in both CTAs
+          else if constexpr (MC)
             tc_commit_mc(&empty[stage], 0x3);  // both CTAs read this stage's B
           else
             tc_commit(&empty[stage]);
@@ -786,11 +841,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             phase ^= 1;
           }
         }
-        if (ok) tc_commit(&acc_full[acc]);
+        if (ok) {
+          if constexpr (CG2)
+            tc_commit_pair(&acc_full[acc], 0x3);  // both CTAs' halves of the tile
+          else
+            tc_commit(&acc_full[acc]);
+        }
       }
       if (!ok && issued_any) {  // wait for the MMAs in flight
         volatile int own = 0;
-        tc_commit(drain);
+        if constexpr (CG2)
+          tc_commit_pair(drain, 0x1);
+        else
+          tc_commit(drain);
         mbar_wait(drain, 0, ep.status, &own);
       }
     }
@@ -853,12 +916,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (lane == 0) {
+        if constexpr (CG2)
+          mbar_arrive_cluster(mapa_rank(&acc_empty[acc], 0));  // rank 0 issues
+        else
+          mbar_arrive(&acc_empty[acc]);
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG2) {
+    // both CTAs are done with the pair's tensor memory (and with each
+    // other's barriers) before the pair frees it
+    cluster_sync();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
+    }
+    return;
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, L::TMEM_COLS);
@@ -867,11 +945,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if constexpr (MC) cluster_sync();
 }
 
-template <int BN, int STAGES, int EPI, bool AMN = false, bool BMN = false, bool MC = false>
+template <int BN, int STAGES, int EPI, bool AMN = false, bool BMN = false, bool MC = false,
+          bool CG2 = false>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
                    int K, const TcEpiArgs& ep, int grid, cudaStream_t s) {
-  using L = Layout<BN, STAGES>;
-  auto kern = gemm_tc_kernel<BN, STAGES, EPI, AMN, BMN, MC>;
+  using L = Layout<BN, STAGES, CG2>;
+  auto kern = gemm_tc_kernel<BN, STAGES, EPI, AMN, BMN, MC, CG2>;
   static std::atomic<uint64_t> attr_done{0};
   if (cudaError_t e = ensure_smem_attr(kern, (int)L::TOTAL, attr_done); e != cudaSuccess)
     return e;
@@ -1024,6 +1103,32 @@ cudaError_t tc_gemm(int epi, int bn, const CUtensorMap& ta,
     // group_m M-tiles = group_m / 2 pair rows
     e.group_m = e.group_m / 2 > 0 ? e.group_m / 2 : 1;
     const int pair_tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + bn - 1) / bn);
+    if (ep.pair == 2) {  // one M = 256 MMA over the pair (K-major operands)
+      switch (epi) {
+        case TC_QKV:
+          return launch<256, 6, TC_QKV, false, false, true, true>(ta, tb, M, N, K, e, pair_tiles, s);
+        case TC_RESID_SS:
+          return launch<256, 6, TC_RESID_SS, false, false, true, true>(ta, tb, M, N, K, e,
+                                                                      pair_tiles, s);
+        case TC_SWIGLU:
+          return launch<256, 6, TC_SWIGLU, false, false, true, true>(ta, tb, M, N, K, e,
+                                                                    pair_tiles, s);
+        case TC_RESID:
+          return launch<256, 6, TC_RESID, false, false, true, true>(ta, tb, M, N, K, e,
+                                                                   pair_tiles, s);
+        case TC_DW:
+          return launch<256, 6, TC_DW, true, true, true, true>(ta, tb, M, N, K, e, pair_tiles, s);
+        case TC_SWIGLU_BWD:
+          return launch<256, 6, TC_SWIGLU_BWD, false, true, true, true>(ta, tb, M, N, K, e,
+                                                                       pair_tiles, s);
+        case TC_F32_DOT:
+          return launch<256, 6, TC_F32_DOT, false, true, true, true>(ta, tb, M, N, K, e,
+                                                                    pair_tiles, s);
+        case TC_DO:
+          return launch<256, 6, TC_DO, false, true, true, true>(ta, tb, M, N, K, e, pair_tiles, s);
+        default: return cudaErrorInvalidValue;
+      }
+    }
     switch (epi) {
       case TC_QKV: return launch<256, 4, TC_QKV, false, false, true>(ta, tb, M, N, K, e, pair_tiles, s);
       case TC_RESID_SS:

@@ -92,10 +92,12 @@ struct TcEpiArgs {
   int sk_tiles = 0;      // set by tc_gemm: tiles of the split phase
   int vec32 = 0;         // set by tc_gemm: out / residual rows are 32-byte aligned
   int group_m = 16;      // set by tc_gemm: M-tiles per band of the tile order
-  // Run as CTA pairs (clusters of 2) on pairs of M-tiles sharing one N-tile:
-  // each CTA loads half of every B K-slice and multicasts it to both, so B
-  // crosses from L2 once per pair.  A K-major B map then needs a box of
-  // bn / 2 rows.  No split-tile phase.  Not for TC_PARTIAL.
+  // Run as CTA pairs (clusters of 2) on pairs of M-tiles sharing one N-tile,
+  // B crossing from L2 once per pair.  1: each CTA loads half of every B
+  // K-slice and multicasts it to both, and each runs its own M = 128 MMAs.
+  // 2: each CTA loads only its half of B and the pair runs one M = 256 MMA
+  // per K step (tcgen05 cta_group::2).  A K-major B map needs a box of
+  // bn / 2 rows.  No split-tile phase.  Not for TC_PARTIAL or TC_STORE.
   int pair = 0;
 };
 

@@ -128,6 +128,10 @@ struct WsLayout {
 // not depend on the order in which tiles finish (TcEpiArgs::ss_np).
 int row_sum_slots(int N) { return 2 * ((N + 255) / 256); }
 
+// TcEpiArgs::pair of the pair GEMMs: 2 runs one M = 256 tcgen05.mma
+// (cta_group::2) per pair and K step.
+constexpr int kPairMode = 2;
+
 WsLayout ws_layout(const llama_layer_config& c, int tokens) {
   size_t es = c.dtype == LLAMA_DTYPE_BF16 ? 2 : 4;
   size_t T = (size_t)(tokens > 0 ? tokens : 0);
@@ -316,10 +320,13 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     // phase (single CTAs, 256-row-box maps) fills: measured on the 1B
     // down_proj, pairs without the split 8 % slower, elsewhere pairs equal or
     // better (the varlen layer 1.8 % faster)
+    // (pair mode 2: one M = 256 tcgen05.mma over each pair, TcEpiArgs::pair)
     auto pairs = [&](int N, int K) {
       const int tiles = ((T + 127) / 128) * ((N + 255) / 256);
       const int grid = tiles < L->sm_count ? tiles : L->sm_count;
-      return L->sm_count > kMaxSkCtas || tc_split_tiles(tiles, grid, (K + 63) / 64) == 0;
+      return L->sm_count > kMaxSkCtas || tc_split_tiles(tiles, grid, (K + 63) / 64) == 0
+                 ? kPairMode
+                 : 0;
     };
     // Split-tile phase: pieces in the workspace, flags in the packed buffer,
     // a new nonzero epoch per launch.
@@ -545,7 +552,7 @@ int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
     ep.status = L->status;
     ep.pdl = 1;
     ep.ab_f16 = 1;
-    ep.pair = 1;  // CTA pairs sharing each B tile (all B maps here are MN-major)
+    ep.pair = kPairMode;  // CTA pairs (all B maps here are MN-major)
     mark(L, s, name);
     if (tc_gemm(epi, 256, ta, tb, M, N, K, ep, L->sm_count, s) != cudaSuccess)
       return LLAMA_ERR_CUDA;
