@@ -315,18 +315,19 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
   if (b16) {
     cudaError_t e;
     CUtensorMap ta;
-    // CTA pairs (shared weight tiles, the 128-row-box weight maps) unless
-    // the GEMM's tiles leave a partly idle last round that the split-tile
-    // phase (single CTAs, 256-row-box maps) fills: measured on the 1B
-    // down_proj, pairs without the split 8 % slower, elsewhere pairs equal or
-    // better (the varlen layer 1.8 % faster)
-    // (pair mode 2: one M = 256 tcgen05.mma over each pair, TcEpiArgs::pair)
-    auto pairs = [&](int N, int K) {
-      const int tiles = ((T + 127) / 128) * ((N + 255) / 256);
-      const int grid = tiles < L->sm_count ? tiles : L->sm_count;
-      return L->sm_count > kMaxSkCtas || tc_split_tiles(tiles, grid, (K + 63) / 64) == 0
-                 ? kPairMode
-                 : 0;
+    // CTA pairs (one M = 256 MMA per pair, the 128-row-box weight maps)
+    // unless the pairs' tiles, rounded up to whole pairs of M-tiles, take a
+    // round more on the SMs than single CTAs' tiles (a small odd M-tile
+    // count); single CTAs then fill a partly idle last round with the
+    // split-tile phase.  Measured with the cta_group::2 pairs on one B300:
+    // the 8B QKV 3.6 % faster as pairs than as split single CTAs, the 1B
+    // down_proj the same either way.
+    auto pairs = [&](int N) {
+      const long m_tiles = (T + 127) / 128, n_tiles = (N + 255) / 256;
+      const long slots = L->sm_count, pair_slots = std::max(1, L->sm_count / 2);
+      const long rounds_single = (m_tiles * n_tiles + slots - 1) / slots;
+      const long rounds_pair = ((m_tiles + 1) / 2 * n_tiles + pair_slots - 1) / pair_slots;
+      return rounds_pair <= rounds_single ? kPairMode : 0;
     };
     // Split-tile phase: pieces in the workspace, flags in the packed buffer,
     // a new nonzero epoch per launch.
@@ -352,7 +353,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.out_f16 = ch ? 0 : 1;
     mark(L, s, "qkv_rope");
     split(ep);
-    ep.pair = pairs(dm.Nqkv, dm.H);
+    ep.pair = pairs(dm.Nqkv);
     e = tc_gemm(TC_QKV, 256, ta, ep.pair ? L->ta_wqkv : L->tm_wqkv, T, dm.Nqkv, dm.H, ep,
                 L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
@@ -397,7 +398,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.ab_f16 = 1; ep.out_f16 = 1; ep.out_scale = kHgScale;
     mark(L, s, "o_proj_residual");
     split(ep);
-    ep.pair = pairs(dm.H, dm.Hq * dm.d);
+    ep.pair = pairs(dm.H);
     e = tc_gemm(TC_RESID_SS, 256, ta, ep.pair ? L->ta_wo : L->tm_wo, T, dm.H, dm.Hq * dm.d,
                 ep, L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
@@ -414,7 +415,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     if (sv) ep.aux_out = sv->gu;
     mark(L, s, "gate_up_swiglu");
     split(ep);
-    ep.pair = pairs(2 * dm.I, dm.H);
+    ep.pair = pairs(2 * dm.I);
     e = tc_gemm(TC_SWIGLU, 256, ta, ep.pair ? L->ta_wgu : L->tm_wgu, T, 2 * dm.I, dm.H, ep,
                 L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;
@@ -431,7 +432,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     ep.ab_f16 = 1; ep.in_scale = 1.0f / kActScale;
     mark(L, s, "down_residual");
     split(ep);
-    ep.pair = pairs(dm.H, dm.I);
+    ep.pair = pairs(dm.H);
     e = tc_gemm(TC_RESID, 256, ta, ep.pair ? L->ta_wd : L->tm_wd, T, dm.H, dm.I, ep,
                 L->sm_count, s);
     if (e != cudaSuccess) return LLAMA_ERR_CUDA;

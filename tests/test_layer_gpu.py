@@ -76,13 +76,17 @@ def test_tiny_fp32_workload():
     ("dynamic_ntk_rope", shape(256, 4, 2, 64, 256, rope_scaling=3, rope_factor=2.0,
                                rope_original_max_pos=1024, max_position=4096),
      "varlen", dict(total_tokens=600, min_len=1, max_len=400)),
-    # GEMMs with 64 K-blocks whose tiles leave the last round of 148 SMs
-    # partly idle run the split-tile phase (tiles cut between two CTAs):
-    # here QKV (384 tiles), o_proj (256) and gate_up (304) ...
-    ("split_tiles_wide", shape(4096, 32, 8, 128, 2432), "padded",
-     dict(batch=2, seq=1024)),
-    # ... and down_proj (200 tiles, ragged last row tile, packed sequences)
-    ("split_tiles_down_varlen", shape(512, 8, 2, 64, 4096, **L3), "varlen",
+    # GEMMs run as single CTAs where CTA pairs would take a round more (a
+    # small odd M-tile count), and then fill a partly idle last round with
+    # the split-tile phase (tiles cut between two CTAs; 64 K-blocks at
+    # least): here QKV (13 M-tiles x 32 N-tiles) ...
+    ("split_tiles_qkv", shape(4096, 32, 16, 128, 1024), "padded",
+     dict(batch=2, seq=832)),
+    # ... and gate_up (3 M-tiles x 76 N-tiles, packed sequences)
+    ("split_tiles_gate_up_varlen", shape(4096, 8, 2, 64, 9728, **L3), "varlen",
+     dict(total_tokens=300, min_len=1, max_len=200)),
+    # CTA pairs on a ragged last M-tile with packed sequences
+    ("pairs_down_varlen", shape(512, 8, 2, 64, 4096, **L3), "varlen",
      dict(total_tokens=12700, min_len=1, max_len=1000)),
 ], ids=lambda case: case[0])
 def test_small_bf16_forward(case):
@@ -94,8 +98,8 @@ def test_small_bf16_forward(case):
 def test_split_tiles_repeated_calls():
     # every launch must find the split-tile flags cleared by the previous one
     # and wait for its own pieces (a new epoch), call after call
-    s = shape(512, 8, 2, 64, 4096, **L3)
-    w = synth.custom_workload("split_rep", s, "padded", batch=4, seq=3200)
+    s = shape(4096, 8, 2, 64, 9728, **L3)  # gate_up: 3 x 76 tiles, split
+    w = synth.custom_workload("split_rep", s, "padded", batch=3, seq=100)
     inp = synth.make_inputs(w)
     layer = build_layer(inp)
     ref = oracle.decoder_layer(synth.to_f64(inp.x), weights_f64(inp.weights),
