@@ -870,13 +870,18 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
                for _ in range(n_e2e)]
 
         if bwd:
-            extra_h.append(to_device(synth.make_dout(inp), pin=True))
-            extra_d.append(dout)
+            dout_h = to_device(synth.make_dout(inp), pin=True)
+            if not train:  # the training step copies it itself
+                extra_h.append(dout_h)
+                extra_d.append(dout)
 
         def host_step():
             for h_, d_ in zip(extra_h, extra_d):
                 d_.copy_(h_, non_blocking=True)
-            if bwd:
+            if train:
+                layer.train_step_from_host(x_h, dout_h, out_h, x, dout, y, out, n_seq=n_seq,
+                                           seq_len=seq, grads=grads)
+            elif bwd:
                 x.copy_(x_h, non_blocking=True)
                 step()
                 out_h.copy_(out, non_blocking=True)
@@ -903,6 +908,8 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
         e2e_ms = max_over_ranks(dist, e2e_ms)
         bi = x_h.numel() * x_h.element_size() + sum(
             h_.numel() * h_.element_size() for h_ in extra_h)
+        if train:
+            bi += dout_h.numel() * dout_h.element_size()
         if cu_h is not None:  # the groups' rebased copies: n_seq + groups entries
             groups = (5 if inp.tokens >= 16384 else
                       min(max(1, inp.tokens // 2048), cu_h.numel() - 1,
@@ -912,9 +919,10 @@ def run_ours(args, rank, local_rank, world, dist=None, wl=None, cpu_seconds=None
         e2e = {"value": job_throughput(world, n_e2e, tokens, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
                "steps": n_e2e, "ms_per_step": e2e_ms / n_e2e,
-               "api": ("LlamaLayer.forward_train + LlamaLayer.backward_saved (pinned "
-                       "host x and dL/d(out) copied in, dx copied out; the layer output "
-                       "and the weight gradients stay on the device)") if train else
+               "api": ("LlamaLayer.train_step_from_host: forward_train + backward_saved "
+                       "(pinned host x copied in, dL/d(out) copied in on a second stream "
+                       "during the forward, dx copied out; the layer output and the "
+                       "weight gradients stay on the device)") if train else
                       ("LlamaLayer.backward (pinned host x and dL/d(out) copied in, "
                        "dx copied out; the weight gradients stay on the device for the "
                        "optimizer)") if bwd else

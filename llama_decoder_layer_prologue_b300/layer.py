@@ -65,6 +65,7 @@ class LlamaLayer:
         self.handle = B.llama_layer_init(self.cfg, wts, self.packed.data_ptr(),
                                          nbytes, stream_ptr())
         self.workspace = torch.empty(0, dtype=torch.uint8, device=dev)
+        self._side = None  # train_step_from_host's copy stream
         # the backward pass reads the weights as given (norm-weight gradients)
         self.weights = ws
         self._wts = wts
@@ -182,6 +183,38 @@ class LlamaLayer:
             n_seq, seq_len, T, self.workspace.data_ptr(), self.workspace.numel(),
             stream_ptr())
         return dict(dx=dx, **grads)
+
+    def train_step_from_host(self, x_host, dout_host, dx_host, x_dev, dout_dev, out_dev,
+                             dx_dev, n_seq=None, seq_len=None, cu_seqlens=None,
+                             grads=None):
+        """One training step whose x, dL/d(out) and dx live in (pinned) host
+        memory: x is copied in on the current stream, then dL/d(out) on a
+        second stream while forward_train runs; backward_saved waits for it,
+        and dx is copied out.  The layer output (out_dev) and the weight
+        gradients stay on the device; ``*_dev`` are device buffers of the
+        host tensors' shapes.  dx_host is valid once the current stream is
+        synchronised."""
+        cur = torch.cuda.current_stream()
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=self.device)
+        x_dev.copy_(x_host, non_blocking=True)
+        # dout_dev is free once earlier work on `cur` is; its copy starts
+        # after x's (the two would share the host link) and runs under the
+        # forward
+        x_in = torch.cuda.Event()
+        x_in.record(cur)
+        self._side.wait_event(x_in)
+        with torch.cuda.stream(self._side):
+            dout_dev.copy_(dout_host, non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(self._side)
+        self.forward_train(x_dev, n_seq=n_seq, seq_len=seq_len, cu_seqlens=cu_seqlens,
+                           out=out_dev)
+        cur.wait_event(ready)
+        res = self.backward_saved(x_dev, dout_dev, n_seq=n_seq, seq_len=seq_len,
+                                  cu_seqlens=cu_seqlens, dx=dx_dev, grads=grads)
+        dx_host.copy_(dx_dev, non_blocking=True)
+        return res
 
     def decode(self, x, cache_k, cache_v, start_pos, out=None):
         Bt = x.shape[0]

@@ -120,3 +120,28 @@ def test_saved_backward_refuses_mismatches():
     torch.cuda.synchronize()
     assert layer.status() == B.LLAMA_OK
     layer.close()
+
+
+def test_train_step_from_host_equals_the_device_pair():
+    # host x and dL/d(out) in, dx out; dL/d(out) crosses on a second stream
+    # while the forward runs: the same bits as the device-resident pair
+    name, s, kind, kw = CASES[0]
+    inp = synth.make_inputs(synth.custom_workload(name, s, kind, index=311, **kw))
+    layer = build_layer(inp)
+    x = to_device(inp.x)
+    dout = to_device(synth.make_dout(inp))
+    args = batch_args(inp, False)
+    y_ref = layer.forward_train(x, **args).clone()
+    g_ref = {k: v.clone() for k, v in layer.backward_saved(x, dout, **args).items()}
+    x_h, dout_h = to_device(inp.x, pin=True), to_device(synth.make_dout(inp), pin=True)
+    dx_h = torch.full_like(x_h, float("nan")).pin_memory()
+    x_d, dout_d, y_d, dx_d = (torch.empty_like(x) for _ in range(4))
+    for _ in range(2):  # the second call reuses the staging buffers
+        g = layer.train_step_from_host(x_h, dout_h, dx_h, x_d, dout_d, y_d, dx_d, **args)
+    torch.cuda.current_stream().synchronize()
+    assert layer.status() == B.LLAMA_OK
+    assert torch.equal(y_d, y_ref)
+    assert torch.equal(dx_h, g_ref["dx"].cpu())
+    for k in GRADS:
+        assert torch.equal(g[k], g_ref[k]), k
+    layer.close()
