@@ -202,12 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = o_free + 2;
   uint64_t* q_empty = q_full + 1;
   uint64_t* drain = q_empty + 1;             // [2] per MMA warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+  ItemRing* ring = reinterpret_cast<ItemRing*>(drain + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int BP = AM / a.hpc;  // positions per query tile
   if (threadIdx.x == 0) {
+    ring_init(ring, 10);  // taken by the two MMA warps and the eight softmax warps
     for (int s = 0; s < L::SLOTS; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 2);  // a commit from each MMA warp
@@ -244,11 +246,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t n = 0, k = 0;  // K / V tiles loaded, items started
+      uint32_t n = 0, k = 0, hand = 0;  // K / V tiles loaded, items started, handed out
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+      while (ok) {
+        // items in index order (longest causal range first), the empty ones
+        // skipped here, the rest handed to the MMA and softmax warps
+        const int i = ring_fetch(a.sched);
+        if (i >= n_items) break;
         const Item it = get_item<CACHED>(a, i, n_hg, n_seq, n_qb, BP, L::AN);
         if (it.n_tiles == 0) continue;
+        if (!ring_put(ring, hand, i, a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
         if (k > 0 && !mbar_wait_sleep(q_empty, (k - 1) & 1, a.status, abort_flag)) {
           ok = false;
           break;
@@ -280,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (ok) ring_put(ring, hand, -1, a.status, abort_flag);  // end of the items
       if (!ok) {  // let the copies already issued land (bounded)
         volatile int own = 0;
         const uint32_t m = n < (uint32_t)L::SLOTS ? n : (uint32_t)L::SLOTS;
@@ -312,11 +323,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t qd = q_desc + t * Q16;
     const uint32_t s_tmem = tmem_base + t * AN;
     const uint32_t o_tmem = tmem_base + 2 * AN + t * D;
-    uint32_t g = 0, n = 0, k = 0;  // tiles, K / V loads consumed, items
+    uint32_t g = 0, n = 0, k = 0, hand = 0;  // tiles, K / V loads consumed, items
     bool ok = true, issued_any = false;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+    while (ok) {
+      int i;
+      if (!ring_get(ring, hand, i, a.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (i < 0) break;
       const Item it = get_item<CACHED>(a, i, n_hg, n_seq, n_qb, BP, L::AN);
-      if (it.n_tiles == 0) continue;
       if (!wait_all(q_full, k & 1)) {
         ok = false;
         break;
@@ -417,16 +433,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_col = t * AN, o_col = 2 * AN + t * D;
     uint8_t* prow = smem + L::P_OFF + t * L::P_BYTES + r * 128;  // head_dim 128
     const float scale = 1.4426950408889634f * rsqrtf((float)D);  // log2(e)/sqrt(d)
-    uint32_t g = 0;
+    uint32_t g = 0, hand = 0;
     bool ok = true;
     auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
       int w_ok = 1;
       if (lane == 0) w_ok = mbar_wait_sleep(b, parity, a.status, abort_flag);
       return __shfl_sync(0xffffffffu, w_ok, 0) != 0;
     };
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+    while (ok) {
+      int i;
+      if (!ring_get(ring, hand, i, a.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (i < 0) break;
       const Item it = get_item<CACHED>(a, i, n_hg, n_seq, n_qb, BP, L::AN);
-      if (it.n_tiles == 0) continue;
       const int q0 = it.q0 + t * BP;  // first position of this tile
       const int pos = q0 + (r % BP);
       const int head = it.h0 + r / BP;
@@ -592,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
+  if (threadIdx.x == 0) ring_leave(a.sched);
 }
 
 int heads_per_cta(int n_rep) {
@@ -621,7 +643,7 @@ cudaError_t launch(const AttnArgs& a, int n_seq, int max_len, int sm_count,
   const int n_hg = a.n_heads / a.hpc;
   const long long items = (long long)n_qb * n_hg * n_seq;
   if (items <= 0) return cudaSuccess;
-  if (items > 0x7fffffff) return cudaErrorInvalidValue;
+  if (items > 0x7fffffff || !a.sched) return cudaErrorInvalidValue;
   auto kern = attn_tc_kernel<D, CACHED>;
   static std::atomic<uint64_t> attr_done{0};
   if (cudaError_t e = ensure_smem_attr(kern, (int)L::TOTAL, attr_done); e != cudaSuccess)

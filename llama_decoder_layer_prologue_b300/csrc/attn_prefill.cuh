@@ -26,10 +26,14 @@ struct AttnArgs {
   const __nv_bfloat16* cache_v = nullptr;
   const int32_t* start_pos = nullptr;
   int max_seq = 0, max_pos = 0;
+  // work-item counter pair {next, done} in device memory, zero between
+  // launches (the kernel leaves it so); one pair per kernel that may overlap
+  // another under programmatic dependent launch
+  int* sched = nullptr;
 };
 
 // max_len: longest sequence (padded: seq_len).  Persistent over
-// min(work items, sm_count) CTAs.
+// min(work items, sm_count) CTAs taking items dynamically (a.sched).
 cudaError_t attn_prefill(const AttnArgs& a, int n_seq, int max_len,
                          int sm_count, cudaStream_t s);
 

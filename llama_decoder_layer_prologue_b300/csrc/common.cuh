@@ -321,6 +321,74 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------- dynamic work items (persistent)
+// The CTAs of a persistent kernel take work items in index order from a
+// global counter pair {next, done} (zero before the launch; the last CTA to
+// leave puts both back to zero), so that items of very different sizes,
+// listed largest first, spread evenly over the SMs whatever their order.
+// Inside a CTA one thread takes the indices and hands them to the consumer
+// warps through a ring of kItemRing shared-memory slots; -1 ends the stream.
+constexpr int kItemRing = 4;
+struct ItemRing {
+  uint64_t full[kItemRing];
+  uint64_t empty[kItemRing];
+  int idx[kItemRing];
+};
+
+// One thread, before the block's first __syncthreads: `consumers` warps
+// release each slot.
+__device__ __forceinline__ void ring_init(ItemRing* r, uint32_t consumers) {
+  for (int k = 0; k < kItemRing; ++k) {
+    mbar_init(&r->full[k], 1);
+    mbar_init(&r->empty[k], consumers);
+  }
+}
+
+// The taking thread: the next item index (>= n_items: none left).
+__device__ __forceinline__ int ring_fetch(int* sched) { return atomicAdd(&sched[0], 1); }
+
+// The taking thread: publishes item (or -1) as handout number n.
+__device__ __forceinline__ bool ring_put(ItemRing* r, uint32_t& n, int item, int* status,
+                                         volatile int* abort_flag) {
+  const int k = n % kItemRing;
+  if (!mbar_wait_sleep(&r->empty[k], ((n / kItemRing) & 1) ^ 1, status, abort_flag))
+    return false;
+  r->idx[k] = item;
+  mbar_arrive(&r->full[k]);
+  ++n;
+  return true;
+}
+
+// A consumer warp (all lanes): handout number n; false on a timeout (item
+// then -1).  Lane 0 releases the slot once the index is read.
+__device__ __forceinline__ bool ring_get(ItemRing* r, uint32_t& n, int& item, int* status,
+                                         volatile int* abort_flag) {
+  const int k = n % kItemRing;
+  int v = -1, ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    ok = mbar_wait_sleep(&r->full[k], (n / kItemRing) & 1, status, abort_flag);
+    if (ok) {
+      v = *reinterpret_cast<volatile int*>(&r->idx[k]);
+      mbar_arrive(&r->empty[k]);
+    }
+  }
+  item = __shfl_sync(0xffffffffu, v, 0);
+  ++n;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Thread 0 after the block's last __syncthreads: the last CTA to get here
+// resets the counter pair for the next launch (every CTA's taking thread
+// has taken its last index before its block got here).
+__device__ __forceinline__ void ring_leave(int* sched) {
+  __threadfence();
+  if (atomicAdd(&sched[1], 1) == (int)gridDim.x - 1) {
+    *reinterpret_cast<volatile int*>(&sched[0]) = 0;
+    *reinterpret_cast<volatile int*>(&sched[1]) = 0;
+    __threadfence();
+  }
+}
+
 // Flags between CTAs of one grid (gpu scope).
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;

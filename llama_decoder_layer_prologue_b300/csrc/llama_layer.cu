@@ -26,6 +26,10 @@ constexpr size_t kAlign = 256;
 // Split-tile phase of the prefill GEMMs: CTAs (one per SM) it supports, and
 // the fp32 slot of one 128 x 256 tile piece.
 constexpr int kMaxSkCtas = 160;
+// Work-item counter pairs in the packed buffer: the prefill attention
+// (plain or cached), the attention backward's dQ and dK / dV kernels (which
+// may overlap under programmatic dependent launch).
+constexpr int kSchedAttn = 0, kSchedDq = 2, kSchedDkv = 4;
 constexpr size_t kSkSlotBytes = 128 * 256 * sizeof(float);
 
 size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
@@ -35,7 +39,7 @@ bool aligned(const void* p, size_t a) {
 }
 
 struct PackedLayout {
-  size_t wqkv, wo, wgu, wd, gpost, cos_t, sin_t, status, skflag, total;
+  size_t wqkv, wo, wgu, wd, gpost, cos_t, sin_t, status, skflag, sched, total;
 };
 
 PackedLayout packed_layout(const llama_layer_config& c) {
@@ -54,6 +58,8 @@ PackedLayout packed_layout(const llama_layer_config& c) {
   p.sin_t = o; o = align_up(o + table);
   p.status = o; o = align_up(o + 64);
   p.skflag = o; o = align_up(o + (kMaxSkCtas + 1) * sizeof(uint32_t));
+  // the attention kernels' work-item counter pairs (kSched*), zeroed at init
+  p.sched = o; o = align_up(o + 16 * sizeof(int));
   p.total = o;
   return p;
 }
@@ -185,6 +191,7 @@ struct llama_layer {
   int* n_marks;              // [ring]
   int launches;  // kernels launched by the last forward / decode call
   uint32_t* sk_flag;  // split-tile flags (packed buffer, zeroed at init)
+  int* sched;         // attention work-item counters (packed buffer, zeroed at init)
   uint32_t sk_epoch;  // value of the last split-tile launch's flags
   // llama_layer_forward_host: copy streams and events, created on first use
   cudaStream_t h2d, d2h;
@@ -374,6 +381,7 @@ int forward_impl(llama_layer* L, const void* x, void* out, const int32_t* pos_in
     aa.cu = cu; aa.tokens = T; aa.seq_len = seq_len; aa.nqkv = dm.Nqkv;
     aa.n_heads = dm.Hq; aa.n_kv_heads = dm.Hkv; aa.head_dim = dm.d;
     aa.status = L->status;
+    aa.sched = L->sched + kSchedAttn;
     if (sv) aa.lse = sv->lse;
     mark(L, s, "attention");
     if (ch) {
@@ -815,6 +823,7 @@ int decode_chunk(llama_layer* L, const void* x, void* out, void* ck, void* cv,
     aa.tokens = B; aa.seq_len = seq_tokens; aa.nqkv = dm.Nqkv;
     aa.n_heads = dm.Hq; aa.n_kv_heads = dm.Hkv; aa.head_dim = dm.d;
     aa.status = L->status;
+    aa.sched = L->sched + kSchedAttn;
     aa.cache_k = a.cache_k + seq0 * cache_seq;
     aa.cache_v = a.cache_v + seq0 * cache_seq;
     aa.start_pos = start_pos + seq0;
@@ -954,6 +963,7 @@ int llama_layer_init(const llama_layer_config* cfg,
   L->pl = pl;
   L->status = reinterpret_cast<int*>(L->packed + pl.status);
   L->sk_flag = reinterpret_cast<uint32_t*>(L->packed + pl.skflag);
+  L->sched = reinterpret_cast<int*>(L->packed + pl.sched);
   L->sk_epoch = 0;
   L->host_ready = false;
   L->cu_host = nullptr;
