@@ -172,7 +172,7 @@ struct DqLayout {
   static constexpr int SLOTS = D == 64 ? 4 : 2;  // (K, V) pairs
   static constexpr uint32_t Q_OFF = 0, DO_OFF = TILE, KV_OFF = 2 * TILE;
   static constexpr uint32_t BAR_OFF = KV_OFF + SLOTS * 2 * TILE;
-  static constexpr uint32_t TOTAL = BAR_OFF + 256 + 1024;
+  static constexpr uint32_t TOTAL = BAR_OFF + 512 + 1024;
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256, DZ_COL = 256 + D;
   static_assert(DZ_COL + 64 <= 512, "tensor memory budget");
   static_assert(TOTAL <= 232448, "shared memory budget");
@@ -241,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_full = dz_free + 2;
   uint64_t* dq_free = dq_full + 1; // 256 arrivals: dQ read out
   uint64_t* drain = dq_free + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  ItemRing* ring = reinterpret_cast<ItemRing*>(drain + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -261,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dq_full, 1);
     mbar_init(dq_free, kCompute);
     mbar_init(drain, 1);
+    ring_init(ring, 9);  // taken by the MMA warp and the eight compute warps
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -279,11 +281,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
-      uint32_t n = 0, k = 0;
+      uint32_t n = 0, k = 0, hand = 0;
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+      while (ok) {
+        const int i = ring_fetch(a.sched);  // in order: the longest range first
+        if (i >= n_items) break;
         const QItem it = q_item(a, i, n_hg, n_seq, n_qb, BP);
         if (it.n_tiles == 0) continue;
+        if (!ring_put(ring, hand, i, a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
         if (k > 0 && !bwait(q_empty, (k - 1) & 1, a.status, abort_flag)) {
           ok = false;
           break;
@@ -308,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_head_tile<D>(dst + L::TILE, &tmKV, &kv_full[sl], vcol, it.a0 + j * AM);
         }
       }
+      if (ok) ring_put(ring, hand, -1, a.status, abort_flag);  // end of the items
       if (!ok) {  // let the copies already issued land (bounded)
         volatile int own = 0;
         const uint32_t m = n < (uint32_t)L::SLOTS ? n : (uint32_t)L::SLOTS;
@@ -330,11 +339,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, bwait(b, parity, a.status, abort_flag));
     };
-    uint32_t g = 0, n = 0, k = 0;
+    uint32_t g = 0, n = 0, k = 0, hand = 0;
     bool ok = true, issued_any = false;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+    while (ok) {
+      int i;
+      if (!ring_get(ring, hand, i, a.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (i < 0) break;
       const QItem it = q_item(a, i, n_hg, n_seq, n_qb, BP);
-      if (it.n_tiles == 0) continue;
       if (!wait_all(q_full, k & 1)) {
         ok = false;
         break;
@@ -415,11 +429,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) w_ok = bwait(b, parity, a.status, abort_flag);
       return __shfl_sync(0xffffffffu, w_ok, 0) != 0;
     };
-    uint32_t g = 0, k = 0;
+    uint32_t g = 0, k = 0, hand = 0;
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+    while (ok) {
+      int i;
+      if (!ring_get(ring, hand, i, a.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (i < 0) break;
       const QItem it = q_item(a, i, n_hg, n_seq, n_qb, BP);
-      if (it.n_tiles == 0) continue;
       ++k;
       const int pos = it.q0 + r % BP, head = it.h0 + r / BP;
       const bool valid = pos < it.L;
@@ -502,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
+  if (threadIdx.x == 0) ring_leave(a.sched);
 }
 
 // =================================================================== dK, dV
@@ -519,7 +539,7 @@ struct DkvLayout {
   static constexpr uint32_t K_OFF = 0, V_OFF = TILE, Q_OFF = 2 * TILE;
   static constexpr uint32_t LSE_OFF = Q_OFF + SLOTS * 2 * TILE;  // [2][128] -lse, [2][128] -D
   static constexpr uint32_t BAR_OFF = LSE_OFF + 4 * AM * 4;
-  static constexpr uint32_t TOTAL = BAR_OFF + 256 + 1024;
+  static constexpr uint32_t TOTAL = BAR_OFF + 512 + 1024;
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DK_COL = 256, DV_COL = 256 + D;
   static_assert(DV_COL + D <= 512, "tensor memory budget");
   static_assert(TOTAL <= 232448, "shared memory budget");
@@ -612,7 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_free = acc_full + 1;  // 256 arrivals: dK, dV read out
   uint64_t* lse_ready = acc_free + 1; // [2] 256 arrivals: lse / D of a tile in smem
   uint64_t* drain = lse_ready + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  ItemRing* ring = reinterpret_cast<ItemRing*>(drain + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -633,6 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_free, kCompute);
     mbar_init(drain, 1);
+    ring_init(ring, 9);  // taken by the MMA warp and the eight compute warps
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -651,11 +673,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
-      uint32_t n = 0, k = 0;
+      uint32_t n = 0, k = 0, hand = 0;
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+      while (ok) {
+        const int i = ring_fetch(a.sched + 2);  // in order: the longest range first
+        if (i >= n_items) break;
         const KItem it = k_item(a, i, n_seq, BP);
         if (it.nq == 0) continue;
+        if (!ring_put(ring, hand, i, a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
         if (k > 0 && !bwait(kv_empty, (k - 1) & 1, a.status, abort_flag)) {
           ok = false;
           break;
@@ -682,6 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                               BP);
         }
       }
+      if (ok) ring_put(ring, hand, -1, a.status, abort_flag);  // end of the items
       if (!ok) {
         volatile int own = 0;
         const uint32_t m = n < (uint32_t)L::SLOTS ? n : (uint32_t)L::SLOTS;
@@ -704,11 +733,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, bwait(b, parity, a.status, abort_flag));
     };
-    uint32_t gi = 0, n = 0, k = 0;
+    uint32_t gi = 0, n = 0, k = 0, hand = 0;
     bool ok = true, issued_any = false;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+    while (ok) {
+      int i;
+      if (!ring_get(ring, hand, i, a.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (i < 0) break;
       const KItem it = k_item(a, i, n_seq, BP);
-      if (it.nq == 0) continue;
       if (!wait_all(kv_full, k & 1)) {
         ok = false;
         break;
@@ -794,11 +828,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) w_ok = bwait(b, parity, a.status, abort_flag);
       return __shfl_sync(0xffffffffu, w_ok, 0) != 0;
     };
-    uint32_t gi = 0, k = 0;
+    uint32_t gi = 0, k = 0, hand = 0;
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+    while (ok) {
+      int i;
+      if (!ring_get(ring, hand, i, a.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (i < 0) break;
       const KItem it = k_item(a, i, n_seq, BP);
-      if (it.nq == 0) continue;
       ++k;
       const int kp = it.k0 + r;
       const bool kvalid = kp < it.L;
@@ -914,6 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
+  if (threadIdx.x == 0) ring_leave(a.sched + 2);
 }
 
 template <int D>
@@ -969,6 +1009,7 @@ cudaError_t attn_backward(const AttnBwdArgs& args, int n_seq, int max_len, int s
   AttnBwdArgs a = args;
   a.hpc = heads_per_tile(a.n_heads / a.n_kv_heads);
   if (n_seq <= 0 || max_len <= 0 || a.tokens <= 0) return cudaSuccess;
+  if (!a.sched) return cudaErrorInvalidValue;
   if (a.head_dim == 128) return launch<128>(a, n_seq, max_len, sm_count, s);
   if (a.head_dim == 64) return launch<64>(a, n_seq, max_len, sm_count, s);
   return cudaErrorInvalidValue;

@@ -21,12 +21,16 @@ struct AttnBwdArgs {
   int tokens, seq_len, nqkv, n_heads, n_kv_heads, head_dim, max_pos;
   int hpc;               // query heads per tile (set by attn_backward)
   int* status;           // device status word (bounded waits)
+  // work-item counter pairs {next, done} of the dQ and the dK / dV kernel
+  // (sched[0..1], sched[2..3]), zero between launches (the kernels leave
+  // them so): items are taken in order, longest range first
+  int* sched = nullptr;
 };
 
 // dq (from the query tiles' side) and dk, dv (from the key tiles' side, the
 // n_rep query heads of a kv head summed), each rotated back by RoPE^T and
 // written into dqkv.  max_len: longest sequence.  Two persistent launches
-// over min(work items, sm_count) CTAs.
+// over min(work items, sm_count) CTAs taking items dynamically (a.sched).
 cudaError_t attn_backward(const AttnBwdArgs& a, int n_seq, int max_len, int sm_count,
                           cudaStream_t s);
 

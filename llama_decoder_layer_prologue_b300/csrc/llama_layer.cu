@@ -29,7 +29,7 @@ constexpr int kMaxSkCtas = 160;
 // Work-item counter pairs in the packed buffer: the prefill attention
 // (plain or cached), the attention backward's dQ and dK / dV kernels (which
 // may overlap under programmatic dependent launch).
-constexpr int kSchedAttn = 0, kSchedDq = 2, kSchedDkv = 4;
+constexpr int kSchedAttn = 0, kSchedDq = 2;  // the dK / dV pair follows the dQ pair
 constexpr size_t kSkSlotBytes = 128 * 256 * sizeof(float);
 
 size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
@@ -644,6 +644,7 @@ int backward_impl(llama_layer* L, const llama_layer_weights* w, const void* x,
     ab.tokens = T; ab.seq_len = seq_len; ab.nqkv = dm.Nqkv; ab.n_heads = dm.Hq;
     ab.n_kv_heads = dm.Hkv; ab.head_dim = dm.d; ab.max_pos = dm.max_pos;
     ab.status = L->status;
+    ab.sched = L->sched + kSchedDq;  // the dQ pair, then the dK / dV pair
     mark(L, s, "bwd_attention");
     if (attn_backward(ab, n_seq, seq_len, L->sm_count, s) != cudaSuccess)
       return LLAMA_ERR_CUDA;
