@@ -33,7 +33,10 @@
 //   and dz^T (fp16, over the S^T / dP^T columns they read), and
 //   dV += P^T dO_i, dK += dz^T Q_i accumulate the whole group in TMEM (no
 //   atomics, no repeat_kv).
-// Every wait is bounded (2 s -> status bit, abort, drain, free TMEM).
+// Both kernels take their items dynamically, longest range first (a global
+// counter; the producer thread hands each to the MMA and compute warps
+// through a shared-memory ring).  Every wait is bounded (2 s -> status bit,
+// abort, drain, free TMEM).
 #include <cuda_fp16.h>
 #include <math.h>
 

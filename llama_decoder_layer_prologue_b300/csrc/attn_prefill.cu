@@ -28,8 +28,11 @@
 //               the other's products.
 // Rescaling of O is lazy: a row's reference max only moves (and O is
 // rescaled in TMEM) when the new max exceeds it by more than 8 in the log2
-// domain, so P stays <= 2^8.  Items run longest causal range first.  Every
-// wait is bounded (2 s -> status bit, abort, drain, free TMEM).
+// domain, so P stays <= 2^8.  Items are listed longest causal range first
+// and taken in that order from a global counter (the producer thread hands
+// each to the MMA and softmax warps through a shared-memory ring), so the
+// CTAs finish together.  Every wait is bounded (2 s -> status bit, abort,
+// drain, free TMEM).
 #include <cuda_bf16.h>
 #include <math.h>
 

@@ -12,8 +12,11 @@
 //               the tile's columns), fused epilogue, stores.  The two
 //               accumulators let the epilogue of tile i overlap the main loop
 //               of tile i + 1.
-// Tiles are visited in bands of 16 M-tiles so that a wave of CTAs shares A
-// and B slices in L2.  Every wait is bounded (see mbar_wait).
+// The layer's GEMMs run as CTA pairs (clusters of 2, CG2 below): rank 0's
+// MMA thread issues one M = 256 tcgen05.mma.cta_group::2 per K step over
+// both CTAs' shared memory and tensor memory.  Tiles are visited in bands of
+// M-tiles sized by L2 (tc_group_m) so that a wave of CTAs shares A and B
+// slices in L2.  Every wait is bounded (see mbar_wait).
 #include <cuda_bf16.h>
 #include <math.h>
 
