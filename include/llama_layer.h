@@ -47,8 +47,9 @@
  *     status word and the kernel returns (llama_layer_status reports
  *     LLAMA_ERR_DEVICE_TIMEOUT).
  *   - One layer handle serves one stream at a time: its status word, its
- *     split-tile flags and the copy streams of llama_layer_forward_host are
- *     per handle, and a workspace holds one call's intermediates.  Calls on
+ *     split-tile flags, its attention work-item counters, and the copy
+ *     streams and page-locked cu_seqlens buffer of llama_layer_forward_host
+ *     are per handle, and a workspace holds one call's intermediates.  Calls on
  *     one stream may share a workspace (and several layers may, as the
  *     layers of a model do); concurrent calls need their own handles and
  *     workspaces.  The handle itself is not locked: call it from one host
@@ -139,7 +140,9 @@ typedef struct {
 typedef struct llama_layer llama_layer_t;
 
 /* Bytes of device memory llama_layer_init needs for the packed weights, the
- * RoPE table and the status word.  Host only. */
+ * RoPE table, the status word and the kernels' per-layer flags and work-item
+ * counters (zeroed by llama_layer_init, left zero by every call).  Host
+ * only. */
 LLAMA_API int llama_layer_packed_bytes(const llama_layer_config* cfg, size_t* bytes);
 
 /* The RoPE inverse frequencies f_i, i = 0 .. head_dim/2 - 1, the layer
