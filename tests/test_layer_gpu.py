@@ -231,6 +231,37 @@ def test_forward_host_five_groups(kind):
     layer.close()
 
 
+@pytest.mark.parametrize("kind", ["padded", "varlen"])
+def test_forward_host_fp32(kind):
+    # the fp32 layer through host buffers: rows of 4-byte values, groups of
+    # whole sequences (three), the fp32 bound
+    s = shape(256, 4, 2, 64, 512, dtype="fp32")
+    if kind == "padded":
+        w = synth.custom_workload("hostf", s, "padded", batch=3, seq=40)
+    else:
+        w = synth.custom_workload("hostfv", s, "varlen", total_tokens=150, min_len=1,
+                                  max_len=60)
+    inp = synth.make_inputs(w)
+    layer = build_layer(inp)
+    x_h = to_device(inp.x, pin=True)
+    out_h = torch.full_like(x_h, float("nan")).pin_memory()
+    stage_x = torch.empty(x_h.shape, dtype=x_h.dtype, device="cuda")
+    stage_out = torch.empty_like(stage_x)
+    S = int(np.diff(inp.cu_seqlens).max())
+    if kind == "padded":
+        layer.forward_from_host(x_h, out_h, stage_x, stage_out, n_seq=3, seq_len=S, chunks=3)
+    else:
+        layer.forward_from_host(x_h, out_h, stage_x, stage_out,
+                                cu_seqlens=torch.from_numpy(inp.cu_seqlens.copy()),
+                                seq_len=S, chunks=3)
+    torch.cuda.current_stream().synchronize()
+    assert layer.status() == B.LLAMA_OK
+    ref = oracle.decoder_layer(synth.to_f64(inp.x), weights_f64(inp.weights),
+                               s, inp.positions, inp.cu_seqlens)
+    assert_close(to_f64(out_h), ref["out"], s.dtype, "host out (fp32)")
+    layer.close()
+
+
 def test_forward_host_rejects_bad_host_cu_seqlens():
     s = shape(256, 4, 2, 64, 256, **L3)
     w = synth.custom_workload("hostbad", s, "varlen", total_tokens=64, min_len=1,
