@@ -122,15 +122,16 @@ def test_saved_backward_refuses_mismatches():
     layer.close()
 
 
-def test_train_step_from_host_equals_the_device_pair():
+@pytest.mark.parametrize("case", CASES[:2], ids=lambda c: c[0])
+def test_train_step_from_host_equals_the_device_pair(case):
     # host x and dL/d(out) in, dx out; dL/d(out) crosses on a second stream
     # while the forward runs: the same bits as the device-resident pair
-    name, s, kind, kw = CASES[0]
+    name, s, kind, kw = case
     inp = synth.make_inputs(synth.custom_workload(name, s, kind, index=311, **kw))
     layer = build_layer(inp)
     x = to_device(inp.x)
     dout = to_device(synth.make_dout(inp))
-    args = batch_args(inp, False)
+    args = batch_args(inp, kind == "varlen")
     y_ref = layer.forward_train(x, **args).clone()
     g_ref = {k: v.clone() for k, v in layer.backward_saved(x, dout, **args).items()}
     x_h, dout_h = to_device(inp.x, pin=True), to_device(synth.make_dout(inp), pin=True)
